@@ -1,0 +1,206 @@
+/*
+ * pfkv.h -- C ABI of libpfkv: a paged FP8 (e4m3) KV cache for decode
+ * attention on GB300 (sm_103a).
+ *
+ * What the operations are, from "Smaller, faster, safer: running Kimi and GLM
+ * at scale" (Cloudflare):
+ *  - section "Quantizing the KV cache": the decode pool keeps K and V in
+ *    8-bit floating point (FP8, e4m3) instead of BF16, halving the cache, and
+ *    the FP8 attention kernel converts the values as it reads them.  Both
+ *    cache precisions exist (BF16 is the default and the prefill pool's).
+ *  - the cache-protection passage: many concurrent requests read and write
+ *    one shared physical cache; each page carries a tag that changes whenever
+ *    the page is reallocated; before a read the mapping's tag is compared
+ *    with the page's, and on a mismatch the request is aborted instead of
+ *    returning wrong data; the check is off by default.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer.  The library never allocates,
+ *    never frees and never synchronises; it only enqueues work on `stream`
+ *    (a cudaStream_t passed as void*; NULL = the legacy default stream).
+ *  - Pointers are DEVICE pointers unless marked "host".  The cache descriptor
+ *    itself is host memory, read during the call only.
+ *  - Return value: 0 (PFKV_OK) or a negative PFKV_ERR_* code for errors that
+ *    the host can see (bad argument, unsupported shape, small workspace,
+ *    launch failure).  Nothing is enqueued when an error is returned.
+ *  - Per-request data faults (stale tag, page id outside the pool, bad
+ *    length) are reported in status[batch] (uint32 bit set, PFKV_ST_*), which
+ *    every call overwrites.  They never trap on the device.
+ *  - An aborted request's attention output rows are all zero.
+ *  - Results are deterministic for identical inputs.
+ */
+#ifndef PFKV_H
+#define PFKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Cache element type. */
+enum { PFKV_DTYPE_BF16 = 0, PFKV_DTYPE_FP8_E4M3 = 1 };
+
+/* FP8 scale granularity.  PER_HEAD: one fp32 scale per KV head for the whole
+ * pool (calibrated, see pfkv_calibrate_scales).  PER_TOKEN: one fp32 scale
+ * per cached (token, KV head) row, computed by the append from that row. */
+enum { PFKV_SCALE_PER_HEAD = 0, PFKV_SCALE_PER_TOKEN = 1 };
+
+/* Call flags.  TAG_CHECK enables the page-tag comparison; it is off unless
+ * set, as in the post. */
+enum { PFKV_FLAG_TAG_CHECK = 1u };
+
+/* Per-request status bits. */
+enum {
+  PFKV_ST_STALE_TAG = 1u, /* a page's tag differs from the mapping's tag  */
+  PFKV_ST_PAGE_OOB = 2u,  /* a page id is outside [0, num_pages)          */
+  PFKV_ST_BAD_LEN = 4u,   /* length < 1 or beyond max_pages * page_size,
+                             or an append position outside the table      */
+  PFKV_ST_TIMEOUT = 8u    /* a pipeline wait inside the kernel gave up;
+                             the output of the call is not valid          */
+};
+
+/* Return codes. */
+enum {
+  PFKV_OK = 0,
+  PFKV_ERR_NULL = -1,        /* a required pointer is NULL                  */
+  PFKV_ERR_SHAPE = -2,       /* inconsistent or out-of-range sizes          */
+  PFKV_ERR_UNSUPPORTED = -3, /* valid but not implemented (head dim, group) */
+  PFKV_ERR_DTYPE = -4,       /* cache dtype does not match the entry point  */
+  PFKV_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than required     */
+  PFKV_ERR_ALIGN = -6,       /* a buffer is not 16-byte aligned             */
+  PFKV_ERR_CUDA = -7         /* a CUDA runtime/driver call failed           */
+};
+
+/*
+ * Paged cache descriptor (host struct; the arrays it points to are device
+ * memory).  Layout (this library's choice; the post gives none):
+ *   k_pool : [num_pages][num_kv_heads][page_size][head_dim]   elements
+ *   v_pool : [num_pages][num_kv_heads][page_size][v_head_dim] elements
+ *   element = 1 byte e4m3 code (FP8) or 2 byte bf16 (BF16).
+ *   k_scale/v_scale (FP8 only): PER_HEAD [num_kv_heads];
+ *                               PER_TOKEN [num_pages][num_kv_heads][page_size].
+ *   page_tags : [num_pages] uint32, the page's current generation tag.
+ * Logical token t of a request lives in page block_table[b][t / page_size],
+ * slot t % page_size.
+ * Latent (shared) stream: kv_shared = 1, num_kv_heads = 1, v_pool = NULL,
+ * v_scale = NULL; V is the first v_head_dim values of each K row.
+ * Every pool base must be 16-byte aligned.
+ */
+typedef struct pfkv_cache {
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t v_head_dim;
+  int32_t kv_shared;
+  int32_t dtype;      /* PFKV_DTYPE_*      */
+  int32_t scale_mode; /* PFKV_SCALE_*      */
+  void *k_pool;
+  void *v_pool;
+  float *k_scale;
+  float *v_scale;
+  const uint32_t *page_tags;
+} pfkv_cache;
+
+/*
+ * kv_append_quantize -- write new K/V rows into the paged cache ("Quantizing
+ * the KV cache": the cache is stored in FP8 e4m3).
+ *
+ * num_rows new tokens.  Row i belongs to request row_req[i] (row_req may be
+ * NULL: row i belongs to request i, the one-token-per-request decode case)
+ * and goes to logical position positions[i]:
+ *   page = block_table[b][positions[i] / page_size], slot = positions[i] % page_size.
+ *   k_new : bf16 [num_rows][num_kv_heads][head_dim]
+ *   v_new : bf16 [num_rows][num_kv_heads][v_head_dim] (ignored when kv_shared)
+ *   block_table, block_tags : [batch][max_pages] int32 / uint32
+ * FP8: code = e4m3(fp32(x) / s), IEEE fp32 division, round to nearest even,
+ * saturating to +-448.  PER_HEAD uses k_scale[h] / v_scale[h] as given.
+ * PER_TOKEN computes s = amax(|row|)/448 (1 when the row is all zero) for each
+ * (token, head) row, stores it in the scale array and quantizes with it.
+ * BF16: the bits are copied.
+ * A row is refused -- nothing of it is written -- when its position is
+ * outside [0, max_pages*page_size) (BAD_LEN), its page id is outside the pool
+ * (PAGE_OOB), or TAG_CHECK is set and page_tags[page] differs from
+ * block_tags[b][positions[i] / page_size] (STALE_TAG).  status[batch] is
+ * cleared and then gets the bits of every refused row of each request.
+ * Rows of one call must not target the same slot.
+ */
+int pfkv_kv_append_quantize(const pfkv_cache *cache, const void *k_new, const void *v_new, int32_t num_rows,
+                            const int32_t *row_req, const int32_t *positions, const int32_t *block_table,
+                            const uint32_t *block_tags, int32_t batch, int32_t max_pages, uint32_t flags,
+                            uint32_t *status, void *stream);
+
+/*
+ * Bytes of device workspace a decode call needs for these sizes (split-KV
+ * partial results and the split plan).  Host-only, no CUDA call.
+ */
+size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32_t num_q_heads,
+                                   int32_t max_splits);
+
+/*
+ * paged_decode_attention -- single-token decode attention over the paged
+ * cache, converting FP8 codes as they are read ("Quantizing the KV cache")
+ * and, when TAG_CHECK is set, comparing every page's tag with the mapping's
+ * before its data may be returned (cache-protection passage).
+ *
+ *   q          : bf16 [batch][num_q_heads][head_dim]
+ *   seq_lens   : int32 [batch], tokens of context per request (>= 1)
+ *   block_table: int32 [batch][max_pages]; block_tags: uint32 [batch][max_pages]
+ *   out        : fp32 [batch][num_q_heads][v_head_dim]
+ *   status     : uint32 [batch]
+ * For query head h (KV head g = h / (num_q_heads / num_kv_heads)):
+ *   z_t = softmax_scale * q[b][h] . k^[g][t],  p = softmax(z over t < L_b),
+ *   out[b][h] = sum_t p_t v^[g][t],  where k^, v^ are the dequantized rows
+ *   (code value * scale for FP8).
+ * Only logical pages i < ceil(L_b / page_size) are inspected.  A request
+ * with any status bit gets zero output.  max_splits (1..256) bounds how many
+ * pieces one request's context is split into (flash-decoding); the pieces
+ * are merged with the log-sum-exp rule.  workspace must hold
+ * pfkv_decode_workspace_bytes(cache, batch, num_q_heads, max_splits) bytes;
+ * its contents need no initialisation and are scratch between calls.
+ * Supported: head_dim 64 or 128 with groups 1, 2, 4, 8 (page_size a
+ * multiple of 16, at most 256); the latent stream head_dim 576 / v_head_dim
+ * 512 with 64 query heads (FP8, PER_TOKEN, page_size 64).
+ * pfkv_paged_decode_attention_fp8 requires an FP8 cache, _bf16 a BF16 cache.
+ */
+int pfkv_paged_decode_attention_fp8(const pfkv_cache *cache, const void *q, int32_t num_q_heads,
+                                    const int32_t *seq_lens, const int32_t *block_table,
+                                    const uint32_t *block_tags, int32_t batch, int32_t max_pages,
+                                    float softmax_scale, uint32_t flags, int32_t max_splits, void *workspace,
+                                    size_t workspace_bytes, float *out, uint32_t *status, void *stream);
+
+int pfkv_paged_decode_attention_bf16(const pfkv_cache *cache, const void *q, int32_t num_q_heads,
+                                     const int32_t *seq_lens, const int32_t *block_table,
+                                     const uint32_t *block_tags, int32_t batch, int32_t max_pages,
+                                     float softmax_scale, uint32_t flags, int32_t max_splits, void *workspace,
+                                     size_t workspace_bytes, float *out, uint32_t *status, void *stream);
+
+/*
+ * calibrate_scales -- per-head FP8 scales s[h] = fp32(amax/448) over
+ * rows[n_rows][num_heads][head_dim] (bf16); s[h] = 1 when the head's rows
+ * are all zero.  This is the "scale = amax / 448" convention of an e4m3 cache
+ * whose largest finite value is 448.  scale: fp32 [num_heads], overwritten.
+ */
+int pfkv_calibrate_scales(const void *rows, int64_t n_rows, int32_t num_heads, int32_t head_dim, float *scale,
+                          void *stream);
+
+/*
+ * e4m3_encode -- codes[i] = e4m3(x[i]) for fp32 x: round to nearest even,
+ * saturate finite overflow to +-448, sign kept on zero, NaN -> NaN code.
+ * The same conversion the append uses (exposed for the codec tests).
+ */
+int pfkv_e4m3_encode(const float *x, uint8_t *codes, int64_t n, void *stream);
+
+/* Human-readable text for a PFKV_ERR_* code. */
+const char *pfkv_strerror(int code);
+
+/* ABI version of this header (bumped when a signature changes). */
+int pfkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PFKV_H */

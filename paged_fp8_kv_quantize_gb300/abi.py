@@ -1,0 +1,250 @@
+"""Thin ctypes binding of libpfkv (include/pfkv.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  If the
+shared library is missing this module raises on import -- there is no other
+implementation behind it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpfkv.so")
+
+DTYPE_BF16 = 0
+DTYPE_FP8_E4M3 = 1
+SCALE_PER_HEAD = 0
+SCALE_PER_TOKEN = 1
+FLAG_TAG_CHECK = 1
+ST_STALE_TAG = 1
+ST_PAGE_OOB = 2
+ST_BAD_LEN = 4
+ST_TIMEOUT = 8
+
+EXPORTS = (
+    "pfkv_kv_append_quantize",
+    "pfkv_decode_workspace_bytes",
+    "pfkv_paged_decode_attention_fp8",
+    "pfkv_paged_decode_attention_bf16",
+    "pfkv_calibrate_scales",
+    "pfkv_e4m3_encode",
+    "pfkv_strerror",
+    "pfkv_abi_version",
+)
+
+
+class PfkvError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+        self.code = code
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_pages", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("v_head_dim", ctypes.c_int32),
+        ("kv_shared", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("scale_mode", ctypes.c_int32),
+        ("k_pool", ctypes.c_void_p),
+        ("v_pool", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
+        ("page_tags", ctypes.c_void_p),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libpfkv.so is not built ({LIB_PATH}); run paged_fp8_kv_quantize_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, u32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_size_t
+    cp = ctypes.POINTER(CacheDesc)
+    L.pfkv_kv_append_quantize.restype = ctypes.c_int
+    L.pfkv_kv_append_quantize.argtypes = [cp, P, P, i32, P, P, P, P, i32, i32, u32, P, P]
+    L.pfkv_decode_workspace_bytes.restype = sz
+    L.pfkv_decode_workspace_bytes.argtypes = [cp, i32, i32, i32]
+    for n in ("pfkv_paged_decode_attention_fp8", "pfkv_paged_decode_attention_bf16"):
+        f = getattr(L, n)
+        f.restype = ctypes.c_int
+        f.argtypes = [cp, P, i32, P, P, P, i32, i32, ctypes.c_float, u32, i32, P, sz, P, P, P]
+    L.pfkv_calibrate_scales.restype = ctypes.c_int
+    L.pfkv_calibrate_scales.argtypes = [P, i64, i32, i32, P, P]
+    L.pfkv_e4m3_encode.restype = ctypes.c_int
+    L.pfkv_e4m3_encode.argtypes = [P, P, i64, P]
+    L.pfkv_strerror.restype = ctypes.c_char_p
+    L.pfkv_strerror.argtypes = [ctypes.c_int]
+    L.pfkv_abi_version.restype = ctypes.c_int
+    L.pfkv_abi_version.argtypes = []
+    return L
+
+
+lib = _load()
+
+
+def strerror(code: int) -> str:
+    return lib.pfkv_strerror(int(code)).decode()
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise PfkvError(fn, rc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+class PagedCache:
+    """Device-resident paged KV cache (pools, scales, page tags) + its descriptor.
+
+    Layout: k_pool [P][Hkv][S][D], v_pool [P][Hkv][S][Dv] (uint8 e4m3 codes or
+    bf16); scales per head [Hkv] or per token [P][Hkv][S]; page_tags [P] uint32
+    (stored as int32 -- torch has no uint32 arithmetic on every version).
+    """
+
+    def __init__(self, num_pages, page_size, num_kv_heads, head_dim, v_head_dim=None, kv_shared=False,
+                 dtype=DTYPE_FP8_E4M3, scale_mode=SCALE_PER_HEAD, device="cuda", fill=None, alloc_pools=True):
+        self.P, self.S, self.H, self.D = int(num_pages), int(page_size), int(num_kv_heads), int(head_dim)
+        self.Dv = int(v_head_dim if v_head_dim is not None else head_dim)
+        self.kv_shared, self.dtype, self.scale_mode = bool(kv_shared), int(dtype), int(scale_mode)
+        self.device = torch.device(device)
+        el = torch.uint8 if self.dtype == DTYPE_FP8_E4M3 else torch.bfloat16
+        rows = self.P * self.H * self.S
+        self.k_pool = self.v_pool = None
+        if alloc_pools:
+            self.k_pool = torch.empty(rows * self.D, dtype=el, device=self.device)
+            self.v_pool = None if kv_shared else torch.empty(rows * self.Dv, dtype=el, device=self.device)
+            if fill is not None:
+                self.fill_pools(fill)
+        if self.dtype == DTYPE_FP8_E4M3:
+            n = rows if self.scale_mode == SCALE_PER_TOKEN else self.H
+            self.k_scale = torch.ones(n, dtype=torch.float32, device=self.device)
+            self.v_scale = None if kv_shared else torch.ones(n, dtype=torch.float32, device=self.device)
+        else:
+            self.k_scale = self.v_scale = None
+        self.page_tags = torch.zeros(self.P, dtype=torch.int32, device=self.device)
+
+    def fill_pools(self, byte):
+        for t in (self.k_pool, self.v_pool):
+            if t is not None:
+                t.view(torch.uint8).fill_(int(byte))
+
+    def desc(self) -> CacheDesc:
+        return CacheDesc(self.P, self.S, self.H, self.D, self.Dv, int(self.kv_shared), self.dtype, self.scale_mode,
+                         _ptr(self.k_pool), _ptr(self.v_pool), _ptr(self.k_scale), _ptr(self.v_scale),
+                         _ptr(self.page_tags))
+
+    def k_rows(self):
+        return self.k_pool.view(self.P, self.H, self.S, self.D)
+
+    def v_rows(self):
+        return None if self.v_pool is None else self.v_pool.view(self.P, self.H, self.S, self.Dv)
+
+
+def kv_append_quantize(cache: PagedCache, k_new, v_new, positions, block_table, block_tags=None, flags=0,
+                       row_req=None, batch=None, status=None, stream=None):
+    """Quantize-and-append rows (see pfkv_kv_append_quantize).  Returns status [batch] (int32 view of uint32)."""
+    i32 = torch.int32
+    n_rows = positions.shape[0]
+    B, MP = block_table.shape
+    batch = B if batch is None else int(batch)
+    if status is None:
+        status = torch.empty(batch, dtype=i32, device=block_table.device)
+    d = cache.desc()
+    rc = lib.pfkv_kv_append_quantize(
+        ctypes.byref(d), _ptr(_dev(k_new, "k_new", torch.bfloat16)),
+        _ptr(_dev(v_new, "v_new", torch.bfloat16)) if v_new is not None else None, n_rows,
+        _ptr(_dev(row_req, "row_req", i32)), _ptr(_dev(positions, "positions", i32)),
+        _ptr(_dev(block_table, "block_table", i32)), _ptr(_dev(block_tags, "block_tags", i32)), batch, MP,
+        int(flags), _ptr(_dev(status, "status", i32)), _stream(stream))
+    _check("pfkv_kv_append_quantize", rc)
+    return status
+
+
+def decode_workspace_bytes(cache: PagedCache, batch, num_q_heads, max_splits=64) -> int:
+    d = cache.desc()
+    return int(lib.pfkv_decode_workspace_bytes(ctypes.byref(d), int(batch), int(num_q_heads), int(max_splits)))
+
+
+def _decode(fn_name, cache, q, seq_lens, block_table, block_tags, softmax_scale, flags, max_splits, workspace, out,
+            status, stream):
+    B, Hq, D = q.shape
+    MP = block_table.shape[1]
+    dev = q.device
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_bytes(cache, B, Hq, max_splits), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(B, Hq, cache.Dv, dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    d = cache.desc()
+    rc = getattr(lib, fn_name)(
+        ctypes.byref(d), _ptr(_dev(q, "q", torch.bfloat16)), Hq, _ptr(_dev(seq_lens, "seq_lens", torch.int32)),
+        _ptr(_dev(block_table, "block_table", torch.int32)), _ptr(_dev(block_tags, "block_tags", torch.int32)), B,
+        MP, float(softmax_scale), int(flags), int(max_splits), _ptr(workspace), workspace.numel(),
+        _ptr(_dev(out, "out", torch.float32)), _ptr(_dev(status, "status", torch.int32)), _stream(stream))
+    _check(fn_name, rc)
+    return out, status
+
+
+def paged_decode_attention_fp8(cache, q, seq_lens, block_table, block_tags, softmax_scale, flags=0, max_splits=64,
+                               workspace=None, out=None, status=None, stream=None):
+    return _decode("pfkv_paged_decode_attention_fp8", cache, q, seq_lens, block_table, block_tags, softmax_scale,
+                   flags, max_splits, workspace, out, status, stream)
+
+
+def paged_decode_attention_bf16(cache, q, seq_lens, block_table, block_tags, softmax_scale, flags=0, max_splits=64,
+                                workspace=None, out=None, status=None, stream=None):
+    return _decode("pfkv_paged_decode_attention_bf16", cache, q, seq_lens, block_table, block_tags, softmax_scale,
+                   flags, max_splits, workspace, out, status, stream)
+
+
+def paged_decode_attention(cache, *args, **kw):
+    """Dispatch on the cache dtype to the FP8 or BF16 entry point."""
+    f = paged_decode_attention_fp8 if cache.dtype == DTYPE_FP8_E4M3 else paged_decode_attention_bf16
+    return f(cache, *args, **kw)
+
+
+def calibrate_scales(rows, scale=None, stream=None):
+    """rows: bf16 [N][H][D] -> fp32 scale[H] = amax/448 (1 for an all-zero head)."""
+    N, H, D = rows.shape
+    if scale is None:
+        scale = torch.empty(H, dtype=torch.float32, device=rows.device)
+    rc = lib.pfkv_calibrate_scales(_ptr(_dev(rows, "rows", torch.bfloat16)), N, H, D,
+                                   _ptr(_dev(scale, "scale", torch.float32)), _stream(stream))
+    _check("pfkv_calibrate_scales", rc)
+    return scale
+
+
+def e4m3_encode(x, out=None, stream=None):
+    x = _dev(x, "x", torch.float32)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    rc = lib.pfkv_e4m3_encode(_ptr(x), _ptr(out), x.numel(), _stream(stream))
+    _check("pfkv_e4m3_encode", rc)
+    return out

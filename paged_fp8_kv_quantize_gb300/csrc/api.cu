@@ -1,0 +1,201 @@
+// api.cu -- the extern "C" entry points of libpfkv: argument checks on the
+// host, workspace layout, and dispatch to the kernels on the caller's stream.
+#include <math.h>
+#include <mutex>
+
+#include "pfkv_internal.h"
+
+namespace pfkv {
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
+  WsLayout w;
+  const size_t slots = (size_t)batch * max_splits * q_heads;
+  w.hdr = 0;
+  w.chunk_start = up256(sizeof(WsHeader));
+  w.ppc = w.chunk_start + up256(sizeof(int) * ((size_t)batch + 1));
+  w.part_ml = w.ppc + up256(sizeof(int) * (size_t)batch);
+  w.part_o = w.part_ml + up256(sizeof(float2) * slots);
+  w.total = w.part_o + up256(sizeof(float) * slots * v_dim);
+  return w;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool is_latent(const pfkv_cache *c) {
+  return c->kv_shared && c->num_kv_heads == 1 && c->head_dim == 576 && c->v_head_dim == 512;
+}
+
+// Checks shared by every call that takes a cache descriptor.
+static int check_cache(const pfkv_cache *c) {
+  if (!c) return PFKV_ERR_NULL;
+  if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1 || c->v_head_dim < 1)
+    return PFKV_ERR_SHAPE;
+  if (c->dtype != PFKV_DTYPE_BF16 && c->dtype != PFKV_DTYPE_FP8_E4M3) return PFKV_ERR_DTYPE;
+  if (c->scale_mode != PFKV_SCALE_PER_HEAD && c->scale_mode != PFKV_SCALE_PER_TOKEN) return PFKV_ERR_SHAPE;
+  if (!c->k_pool) return PFKV_ERR_NULL;
+  if (c->kv_shared) {
+    if (c->num_kv_heads != 1 || c->v_head_dim > c->head_dim) return PFKV_ERR_SHAPE;
+  } else {
+    if (!c->v_pool) return PFKV_ERR_NULL;
+    if (c->v_head_dim != c->head_dim) return PFKV_ERR_UNSUPPORTED;
+  }
+  if (c->dtype == PFKV_DTYPE_FP8_E4M3 && (!c->k_scale || (!c->kv_shared && !c->v_scale))) return PFKV_ERR_NULL;
+  if (c->head_dim % 8 || c->v_head_dim % 8) return PFKV_ERR_UNSUPPORTED;
+  if (!aligned16(c->k_pool) || (c->v_pool && !aligned16(c->v_pool))) return PFKV_ERR_ALIGN;
+  if (c->scale_mode == PFKV_SCALE_PER_TOKEN &&
+      (!aligned16(c->k_scale) || (c->v_scale && !aligned16(c->v_scale))))
+    return PFKV_ERR_ALIGN;
+  return PFKV_OK;
+}
+
+static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int32_t Hq, const int32_t *seq_lens,
+                         const int32_t *block_table, const uint32_t *block_tags, int32_t batch, int32_t max_pages,
+                         float softmax_scale, uint32_t flags, int32_t max_splits, void *ws, size_t ws_bytes,
+                         float *out, uint32_t *status, void *stream) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if (c->dtype != want_dtype) return PFKV_ERR_DTYPE;
+  if (batch < 0 || max_pages < 1 || Hq < 1 || max_splits < 1 || max_splits > 256) return PFKV_ERR_SHAPE;
+  if (!isfinite(softmax_scale)) return PFKV_ERR_SHAPE;
+  if (batch == 0) return PFKV_OK;
+  if (!q || !seq_lens || !block_table || !out || !status || !ws) return PFKV_ERR_NULL;
+  if ((flags & PFKV_FLAG_TAG_CHECK) && (!c->page_tags || !block_tags)) return PFKV_ERR_NULL;
+  if (Hq % c->num_kv_heads) return PFKV_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(out)) return PFKV_ERR_ALIGN;
+  if (c->page_size % 16 || c->page_size > 256) return PFKV_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(batch, Hq, c->v_head_dim, max_splits);
+  if (ws_bytes < L.total) return PFKV_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return PFKV_ERR_ALIGN;
+
+  DecodeArgs a;
+  a.P = c->num_pages; a.S = c->page_size; a.Hkv = c->num_kv_heads; a.D = c->head_dim; a.Dv = c->v_head_dim;
+  a.scale_mode = c->scale_mode; a.dtype = c->dtype; a.kv_shared = c->kv_shared;
+  a.k_pool = c->k_pool; a.v_pool = c->v_pool; a.k_scale = c->k_scale; a.v_scale = c->v_scale;
+  a.page_tags = c->page_tags;
+  a.q = q; a.Hq = Hq; a.G = Hq / c->num_kv_heads;
+  a.seq_lens = seq_lens; a.block_table = block_table; a.block_tags = block_tags;
+  a.B = batch; a.MP = max_pages;
+  a.sm_scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.flags = flags; a.max_splits = max_splits;
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  a.hdr = reinterpret_cast<WsHeader *>(w + L.hdr);
+  a.chunk_start = reinterpret_cast<int *>(w + L.chunk_start);
+  a.ppc = reinterpret_cast<int *>(w + L.ppc);
+  a.part_ml = reinterpret_cast<float2 *>(w + L.part_ml);
+  a.part_o = reinterpret_cast<float *>(w + L.part_o);
+  a.out = out; a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c->kv_shared) {
+    if (!is_latent(c) || Hq != 64 || c->dtype != PFKV_DTYPE_FP8_E4M3 || c->scale_mode != PFKV_SCALE_PER_TOKEN ||
+        c->page_size != 64)
+      return PFKV_ERR_UNSUPPORTED;
+    return launch_latent_decode(a, s);
+  }
+  if ((c->head_dim != 64 && c->head_dim != 128) || (a.G != 1 && a.G != 2 && a.G != 4 && a.G != 8))
+    return PFKV_ERR_UNSUPPORTED;
+  if (c->dtype == PFKV_DTYPE_BF16 && c->scale_mode != PFKV_SCALE_PER_HEAD) return PFKV_ERR_SHAPE;
+  return launch_gqa_decode(a, s);
+}
+
+}  // namespace pfkv
+
+using namespace pfkv;
+
+extern "C" {
+
+int pfkv_abi_version(void) { return 1; }
+
+const char *pfkv_strerror(int code) {
+  switch (code) {
+    case PFKV_OK: return "ok";
+    case PFKV_ERR_NULL: return "a required pointer is NULL";
+    case PFKV_ERR_SHAPE: return "inconsistent or out-of-range sizes";
+    case PFKV_ERR_UNSUPPORTED: return "shape or mode not implemented";
+    case PFKV_ERR_DTYPE: return "cache dtype does not match the entry point";
+    case PFKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PFKV_ERR_ALIGN: return "buffer not aligned (16 bytes; workspace 256 bytes)";
+    case PFKV_ERR_CUDA: return "CUDA runtime or driver call failed";
+    default: return "unknown error";
+  }
+}
+
+int pfkv_kv_append_quantize(const pfkv_cache *cache, const void *k_new, const void *v_new, int32_t num_rows,
+                            const int32_t *row_req, const int32_t *positions, const int32_t *block_table,
+                            const uint32_t *block_tags, int32_t batch, int32_t max_pages, uint32_t flags,
+                            uint32_t *status, void *stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_rows < 0 || batch < 0 || max_pages < 1) return PFKV_ERR_SHAPE;
+  if (!row_req && num_rows > batch) return PFKV_ERR_SHAPE;
+  if (batch == 0) return PFKV_OK;
+  if (!status) return PFKV_ERR_NULL;
+  if (num_rows > 0) {
+    if (!k_new || !positions || !block_table || (!cache->kv_shared && !v_new)) return PFKV_ERR_NULL;
+    if ((flags & PFKV_FLAG_TAG_CHECK) && (!cache->page_tags || !block_tags)) return PFKV_ERR_NULL;
+    if (!aligned16(k_new) || (v_new && !cache->kv_shared && !aligned16(v_new))) return PFKV_ERR_ALIGN;
+  }
+  if (cache->dtype == PFKV_DTYPE_BF16 && cache->scale_mode != PFKV_SCALE_PER_HEAD) return PFKV_ERR_SHAPE;
+  return launch_append(*cache, k_new, v_new, num_rows, row_req, positions, block_table, block_tags, batch,
+                       max_pages, flags, status, static_cast<cudaStream_t>(stream));
+}
+
+size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32_t num_q_heads, int32_t max_splits) {
+  if (!cache || batch < 0 || num_q_heads < 1 || max_splits < 1) return 0;
+  return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits).total;
+}
+
+int pfkv_paged_decode_attention_fp8(const pfkv_cache *cache, const void *q, int32_t num_q_heads,
+                                    const int32_t *seq_lens, const int32_t *block_table,
+                                    const uint32_t *block_tags, int32_t batch, int32_t max_pages,
+                                    float softmax_scale, uint32_t flags, int32_t max_splits, void *workspace,
+                                    size_t workspace_bytes, float *out, uint32_t *status, void *stream) {
+  return decode_common(PFKV_DTYPE_FP8_E4M3, cache, q, num_q_heads, seq_lens, block_table, block_tags, batch,
+                       max_pages, softmax_scale, flags, max_splits, workspace, workspace_bytes, out, status, stream);
+}
+
+int pfkv_paged_decode_attention_bf16(const pfkv_cache *cache, const void *q, int32_t num_q_heads,
+                                     const int32_t *seq_lens, const int32_t *block_table,
+                                     const uint32_t *block_tags, int32_t batch, int32_t max_pages,
+                                     float softmax_scale, uint32_t flags, int32_t max_splits, void *workspace,
+                                     size_t workspace_bytes, float *out, uint32_t *status, void *stream) {
+  return decode_common(PFKV_DTYPE_BF16, cache, q, num_q_heads, seq_lens, block_table, block_tags, batch, max_pages,
+                       softmax_scale, flags, max_splits, workspace, workspace_bytes, out, status, stream);
+}
+
+int pfkv_calibrate_scales(const void *rows, int64_t n_rows, int32_t num_heads, int32_t head_dim, float *scale,
+                          void *stream) {
+  if (n_rows < 0 || num_heads < 1 || head_dim < 1 || num_heads > 65535) return PFKV_ERR_SHAPE;
+  if (!scale || (n_rows > 0 && !rows)) return PFKV_ERR_NULL;
+  return launch_calibrate(rows, n_rows, num_heads, head_dim, scale, static_cast<cudaStream_t>(stream));
+}
+
+int pfkv_e4m3_encode(const float *x, uint8_t *codes, int64_t n, void *stream) {
+  if (n < 0) return PFKV_ERR_SHAPE;
+  if (n > 0 && (!x || !codes)) return PFKV_ERR_NULL;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 3u)) return PFKV_ERR_ALIGN;
+  return launch_encode(x, codes, n, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

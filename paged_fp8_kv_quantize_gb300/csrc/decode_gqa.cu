@@ -1,0 +1,728 @@
+// decode_gqa.cu -- split-KV paged decode attention for grouped-query heads
+// (head_dim 64/128, group 1..8) over an FP8 e4m3 or a BF16 paged cache.
+//
+// "Smaller, faster, safer: running Kimi and GLM at scale", section
+// "Quantizing the KV cache": the cache is FP8 e4m3 and the attention kernel
+// converts the values as it reads them.  Cache-protection passage: each
+// page's tag is compared with the mapping's tag before its data may be
+// returned; a mismatch aborts the request.
+//
+// Kernels (all on the caller's stream):
+//   1. plan   -- one CTA: validates lengths, zeroes status, splits every
+//                request into page-aligned chunks (flash-decoding) and
+//                writes the chunk prefix into the workspace.
+//   2. split  -- persistent CTAs, one producer warp + NCW consumer warps.
+//                The producer takes work items (request, chunk, KV head)
+//                from a device counter, walks the chunk's page-table
+//                entries 32 at a time, bounds-checks every page id before
+//                any fetch, compares tags off the critical path (the tag
+//                load is issued next to the page copy; a mismatch only sets
+//                the request's status bit), and stages whole (page, head)
+//                K and V slices into a shared-memory ring with TMA tensor
+//                copies (128-byte swizzle).  Consumer warps take 16-token
+//                tiles: e4m3 -> f16 in registers (exact), QK^T and PV on
+//                register-operand tensor-core MMA, online softmax in fp32.
+//                Each item leaves an unnormalised partial (m, l, O).
+//   3. merge  -- one warp per (request, query head): log-sum-exp merge of
+//                the partials; zero output for any request with a status.
+#include <math.h>
+
+#include "pfkv_device.cuh"
+#include "pfkv_internal.h"
+
+namespace pfkv {
+
+namespace {
+
+constexpr float kNegInf = -INFINITY;
+constexpr int kNIQ = 4;  // item descriptors in flight per CTA
+
+struct ItemDesc {
+  int b, cg, g, p0, p1, L;
+  uint32_t ring;
+  int pad;
+};
+
+// ---------------------------------------------------------------- plan
+
+__global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
+  __shared__ long long s_red[32];
+  __shared__ int s_scan[32];
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int S = a.S;
+  const long long max_len = (long long)a.MP * S;
+  // total pages (for the split size)
+  long long tot = 0;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    const int L = a.seq_lens[b];
+    const bool bad = L < 1 || (long long)L > max_len;
+    a.status[b] = bad ? PFKV_ST_BAD_LEN : 0u;
+    if (!bad) tot += (L + S - 1) / S;
+  }
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (lane == 0) s_red[wid] = tot;
+  __syncthreads();
+  if (wid == 0) {
+    long long v = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0;
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_red[0] = v;
+  }
+  __syncthreads();
+  const long long total_units = s_red[0] * a.Hkv;
+  long long cp = (total_units + target_items - 1) / target_items;
+  if (cp < min_chunk_pages) cp = min_chunk_pages;
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  // chunk counts and exclusive prefix, 1024 requests per pass
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int b = base + tid;
+    int n = 0, ppc = 0;
+    if (b < a.B) {
+      const int L = a.seq_lens[b];
+      if (L >= 1 && (long long)L <= max_len) {
+        const long long pages = (L + S - 1) / S;
+        long long nn = (pages + cp - 1) / cp;
+        if (nn > a.max_splits) nn = a.max_splits;
+        ppc = (int)((pages + nn - 1) / nn);
+        n = (int)((pages + ppc - 1) / ppc);
+      }
+      a.ppc[b] = ppc;
+    }
+    int x = n;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_scan[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int v = lane < (int)(blockDim.x >> 5) ? s_scan[lane] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      s_scan[lane] = v;  // inclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int warp_off = wid ? s_scan[wid - 1] : 0;
+    const int excl = s_carry + warp_off + x - n;
+    if (b < a.B) a.chunk_start[b] = excl;
+    __syncthreads();
+    if (tid == blockDim.x - 1) s_carry = excl + n;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.chunk_start[a.B] = s_carry;
+    a.hdr->n_chunks = s_carry;
+    a.hdr->n_items = s_carry * a.Hkv;
+    a.hdr->work = 0u;
+    a.hdr->err = 0u;
+    a.hdr->chunk_pages = (int)cp;
+  }
+}
+
+// ---------------------------------------------------------------- split
+
+template <bool kFp8, int kD, int kG, int kNCW>
+struct Cfg {
+  static constexpr int kEsz = kFp8 ? 1 : 2;
+  static constexpr int kRowBytes = kD * kEsz;       // 64, 128 or 256
+  static constexpr bool kSwz = kRowBytes >= 128;    // 64-byte rows are read conflict-free unswizzled
+  static constexpr int kKsteps = kD / 16;           // QK^T k-steps; also PV m-tiles
+  static constexpr int kSegK = kD / 4 * kEsz;       // bytes of a K row held by one thread
+  static constexpr int kSegV = kD / 8 * kEsz;       // bytes of a V row held by one thread
+  static constexpr int kNP = (2 * kG + 7) / 8;      // PV n-tiles (hi and lo columns)
+  static constexpr int kThreads = (kNCW + 1) * 32;
+  static constexpr float kPScale = kFp8 ? 16384.0f : 1.0f;  // keeps f16 P away from subnormals
+};
+
+struct SmemPlan {
+  uint32_t stage_bytes, page_bytes, stages_off, bars_off, items_off, merge_off, total;
+};
+
+__host__ __device__ inline SmemPlan smem_plan(int S, int row_bytes, bool per_token, int nst, int ncw, int G, int D) {
+  SmemPlan p;
+  p.page_bytes = 2u * S * row_bytes + (per_token ? 8u * S : 0u);
+  p.stage_bytes = (p.page_bytes + 1023u) & ~1023u;
+  p.stages_off = 0;
+  p.bars_off = p.stages_off + p.stage_bytes * nst;
+  p.items_off = p.bars_off + 8u * (2 * nst + 2 * kNIQ) + 16u;  // + abort flag
+  p.merge_off = (p.items_off + sizeof(ItemDesc) * kNIQ + 15u) & ~15u;
+  p.total = p.merge_off + 4u * ncw * (2 * G + G * D) + 1024u;  // + alignment slack
+  return p;
+}
+
+template <bool kFp8>
+__device__ __forceinline__ void mma_t(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (kFp8) mma_f16(d, a, b0, b1);
+  else mma_bf16(d, a, b0, b1);
+}
+
+template <bool kFp8>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kFp8) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
+template <bool kFp8>
+__device__ __forceinline__ float round16(float x) {
+  if constexpr (kFp8) return __half2float(__float2half_rn(x));
+  else return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+template <bool kFp8, int kD, int kG, int kNCW>
+__global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads)
+    gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const DecodeArgs a, const int nst) {
+  using C = Cfg<kFp8, kD, kG, kNCW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const bool per_token = kFp8 && a.scale_mode == PFKV_SCALE_PER_TOKEN;
+  const SmemPlan sp = smem_plan(a.S, C::kRowBytes, per_token, nst, kNCW, kG, kD);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + sp.bars_off);
+  uint64_t *empty = full + nst;
+  uint64_t *item_full = empty + nst;
+  uint64_t *item_empty = item_full + kNIQ;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(item_empty + kNIQ);
+  ItemDesc *items = reinterpret_cast<ItemDesc *>(smem + sp.items_off);
+  float *sm_m = reinterpret_cast<float *>(smem + sp.merge_off);  // [NCW][G]
+  float *sm_l = sm_m + kNCW * kG;                                 // [NCW][G]
+  float *sm_o = sm_l + kNCW * kG;                                 // [NCW][G][D]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.S, mpp = S / 16;  // 16-token tiles per page
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], mpp);
+    }
+    for (int i = 0; i < kNIQ; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_empty[i], 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == kNCW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    const int n_items = a.hdr->n_items;
+    const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
+    uint32_t ring = 0;
+    for (uint32_t iq = 0;; ++iq) {
+      int item = 0;
+      if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      const uint32_t slot = iq % kNIQ;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&item_empty[slot], ((iq / kNIQ) & 1u) ^ 1u, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (item >= n_items) {
+        if (lane == 0) {
+          items[slot].b = -1;
+          mbar_arrive(&item_full[slot]);
+        }
+        break;
+      }
+      const int cg = item / a.Hkv, g = item - cg * a.Hkv;
+      // request owning chunk cg: last b with chunk_start[b] <= cg
+      int lo = 0, hi = a.B;  // chunk_start[lo] <= cg < chunk_start[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(&a.chunk_start[mid]) <= cg) lo = mid; else hi = mid;
+      }
+      const int b = lo;
+      const int L = a.seq_lens[b];
+      const int ppc = a.ppc[b];
+      const int pages_b = (L + S - 1) / S;
+      const int p0 = (cg - a.chunk_start[b]) * ppc;
+      const int p1 = min(p0 + ppc, pages_b);
+      if (lane == 0) {
+        ItemDesc d;
+        d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.pad = 0;
+        items[slot] = d;
+        mbar_arrive(&item_full[slot]);
+      }
+      const int *trow = a.block_table + (size_t)b * a.MP;
+      const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
+      uint32_t st_bits = 0;
+      for (int i0 = p0; i0 < p1 && ok; i0 += 32) {
+        const int i = i0 + lane;
+        const bool valid = i < p1;
+        const int pid = valid ? __ldg(&trow[i]) : 0;
+        const bool oob = valid && (pid < 0 || pid >= a.P);
+        uint32_t page_tag = 0, want_tag = 0;
+        if (tag_check && valid && !oob) {  // loads issued now, compared after the copies
+          page_tag = __ldg(&a.page_tags[pid]);
+          want_tag = __ldg(&tagrow[i]);
+        }
+        const int n = min(32, p1 - i0);
+        for (int j = 0; j < n; ++j) {
+          const int pj = __shfl_sync(0xffffffffu, pid, j);
+          const bool oj = __shfl_sync(0xffffffffu, oob, j);
+          if (lane == 0) {
+            const uint32_t st = ring % (uint32_t)nst;
+            ok = mbar_wait(&empty[st], ((ring / (uint32_t)nst) & 1u) ^ 1u, abort_flag);
+            if (ok) {
+              uint8_t *stage = smem + sp.stages_off + (size_t)st * sp.stage_bytes;
+              if (oj) {
+                mbar_arrive(&full[st]);  // never fetched; the request is aborted
+              } else {
+                mbar_arrive_expect_tx(&full[st], sp.page_bytes);
+                if constexpr (C::kRowBytes == 256) {
+                  tma_load_5d(stage, &tmK, &full[st], 0, 0, 0, g, pj);
+                  tma_load_5d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, 0, g, pj);
+                } else {
+                  tma_load_4d(stage, &tmK, &full[st], 0, 0, g, pj);
+                  tma_load_4d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, g, pj);
+                }
+                if (per_token) {
+                  const size_t r = ((size_t)pj * a.Hkv + g) * S;
+                  bulk_load(stage + 2 * S * C::kRowBytes, a.k_scale + r, 4u * S, &full[st]);
+                  bulk_load(stage + 2 * S * C::kRowBytes + 4 * S, a.v_scale + r, 4u * S, &full[st]);
+                }
+              }
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          ++ring;
+          if (!ok) break;
+        }
+        if (__any_sync(0xffffffffu, oob)) st_bits |= PFKV_ST_PAGE_OOB;
+        if (__any_sync(0xffffffffu, page_tag != want_tag)) st_bits |= PFKV_ST_STALE_TAG;
+      }
+      if (lane == 0 && st_bits) atomicOr(&a.status[b], st_bits);
+      if (!ok) break;
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int gid = lane >> 2, tq = lane & 3;
+    constexpr int kSrcMask = (kG == 4) ? 1 : 0;  // PV column -> QK column owner
+    const int src_lane = (lane & ~3) | (tq & kSrcMask);
+    for (uint32_t iq = 0;; ++iq) {
+      const uint32_t slot = iq % kNIQ;
+      if (!mbar_wait(&item_full[slot], (iq / kNIQ) & 1u, abort_flag)) break;
+      const ItemDesc d = items[slot];
+      if (d.b < 0) break;
+
+      // query fragments of the group's heads (row gid of the B operand)
+      uint32_t qf[C::kKsteps][2];
+      float mult[2];
+      {
+        const int h = d.g * kG + gid;
+        float qv[kD / 4];
+        if (gid < kG) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) +
+                                                              ((size_t)d.b * a.Hq + h) * kD + tq * (kD / 4));
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c) {
+            const uint4 v = __ldg(&src[c]);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              qv[c * 8 + 2 * k] = __uint_as_float(w[k] << 16);
+              qv[c * 8 + 2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kD / 4; ++k) qv[k] = 0.f;
+        }
+        int e = 0;
+        if constexpr (kFp8) {
+          // exact bf16 -> f16: scale the head by 2^e so that max|q| lands in [2^14, 2^15)
+          float mx = 0.f;
+#pragma unroll
+          for (int k = 0; k < kD / 4; ++k) mx = fmaxf(mx, fabsf(qv[k]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          if (mx > 0.f) {
+            int k2;
+            frexpf(mx, &k2);
+            e = 15 - k2;
+          }
+        }
+#pragma unroll
+        for (int s = 0; s < C::kKsteps; ++s) {
+          if constexpr (kFp8) {
+            qf[s][0] = pack_f16x2(ldexpf(qv[4 * s], e), ldexpf(qv[4 * s + 1], e));
+            qf[s][1] = pack_f16x2(ldexpf(qv[4 * s + 2], e), ldexpf(qv[4 * s + 3], e));
+          } else {
+            qf[s][0] = pack_bf16x2(qv[4 * s], qv[4 * s + 1]);
+            qf[s][1] = pack_bf16x2(qv[4 * s + 2], qv[4 * s + 3]);
+          }
+        }
+        float base = a.sm_scale_log2;
+        if (kFp8 && !per_token) base *= __ldg(&a.k_scale[d.g]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int ec = __shfl_sync(0xffffffffu, e, ((2 * tq + c) & 7) * 4);
+          mult[c] = ldexpf(base, -ec);
+        }
+      }
+
+      float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+      float o[C::kKsteps][C::kNP][4];
+#pragma unroll
+      for (int i = 0; i < C::kKsteps; ++i)
+#pragma unroll
+        for (int j = 0; j < C::kNP; ++j)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[i][j][k] = 0.f;
+
+      const int n_mt = (d.p1 - d.p0) * mpp;
+      bool alive = true;
+      for (int j = warp; j < n_mt; j += kNCW) {
+        const int page_local = j / mpp, mt_in_page = j - page_local * mpp;
+        const uint32_t rp = d.ring + (uint32_t)page_local;
+        const uint32_t st = rp % (uint32_t)nst;
+        if (!mbar_wait(&full[st], (rp / (uint32_t)nst) & 1u, abort_flag)) {
+          alive = false;
+          break;
+        }
+        const int tok_base = (d.p0 + page_local) * S + mt_in_page * 16;
+        if (tok_base < d.L) {
+          const uint32_t sK = smem_addr(smem + sp.stages_off + (size_t)st * sp.stage_bytes);
+          const uint32_t sV = sK + S * C::kRowBytes;
+          const uint32_t sKS = sK + 2 * S * C::kRowBytes, sVS = sKS + 4 * S;
+          const int rbase = mt_in_page * 16;
+          // ---- S = K q^T : A = K tile rows (gid, gid+8), this thread's D/4 slice
+          float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            uint32_t wk[2][C::kSegK / 4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const uint32_t rowoff = (uint32_t)(rbase + gid + 8 * r) * C::kRowBytes + tq * C::kSegK;
+#pragma unroll
+              for (int c = 0; c < C::kSegK / 16; ++c) {
+                const uint32_t off = rowoff + 16 * c;
+                const uint4 v = lds128(sK + (C::kSwz ? swz128(off) : off));
+                wk[r][4 * c] = v.x; wk[r][4 * c + 1] = v.y; wk[r][4 * c + 2] = v.z; wk[r][4 * c + 3] = v.w;
+              }
+            }
+#pragma unroll
+            for (int s = 0; s < C::kKsteps; ++s) {
+              uint32_t af[4];
+              if constexpr (kFp8) {
+                af[0] = e4m3x2_to_f16x2(wk[0][s]);
+                af[1] = e4m3x2_to_f16x2(wk[1][s]);
+                af[2] = e4m3x2_to_f16x2(wk[0][s] >> 16);
+                af[3] = e4m3x2_to_f16x2(wk[1][s] >> 16);
+              } else {
+                af[0] = wk[0][2 * s];
+                af[1] = wk[1][2 * s];
+                af[2] = wk[0][2 * s + 1];
+                af[3] = wk[1][2 * s + 1];
+              }
+              mma_t<kFp8>(sacc, af, qf[s][0], qf[s][1]);
+            }
+          }
+          // ---- online softmax over the tile's 16 tokens (log2 domain)
+          float z[4] = {sacc[0] * mult[0], sacc[1] * mult[1], sacc[2] * mult[0], sacc[3] * mult[1]};
+          if (per_token) {
+            const float k0 = lds_f32(sKS + 4 * (rbase + gid)), k1 = lds_f32(sKS + 4 * (rbase + gid + 8));
+            z[0] *= k0; z[1] *= k0; z[2] *= k1; z[3] *= k1;
+          }
+          if (tok_base + gid >= d.L) z[0] = z[1] = kNegInf;
+          if (tok_base + gid + 8 >= d.L) z[2] = z[3] = kNegInf;
+          float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+          const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
+          m[0] = mn0;
+          m[1] = mn1;
+          float p[4] = {fast_exp2(z[0] - mn0), fast_exp2(z[1] - mn1), fast_exp2(z[2] - mn0), fast_exp2(z[3] - mn1)};
+          l[0] = l[0] * al0 + p[0] + p[2];
+          l[1] = l[1] * al1 + p[1] + p[3];
+          // PV columns: v = 8*nt + 2*tq + e -> head v % G, hi part for v < G, lo part for G <= v < 2G
+          float apv0 = al0, apv1 = al1, pv[4] = {p[0], p[1], p[2], p[3]};
+          if constexpr (kG == 1) {
+            apv0 = apv1 = __shfl_sync(0xffffffffu, al0, lane & ~3);
+            pv[0] = pv[1] = __shfl_sync(0xffffffffu, p[0], lane & ~3);
+            pv[2] = pv[3] = __shfl_sync(0xffffffffu, p[2], lane & ~3);
+          } else if constexpr (kG < 8) {
+            apv0 = __shfl_sync(0xffffffffu, al0, src_lane);
+            apv1 = __shfl_sync(0xffffffffu, al1, src_lane);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) pv[k] = __shfl_sync(0xffffffffu, p[k], src_lane);
+          }
+#pragma unroll
+          for (int i = 0; i < C::kKsteps; ++i)
+#pragma unroll
+            for (int nt = 0; nt < C::kNP; ++nt) {
+              o[i][nt][0] *= apv0; o[i][nt][1] *= apv1; o[i][nt][2] *= apv0; o[i][nt][3] *= apv1;
+            }
+          float vs0 = 1.f, vs1 = 1.f;
+          if (per_token) {
+            vs0 = lds_f32(sVS + 4 * (rbase + gid));
+            vs1 = lds_f32(sVS + 4 * (rbase + gid + 8));
+          }
+          uint32_t pb[C::kNP][2];
+#pragma unroll
+          for (int nt = 0; nt < C::kNP; ++nt) {
+            float val[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int e = k & 1;
+              const int v = 8 * nt + 2 * tq + e;
+              const float pp = pv[k] * C::kPScale * ((k < 2) ? vs0 : vs1);
+              const float hi = round16<kFp8>(pp);
+              const bool lo_part = (kG == 1) ? (e == 1) : (v >= kG);
+              val[k] = (v < 2 * kG) ? (lo_part ? pp - hi : hi) : 0.f;
+            }
+            pb[nt][0] = movmatrix_trans(pack2<kFp8>(val[0], val[1]));
+            pb[nt][1] = movmatrix_trans(pack2<kFp8>(val[2], val[3]));
+          }
+          // ---- O^T += V^T P^T : A = V tile rows (2tq, 2tq+1, 2tq+8, 2tq+9), this thread's D/8 slice
+          {
+            uint32_t wv[4][C::kSegV / 4];
+            const int trow[4] = {2 * tq, 2 * tq + 1, 2 * tq + 8, 2 * tq + 9};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const uint32_t rowoff = (uint32_t)(rbase + trow[r]) * C::kRowBytes + gid * C::kSegV;
+              if constexpr (C::kSegV == 8) {
+                const uint2 v = lds64(sV + rowoff);
+                wv[r][0] = v.x; wv[r][1] = v.y;
+              } else {
+#pragma unroll
+                for (int c = 0; c < C::kSegV / 16; ++c) {
+                  const uint32_t off = rowoff + 16 * c;
+                  const uint4 v = lds128(sV + (C::kSwz ? swz128(off) : off));
+                  wv[r][4 * c] = v.x; wv[r][4 * c + 1] = v.y; wv[r][4 * c + 2] = v.z; wv[r][4 * c + 3] = v.w;
+                }
+              }
+            }
+#pragma unroll
+            for (int mt = 0; mt < C::kKsteps; ++mt) {
+              uint32_t af[4];
+              if constexpr (kFp8) {
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t t01 = prmt(wv[0][mt >> 1], wv[1][mt >> 1], sel);
+                const uint32_t t89 = prmt(wv[2][mt >> 1], wv[3][mt >> 1], sel);
+                af[0] = e4m3x2_to_f16x2(t01);
+                af[1] = e4m3x2_to_f16x2(t01 >> 16);
+                af[2] = e4m3x2_to_f16x2(t89);
+                af[3] = e4m3x2_to_f16x2(t89 >> 16);
+              } else {
+                af[0] = prmt(wv[0][mt], wv[1][mt], 0x5410u);
+                af[1] = prmt(wv[0][mt], wv[1][mt], 0x7632u);
+                af[2] = prmt(wv[2][mt], wv[3][mt], 0x5410u);
+                af[3] = prmt(wv[2][mt], wv[3][mt], 0x7632u);
+              }
+#pragma unroll
+              for (int nt = 0; nt < C::kNP; ++nt) mma_t<kFp8>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      // ---- per-warp state -> shared memory
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+      }
+      if (gid == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (2 * tq + e < kG) {
+            sm_m[warp * kG + 2 * tq + e] = m[e];
+            sm_l[warp * kG + 2 * tq + e] = l[e];
+          }
+      }
+#pragma unroll
+      for (int mt = 0; mt < C::kKsteps; ++mt) {
+        float hv[4];
+        if constexpr (kG == 8) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) hv[k] = o[mt][0][k] + o[mt][1][k];
+        } else if constexpr (kG == 1) {
+          hv[0] = o[mt][0][0] + o[mt][0][1];
+          hv[2] = o[mt][0][2] + o[mt][0][3];
+          hv[1] = hv[3] = 0.f;
+        } else {
+          constexpr int kX = kG / 2;  // lane distance from a lo column to its hi column
+#pragma unroll
+          for (int k = 0; k < 4; ++k) hv[k] = o[mt][0][k] + __shfl_xor_sync(0xffffffffu, o[mt][0][k], kX);
+        }
+        const int d0 = gid * (kD / 8) + 2 * mt;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hh = 2 * tq + e;
+          if (hh < kG && !(kG == 1 && e == 1)) {
+            sm_o[(warp * kG + hh) * kD + d0] = hv[e];
+            sm_o[(warp * kG + hh) * kD + d0 + 1] = hv[2 + e];
+          }
+        }
+      }
+      named_bar_sync(1, kNCW * 32);
+      // ---- merge the consumer warps' states, write the item's partial
+      {
+        const int t = threadIdx.x;
+        float ofac = 1.f;
+        if constexpr (kFp8) ofac = (per_token ? 1.f : __ldg(&a.v_scale[d.g])) / C::kPScale;
+        for (int idx = t; idx < kG * kD; idx += kNCW * 32) {
+          const int jh = idx / kD, dd = idx - jh * kD;
+          float M = kNegInf;
+#pragma unroll
+          for (int w = 0; w < kNCW; ++w) M = fmaxf(M, sm_m[w * kG + jh]);
+          float acc = 0.f;
+#pragma unroll
+          for (int w = 0; w < kNCW; ++w) {
+            const float mw = sm_m[w * kG + jh];
+            if (mw != kNegInf) acc += sm_o[(w * kG + jh) * kD + dd] * fast_exp2(mw - M);
+          }
+          a.part_o[((size_t)d.cg * a.Hq + d.g * kG + jh) * kD + dd] = acc * ofac;
+        }
+        if (t < kG) {
+          float M = kNegInf;
+#pragma unroll
+          for (int w = 0; w < kNCW; ++w) M = fmaxf(M, sm_m[w * kG + t]);
+          float ls = 0.f;
+#pragma unroll
+          for (int w = 0; w < kNCW; ++w) {
+            const float mw = sm_m[w * kG + t];
+            if (mw != kNegInf) ls += sm_l[w * kG + t] * fast_exp2(mw - M);
+          }
+          a.part_ml[(size_t)d.cg * a.Hq + d.g * kG + t] = make_float2(M, ls);
+        }
+      }
+      named_bar_sync(1, kNCW * 32);
+      if (threadIdx.x == 0) mbar_arrive(&item_empty[slot]);
+      if (!alive) break;
+    }
+  }
+  // a wait gave up somewhere in this block: the merge reports PFKV_ST_TIMEOUT
+  if (lane == 0 && *abort_flag) atomicOr(&a.hdr->err, 1u);
+}
+
+// ---------------------------------------------------------------- merge
+
+template <int kD>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
+  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (wg >= a.B * a.Hq) return;
+  const int b = wg / a.Hq, h = wg - b * a.Hq;
+  float *dst = a.out + (size_t)wg * kD;
+  const bool err = a.hdr->err != 0u;
+  uint32_t st = a.status[b];
+  const int c0 = a.chunk_start[b], n = a.chunk_start[b + 1] - c0;
+  if (err && h == 0 && lane == 0) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
+  if (st != 0u || err || n <= 0) {
+    for (int dd = lane * 4; dd < kD; dd += 128) *reinterpret_cast<float4 *>(dst + dd) = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  float M = kNegInf;
+  for (int c = lane; c < n; c += 32) M = fmaxf(M, a.part_ml[(size_t)(c0 + c) * a.Hq + h].x);
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float W = 0.f;
+  for (int c = lane; c < n; c += 32) {
+    const float2 ml = a.part_ml[(size_t)(c0 + c) * a.Hq + h];
+    W += ml.y * fast_exp2(ml.x - M);
+  }
+  for (int off = 16; off; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  const float inv = 1.f / W;
+  for (int dd = lane * 4; dd < kD; dd += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < n; ++c) {
+      const float2 ml = a.part_ml[(size_t)(c0 + c) * a.Hq + h];
+      const float w = fast_exp2(ml.x - M);
+      const float4 v = *reinterpret_cast<const float4 *>(a.part_o + ((size_t)(c0 + c) * a.Hq + h) * kD + dd);
+      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    }
+    *reinterpret_cast<float4 *>(dst + dd) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+int make_pool_map(CUtensorMap *map, const void *pool, int dtype, int D, int S, int Hkv, int P) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return PFKV_ERR_CUDA;
+  const int esz = dtype == PFKV_DTYPE_FP8_E4M3 ? 1 : 2;
+  const CUtensorMapDataType dt = esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t row = (uint64_t)D * esz;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r;
+  if (row == 256) {  // two 128-byte halves per row
+    cuuint64_t dims[5] = {64, 2, (cuuint64_t)S, (cuuint64_t)Hkv, (cuuint64_t)P};
+    cuuint64_t strides[4] = {128, 256, 256ull * S, 256ull * S * Hkv};
+    cuuint32_t box[5] = {64, 2, (cuuint32_t)S, 1, 1};
+    r = enc(map, dt, 5, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)Hkv, (cuuint64_t)P};
+    cuuint64_t strides[3] = {row, row * S, row * S * Hkv};
+    cuuint32_t box[4] = {(cuuint32_t)D, (cuuint32_t)S, 1, 1};
+    r = enc(map, dt, 4, const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            row >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? PFKV_OK : PFKV_ERR_CUDA;
+}
+
+constexpr int kNCW = 4;
+
+template <bool kFp8, int kD, int kG>
+int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const CUtensorMap &mv) {
+  using C = Cfg<kFp8, kD, kG, kNCW>;
+  const bool per_token = kFp8 && a.scale_mode == PFKV_SCALE_PER_TOKEN;
+  // stage ring of roughly 64 KB (at least 4 pages) so that two or three CTAs share an SM
+  const SmemPlan one = smem_plan(a.S, C::kRowBytes, per_token, 1, kNCW, kG, kD);
+  int nst = (int)(65536u / one.stage_bytes);
+  if (nst < 4) nst = 4;
+  if (nst > 32) nst = 32;
+  SmemPlan sp = smem_plan(a.S, C::kRowBytes, per_token, nst, kNCW, kG, kD);
+  while (sp.total > 200u * 1024u && nst > 2) sp = smem_plan(a.S, C::kRowBytes, per_token, --nst, kNCW, kG, kD);
+  auto kern = gqa_split_kernel<kFp8, kD, kG, kNCW>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp.total) != cudaSuccess)
+    return PFKV_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, sp.total) != cudaSuccess || per_sm < 1)
+    return PFKV_ERR_CUDA;
+  const int grid = num_sms() * per_sm;
+  plan_kernel<<<1, 1024, 0, s>>>(a, grid * 8, (1024 + a.S - 1) / a.S);
+  kern<<<grid, C::kThreads, sp.total, s>>>(mk, mv, a, nst);
+  merge_kernel<kD><<<(a.B * a.Hq + 3) / 4, 128, 0, s>>>(a);
+  return cuda_ok(cudaGetLastError());
+}
+
+template <bool kFp8, int kD>
+int dispatch_g(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const CUtensorMap &mv) {
+  switch (a.G) {
+    case 1: return run_split<kFp8, kD, 1>(a, s, mk, mv);
+    case 2: return run_split<kFp8, kD, 2>(a, s, mk, mv);
+    case 4: return run_split<kFp8, kD, 4>(a, s, mk, mv);
+    case 8: return run_split<kFp8, kD, 8>(a, s, mk, mv);
+    default: return PFKV_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+int launch_gqa_decode(const DecodeArgs &a, cudaStream_t s) {
+  CUtensorMap mk, mv;
+  int rc = make_pool_map(&mk, a.k_pool, a.dtype, a.D, a.S, a.Hkv, a.P);
+  if (rc) return rc;
+  rc = make_pool_map(&mv, a.v_pool, a.dtype, a.D, a.S, a.Hkv, a.P);
+  if (rc) return rc;
+  const bool fp8 = a.dtype == PFKV_DTYPE_FP8_E4M3;
+  if (a.D == 128) return fp8 ? dispatch_g<true, 128>(a, s, mk, mv) : dispatch_g<false, 128>(a, s, mk, mv);
+  if (a.D == 64) return fp8 ? dispatch_g<true, 64>(a, s, mk, mv) : dispatch_g<false, 64>(a, s, mk, mv);
+  return PFKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pfkv

@@ -1,0 +1,72 @@
+// pfkv_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pfkv.h"
+
+namespace pfkv {
+
+// Workspace header (first 256 bytes of the decode workspace).
+struct WsHeader {
+  int n_chunks;     // sum over requests of split count
+  int n_items;      // n_chunks * num_kv_heads
+  unsigned work;    // dynamic work counter
+  unsigned err;     // nonzero: a kernel wait timed out
+  int chunk_pages;  // pages per split target
+  int pad[59];
+};
+
+// Decode workspace carve-up.
+struct WsLayout {
+  size_t hdr, chunk_start, ppc, part_ml, part_o, total;
+};
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits);
+
+struct DecodeArgs {
+  // cache
+  int P, S, Hkv, D, Dv, scale_mode, dtype, kv_shared;
+  const void *k_pool, *v_pool;
+  const float *k_scale, *v_scale;
+  const uint32_t *page_tags;
+  // request batch
+  const void *q;
+  int Hq, G;
+  const int *seq_lens, *block_table;
+  const uint32_t *block_tags;
+  int B, MP;
+  float sm_scale_log2;  // softmax_scale * log2(e)
+  uint32_t flags;
+  int max_splits;
+  // workspace and outputs
+  WsHeader *hdr;
+  int *chunk_start, *ppc;
+  float2 *part_ml;
+  float *part_o;
+  float *out;
+  uint32_t *status;
+};
+
+// Tensor-map encoder obtained from the driver without linking libcuda.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+int num_sms();
+
+// launchers (return PFKV_* codes)
+int launch_gqa_decode(const DecodeArgs &a, cudaStream_t s);
+int launch_latent_decode(const DecodeArgs &a, cudaStream_t s);
+int launch_append(const pfkv_cache &c, const void *k_new, const void *v_new, int n_rows, const int *row_req,
+                  const int *positions, const int *block_table, const uint32_t *block_tags, int batch,
+                  int max_pages, uint32_t flags, uint32_t *status, cudaStream_t s);
+int launch_calibrate(const void *rows, int64_t n_rows, int heads, int dim, float *scale, cudaStream_t s);
+int launch_encode(const float *x, uint8_t *codes, int64_t n, cudaStream_t s);
+
+inline int cuda_ok(cudaError_t e) { return e == cudaSuccess ? PFKV_OK : PFKV_ERR_CUDA; }
+
+}  // namespace pfkv

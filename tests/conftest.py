@@ -10,9 +10,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: long-running CPU test")
+    # Both native pieces are built from source on whichever machine runs the
+    # tests (nvcc cross-compiles here; the GPU machine builds its own).
+    import oracle
+    from paged_fp8_kv_quantize_gb300 import build as libbuild
+
+    oracle.build()
+    libbuild.build()
 
 
 def pytest_collection_modifyitems(config, items):
-    # run the GPU test files in file-name order so that test_zz_* comes last
-    items.sort(key=lambda it: (os.path.basename(str(it.fspath)).startswith("test_zz"),))
+    # keep file order, but make sure test_zz_* files run last
+    items.sort(key=lambda it: os.path.basename(str(it.fspath)).startswith("test_zz"))

@@ -1,0 +1,55 @@
+"""CPU-only checks of the C ABI: the shared library loads, exports every
+function include/pfkv.h declares, and its host-only paths (workspace sizing,
+error strings, argument checks that return before any CUDA call) behave."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_fp8_kv_quantize_gb300 import abi
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pfkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pfkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(abi.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(abi.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_only_entry_points():
+    assert abi.lib.pfkv_abi_version() == 1
+    assert abi.strerror(0) == "ok"
+    assert "workspace" in abi.strerror(-5)
+    d = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, 16)
+    n = abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 64)
+    # header + plan + (m, l) and O partials for every (request, split, head)
+    assert n >= 64 * 64 * 32 * (8 + 4 * 128)
+    assert n < 64 * 64 * 32 * (8 + 4 * 128) + 64 * 1024
+
+
+def test_argument_errors_return_before_any_cuda_call():
+    f = abi.lib.pfkv_paged_decode_attention_fp8
+    args_tail = [None, 32, None, None, None, 4, 8, 1.0, 0, 64, None, 0, None, None, None]
+    assert f(None, *args_tail) == -1  # NULL cache
+    bf16 = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_BF16, 0, 16, 16, None, None, None)
+    assert f(ctypes.byref(bf16), *args_tail) == -4  # FP8 entry point, BF16 cache
+    fp8 = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, None, None, None)
+    assert f(ctypes.byref(fp8), *args_tail) == -1  # FP8 cache without scales
+    bad = abi.CacheDesc(100, 16, 8, 128, 128, 0, 7, 0, 16, 16, 16, 16, None)
+    assert f(ctypes.byref(bad), *args_tail) == -4  # unknown dtype
+    unal = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 17, 16, 16, 16, None)
+    assert f(ctypes.byref(unal), *args_tail) == -6  # misaligned pool
+    g = abi.lib.pfkv_kv_append_quantize
+    assert g(None, None, None, 0, None, None, None, None, 1, 1, 0, None, None) == -1
