@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark: FP8 paged decode attention with the tag check, batch 64.
+
+Workload (one "step" = the whole hot path once): the mixed ragged batch --
+64 requests with context lengths log-uniform in [1, 65536], 32 query / 8 KV
+heads, head_dim 128, 16-token pages, FP8 e4m3 cache with per-head scales,
+0.1% of the used page-table entries stale after a simulated reallocation.
+Each step appends one new token per request (quantize-on-append) and then
+runs tag-checked paged decode attention over every request's context.
+
+Prints ONE JSON line (rank 0).  value = algorithmic KV GB/s of the step with
+inputs resident in HBM; e2e = the same with per-step inputs copied from
+pinned host memory and results copied back inside the timed region.
+Inputs are larger than L2 (the cache alone is ~0.8 GB), so no flush.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_fp8_kv_quantize_gb300 import synth  # noqa: E402
+
+METRIC = "FP8 paged decode-attention KV GB/s and tokens/s at batch 64 (% of HBM peak)"
+WORKLOAD = ("mixed ragged decode: batch 64, lengths log-uniform [1, 65536], 32 q / 8 KV heads, head_dim 128, "
+            "page 16, FP8 e4m3 per-head scales, tag check on, 0.1% stale entries; step = append 1 token/request "
+            "+ paged decode attention")
+
+
+# ---------------------------------------------------------------- accounting
+
+
+def decode_alg_bytes(lens, Hkv, D, S, Hq, Dv, fp8=True, tag_check=True):
+    """Algorithmic bytes of one decode call: KV rows + table/tag words + q + out."""
+    lens = np.asarray(lens, dtype=np.int64)
+    per_tok = 2 * Hkv * D * (1 if fp8 else 2)
+    pages = (lens + S - 1) // S
+    b = int(lens.sum()) * per_tok + int(pages.sum()) * (8 + (4 if tag_check else 0))
+    b += len(lens) * Hq * D * 2 + len(lens) * Hq * Dv * 4
+    return b
+
+
+def append_alg_bytes(B, Hkv, D, fp8=True):
+    # bf16 rows in, cache rows out (K and V), positions + table entries
+    return B * (2 * Hkv * D * 2 + 2 * Hkv * D * (1 if fp8 else 2) + 12)
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            for n, v in zip(names, s[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- peaks
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+
+def oracle_step_sample(w, frac):
+    """Build the oracle's cache for a bounded sample of requests; return a callable step."""
+    import oracle
+
+    total = w.total_tokens
+    idx, acc = [], 0
+    for b in range(w.batch):
+        idx.append(b)
+        acc += int(w.seq_lens[b])
+        if acc >= frac * total:
+            break
+    idx = np.array(idx)
+    # compact page ids for the sample (bookkeeping only)
+    tab = w.block_table[idx]
+    used = np.unique(tab[tab >= 0])
+    remap = np.full(w.num_pages, -1, dtype=np.int64)
+    remap[used] = np.arange(used.size)
+    ctab = np.where(tab >= 0, remap[np.maximum(tab, 0)], -1).astype(np.int32)
+    ks = oracle.calibrate_per_head(w.k_rows)
+    vs = oracle.calibrate_per_head(w.v_rows)
+    c = oracle.Cache(used.size, w.page_size, w.kv_heads, w.head_dim, page_tags=w.page_tags[used], k_scale=ks,
+                     v_scale=vs)
+    sel = np.isin(w.row_req, idx)
+    rr = np.searchsorted(idx, w.row_req[sel]).astype(np.int32)
+    c.append(w.k_rows[sel], w.v_rows[sel], w.row_pos[sel], ctab, w.block_tags[idx], row_req=rr, batch=idx.size)
+    threads = len(os.sched_getaffinity(0))
+    lens0 = w.seq_lens[idx].astype(np.int32)
+    state = {"j": 0}
+
+    def step():
+        j = state["j"] % max(1, w.steps)
+        state["j"] += 1
+        pos = lens0 + j
+        c.append(w.k_steps[j][idx], w.v_steps[j][idx], pos, ctab, w.block_tags[idx], flags=1)
+        c.decode(w.q_steps[j][idx], pos + 1, ctab, w.block_tags[idx], w.softmax_scale, flags=1, threads=threads)
+        return decode_alg_bytes(pos + 1, w.kv_heads, w.head_dim, w.page_size, w.q_heads, w.v_head_dim) + \
+            append_alg_bytes(idx.size, w.kv_heads, w.head_dim)
+
+    desc = f"{idx.size} of {w.batch} requests ({int(lens0.sum())} of {total} context tokens), full step each"
+    return step, threads, desc, idx.size
+
+
+def run_reference(args, w):
+    """The oracle as it stands, timed on the host cores (the reference arm)."""
+    step, threads, desc, nb = oracle_step_sample(w, args.cpu_frac)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    tot = 0
+    for _ in range(args.steps):
+        tot += step()
+    dt = time.perf_counter() - t0
+    gbs = tot / dt / 1e9
+    return {"metric": METRIC, "value": gbs, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "seed": w.seed, "sample": desc},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- GPU leg
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-frac", type=float, default=0.5, help="share of context tokens in the CPU sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-variants", action="store_true", help="skip the BF16 / tag-off comparisons")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    w = synth.ragged()  # seeded; every rank draws the same replica
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+
+    import torch
+
+    from paged_fp8_kv_quantize_gb300 import abi
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def i32(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int32) if a.dtype == np.uint32 else a.astype(np.int32)).to(dev)
+
+    B, Hq, Hkv, D, S, T = w.batch, w.q_heads, w.kv_heads, w.head_dim, w.page_size, w.steps
+    table, tags = i32(w.block_table), i32(w.block_tags)
+    lens0 = w.seq_lens.astype(np.int64)
+    pos_steps = i32(np.stack([lens0 + j for j in range(T)]))            # [T][B]
+    len_steps = i32(np.stack([lens0 + j + 1 for j in range(T)]))        # [T][B]
+    q_steps, k_steps, v_steps = bf16(w.q_steps), bf16(w.k_steps), bf16(w.v_steps)
+
+    def make_cache(dtype):
+        c = abi.PagedCache(w.num_pages, S, Hkv, D, dtype=dtype, device=dev, fill=0)
+        c.page_tags.copy_(i32(w.page_tags))
+        return c
+
+    caches = {"fp8": make_cache(abi.DTYPE_FP8_E4M3)}
+    if not args.no_variants:
+        caches["bf16"] = make_cache(abi.DTYPE_BF16)
+    k_rows, v_rows = bf16(w.k_rows), bf16(w.v_rows)
+    abi.calibrate_scales(k_rows, caches["fp8"].k_scale)
+    abi.calibrate_scales(v_rows, caches["fp8"].v_scale)
+    rr, rp = i32(w.row_req), i32(w.row_pos)
+    for c in caches.values():
+        abi.kv_append_quantize(c, k_rows, v_rows, rp, table, tags, row_req=rr, batch=B)  # prefill hand-off
+    del k_rows, v_rows
+    torch.cuda.synchronize()
+
+    max_splits = w.max_splits
+    ws = torch.empty(abi.decode_workspace_bytes(caches["fp8"], B, Hq, max_splits), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
+    st_dec = torch.empty(B, dtype=torch.int32, device=dev)
+    st_app = torch.empty(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    FLAGS = abi.FLAG_TAG_CHECK
+
+    def step(cache, j, flags=FLAGS, do_append=True):
+        j %= T
+        if do_append:
+            abi.kv_append_quantize(cache, k_steps[j], v_steps[j], pos_steps[j], table, tags, flags=flags,
+                                   status=st_app)
+        abi.paged_decode_attention(cache, q_steps[j], len_steps[j], table, tags, w.softmax_scale, flags=flags,
+                                   max_splits=max_splits, workspace=ws, out=out, status=st_dec)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for j in range(n):
+                fn(j)
+        return g
+
+    def time_graph(g, reps=1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    K = args.steps
+    fp8 = caches["fp8"]
+    # warm-up: W untimed steps
+    for j in range(args.warmup):
+        step(fp8, j)
+    torch.cuda.synchronize()
+
+    # ---- headline: K full steps (append + decode), inputs resident in HBM
+    g_step = capture(lambda j: step(fp8, j), K)
+    g_step.replay()  # untimed replay (graph upload)
+    with ClockSampler(local) as clk:
+        ms_step = time_graph(g_step)
+    ms_per_step = ms_step / K
+    step_bytes = [decode_alg_bytes(lens0 + j % T + 1, Hkv, D, S, Hq, D) + append_alg_bytes(B, Hkv, D) for j in range(K)]
+    value = world * sum(step_bytes) / (ms_step * 1e-3) / 1e9
+    dec_bytes = [decode_alg_bytes(lens0 + j % T + 1, Hkv, D, S, Hq, D) for j in range(K)]
+
+    # ---- dominant kernel group: decode alone (plan + split + merge), same stream
+    g_dec = capture(lambda j: step(fp8, j, do_append=False), K)
+    g_dec.replay()
+    ms_dec = time_graph(g_dec) / K
+    dec_gbs = statistics.mean(dec_bytes) / (ms_dec * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    extra = {}
+    if not args.no_variants:
+        # tag-check overhead: interleaved replays, median ratio
+        g_off = capture(lambda j: step(fp8, j, flags=0, do_append=False), K)
+        g_off.replay()
+        ratios, on_ms, off_ms = [], [], []
+        for _ in range(11):
+            a = time_graph(g_dec)
+            b = time_graph(g_off)
+            on_ms.append(a)
+            off_ms.append(b)
+            ratios.append(a / b)
+        extra["tag_check_overhead"] = {"median_ratio_on_over_off": statistics.median(ratios),
+                                       "on_us_per_call": statistics.median(on_ms) / K * 1e3,
+                                       "off_us_per_call": statistics.median(off_ms) / K * 1e3, "alternations": 11}
+        bf = caches["bf16"]
+        g_bf = capture(lambda j: step(bf, j, do_append=False), K)
+        g_bf.replay()
+        ms_bf = time_graph(g_bf) / K
+        bf_bytes = statistics.mean(decode_alg_bytes(lens0 + j % T + 1, Hkv, D, S, Hq, D, fp8=False) for j in range(K))
+        extra["bf16_cache"] = {"us_per_decode": ms_bf * 1e3, "kv_gbs": bf_bytes / (ms_bf * 1e-3) / 1e9,
+                               "hbm_frac": bf_bytes / (ms_bf * 1e-3) / 1e9 / peak,
+                               "fp8_speedup_per_call": ms_bf / ms_dec}
+
+    # ---- end to end: per-step inputs from pinned host memory, results back to host
+    h_q = torch.from_numpy(np.ascontiguousarray(w.q_steps).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_k = torch.from_numpy(np.ascontiguousarray(w.k_steps).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_v = torch.from_numpy(np.ascontiguousarray(w.v_steps).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_pos = torch.from_numpy(np.stack([lens0 + j for j in range(T)]).astype(np.int32)).pin_memory()
+    h_len = torch.from_numpy(np.stack([lens0 + j + 1 for j in range(T)]).astype(np.int32)).pin_memory()
+    h_out = torch.empty(B, Hq, D, dtype=torch.float32).pin_memory()
+    h_st = torch.empty(B, dtype=torch.int32).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(q_steps[0]), torch.empty_like(k_steps[0]), torch.empty_like(v_steps[0])
+    d_pos, d_len = torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev)
+
+    def e2e_step(j):
+        j %= T
+        d_q.copy_(h_q[j], non_blocking=True)
+        d_k.copy_(h_k[j], non_blocking=True)
+        d_v.copy_(h_v[j], non_blocking=True)
+        d_pos.copy_(h_pos[j], non_blocking=True)
+        d_len.copy_(h_len[j], non_blocking=True)
+        abi.kv_append_quantize(fp8, d_k, d_v, d_pos, table, tags, flags=FLAGS, status=st_app)
+        abi.paged_decode_attention(fp8, d_q, d_len, table, tags, w.softmax_scale, flags=FLAGS,
+                                   max_splits=max_splits, workspace=ws, out=out, status=st_dec)
+        h_out.copy_(out, non_blocking=True)
+        h_st.copy_(st_dec, non_blocking=True)
+
+    g_e2e = capture(e2e_step, K)
+    g_e2e.replay()
+    ms_e2e = time_graph(g_e2e)
+    e2e_val = world * sum(step_bytes) / (ms_e2e * 1e-3) / 1e9
+    h2d = h_q[0].numel() * 2 + h_k[0].numel() * 2 + h_v[0].numel() * 2 + 2 * B * 4
+    d2h = h_out.numel() * 4 + B * 4
+
+    # ---- the CPU oracle on the host cores (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        stepc, threads, desc, nb = oracle_step_sample(w, args.cpu_frac)
+        t0 = time.perf_counter()
+        tot = stepc()
+        dt = time.perf_counter() - t0
+        cpu = {"value": tot / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    st_final = st_dec.cpu().numpy()
+    launches_per_step = 4  # append kernel; decode: plan + split + merge kernels
+    mean_lens = lens0 + (K - 1) % T + 1
+    res = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3 cache, f16/bf16 MMA, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "seed": w.seed, "batch": B, "context_tokens": int(lens0.sum()),
+                   "steps_in_cycle": T, "l2": "inputs larger than L2 (FP8 cache ~0.8 GB per step)",
+                   "timing": "CUDA graph of K steps, CUDA events on the launching stream"},
+        "decode_tokens_per_s": world * B / (ms_per_step * 1e-3),
+        "kv_tokens_per_s": world * float(mean_lens.sum()) / (ms_per_step * 1e-3),
+        "hbm_frac_step": value / world / peak,
+        "aborted_requests": int((st_final != 0).sum()),
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention_fp8 (plan + split + merge kernels)",
+                     "achieved": dec_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": dec_gbs / peak, "us_per_launch": ms_dec * 1e3,
+                     "alg_bytes_per_launch": statistics.mean(dec_bytes), "traffic": None},
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": ms_e2e / K},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    res.update(extra)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

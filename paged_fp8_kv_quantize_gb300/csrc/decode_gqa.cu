@@ -27,6 +27,8 @@
 //                the partials; zero output for any request with a status.
 #include <math.h>
 
+#include <mutex>
+
 #include "pfkv_device.cuh"
 #include "pfkv_internal.h"
 
@@ -676,26 +678,57 @@ int make_pool_map(CUtensorMap *map, const void *pool, int dtype, int D, int S, i
 
 constexpr int kNCW = 4;
 
+// Launch shape of one split-kernel instantiation for one (page size, scale
+// mode), worked out on its first use and reused afterwards, so that later
+// calls -- including calls under stream capture -- only enqueue kernels.
+struct SplitShape {
+  int S = 0, per_token = -1, dev = -1, nst = 0, grid = 0;
+  uint32_t smem = 0;
+};
+
 template <bool kFp8, int kD, int kG>
 int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const CUtensorMap &mv) {
   using C = Cfg<kFp8, kD, kG, kNCW>;
   const bool per_token = kFp8 && a.scale_mode == PFKV_SCALE_PER_TOKEN;
-  // stage ring of roughly 64 KB (at least 4 pages) so that two or three CTAs share an SM
-  const SmemPlan one = smem_plan(a.S, C::kRowBytes, per_token, 1, kNCW, kG, kD);
-  int nst = (int)(65536u / one.stage_bytes);
-  if (nst < 4) nst = 4;
-  if (nst > 32) nst = 32;
-  SmemPlan sp = smem_plan(a.S, C::kRowBytes, per_token, nst, kNCW, kG, kD);
-  while (sp.total > 200u * 1024u && nst > 2) sp = smem_plan(a.S, C::kRowBytes, per_token, --nst, kNCW, kG, kD);
   auto kern = gqa_split_kernel<kFp8, kD, kG, kNCW>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp.total) != cudaSuccess)
-    return PFKV_ERR_CUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, sp.total) != cudaSuccess || per_sm < 1)
-    return PFKV_ERR_CUDA;
-  const int grid = num_sms() * per_sm;
-  plan_kernel<<<1, 1024, 0, s>>>(a, grid * 8, (1024 + a.S - 1) / a.S);
-  kern<<<grid, C::kThreads, sp.total, s>>>(mk, mv, a, nst);
+  static SplitShape cache[4];
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  SplitShape sh;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    bool found = false;
+    for (auto &e : cache)
+      if (e.S == a.S && e.per_token == (int)per_token && e.dev == dev) {
+        sh = e;
+        found = true;
+        break;
+      }
+    if (!found) {
+      // stage ring of roughly 64 KB (at least 4 pages) so that two or three CTAs share an SM
+      const SmemPlan one = smem_plan(a.S, C::kRowBytes, per_token, 1, kNCW, kG, kD);
+      int nst = (int)(65536u / one.stage_bytes);
+      if (nst < 4) nst = 4;
+      if (nst > 32) nst = 32;
+      SmemPlan sp = smem_plan(a.S, C::kRowBytes, per_token, nst, kNCW, kG, kD);
+      while (sp.total > 200u * 1024u && nst > 2) sp = smem_plan(a.S, C::kRowBytes, per_token, --nst, kNCW, kG, kD);
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp.total) != cudaSuccess)
+        return PFKV_ERR_CUDA;
+      int per_sm = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, sp.total) != cudaSuccess ||
+          per_sm < 1)
+        return PFKV_ERR_CUDA;
+      sh.S = a.S; sh.per_token = (int)per_token; sh.dev = dev; sh.nst = nst; sh.smem = sp.total;
+      sh.grid = num_sms() * per_sm;
+      int slot = 0;
+      for (int i = 0; i < 4; ++i)
+        if (cache[i].S == 0) { slot = i; break; }
+      cache[slot] = sh;
+    }
+  }
+  plan_kernel<<<1, 1024, 0, s>>>(a, sh.grid * 8, (1024 + a.S - 1) / a.S);
+  kern<<<sh.grid, C::kThreads, sh.smem, s>>>(mk, mv, a, sh.nst);
   merge_kernel<kD><<<(a.B * a.Hq + 3) / 4, 128, 0, s>>>(a);
   return cuda_ok(cudaGetLastError());
 }
