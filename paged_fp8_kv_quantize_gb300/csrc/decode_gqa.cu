@@ -136,6 +136,7 @@ struct Cfg {
   static constexpr int kSegV = kD / 8 * kEsz;       // bytes of a V row held by one thread
   static constexpr int kNP = (2 * kG + 7) / 8;      // PV n-tiles (hi and lo columns)
   static constexpr int kThreads = (kNCW + 1) * 32;
+  static constexpr int kMinBlocks = (kG == 8 && kD == 128) ? 2 : 3;  // register budget per thread
   static constexpr float kPScale = kFp8 ? 16384.0f : 1.0f;  // keeps f16 P away from subnormals
 };
 
@@ -174,7 +175,7 @@ __device__ __forceinline__ float round16(float x) {
 }
 
 template <bool kFp8, int kD, int kG, int kNCW>
-__global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads)
+__global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, kD, kG, kNCW>::kMinBlocks)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const DecodeArgs a, const int nst) {
   using C = Cfg<kFp8, kD, kG, kNCW>;
@@ -309,6 +310,30 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads)
     const int gid = lane >> 2, tq = lane & 3;
     constexpr int kSrcMask = (kG == 4) ? 1 : 0;  // PV column -> QK column owner
     const int src_lane = (lane & ~3) | (tq & kSrcMask);
+    // Shared-memory offsets of this thread's fragments inside a 16-row tile.
+    // Tiles start at multiples of 16 rows, which leaves the 128-byte swizzle
+    // pattern unchanged, so the offsets are computed once.
+    constexpr int kKC = C::kSegK / 16;                 // 16-byte chunks of a K row segment
+    constexpr int kVC = C::kSegV >= 16 ? C::kSegV / 16 : 1;
+    uint32_t koff[2][kKC], voff[4][kVC];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int c = 0; c < kKC; ++c) {
+        const uint32_t off = (uint32_t)(gid + 8 * r) * C::kRowBytes + tq * C::kSegK + 16 * c;
+        koff[r][c] = C::kSwz ? swz128(off) : off;
+      }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int trow = 2 * tq + (r & 1) + 8 * (r >> 1);
+#pragma unroll
+      for (int c = 0; c < kVC; ++c) {
+        const uint32_t off = (uint32_t)trow * C::kRowBytes + gid * C::kSegV + 16 * c;
+        voff[r][c] = C::kSwz ? swz128(off) : off;
+      }
+    }
+    const uint32_t smem_base = smem_addr(smem + sp.stages_off);
+
     for (uint32_t iq = 0;; ++iq) {
       const uint32_t slot = iq % kNIQ;
       if (!mbar_wait(&item_full[slot], (iq / kNIQ) & 1u, abort_flag)) break;
@@ -382,42 +407,44 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads)
 
       const int n_mt = (d.p1 - d.p0) * mpp;
       bool alive = true;
-      for (int j = warp; j < n_mt; j += kNCW) {
-        const int page_local = j / mpp, mt_in_page = j - page_local * mpp;
-        const uint32_t rp = d.ring + (uint32_t)page_local;
-        const uint32_t st = rp % (uint32_t)nst;
-        if (!mbar_wait(&full[st], (rp / (uint32_t)nst) & 1u, abort_flag)) {
-          alive = false;
-          break;
+      // Each iteration takes two consecutive 16-token tiles of the item.
+      for (int jp = warp; 2 * jp < n_mt; jp += kNCW) {
+        uint32_t stg[2], tbase[2];
+        bool valid[2], live[2];
+        int tok_base[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int j = 2 * jp + t;
+          valid[t] = j < n_mt;
+          const int page_local = j / mpp, mt_in_page = j - page_local * mpp;
+          const uint32_t rp = d.ring + (uint32_t)page_local;
+          stg[t] = rp % (uint32_t)nst;
+          if (valid[t] && !mbar_wait(&full[stg[t]], (rp / (uint32_t)nst) & 1u, abort_flag)) alive = false;
+          tok_base[t] = (d.p0 + page_local) * S + mt_in_page * 16;
+          live[t] = valid[t] && tok_base[t] < d.L;
+          tbase[t] = smem_base + stg[t] * sp.stage_bytes + (uint32_t)(mt_in_page * 16 * C::kRowBytes);
         }
-        const int tok_base = (d.p0 + page_local) * S + mt_in_page * 16;
-        if (tok_base < d.L) {
-          const uint32_t sK = smem_addr(smem + sp.stages_off + (size_t)st * sp.stage_bytes);
-          const uint32_t sV = sK + S * C::kRowBytes;
-          const uint32_t sKS = sK + 2 * S * C::kRowBytes, sVS = sKS + 4 * S;
-          const int rbase = mt_in_page * 16;
-          // ---- S = K q^T : A = K tile rows (gid, gid+8), this thread's D/4 slice
+        if (!alive) break;
+        // ---- S = K q^T for both tiles
+        float z[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
           float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-          {
+          if (live[t]) {
             uint32_t wk[2][C::kSegK / 4];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const uint32_t rowoff = (uint32_t)(rbase + gid + 8 * r) * C::kRowBytes + tq * C::kSegK;
+            for (int r = 0; r < 2; ++r)
 #pragma unroll
-              for (int c = 0; c < C::kSegK / 16; ++c) {
-                const uint32_t off = rowoff + 16 * c;
-                const uint4 v = lds128(sK + (C::kSwz ? swz128(off) : off));
+              for (int c = 0; c < kKC; ++c) {
+                const uint4 v = lds128(tbase[t] + koff[r][c]);
                 wk[r][4 * c] = v.x; wk[r][4 * c + 1] = v.y; wk[r][4 * c + 2] = v.z; wk[r][4 * c + 3] = v.w;
               }
-            }
 #pragma unroll
             for (int s = 0; s < C::kKsteps; ++s) {
               uint32_t af[4];
               if constexpr (kFp8) {
-                af[0] = e4m3x2_to_f16x2(wk[0][s]);
-                af[1] = e4m3x2_to_f16x2(wk[1][s]);
-                af[2] = e4m3x2_to_f16x2(wk[0][s] >> 16);
-                af[3] = e4m3x2_to_f16x2(wk[1][s] >> 16);
+                e4m3x4_to_f16x4(wk[0][s], af[0], af[2]);
+                e4m3x4_to_f16x4(wk[1][s], af[1], af[3]);
               } else {
                 af[0] = wk[0][2 * s];
                 af[1] = wk[1][2 * s];
@@ -427,38 +454,45 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads)
               mma_t<kFp8>(sacc, af, qf[s][0], qf[s][1]);
             }
           }
-          // ---- online softmax over the tile's 16 tokens (log2 domain)
-          float z[4] = {sacc[0] * mult[0], sacc[1] * mult[1], sacc[2] * mult[0], sacc[3] * mult[1]};
-          if (per_token) {
-            const float k0 = lds_f32(sKS + 4 * (rbase + gid)), k1 = lds_f32(sKS + 4 * (rbase + gid + 8));
-            z[0] *= k0; z[1] *= k0; z[2] *= k1; z[3] *= k1;
+          z[t][0] = sacc[0] * mult[0]; z[t][1] = sacc[1] * mult[1];
+          z[t][2] = sacc[2] * mult[0]; z[t][3] = sacc[3] * mult[1];
+          if (per_token && live[t]) {
+            const uint32_t sks = smem_base + stg[t] * sp.stage_bytes + 2 * S * C::kRowBytes +
+                                 4 * ((tok_base[t] - (tok_base[t] / S) * S) + gid);
+            const float k0 = lds_f32(sks), k1 = lds_f32(sks + 32);
+            z[t][0] *= k0; z[t][1] *= k0; z[t][2] *= k1; z[t][3] *= k1;
           }
-          if (tok_base + gid >= d.L) z[0] = z[1] = kNegInf;
-          if (tok_base + gid + 8 >= d.L) z[2] = z[3] = kNegInf;
-          float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+          if (!live[t] || tok_base[t] + gid >= d.L) z[t][0] = z[t][1] = kNegInf;
+          if (!live[t] || tok_base[t] + gid + 8 >= d.L) z[t][2] = z[t][3] = kNegInf;
+        }
+        // ---- online softmax over the 32 tokens (log2 domain)
+        float mx0 = fmaxf(fmaxf(z[0][0], z[0][2]), fmaxf(z[1][0], z[1][2]));
+        float mx1 = fmaxf(fmaxf(z[0][1], z[0][3]), fmaxf(z[1][1], z[1][3]));
 #pragma unroll
-          for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-          }
-          const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-          const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
-          m[0] = mn0;
-          m[1] = mn1;
-          float p[4] = {fast_exp2(z[0] - mn0), fast_exp2(z[1] - mn1), fast_exp2(z[2] - mn0), fast_exp2(z[3] - mn1)};
-          l[0] = l[0] * al0 + p[0] + p[2];
-          l[1] = l[1] * al1 + p[1] + p[3];
-          // PV columns: v = 8*nt + 2*tq + e -> head v % G, hi part for v < G, lo part for G <= v < 2G
-          float apv0 = al0, apv1 = al1, pv[4] = {p[0], p[1], p[2], p[3]};
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float al0 = fast_exp2(m[0] - mn0), al1 = fast_exp2(m[1] - mn1);
+        const bool moved = __any_sync(0xffffffffu, (mn0 != m[0]) | (mn1 != m[1]));
+        m[0] = mn0;
+        m[1] = mn1;
+        float p[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          p[t][0] = fast_exp2(z[t][0] - mn0); p[t][1] = fast_exp2(z[t][1] - mn1);
+          p[t][2] = fast_exp2(z[t][2] - mn0); p[t][3] = fast_exp2(z[t][3] - mn1);
+        }
+        l[0] = l[0] * al0 + (p[0][0] + p[0][2]) + (p[1][0] + p[1][2]);
+        l[1] = l[1] * al1 + (p[0][1] + p[0][3]) + (p[1][1] + p[1][3]);
+        if (moved) {  // rescale the accumulators only when some running max moved
+          float apv0 = al0, apv1 = al1;
           if constexpr (kG == 1) {
             apv0 = apv1 = __shfl_sync(0xffffffffu, al0, lane & ~3);
-            pv[0] = pv[1] = __shfl_sync(0xffffffffu, p[0], lane & ~3);
-            pv[2] = pv[3] = __shfl_sync(0xffffffffu, p[2], lane & ~3);
           } else if constexpr (kG < 8) {
             apv0 = __shfl_sync(0xffffffffu, al0, src_lane);
             apv1 = __shfl_sync(0xffffffffu, al1, src_lane);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) pv[k] = __shfl_sync(0xffffffffu, p[k], src_lane);
           }
 #pragma unroll
           for (int i = 0; i < C::kKsteps; ++i)
@@ -466,10 +500,26 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads)
             for (int nt = 0; nt < C::kNP; ++nt) {
               o[i][nt][0] *= apv0; o[i][nt][1] *= apv1; o[i][nt][2] *= apv0; o[i][nt][3] *= apv1;
             }
+        }
+        // ---- O^T += V^T P^T, one 16-token k-step per tile
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!live[t]) continue;
+          // PV columns: v = 8*nt + 2*tq + e -> head v % G; hi part for v < G, lo part for G <= v < 2G
+          float pv[4] = {p[t][0], p[t][1], p[t][2], p[t][3]};
+          if constexpr (kG == 1) {
+            pv[0] = pv[1] = __shfl_sync(0xffffffffu, p[t][0], lane & ~3);
+            pv[2] = pv[3] = __shfl_sync(0xffffffffu, p[t][2], lane & ~3);
+          } else if constexpr (kG < 8) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) pv[k] = __shfl_sync(0xffffffffu, p[t][k], src_lane);
+          }
           float vs0 = 1.f, vs1 = 1.f;
           if (per_token) {
-            vs0 = lds_f32(sVS + 4 * (rbase + gid));
-            vs1 = lds_f32(sVS + 4 * (rbase + gid + 8));
+            const uint32_t svs = smem_base + stg[t] * sp.stage_bytes + 2 * S * C::kRowBytes + 4 * S +
+                                 4 * ((tok_base[t] - (tok_base[t] / S) * S) + gid);
+            vs0 = lds_f32(svs);
+            vs1 = lds_f32(svs + 32);
           }
           uint32_t pb[C::kNP][2];
 #pragma unroll
@@ -487,49 +537,42 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads)
             pb[nt][0] = movmatrix_trans(pack2<kFp8>(val[0], val[1]));
             pb[nt][1] = movmatrix_trans(pack2<kFp8>(val[2], val[3]));
           }
-          // ---- O^T += V^T P^T : A = V tile rows (2tq, 2tq+1, 2tq+8, 2tq+9), this thread's D/8 slice
-          {
-            uint32_t wv[4][C::kSegV / 4];
-            const int trow[4] = {2 * tq, 2 * tq + 1, 2 * tq + 8, 2 * tq + 9};
+          uint32_t wv[4][C::kSegV / 4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const uint32_t rowoff = (uint32_t)(rbase + trow[r]) * C::kRowBytes + gid * C::kSegV;
-              if constexpr (C::kSegV == 8) {
-                const uint2 v = lds64(sV + rowoff);
-                wv[r][0] = v.x; wv[r][1] = v.y;
-              } else {
+          for (int r = 0; r < 4; ++r) {
+            if constexpr (C::kSegV == 8) {
+              const uint2 v = lds64(tbase[t] + voff[r][0]);
+              wv[r][0] = v.x; wv[r][1] = v.y;
+            } else {
 #pragma unroll
-                for (int c = 0; c < C::kSegV / 16; ++c) {
-                  const uint32_t off = rowoff + 16 * c;
-                  const uint4 v = lds128(sV + (C::kSwz ? swz128(off) : off));
-                  wv[r][4 * c] = v.x; wv[r][4 * c + 1] = v.y; wv[r][4 * c + 2] = v.z; wv[r][4 * c + 3] = v.w;
-                }
+              for (int c = 0; c < kVC; ++c) {
+                const uint4 v = lds128(tbase[t] + voff[r][c]);
+                wv[r][4 * c] = v.x; wv[r][4 * c + 1] = v.y; wv[r][4 * c + 2] = v.z; wv[r][4 * c + 3] = v.w;
               }
             }
+          }
 #pragma unroll
-            for (int mt = 0; mt < C::kKsteps; ++mt) {
-              uint32_t af[4];
-              if constexpr (kFp8) {
-                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-                const uint32_t t01 = prmt(wv[0][mt >> 1], wv[1][mt >> 1], sel);
-                const uint32_t t89 = prmt(wv[2][mt >> 1], wv[3][mt >> 1], sel);
-                af[0] = e4m3x2_to_f16x2(t01);
-                af[1] = e4m3x2_to_f16x2(t01 >> 16);
-                af[2] = e4m3x2_to_f16x2(t89);
-                af[3] = e4m3x2_to_f16x2(t89 >> 16);
-              } else {
-                af[0] = prmt(wv[0][mt], wv[1][mt], 0x5410u);
-                af[1] = prmt(wv[0][mt], wv[1][mt], 0x7632u);
-                af[2] = prmt(wv[2][mt], wv[3][mt], 0x5410u);
-                af[3] = prmt(wv[2][mt], wv[3][mt], 0x7632u);
-              }
-#pragma unroll
-              for (int nt = 0; nt < C::kNP; ++nt) mma_t<kFp8>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
+          for (int mt = 0; mt < C::kKsteps; ++mt) {
+            uint32_t af[4];
+            if constexpr (kFp8) {
+              const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+              e4m3x4_to_f16x4(prmt(wv[0][mt >> 1], wv[1][mt >> 1], sel), af[0], af[1]);
+              e4m3x4_to_f16x4(prmt(wv[2][mt >> 1], wv[3][mt >> 1], sel), af[2], af[3]);
+            } else {
+              af[0] = prmt(wv[0][mt], wv[1][mt], 0x5410u);
+              af[1] = prmt(wv[0][mt], wv[1][mt], 0x7632u);
+              af[2] = prmt(wv[2][mt], wv[3][mt], 0x5410u);
+              af[3] = prmt(wv[2][mt], wv[3][mt], 0x7632u);
             }
+#pragma unroll
+            for (int nt = 0; nt < C::kNP; ++nt) mma_t<kFp8>(o[mt][nt], af, pb[nt][0], pb[nt][1]);
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
+        if (lane == 0) {
+          if (valid[0]) mbar_arrive(&empty[stg[0]]);
+          if (valid[1]) mbar_arrive(&empty[stg[1]]);
+        }
       }
       // ---- per-warp state -> shared memory
 #pragma unroll
