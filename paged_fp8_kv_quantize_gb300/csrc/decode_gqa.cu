@@ -538,15 +538,16 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
             pb[nt][1] = movmatrix_trans(pack2<kFp8>(val[2], val[3]));
           }
           uint32_t wv[4][C::kSegV / 4];
+          const uint32_t vbase = tbase[t] + S * C::kRowBytes;  // V tile follows the K tile in the stage
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             if constexpr (C::kSegV == 8) {
-              const uint2 v = lds64(tbase[t] + voff[r][0]);
+              const uint2 v = lds64(vbase + voff[r][0]);
               wv[r][0] = v.x; wv[r][1] = v.y;
             } else {
 #pragma unroll
               for (int c = 0; c < kVC; ++c) {
-                const uint4 v = lds128(tbase[t] + voff[r][c]);
+                const uint4 v = lds128(vbase + voff[r][c]);
                 wv[r][4 * c] = v.x; wv[r][4 * c + 1] = v.y; wv[r][4 * c + 2] = v.z; wv[r][4 * c + 3] = v.w;
               }
             }
