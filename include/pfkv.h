@@ -196,6 +196,11 @@ int pfkv_e4m3_encode(const float *x, uint8_t *codes, int64_t n, void *stream);
 /* Human-readable text for a PFKV_ERR_* code. */
 const char *pfkv_strerror(int code);
 
+/* Text of the CUDA error behind the calling thread's most recent
+ * PFKV_ERR_CUDA return (which call failed and the runtime's message); empty
+ * if there was none.  The string is owned by the library. */
+const char *pfkv_last_error_detail(void);
+
 /* ABI version of this header (bumped when a signature changes). */
 int pfkv_abi_version(void);
 

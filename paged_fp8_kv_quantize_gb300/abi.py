@@ -33,13 +33,15 @@ EXPORTS = (
     "pfkv_calibrate_scales",
     "pfkv_e4m3_encode",
     "pfkv_strerror",
+    "pfkv_last_error_detail",
     "pfkv_abi_version",
 )
 
 
 class PfkvError(RuntimeError):
     def __init__(self, fn, code):
-        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+        detail = lib.pfkv_last_error_detail().decode() if code == -7 else ""
+        super().__init__(f"{fn} failed: {code} ({strerror(code)}){': ' + detail if detail else ''}")
         self.code = code
 
 
@@ -81,6 +83,8 @@ def _load():
     L.pfkv_e4m3_encode.argtypes = [P, P, i64, P]
     L.pfkv_strerror.restype = ctypes.c_char_p
     L.pfkv_strerror.argtypes = [ctypes.c_int]
+    L.pfkv_last_error_detail.restype = ctypes.c_char_p
+    L.pfkv_last_error_detail.argtypes = []
     L.pfkv_abi_version.restype = ctypes.c_int
     L.pfkv_abi_version.argtypes = []
     return L

@@ -1,11 +1,20 @@
 // api.cu -- the extern "C" entry points of libpfkv: argument checks on the
 // host, workspace layout, and dispatch to the kernels on the caller's stream.
 #include <math.h>
+#include <stdio.h>
+
 #include <mutex>
 
 #include "pfkv_internal.h"
 
 namespace pfkv {
+
+static thread_local char g_last_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char *where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  return PFKV_ERR_CUDA;
+}
 
 EncodeTiledFn encode_tiled_fn() {
   static EncodeTiledFn fn = nullptr;
@@ -126,6 +135,8 @@ using namespace pfkv;
 extern "C" {
 
 int pfkv_abi_version(void) { return 1; }
+
+const char *pfkv_last_error_detail(void) { return g_last_error; }
 
 const char *pfkv_strerror(int code) {
   switch (code) {

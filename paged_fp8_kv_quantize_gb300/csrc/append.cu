@@ -133,7 +133,8 @@ __global__ void encode_kernel(const float *x, uint8_t *codes, int64_t n) {
 int launch_append(const pfkv_cache &c, const void *k_new, const void *v_new, int n_rows, const int *row_req,
                   const int *positions, const int *block_table, const uint32_t *block_tags, int batch,
                   int max_pages, uint32_t flags, uint32_t *status, cudaStream_t s) {
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t) * (size_t)batch, s) != cudaSuccess) return PFKV_ERR_CUDA;
+  int rc = cuda_ok(cudaMemsetAsync(status, 0, sizeof(uint32_t) * (size_t)batch, s), "status memset");
+  if (rc) return rc;
   if (n_rows == 0) return PFKV_OK;
   const int units = (c.kv_shared ? 1 : 2) * c.num_kv_heads;
   const dim3 grid(n_rows, (units + 3) / 4);
@@ -147,7 +148,8 @@ int launch_append(const pfkv_cache &c, const void *k_new, const void *v_new, int
 }
 
 int launch_calibrate(const void *rows, int64_t n_rows, int heads, int dim, float *scale, cudaStream_t s) {
-  if (cudaMemsetAsync(scale, 0, sizeof(float) * (size_t)heads, s) != cudaSuccess) return PFKV_ERR_CUDA;
+  int rc = cuda_ok(cudaMemsetAsync(scale, 0, sizeof(float) * (size_t)heads, s), "scale memset");
+  if (rc) return rc;
   if (n_rows > 0) {
     const int gx = (int)(n_rows < 4096 ? n_rows : 4096);
     amax_kernel<<<dim3(gx, heads), 256, 0, s>>>((const uint16_t *)rows, n_rows, heads, dim, (unsigned *)scale);

@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
 
 int make_pool_map(CUtensorMap *map, const void *pool, int dtype, int D, int S, int Hkv, int P) {
   EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return PFKV_ERR_CUDA;
+  if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
   const int esz = dtype == PFKV_DTYPE_FP8_E4M3 ? 1 : 2;
   const CUtensorMapDataType dt = esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t row = (uint64_t)D * esz;
@@ -717,7 +717,8 @@ int make_pool_map(CUtensorMap *map, const void *pool, int dtype, int D, int S, i
             row >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   }
-  return r == CUDA_SUCCESS ? PFKV_OK : PFKV_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+  return PFKV_OK;
 }
 
 constexpr int kNCW = 4;
@@ -757,12 +758,18 @@ int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const 
       if (nst > 32) nst = 32;
       SmemPlan sp = smem_plan(a.S, C::kRowBytes, per_token, nst, kNCW, kG, kD);
       while (sp.total > 200u * 1024u && nst > 2) sp = smem_plan(a.S, C::kRowBytes, per_token, --nst, kNCW, kG, kD);
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp.total) != cudaSuccess)
-        return PFKV_ERR_CUDA;
+      // The attribute is a per-kernel cap on the device: only ever raise it, so
+      // that a shape with a larger ring, cached earlier, keeps launching.
+      static uint32_t attr_set[64] = {};
+      if (dev < 64 && sp.total > attr_set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp.total);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(split kernel)");
+        attr_set[dev] = sp.total;
+      }
       int per_sm = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, sp.total) != cudaSuccess ||
-          per_sm < 1)
-        return PFKV_ERR_CUDA;
+      const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, sp.total);
+      if (e != cudaSuccess) return cuda_fail(e, "occupancy query (split kernel)");
+      if (per_sm < 1) return cuda_fail(cudaErrorInvalidConfiguration, "split kernel does not fit on an SM");
       sh.S = a.S; sh.per_token = (int)per_token; sh.dev = dev; sh.nst = nst; sh.smem = sp.total;
       sh.grid = num_sms() * per_sm;
       int slot = 0;
@@ -772,9 +779,13 @@ int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const 
     }
   }
   plan_kernel<<<1, 1024, 0, s>>>(a, sh.grid * 8, (1024 + a.S - 1) / a.S);
+  int rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
+  if (rc) return rc;
   kern<<<sh.grid, C::kThreads, sh.smem, s>>>(mk, mv, a, sh.nst);
+  rc = cuda_ok(cudaGetLastError(), "split kernel launch");
+  if (rc) return rc;
   merge_kernel<kD><<<(a.B * a.Hq + 3) / 4, 128, 0, s>>>(a);
-  return cuda_ok(cudaGetLastError());
+  return cuda_ok(cudaGetLastError(), "merge kernel launch");
 }
 
 template <bool kFp8, int kD>

@@ -67,6 +67,10 @@ int launch_append(const pfkv_cache &c, const void *k_new, const void *v_new, int
 int launch_calibrate(const void *rows, int64_t n_rows, int heads, int dim, float *scale, cudaStream_t s);
 int launch_encode(const float *x, uint8_t *codes, int64_t n, cudaStream_t s);
 
-inline int cuda_ok(cudaError_t e) { return e == cudaSuccess ? PFKV_OK : PFKV_ERR_CUDA; }
+// Records the CUDA error behind a PFKV_ERR_CUDA return (per host thread).
+int cuda_fail(cudaError_t e, const char *where);
+inline int cuda_ok(cudaError_t e, const char *where = "kernel launch") {
+  return e == cudaSuccess ? PFKV_OK : cuda_fail(e, where);
+}
 
 }  // namespace pfkv
