@@ -178,6 +178,40 @@ int pfkv_paged_decode_attention_bf16(const pfkv_cache *cache, const void *q, int
                                      size_t workspace_bytes, float *out, uint32_t *status, void *stream);
 
 /*
+ * paged_decode_attention_fp8_noalloc -- the FP8 decode above for callers
+ * that cannot allocate device memory.  (The post has no counterpart; this is
+ * an interface convenience of this library.)
+ *
+ * Some callers have no way to hand the library a workspace: code embedded in
+ * a host framework that owns every device allocation and passes in only its
+ * input and output buffers, plugins that must not bypass their host's
+ * allocator, or serving paths where a cudaMalloc would synchronise the
+ * device.  This entry point takes no workspace; it uses a scratch buffer of
+ * PFKV_NOALLOC_SCRATCH_BYTES that lives in the library as a file-scope device
+ * array (every GPU that loads the library holds it until the process exits)
+ * and otherwise behaves exactly like pfkv_paged_decode_attention_fp8 with the
+ * same arguments.  It calls no cudaMalloc, cudaFree or allocating routine.
+ *  - Returns PFKV_ERR_WORKSPACE, before any device work, when
+ *    pfkv_decode_workspace_bytes(cache, batch, num_q_heads, max_splits) is
+ *    larger than PFKV_NOALLOC_SCRATCH_BYTES (lower max_splits or split the
+ *    batch).
+ *  - The first call on each device looks up the buffer's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - Every call shares the one buffer, which keeps the last call's contents;
+ *    the kernels reset what must start at zero themselves.  Calls that
+ *    overlap on the GPU (different streams, or different host threads, at
+ *    the same time) race on the buffer and give wrong results.
+ */
+#define PFKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, const void *q, int32_t num_q_heads,
+                                            const int32_t *seq_lens, const int32_t *block_table,
+                                            const uint32_t *block_tags, int32_t batch, int32_t max_pages,
+                                            float softmax_scale, uint32_t flags, int32_t max_splits, float *out,
+                                            uint32_t *status, void *stream);
+
+/*
  * calibrate_scales -- per-head FP8 scales s[h] = fp32(amax/448) over
  * rows[n_rows][num_heads][head_dim] (bf16); s[h] = 1 when the head's rows
  * are all zero.  This is the "scale = amax / 448" convention of an e4m3 cache

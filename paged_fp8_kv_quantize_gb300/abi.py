@@ -30,6 +30,7 @@ EXPORTS = (
     "pfkv_decode_workspace_bytes",
     "pfkv_paged_decode_attention_fp8",
     "pfkv_paged_decode_attention_bf16",
+    "pfkv_paged_decode_attention_fp8_noalloc",
     "pfkv_calibrate_scales",
     "pfkv_e4m3_encode",
     "pfkv_strerror",
@@ -77,6 +78,9 @@ def _load():
         f = getattr(L, n)
         f.restype = ctypes.c_int
         f.argtypes = [cp, P, i32, P, P, P, i32, i32, ctypes.c_float, u32, i32, P, sz, P, P, P]
+    L.pfkv_paged_decode_attention_fp8_noalloc.restype = ctypes.c_int
+    L.pfkv_paged_decode_attention_fp8_noalloc.argtypes = [cp, P, i32, P, P, P, i32, i32, ctypes.c_float, u32, i32,
+                                                          P, P, P]
     L.pfkv_calibrate_scales.restype = ctypes.c_int
     L.pfkv_calibrate_scales.argtypes = [P, i64, i32, i32, P, P]
     L.pfkv_e4m3_encode.restype = ctypes.c_int
@@ -226,6 +230,33 @@ def paged_decode_attention_bf16(cache, q, seq_lens, block_table, block_tags, sof
                                 workspace=None, out=None, status=None, stream=None):
     return _decode("pfkv_paged_decode_attention_bf16", cache, q, seq_lens, block_table, block_tags, softmax_scale,
                    flags, max_splits, workspace, out, status, stream)
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # PFKV_NOALLOC_SCRATCH_BYTES
+
+
+def paged_decode_attention_fp8_noalloc(cache, q, seq_lens, block_table, block_tags, softmax_scale, flags=0,
+                                       max_splits=64, out=None, status=None, stream=None):
+    """FP8 decode without a caller-provided workspace (see pfkv_paged_decode_attention_fp8_noalloc).
+
+    For callers that cannot allocate device scratch: the library uses its own
+    fixed buffer of NOALLOC_SCRATCH_BYTES.  Pass `out` and `status` to keep the
+    call free of allocations on the Python side as well; calls that overlap on
+    the GPU race on the shared buffer."""
+    B, Hq, D = q.shape
+    MP = block_table.shape[1]
+    if out is None:
+        out = torch.empty(B, Hq, cache.Dv, dtype=torch.float32, device=q.device)
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=q.device)
+    d = cache.desc()
+    rc = lib.pfkv_paged_decode_attention_fp8_noalloc(
+        ctypes.byref(d), _ptr(_dev(q, "q", torch.bfloat16)), Hq, _ptr(_dev(seq_lens, "seq_lens", torch.int32)),
+        _ptr(_dev(block_table, "block_table", torch.int32)), _ptr(_dev(block_tags, "block_tags", torch.int32)), B,
+        MP, float(softmax_scale), int(flags), int(max_splits), _ptr(_dev(out, "out", torch.float32)),
+        _ptr(_dev(status, "status", torch.int32)), _stream(stream))
+    _check("pfkv_paged_decode_attention_fp8_noalloc", rc)
+    return out, status
 
 
 def paged_decode_attention(cache, *args, **kw):
