@@ -109,7 +109,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
     __syncthreads();
     const int warp_off = wid ? s_scan[wid - 1] : 0;
     const int excl = s_carry + warp_off + x - n;
-    if (b < a.B) a.chunk_start[b] = excl;
+    if (b < a.B) {
+      a.chunk_start[b] = excl;
+      const int L = a.seq_lens[b];
+      const int pages = n ? (L + S - 1) / S : 0;
+      for (int c = 0; c < n; ++c) a.chunk_info[excl + c] = make_int4(b, c * ppc, min((c + 1) * ppc, pages), L);
+    }
     __syncthreads();
     if (tid == blockDim.x - 1) s_carry = excl + n;
     __syncthreads();
@@ -218,11 +223,21 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     }
     const int n_items = a.hdr->n_items;
     const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
+    // Pages of one batch are issued by separate lanes at once.  A batch never
+    // holds more pages than the ring has stages, so no two lanes of a batch
+    // share a stage and every empty-barrier wait is for the stage's previous
+    // use only (no parity aliasing).
+    const int batch_pages = min(32, nst);
     uint32_t ring = 0;
+    // Work items are claimed one ahead: the id and the split descriptor of
+    // the next item are in flight while the current item's pages go out.
+    int item = 0, item_next = 0;
+    if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    int4 info = make_int4(0, 0, 0, 0);
+    if (item < n_items) info = a.chunk_info[item / a.Hkv];
     for (uint32_t iq = 0;; ++iq) {
-      int item = 0;
-      if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
-      item = __shfl_sync(0xffffffffu, item, 0);
+      if (lane == 0) item_next = (int)atomicAdd(&a.hdr->work, 1u);
       const uint32_t slot = iq % kNIQ;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&item_empty[slot], ((iq / kNIQ) & 1u) ^ 1u, abort_flag);
@@ -236,30 +251,22 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         break;
       }
       const int cg = item / a.Hkv, g = item - cg * a.Hkv;
-      // request owning chunk cg: last b with chunk_start[b] <= cg
-      int lo = 0, hi = a.B;  // chunk_start[lo] <= cg < chunk_start[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(&a.chunk_start[mid]) <= cg) lo = mid; else hi = mid;
-      }
-      const int b = lo;
-      const int L = a.seq_lens[b];
-      const int ppc = a.ppc[b];
-      const int pages_b = (L + S - 1) / S;
-      const int p0 = (cg - a.chunk_start[b]) * ppc;
-      const int p1 = min(p0 + ppc, pages_b);
+      const int b = info.x, p0 = info.y, p1 = info.z, L = info.w;
       if (lane == 0) {
         ItemDesc d;
         d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.pad = 0;
         items[slot] = d;
         mbar_arrive(&item_full[slot]);
       }
+      item_next = __shfl_sync(0xffffffffu, item_next, 0);
+      int4 info_next = make_int4(0, 0, 0, 0);
+      if (item_next < n_items) info_next = a.chunk_info[item_next / a.Hkv];  // used by the next iteration
       const int *trow = a.block_table + (size_t)b * a.MP;
       const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
       uint32_t st_bits = 0;
-      for (int i0 = p0; i0 < p1 && ok; i0 += 32) {
+      for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages) {
         const int i = i0 + lane;
-        const bool valid = i < p1;
+        const bool valid = lane < batch_pages && i < p1;
         const int pid = valid ? __ldg(&trow[i]) : 0;
         const bool oob = valid && (pid < 0 || pid >= a.P);
         uint32_t page_tag = 0, want_tag = 0;
@@ -267,43 +274,41 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           page_tag = __ldg(&a.page_tags[pid]);
           want_tag = __ldg(&tagrow[i]);
         }
-        const int n = min(32, p1 - i0);
-        for (int j = 0; j < n; ++j) {
-          const int pj = __shfl_sync(0xffffffffu, pid, j);
-          const bool oj = __shfl_sync(0xffffffffu, oob, j);
-          if (lane == 0) {
-            const uint32_t st = ring % (uint32_t)nst;
-            ok = mbar_wait(&empty[st], ((ring / (uint32_t)nst) & 1u) ^ 1u, abort_flag);
-            if (ok) {
-              uint8_t *stage = smem + sp.stages_off + (size_t)st * sp.stage_bytes;
-              if (oj) {
-                mbar_arrive(&full[st]);  // never fetched; the request is aborted
+        bool lane_ok = true;
+        if (valid) {
+          const uint32_t r = ring + (uint32_t)lane;
+          const uint32_t st = r % (uint32_t)nst;
+          lane_ok = mbar_wait(&empty[st], ((r / (uint32_t)nst) & 1u) ^ 1u, abort_flag);
+          if (lane_ok) {
+            uint8_t *stage = smem + sp.stages_off + (size_t)st * sp.stage_bytes;
+            if (oob) {
+              mbar_arrive(&full[st]);  // never fetched; the request is aborted
+            } else {
+              mbar_arrive_expect_tx(&full[st], sp.page_bytes);
+              if constexpr (C::kRowBytes == 256) {
+                tma_load_5d(stage, &tmK, &full[st], 0, 0, 0, g, pid);
+                tma_load_5d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, 0, g, pid);
               } else {
-                mbar_arrive_expect_tx(&full[st], sp.page_bytes);
-                if constexpr (C::kRowBytes == 256) {
-                  tma_load_5d(stage, &tmK, &full[st], 0, 0, 0, g, pj);
-                  tma_load_5d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, 0, g, pj);
-                } else {
-                  tma_load_4d(stage, &tmK, &full[st], 0, 0, g, pj);
-                  tma_load_4d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, g, pj);
-                }
-                if (per_token) {
-                  const size_t r = ((size_t)pj * a.Hkv + g) * S;
-                  bulk_load(stage + 2 * S * C::kRowBytes, a.k_scale + r, 4u * S, &full[st]);
-                  bulk_load(stage + 2 * S * C::kRowBytes + 4 * S, a.v_scale + r, 4u * S, &full[st]);
-                }
+                tma_load_4d(stage, &tmK, &full[st], 0, 0, g, pid);
+                tma_load_4d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, g, pid);
+              }
+              if (per_token) {
+                const size_t rr = ((size_t)pid * a.Hkv + g) * S;
+                bulk_load(stage + 2 * S * C::kRowBytes, a.k_scale + rr, 4u * S, &full[st]);
+                bulk_load(stage + 2 * S * C::kRowBytes + 4 * S, a.v_scale + rr, 4u * S, &full[st]);
               }
             }
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          ++ring;
-          if (!ok) break;
         }
+        ring += (uint32_t)min(batch_pages, p1 - i0);
+        ok = __all_sync(0xffffffffu, lane_ok);
         if (__any_sync(0xffffffffu, oob)) st_bits |= PFKV_ST_PAGE_OOB;
         if (__any_sync(0xffffffffu, page_tag != want_tag)) st_bits |= PFKV_ST_STALE_TAG;
       }
       if (lane == 0 && st_bits) atomicOr(&a.status[b], st_bits);
       if (!ok) break;
+      item = item_next;
+      info = info_next;
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -664,33 +669,42 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
   const int b = wg / a.Hq, h = wg - b * a.Hq;
   float *dst = a.out + (size_t)wg * kD;
   const bool err = a.hdr->err != 0u;
-  uint32_t st = a.status[b];
+  const uint32_t st = a.status[b];
   const int c0 = a.chunk_start[b], n = a.chunk_start[b + 1] - c0;
+  const int dd = lane * 4;  // this lane's four output dims (kD <= 128)
   if (err && h == 0 && lane == 0) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
   if (st != 0u || err || n <= 0) {
-    for (int dd = lane * 4; dd < kD; dd += 128) *reinterpret_cast<float4 *>(dst + dd) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dd < kD) *reinterpret_cast<float4 *>(dst + dd) = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
+  const float2 *ml = a.part_ml + (size_t)c0 * a.Hq + h;
   float M = kNegInf;
-  for (int c = lane; c < n; c += 32) M = fmaxf(M, a.part_ml[(size_t)(c0 + c) * a.Hq + h].x);
+  for (int c = lane; c < n; c += 32) M = fmaxf(M, ml[(size_t)c * a.Hq].x);
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float W = 0.f;
   for (int c = lane; c < n; c += 32) {
-    const float2 ml = a.part_ml[(size_t)(c0 + c) * a.Hq + h];
-    W += ml.y * fast_exp2(ml.x - M);
+    const float2 v = ml[(size_t)c * a.Hq];
+    W += v.y * fast_exp2(v.x - M);
   }
   for (int off = 16; off; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
-  const float inv = 1.f / W;
-  for (int dd = lane * 4; dd < kD; dd += 128) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = 0; c < n; ++c) {
-      const float2 ml = a.part_ml[(size_t)(c0 + c) * a.Hq + h];
-      const float w = fast_exp2(ml.x - M);
-      const float4 v = *reinterpret_cast<const float4 *>(a.part_o + ((size_t)(c0 + c) * a.Hq + h) * kD + dd);
-      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  const float *po = a.part_o + ((size_t)c0 * a.Hq + h) * kD + dd;
+  const size_t cstride = (size_t)a.Hq * kD;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cb = 0; cb < n; cb += 32) {
+    // lane j holds the weight of chunk cb + j; the loop broadcasts it
+    const float wl = (cb + lane < n) ? fast_exp2(ml[(size_t)(cb + lane) * a.Hq].x - M) : 0.f;
+    const int nn = min(32, n - cb);
+#pragma unroll 4
+    for (int j = 0; j < nn; ++j) {
+      const float w = __shfl_sync(0xffffffffu, wl, j);
+      if (dd < kD) {
+        const float4 v = *reinterpret_cast<const float4 *>(po + (size_t)(cb + j) * cstride);
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+      }
     }
-    *reinterpret_cast<float4 *>(dst + dd) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
+  const float inv = 1.f / W;
+  if (dd < kD) *reinterpret_cast<float4 *>(dst + dd) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 // ---------------------------------------------------------------- host side
