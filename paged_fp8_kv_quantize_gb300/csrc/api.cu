@@ -45,7 +45,8 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
   w.chunk_start = up256(sizeof(WsHeader));
   w.ppc = w.chunk_start + up256(sizeof(int) * ((size_t)batch + 1));
   w.chunk_info = w.ppc + up256(sizeof(int) * (size_t)batch);
-  w.part_ml = w.chunk_info + up256(sizeof(int4) * (size_t)batch * max_splits);
+  w.counters = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
+  w.part_ml = w.counters + up256(sizeof(int) * (size_t)batch * q_heads);
   w.part_o = w.part_ml + up256(sizeof(float2) * slots);
   w.total = w.part_o + up256(sizeof(float) * slots * v_dim);
   return w;
@@ -114,6 +115,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.chunk_start = reinterpret_cast<int *>(w + L.chunk_start);
   a.ppc = reinterpret_cast<int *>(w + L.ppc);
   a.chunk_info = reinterpret_cast<int4 *>(w + L.chunk_info);
+  a.counters = reinterpret_cast<int *>(w + L.counters);
   a.part_ml = reinterpret_cast<float2 *>(w + L.part_ml);
   a.part_o = reinterpret_cast<float *>(w + L.part_o);
   a.out = out; a.status = status;

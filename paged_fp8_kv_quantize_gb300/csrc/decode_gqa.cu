@@ -22,9 +22,14 @@
 //                copies (128-byte swizzle).  Consumer warps take 16-token
 //                tiles: e4m3 -> f16 in registers (exact), QK^T and PV on
 //                register-operand tensor-core MMA, online softmax in fp32.
-//                Each item leaves an unnormalised partial (m, l, O).
-//   3. merge  -- one warp per (request, query head): log-sum-exp merge of
-//                the partials; zero output for any request with a status.
+//                An item that covers a whole request writes its output
+//                directly.  Otherwise it leaves an unnormalised partial
+//                (m, l, O); the last CTA to finish a (request, KV head) --
+//                found with an arrive-only counter, no waiting -- merges the
+//                partials with the log-sum-exp rule.  A request with any
+//                status bit gets zero output.  The split kernel is launched
+//                as a programmatic dependent of the plan kernel, so its
+//                prologue overlaps the plan.
 #include <math.h>
 
 #include <mutex>
@@ -42,12 +47,13 @@ constexpr int kNIQ = 4;  // item descriptors in flight per CTA
 struct ItemDesc {
   int b, cg, g, p0, p1, L;
   uint32_t ring;
-  int pad;
+  int nb;  // splits of request b
 };
 
 // ---------------------------------------------------------------- plan
 
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
+  pdl_launch_dependents();  // the split kernel waits for this grid's results before reading them
   __shared__ long long s_red[32];
   __shared__ int s_scan[32];
   __shared__ int s_carry;
@@ -113,7 +119,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
       a.chunk_start[b] = excl;
       const int L = a.seq_lens[b];
       const int pages = n ? (L + S - 1) / S : 0;
-      for (int c = 0; c < n; ++c) a.chunk_info[excl + c] = make_int4(b, c * ppc, min((c + 1) * ppc, pages), L);
+      for (int c = 0; c < n; ++c) {
+        a.chunk_info[2 * (excl + c)] = make_int4(b, c * ppc, min((c + 1) * ppc, pages), L);
+        a.chunk_info[2 * (excl + c) + 1] = make_int4(n, c, 0, 0);
+      }
+      for (int g = 0; g < a.Hkv; ++g) a.counters[(size_t)b * a.Hkv + g] = 0;
+      if (n == 0)  // bad length: no split will write this request's rows
+        for (size_t k = 0; k < (size_t)a.Hq * a.Dv; ++k) a.out[(size_t)b * a.Hq * a.Dv + k] = 0.f;
     }
     __syncthreads();
     if (tid == blockDim.x - 1) s_carry = excl + n;
@@ -155,9 +167,9 @@ __host__ __device__ inline SmemPlan smem_plan(int S, int row_bytes, bool per_tok
   p.stage_bytes = (p.page_bytes + 1023u) & ~1023u;
   p.stages_off = 0;
   p.bars_off = p.stages_off + p.stage_bytes * nst;
-  p.items_off = p.bars_off + 8u * (2 * nst + 2 * kNIQ) + 16u;  // + abort flag
-  p.merge_off = (p.items_off + sizeof(ItemDesc) * kNIQ + 15u) & ~15u;
-  p.total = p.merge_off + 4u * ncw * (2 * G + G * D) + 1024u;  // + alignment slack
+  p.items_off = p.bars_off + 8u * (2 * nst + 3 * kNIQ) + 16u;  // + abort flag
+  p.merge_off = (p.items_off + (sizeof(ItemDesc) + 4u) * kNIQ + 15u) & ~15u;
+  p.total = p.merge_off + 4u * ncw * (2 * G + G * D) + 4u * (2 * G + 4) + 1024u;  // + alignment slack
   return p;
 }
 
@@ -192,11 +204,15 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
   uint64_t *empty = full + nst;
   uint64_t *item_full = empty + nst;
   uint64_t *item_empty = item_full + kNIQ;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(item_empty + kNIQ);
+  uint64_t *item_done = item_empty + kNIQ;  // the producer finished the item's page walk
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(item_done + kNIQ);
   ItemDesc *items = reinterpret_cast<ItemDesc *>(smem + sp.items_off);
+  uint32_t *item_status = reinterpret_cast<uint32_t *>(items + kNIQ);  // status bits found by the walk
   float *sm_m = reinterpret_cast<float *>(smem + sp.merge_off);  // [NCW][G]
   float *sm_l = sm_m + kNCW * kG;                                 // [NCW][G]
   float *sm_o = sm_l + kNCW * kG;                                 // [NCW][G][D]
+  float *sm_fin = sm_o + kNCW * kG * kD;                          // [G] (m, l) of the item
+  volatile int *sm_ctl = reinterpret_cast<volatile int *>(sm_fin + 2 * kG);  // [4] broadcast words
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.S, mpp = S / 16;  // 16-token tiles per page
@@ -209,11 +225,13 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     for (int i = 0; i < kNIQ; ++i) {
       mbar_init(&item_full[i], 1);
       mbar_init(&item_empty[i], 1);
+      mbar_init(&item_done[i], 1);
     }
     *abort_flag = 0;
     mbar_init_fence();
   }
   __syncthreads();
+  pdl_wait();  // the plan kernel's outputs (splits, counters, status) are visible from here on
 
   if (warp == kNCW) {
     // ------------------------------------------------------------ producer
@@ -234,8 +252,11 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     int item = 0, item_next = 0;
     if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
     item = __shfl_sync(0xffffffffu, item, 0);
-    int4 info = make_int4(0, 0, 0, 0);
-    if (item < n_items) info = a.chunk_info[item / a.Hkv];
+    int4 info = make_int4(0, 0, 0, 0), info2 = make_int4(0, 0, 0, 0);
+    if (item < n_items) {
+      info = a.chunk_info[2 * (item / a.Hkv)];
+      info2 = a.chunk_info[2 * (item / a.Hkv) + 1];
+    }
     for (uint32_t iq = 0;; ++iq) {
       if (lane == 0) item_next = (int)atomicAdd(&a.hdr->work, 1u);
       const uint32_t slot = iq % kNIQ;
@@ -254,13 +275,16 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       const int b = info.x, p0 = info.y, p1 = info.z, L = info.w;
       if (lane == 0) {
         ItemDesc d;
-        d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.pad = 0;
+        d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = info2.x;
         items[slot] = d;
         mbar_arrive(&item_full[slot]);
       }
       item_next = __shfl_sync(0xffffffffu, item_next, 0);
-      int4 info_next = make_int4(0, 0, 0, 0);
-      if (item_next < n_items) info_next = a.chunk_info[item_next / a.Hkv];  // used by the next iteration
+      int4 info_next = make_int4(0, 0, 0, 0), info2_next = make_int4(0, 0, 0, 0);
+      if (item_next < n_items) {  // used by the next iteration
+        info_next = a.chunk_info[2 * (item_next / a.Hkv)];
+        info2_next = a.chunk_info[2 * (item_next / a.Hkv) + 1];
+      }
       const int *trow = a.block_table + (size_t)b * a.MP;
       const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
       uint32_t st_bits = 0;
@@ -305,10 +329,14 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         if (__any_sync(0xffffffffu, oob)) st_bits |= PFKV_ST_PAGE_OOB;
         if (__any_sync(0xffffffffu, page_tag != want_tag)) st_bits |= PFKV_ST_STALE_TAG;
       }
-      if (lane == 0 && st_bits) atomicOr(&a.status[b], st_bits);
+      if (lane == 0) {
+        item_status[slot] = st_bits;  // read by the consumers when they finish the item
+        mbar_arrive(&item_done[slot]);
+      }
       if (!ok) break;
       item = item_next;
       info = info_next;
+      info2 = info2_next;
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -620,91 +648,104 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         }
       }
       named_bar_sync(1, kNCW * 32);
-      // ---- merge the consumer warps' states, write the item's partial
-      {
-        const int t = threadIdx.x;
-        float ofac = 1.f;
-        if constexpr (kFp8) ofac = (per_token ? 1.f : __ldg(&a.v_scale[d.g])) / C::kPScale;
-        for (int idx = t; idx < kG * kD; idx += kNCW * 32) {
-          const int jh = idx / kD, dd = idx - jh * kD;
-          float M = kNegInf;
+      // ---- merge the consumer warps' states
+      const int t = threadIdx.x;
+      constexpr int kCT = kNCW * 32;
+      if (t == 0) {
+        uint32_t stv = PFKV_ST_TIMEOUT;
+        if (mbar_wait(&item_done[slot], (iq / kNIQ) & 1u, abort_flag)) stv = item_status[slot];
+        sm_ctl[0] = (int)stv;
+      }
+      if (t < kG) {
+        float M = kNegInf;
 #pragma unroll
-          for (int w = 0; w < kNCW; ++w) M = fmaxf(M, sm_m[w * kG + jh]);
+        for (int w = 0; w < kNCW; ++w) M = fmaxf(M, sm_m[w * kG + t]);
+        float ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNCW; ++w) {
+          const float mw = sm_m[w * kG + t];
+          if (mw != kNegInf) ls += sm_l[w * kG + t] * fast_exp2(mw - M);
+        }
+        sm_fin[2 * t] = M;
+        sm_fin[2 * t + 1] = ls;
+      }
+      named_bar_sync(1, kCT);
+      const uint32_t item_st = (uint32_t)sm_ctl[0];
+      float ofac = 1.f;
+      if constexpr (kFp8) ofac = (per_token ? 1.f : __ldg(&a.v_scale[d.g])) / C::kPScale;
+      float *out_bg = a.out + ((size_t)d.b * a.Hq + d.g * kG) * kD;  // rows of this (request, KV head)
+      if (d.nb == 1) {
+        // the item covers the whole request: finish it here
+        for (int idx = t; idx < kG * kD; idx += kCT) {
+          const int jh = idx / kD, dd = idx - jh * kD;
+          const float M = sm_fin[2 * jh];
           float acc = 0.f;
 #pragma unroll
           for (int w = 0; w < kNCW; ++w) {
             const float mw = sm_m[w * kG + jh];
             if (mw != kNegInf) acc += sm_o[(w * kG + jh) * kD + dd] * fast_exp2(mw - M);
           }
-          a.part_o[((size_t)d.cg * a.Hq + d.g * kG + jh) * kD + dd] = acc * ofac;
+          out_bg[idx] = item_st ? 0.f : acc * ofac / sm_fin[2 * jh + 1];
         }
-        if (t < kG) {
-          float M = kNegInf;
-#pragma unroll
-          for (int w = 0; w < kNCW; ++w) M = fmaxf(M, sm_m[w * kG + t]);
-          float ls = 0.f;
+        if (t == 0 && item_st) atomicOr(&a.status[d.b], item_st);
+      } else {
+        for (int idx = t; idx < kG * kD; idx += kCT) {
+          const int jh = idx / kD, dd = idx - jh * kD;
+          const float M = sm_fin[2 * jh];
+          float acc = 0.f;
 #pragma unroll
           for (int w = 0; w < kNCW; ++w) {
-            const float mw = sm_m[w * kG + t];
-            if (mw != kNegInf) ls += sm_l[w * kG + t] * fast_exp2(mw - M);
+            const float mw = sm_m[w * kG + jh];
+            if (mw != kNegInf) acc += sm_o[(w * kG + jh) * kD + dd] * fast_exp2(mw - M);
           }
-          a.part_ml[(size_t)d.cg * a.Hq + d.g * kG + t] = make_float2(M, ls);
+          a.part_o[((size_t)d.cg * a.Hq + d.g * kG) * kD + idx] = acc * ofac;
+        }
+        if (t < kG) a.part_ml[(size_t)d.cg * a.Hq + d.g * kG + t] = make_float2(sm_fin[2 * t], sm_fin[2 * t + 1]);
+        __threadfence();  // this item's partial is visible device-wide before it is counted
+        named_bar_sync(1, kCT);
+        if (t == 0) {
+          if (item_st) atomicOr(&a.status[d.b], item_st);
+          __threadfence();
+          const int done = atomicAdd(&a.counters[(size_t)d.b * a.Hkv + d.g], 1);
+          sm_ctl[1] = (done == d.nb - 1);
+        }
+        named_bar_sync(1, kCT);
+        if (sm_ctl[1]) {
+          // last split of this (request, KV head) to finish: merge them all.
+          // Other CTAs wrote the partials, so read them from L2 (.cg).
+          __threadfence();
+          const uint32_t stb = __ldcg(&a.status[d.b]);
+          const int c0 = d.cg - (int)__ldg(&a.chunk_info[2 * d.cg + 1].y);  // first split of the request
+          for (int idx4 = t; idx4 < kG * kD / 4; idx4 += kCT) {
+            const int jh = (idx4 * 4) / kD;
+            const size_t col = (size_t)(d.g * kG + jh);
+            float M = kNegInf;
+            for (int c = 0; c < d.nb; ++c) M = fmaxf(M, __ldcg(&a.part_ml[(size_t)(c0 + c) * a.Hq + col]).x);
+            float W = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int c = 0; c < d.nb; ++c) {
+              const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + c) * a.Hq + col]);
+              const float w = fast_exp2(ml.x - M);
+              const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                  a.part_o + ((size_t)(c0 + c) * a.Hq + d.g * kG) * kD) + idx4);
+              W += ml.y * w;
+              acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+            }
+            const float inv = stb ? 0.f : 1.f / W;
+            reinterpret_cast<float4 *>(out_bg)[idx4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          }
         }
       }
-      named_bar_sync(1, kNCW * 32);
+      named_bar_sync(1, kCT);
       if (threadIdx.x == 0) mbar_arrive(&item_empty[slot]);
       if (!alive) break;
     }
   }
-  // a wait gave up somewhere in this block: the merge reports PFKV_ST_TIMEOUT
-  if (lane == 0 && *abort_flag) atomicOr(&a.hdr->err, 1u);
-}
-
-// ---------------------------------------------------------------- merge
-
-template <int kD>
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
-  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (wg >= a.B * a.Hq) return;
-  const int b = wg / a.Hq, h = wg - b * a.Hq;
-  float *dst = a.out + (size_t)wg * kD;
-  const bool err = a.hdr->err != 0u;
-  const uint32_t st = a.status[b];
-  const int c0 = a.chunk_start[b], n = a.chunk_start[b + 1] - c0;
-  const int dd = lane * 4;  // this lane's four output dims (kD <= 128)
-  if (err && h == 0 && lane == 0) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
-  if (st != 0u || err || n <= 0) {
-    if (dd < kD) *reinterpret_cast<float4 *>(dst + dd) = make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
-  }
-  const float2 *ml = a.part_ml + (size_t)c0 * a.Hq + h;
-  float M = kNegInf;
-  for (int c = lane; c < n; c += 32) M = fmaxf(M, ml[(size_t)c * a.Hq].x);
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float W = 0.f;
-  for (int c = lane; c < n; c += 32) {
-    const float2 v = ml[(size_t)c * a.Hq];
-    W += v.y * fast_exp2(v.x - M);
-  }
-  for (int off = 16; off; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
-  const float *po = a.part_o + ((size_t)c0 * a.Hq + h) * kD + dd;
-  const size_t cstride = (size_t)a.Hq * kD;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int cb = 0; cb < n; cb += 32) {
-    // lane j holds the weight of chunk cb + j; the loop broadcasts it
-    const float wl = (cb + lane < n) ? fast_exp2(ml[(size_t)(cb + lane) * a.Hq].x - M) : 0.f;
-    const int nn = min(32, n - cb);
-#pragma unroll 4
-    for (int j = 0; j < nn; ++j) {
-      const float w = __shfl_sync(0xffffffffu, wl, j);
-      if (dd < kD) {
-        const float4 v = *reinterpret_cast<const float4 *>(po + (size_t)(cb + j) * cstride);
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-      }
-    }
-  }
-  const float inv = 1.f / W;
-  if (dd < kD) *reinterpret_cast<float4 *>(dst + dd) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  // A wait gave up somewhere in this block: every request of the call is
+  // reported as timed out (its output is not valid).
+  if (lane == 0 && *abort_flag)
+    for (int b = 0; b < a.B; ++b) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
 }
 
 // ---------------------------------------------------------------- host side
@@ -795,11 +836,19 @@ int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const 
   plan_kernel<<<1, 1024, 0, s>>>(a, sh.grid * 8, (1024 + a.S - 1) / a.S);
   int rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
   if (rc) return rc;
-  kern<<<sh.grid, C::kThreads, sh.smem, s>>>(mk, mv, a, sh.nst);
-  rc = cuda_ok(cudaGetLastError(), "split kernel launch");
-  if (rc) return rc;
-  merge_kernel<kD><<<(a.B * a.Hq + 3) / 4, 128, 0, s>>>(a);
-  return cuda_ok(cudaGetLastError(), "merge kernel launch");
+  // The split kernel may start while the plan kernel runs; it waits for the
+  // plan's results (griddepcontrol.wait) before it reads them.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sh.grid);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = sh.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cuda_ok(cudaLaunchKernelEx(&cfg, kern, mk, mv, a, sh.nst), "split kernel launch");
 }
 
 template <bool kFp8, int kD>

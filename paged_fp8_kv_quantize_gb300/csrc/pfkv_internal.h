@@ -22,7 +22,7 @@ struct WsHeader {
 
 // Decode workspace carve-up.
 struct WsLayout {
-  size_t hdr, chunk_start, ppc, chunk_info, part_ml, part_o, total;
+  size_t hdr, chunk_start, ppc, chunk_info, counters, part_ml, part_o, total;
 };
 WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits);
 
@@ -44,7 +44,8 @@ struct DecodeArgs {
   // workspace and outputs
   WsHeader *hdr;
   int *chunk_start, *ppc;
-  int4 *chunk_info;  // per split: {request, first page, end page, length}
+  int4 *chunk_info;  // per split, two int4: {request, first page, end page, length}, {splits of the request, 0, 0, 0}
+  int *counters;     // per (request, KV head): splits finished in this call
   float2 *part_ml;
   float *part_o;
   float *out;
