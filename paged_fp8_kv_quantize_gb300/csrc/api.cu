@@ -42,11 +42,10 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
   WsLayout w;
   const size_t slots = (size_t)batch * max_splits * q_heads;
   w.hdr = 0;
-  w.chunk_start = up256(sizeof(WsHeader));
-  w.ppc = w.chunk_start + up256(sizeof(int) * ((size_t)batch + 1));
-  w.chunk_info = w.ppc + up256(sizeof(int) * (size_t)batch);
-  w.counters = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
-  w.part_ml = w.counters + up256(sizeof(int) * (size_t)batch * q_heads);
+  w.split_first = up256(sizeof(WsHeader));
+  w.split_count = w.split_first + up256(sizeof(int) * ((size_t)batch + 1));
+  w.chunk_info = w.split_count + up256(sizeof(int) * (size_t)batch);
+  w.part_ml = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
   w.part_o = w.part_ml + up256(sizeof(float2) * slots);
   w.total = w.part_o + up256(sizeof(float) * slots * v_dim);
   return w;
@@ -112,10 +111,9 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.flags = flags; a.max_splits = max_splits;
   uint8_t *w = static_cast<uint8_t *>(ws);
   a.hdr = reinterpret_cast<WsHeader *>(w + L.hdr);
-  a.chunk_start = reinterpret_cast<int *>(w + L.chunk_start);
-  a.ppc = reinterpret_cast<int *>(w + L.ppc);
+  a.split_first = reinterpret_cast<int *>(w + L.split_first);
+  a.split_count = reinterpret_cast<int *>(w + L.split_count);
   a.chunk_info = reinterpret_cast<int4 *>(w + L.chunk_info);
-  a.counters = reinterpret_cast<int *>(w + L.counters);
   a.part_ml = reinterpret_cast<float2 *>(w + L.part_ml);
   a.part_o = reinterpret_cast<float *>(w + L.part_o);
   a.out = out; a.status = status;

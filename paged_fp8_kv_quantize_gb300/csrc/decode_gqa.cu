@@ -23,13 +23,15 @@
 //                tiles: e4m3 -> f16 in registers (exact), QK^T and PV on
 //                register-operand tensor-core MMA, online softmax in fp32.
 //                An item that covers a whole request writes its output
-//                directly.  Otherwise it leaves an unnormalised partial
-//                (m, l, O); the last CTA to finish a (request, KV head) --
-//                found with an arrive-only counter, no waiting -- merges the
-//                partials with the log-sum-exp rule.  A request with any
-//                status bit gets zero output.  The split kernel is launched
-//                as a programmatic dependent of the plan kernel, so its
-//                prologue overlaps the plan.
+//                directly; otherwise it leaves an unnormalised partial
+//                (m, l, O).
+//   3. merge  -- one CTA per (request, KV head) with more than one split:
+//                log-sum-exp merge of the partials, split weights staged in
+//                shared memory and splits spread over thread groups.
+//   A request with any status bit gets zero output.  The split and merge
+//   kernels are programmatic dependents of the kernel before them, so their
+//   launch and prologue overlap it.  Splits are ordered longest request
+//   first, which balances the dynamic schedule.
 #include <math.h>
 
 #include <mutex>
@@ -52,15 +54,22 @@ struct ItemDesc {
 
 // ---------------------------------------------------------------- plan
 
+constexpr int kSortMax = 2048;  // requests ordered by length when the batch is at most this
+
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
   pdl_launch_dependents();  // the split kernel waits for this grid's results before reading them
   __shared__ long long s_red[32];
   __shared__ int s_scan[32];
   __shared__ int s_carry;
+  __shared__ int s_order[kSortMax];  // position -> request, longest first
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int S = a.S;
   const long long max_len = (long long)a.MP * S;
-  // total pages (for the split size)
+  auto pages_of = [&](int b) -> int {
+    const int L = a.seq_lens[b];
+    return (L < 1 || (long long)L > max_len) ? 0 : (L + S - 1) / S;
+  };
+  // status (bad lengths) and total pages, which sets the split size
   long long tot = 0;
   for (int b = tid; b < a.B; b += blockDim.x) {
     const int L = a.seq_lens[b];
@@ -80,22 +89,32 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
   const long long total_units = s_red[0] * a.Hkv;
   long long cp = (total_units + target_items - 1) / target_items;
   if (cp < min_chunk_pages) cp = min_chunk_pages;
+  const bool sorted = a.B <= kSortMax;
+  if (sorted)  // rank by (pages descending, index ascending)
+    for (int b = tid; b < a.B; b += blockDim.x) {
+      const int pb = pages_of(b);
+      int rank = 0;
+      for (int o = 0; o < a.B; ++o) {
+        const int po = pages_of(o);
+        rank += (po > pb) || (po == pb && o < b);
+      }
+      s_order[rank] = b;
+    }
   if (tid == 0) s_carry = 0;
   __syncthreads();
-  // chunk counts and exclusive prefix, 1024 requests per pass
+  // split counts and their exclusive prefix in processing order, 1024 per pass
   for (int base = 0; base < a.B; base += blockDim.x) {
-    const int b = base + tid;
-    int n = 0, ppc = 0;
-    if (b < a.B) {
-      const int L = a.seq_lens[b];
-      if (L >= 1 && (long long)L <= max_len) {
-        const long long pages = (L + S - 1) / S;
+    const int r = base + tid;
+    const int b = r < a.B ? (sorted ? s_order[r] : r) : -1;
+    int n = 0, ppc = 0, pages = 0;
+    if (b >= 0) {
+      pages = pages_of(b);
+      if (pages) {
         long long nn = (pages + cp - 1) / cp;
         if (nn > a.max_splits) nn = a.max_splits;
         ppc = (int)((pages + nn - 1) / nn);
-        n = (int)((pages + ppc - 1) / ppc);
+        n = (pages + ppc - 1) / ppc;
       }
-      a.ppc[b] = ppc;
     }
     int x = n;
     for (int o = 1; o < 32; o <<= 1) {
@@ -115,16 +134,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
     __syncthreads();
     const int warp_off = wid ? s_scan[wid - 1] : 0;
     const int excl = s_carry + warp_off + x - n;
-    if (b < a.B) {
-      a.chunk_start[b] = excl;
+    if (b >= 0) {
+      a.split_first[b] = excl;
+      a.split_count[b] = n;
       const int L = a.seq_lens[b];
-      const int pages = n ? (L + S - 1) / S : 0;
       for (int c = 0; c < n; ++c) {
         a.chunk_info[2 * (excl + c)] = make_int4(b, c * ppc, min((c + 1) * ppc, pages), L);
         a.chunk_info[2 * (excl + c) + 1] = make_int4(n, c, 0, 0);
       }
-      for (int g = 0; g < a.Hkv; ++g) a.counters[(size_t)b * a.Hkv + g] = 0;
-      if (n == 0)  // bad length: no split will write this request's rows
+      if (n == 0)  // bad length: no split writes this request's rows
         for (size_t k = 0; k < (size_t)a.Hq * a.Dv; ++k) a.out[(size_t)b * a.Hq * a.Dv + k] = 0.f;
     }
     __syncthreads();
@@ -132,7 +150,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
     __syncthreads();
   }
   if (tid == 0) {
-    a.chunk_start[a.B] = s_carry;
     a.hdr->n_chunks = s_carry;
     a.hdr->n_items = s_carry * a.Hkv;
     a.hdr->work = 0u;
@@ -231,7 +248,8 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     mbar_init_fence();
   }
   __syncthreads();
-  pdl_wait();  // the plan kernel's outputs (splits, counters, status) are visible from here on
+  pdl_wait();  // the plan kernel's outputs (splits, status) are visible from here on
+  pdl_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to finish
 
   if (warp == kNCW) {
     // ------------------------------------------------------------ producer
@@ -701,41 +719,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           a.part_o[((size_t)d.cg * a.Hq + d.g * kG) * kD + idx] = acc * ofac;
         }
         if (t < kG) a.part_ml[(size_t)d.cg * a.Hq + d.g * kG + t] = make_float2(sm_fin[2 * t], sm_fin[2 * t + 1]);
-        __threadfence();  // this item's partial is visible device-wide before it is counted
-        named_bar_sync(1, kCT);
-        if (t == 0) {
-          if (item_st) atomicOr(&a.status[d.b], item_st);
-          __threadfence();
-          const int done = atomicAdd(&a.counters[(size_t)d.b * a.Hkv + d.g], 1);
-          sm_ctl[1] = (done == d.nb - 1);
-        }
-        named_bar_sync(1, kCT);
-        if (sm_ctl[1]) {
-          // last split of this (request, KV head) to finish: merge them all.
-          // Other CTAs wrote the partials, so read them from L2 (.cg).
-          __threadfence();
-          const uint32_t stb = __ldcg(&a.status[d.b]);
-          const int c0 = d.cg - (int)__ldg(&a.chunk_info[2 * d.cg + 1].y);  // first split of the request
-          for (int idx4 = t; idx4 < kG * kD / 4; idx4 += kCT) {
-            const int jh = (idx4 * 4) / kD;
-            const size_t col = (size_t)(d.g * kG + jh);
-            float M = kNegInf;
-            for (int c = 0; c < d.nb; ++c) M = fmaxf(M, __ldcg(&a.part_ml[(size_t)(c0 + c) * a.Hq + col]).x);
-            float W = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int c = 0; c < d.nb; ++c) {
-              const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + c) * a.Hq + col]);
-              const float w = fast_exp2(ml.x - M);
-              const float4 v = __ldcg(reinterpret_cast<const float4 *>(
-                  a.part_o + ((size_t)(c0 + c) * a.Hq + d.g * kG) * kD) + idx4);
-              W += ml.y * w;
-              acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-            }
-            const float inv = stb ? 0.f : 1.f / W;
-            reinterpret_cast<float4 *>(out_bg)[idx4] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-          }
-        }
+        if (t == 0 && item_st) atomicOr(&a.status[d.b], item_st);
       }
       named_bar_sync(1, kCT);
       if (threadIdx.x == 0) mbar_arrive(&item_empty[slot]);
@@ -746,6 +730,73 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
   // reported as timed out (its output is not valid).
   if (lane == 0 && *abort_flag)
     for (int b = 0; b < a.B; ++b) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- merge
+
+template <int kD, int kG>
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
+  __shared__ float s_w[256 * kG];  // per (split, head): m, then the split's weight
+  __shared__ float s_l[256 * kG];
+  __shared__ float s_M[kG], s_W[kG];
+  __shared__ float4 s_acc[256];
+  pdl_wait();  // partials and status of the split kernel are visible from here on
+  const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
+  const int nb = a.split_count[b];
+  if (nb <= 1) return;  // finished by the split kernel (or zeroed by the plan kernel)
+  const int t = threadIdx.x, c0 = a.split_first[b];
+  float *out_bg = a.out + ((size_t)b * a.Hq + g * kG) * kD;
+  if (__ldcg(&a.status[b]) != 0u) {
+    for (int i = t; i < kG * kD; i += 256) out_bg[i] = 0.f;
+    return;
+  }
+  for (int i = t; i < nb * kG; i += 256) {
+    const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / kG) * a.Hq + g * kG + i % kG]);
+    s_w[i] = ml.x;
+    s_l[i] = ml.y;
+  }
+  __syncthreads();
+  const int warp = t >> 5, lane = t & 31;
+  if (warp < kG) {
+    float M = -INFINITY;
+    for (int c = lane; c < nb; c += 32) M = fmaxf(M, s_w[c * kG + warp]);
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float W = 0.f;
+    for (int c = lane; c < nb; c += 32) W += s_l[c * kG + warp] * fast_exp2(s_w[c * kG + warp] - M);
+    for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    if (lane == 0) {
+      s_M[warp] = M;
+      s_W[warp] = W;
+    }
+  }
+  __syncthreads();
+  for (int i = t; i < nb * kG; i += 256) s_w[i] = fast_exp2(s_w[i] - s_M[i % kG]);
+  __syncthreads();
+  // thread = (float4 column, group of splits)
+  constexpr int kCols = kG * kD / 4;
+  constexpr int kGroups = kCols >= 256 ? 1 : 256 / kCols;
+  const int col = t % kCols, grp = t / kCols, jh = (col * 4) / kD;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (grp < kGroups) {
+    const float4 *po = reinterpret_cast<const float4 *>(a.part_o + ((size_t)c0 * a.Hq + g * kG) * kD) + col;
+    const size_t cstride = (size_t)a.Hq * kD / 4;
+#pragma unroll 8
+    for (int c = grp; c < nb; c += kGroups) {
+      const float w = s_w[c * kG + jh];
+      const float4 v = __ldcg(po + (size_t)c * cstride);
+      acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    }
+  }
+  s_acc[t] = acc;
+  __syncthreads();
+  if (t < kCols) {
+    for (int k = 1; k < kGroups; ++k) {
+      const float4 v = s_acc[t + k * kCols];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const float inv = 1.f / s_W[jh];
+    reinterpret_cast<float4 *>(out_bg)[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -838,17 +889,25 @@ int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const 
   if (rc) return rc;
   // The split kernel may start while the plan kernel runs; it waits for the
   // plan's results (griddepcontrol.wait) before it reads them.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.grid);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = sh.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&cfg, kern, mk, mv, a, sh.nst), "split kernel launch");
+  rc = cuda_ok(cudaLaunchKernelEx(&cfg, kern, mk, mv, a, sh.nst), "split kernel launch");
+  if (rc) return rc;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(a.B * a.Hkv);
+  mcfg.blockDim = dim3(256);
+  mcfg.stream = s;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
+  return cuda_ok(cudaLaunchKernelEx(&mcfg, merge_kernel<kD, kG>, a), "merge kernel launch");
 }
 
 template <bool kFp8, int kD>

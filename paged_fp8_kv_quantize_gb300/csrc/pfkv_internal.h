@@ -22,7 +22,7 @@ struct WsHeader {
 
 // Decode workspace carve-up.
 struct WsLayout {
-  size_t hdr, chunk_start, ppc, chunk_info, counters, part_ml, part_o, total;
+  size_t hdr, split_first, split_count, chunk_info, part_ml, part_o, total;
 };
 WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits);
 
@@ -43,9 +43,8 @@ struct DecodeArgs {
   int max_splits;
   // workspace and outputs
   WsHeader *hdr;
-  int *chunk_start, *ppc;
+  int *split_first, *split_count;  // per request: index of its first split, number of splits
   int4 *chunk_info;  // per split, two int4: {request, first page, end page, length}, {splits of the request, 0, 0, 0}
-  int *counters;     // per (request, KV head): splits finished in this call
   float2 *part_ml;
   float *part_o;
   float *out;

@@ -35,7 +35,7 @@ def test_host_only_entry_points():
     d = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, 16)
     n = abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 64)
     # header + plan + split descriptors + (m, l) and O partials for every (request, split, head)
-    fixed = 64 * 64 * 32 * (8 + 4 * 128) + 64 * 64 * 32 + 64 * 32 * 4
+    fixed = 64 * 64 * 32 * (8 + 4 * 128) + 64 * 64 * 32
     assert fixed <= n < fixed + 64 * 1024
 
 
