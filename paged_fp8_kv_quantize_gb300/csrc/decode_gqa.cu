@@ -62,10 +62,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
   __shared__ int s_scan[32];
   __shared__ int s_carry;
   __shared__ int s_order[kSortMax];  // position -> request, longest first
+  __shared__ int s_pages[kSortMax];  // request -> pages (0 for a bad length)
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int S = a.S;
   const long long max_len = (long long)a.MP * S;
+  const bool sorted = a.B <= kSortMax;
   auto pages_of = [&](int b) -> int {
+    if (sorted) return s_pages[b];
     const int L = a.seq_lens[b];
     return (L < 1 || (long long)L > max_len) ? 0 : (L + S - 1) / S;
   };
@@ -76,6 +79,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
     const bool bad = L < 1 || (long long)L > max_len;
     a.status[b] = bad ? PFKV_ST_BAD_LEN : 0u;
     if (!bad) tot += (L + S - 1) / S;
+    if (sorted) s_pages[b] = bad ? 0 : (L + S - 1) / S;
   }
   for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   if (lane == 0) s_red[wid] = tot;
@@ -89,7 +93,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
   const long long total_units = s_red[0] * a.Hkv;
   long long cp = (total_units + target_items - 1) / target_items;
   if (cp < min_chunk_pages) cp = min_chunk_pages;
-  const bool sorted = a.B <= kSortMax;
   if (sorted)  // rank by (pages descending, index ascending)
     for (int b = tid; b < a.B; b += blockDim.x) {
       const int pb = pages_of(b);
