@@ -126,6 +126,22 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def global_max(value, dist=None, device="cpu"):
+    """Max of a per-rank float over all ranks (the job's time is its slowest rank)."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, max_ms):
+    """Whole-job rate: every rank runs the same replica, timed by the slowest."""
+    return world * units_per_rank / (max_ms * 1e-3)
+
+
 def recorded_traffic():
     """DRAM bytes per launch of the split kernel from the committed ncu record,
     or None when the kernel sources changed since the counters were taken."""
@@ -318,12 +334,7 @@ def main():
             g.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return global_max(e0.elapsed_time(e1), dist, dev)
 
     K = args.steps
     fp8 = caches["fp8"]
@@ -339,7 +350,7 @@ def main():
         ms_step = time_graph(g_step)
     ms_per_step = ms_step / K
     step_bytes = [decode_alg_bytes(lens0 + j % T + 1, Hkv, D, S, Hq, D) + append_alg_bytes(B, Hkv, D) for j in range(K)]
-    value = world * sum(step_bytes) / (ms_step * 1e-3) / 1e9
+    value = job_throughput(sum(step_bytes), world, ms_step) / 1e9
     dec_bytes = [decode_alg_bytes(lens0 + j % T + 1, Hkv, D, S, Hq, D) for j in range(K)]
 
     # ---- dominant kernel group: decode alone (plan + split + merge), same stream
@@ -411,7 +422,7 @@ def main():
     g_e2e = capture(e2e_step, K)
     g_e2e.replay()
     ms_e2e = time_graph(g_e2e)
-    e2e_val = world * sum(step_bytes) / (ms_e2e * 1e-3) / 1e9
+    e2e_val = job_throughput(sum(step_bytes), world, ms_e2e) / 1e9
     h2d = h_q[0].numel() * 2 + h_k[0].numel() * 2 + h_v[0].numel() * 2 + 2 * B * 4
     d2h = h_out.numel() * 4 + B * 4
 

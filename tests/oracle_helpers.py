@@ -57,3 +57,28 @@ def dense_reference(c: oracle.Cache, q_bits, seq_lens, block_table, tau):
             scale=tau, enable_gqa=True)
         out[b] = o.reshape(Hq, c.Dv).numpy()
     return out
+
+
+def oracle_cache_subset(w: synth.Workload, idx, dtype=oracle.DTYPE_FP8, scales=None):
+    """Oracle cache holding only requests `idx`, page ids renumbered densely.
+
+    Per-head scales are calibrated over ALL of the workload's rows (as the GPU
+    path does) unless given.  Returns (cache, table, tags, used_pages) where
+    used_pages[k] is the workload's page id stored at compact page k."""
+    idx = np.asarray(idx)
+    tab = w.block_table[idx]
+    used = np.unique(tab[tab >= 0])
+    remap = np.full(w.num_pages, -1, dtype=np.int64)
+    remap[used] = np.arange(used.size)
+    ctab = np.where(tab >= 0, remap[np.maximum(tab, 0)], -1).astype(np.int32)
+    ks = vs = None
+    if dtype == oracle.DTYPE_FP8 and w.scale_mode == synth.PER_HEAD:
+        ks, vs = scales if scales is not None else (oracle.calibrate_per_head(w.k_rows),
+                                                    None if w.kv_shared else oracle.calibrate_per_head(w.v_rows))
+    c = oracle.Cache(used.size, w.page_size, w.kv_heads, w.head_dim, w.v_head_dim, w.kv_shared, dtype,
+                     w.scale_mode if dtype == oracle.DTYPE_FP8 else synth.PER_HEAD, w.page_tags[used], ks, vs)
+    sel = np.isin(w.row_req, idx)
+    rr = np.searchsorted(idx, w.row_req[sel]).astype(np.int32)
+    c.append(w.k_rows[sel], None if w.kv_shared else w.v_rows[sel], w.row_pos[sel], ctab, w.block_tags[idx],
+             row_req=rr, batch=idx.size)
+    return c, ctab, w.block_tags[idx].copy(), used
