@@ -194,6 +194,26 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// D = A*B + D, m16n8k32, e4m3 operands (A 16x32 row-major, B 32x8), fp32 accum.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Value of the e4m3 code in the low byte (exact, via f16).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  const uint32_t h = e4m3x2_to_f16x2(code & 0xffu);
+  return __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+}
+
 // 8x8 16-bit transpose across the warp: in, thread t holds row t/4, columns
 // 2(t%4), 2(t%4)+1; out, the same positions of the transposed matrix.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
