@@ -155,16 +155,16 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   }
   __syncthreads();
   const int warp = t >> 5, lane = t & 31;
-  if (warp < kG) {
+  for (int hh = warp; hh < kG; hh += 8) {  // 8 warps cover the group's heads
     float M = -INFINITY;
-    for (int c = lane; c < nb; c += 32) M = fmaxf(M, s_w[c * kG + warp]);
+    for (int c = lane; c < nb; c += 32) M = fmaxf(M, s_w[c * kG + hh]);
     for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float W = 0.f;
-    for (int c = lane; c < nb; c += 32) W += s_l[c * kG + warp] * fast_exp2(s_w[c * kG + warp] - M);
+    for (int c = lane; c < nb; c += 32) W += s_l[c * kG + hh] * fast_exp2(s_w[c * kG + hh] - M);
     for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
     if (lane == 0) {
-      s_M[warp] = M;
-      s_W[warp] = W;
+      s_M[hh] = M;
+      s_W[hh] = W;
     }
   }
   __syncthreads();
