@@ -235,6 +235,45 @@ def run_reference(args, w):
 # ---------------------------------------------------------------- GPU leg
 
 
+def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
+    """Tag-checked decode over the latent-shared workload (64 requests,
+    lengths U[4096, 32768], 576-wide stream, per-token scales, page 64)."""
+    import torch
+
+    B, S = wl.batch, wl.page_size
+    cache = abi.PagedCache(wl.num_pages, S, 1, wl.head_dim, wl.v_head_dim, True, abi.DTYPE_FP8_E4M3,
+                           abi.SCALE_PER_TOKEN, device=dev, fill=0)
+    cache.page_tags.copy_(i32(wl.page_tags))
+    table, tags, lens = i32(wl.block_table), i32(wl.block_tags), i32(wl.seq_lens)
+    k = bf16(wl.k_rows)
+    abi.kv_append_quantize(cache, k, None, i32(wl.row_pos), table, tags, row_req=i32(wl.row_req), batch=B)
+    del k
+    q = bf16(wl.q)
+    ws = torch.empty(abi.decode_workspace_bytes(cache, B, wl.q_heads, wl.max_splits), dtype=torch.uint8, device=dev)
+    out = torch.empty(B, wl.q_heads, wl.v_head_dim, dtype=torch.float32, device=dev)
+    st = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def call(_):
+        abi.paged_decode_attention_fp8(cache, q, lens, table, tags, wl.softmax_scale, flags=abi.FLAG_TAG_CHECK,
+                                       max_splits=wl.max_splits, workspace=ws, out=out, status=st)
+
+    for _ in range(3):
+        call(0)
+    g = capture(call, n_calls)
+    g.replay()
+    ms = time_graph(g) / n_calls
+    tokens = int(wl.seq_lens.astype(np.int64).sum())
+    pages = int(((wl.seq_lens.astype(np.int64) + S - 1) // S).sum())
+    nbytes = tokens * (wl.head_dim + 4) + pages * 12 + q.numel() * 2 + out.numel() * 4
+    flops = tokens * wl.q_heads * (wl.head_dim + wl.v_head_dim) * 2
+    return {"workload": "latent-shared stream: batch 64, lengths U[4096, 32768], 64 q heads over one 576-wide "
+                        "FP8 stream (V = first 512), per-token scales, page 64, tag check on",
+            "us_per_call": ms * 1e3, "kv_gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak,
+            "tflops": flops / (ms * 1e-3) / 1e12, "context_tokens": tokens, "alg_bytes_per_call": nbytes,
+            "decode_tokens_per_s": B / (ms * 1e-3), "aborted_requests": int((st.cpu().numpy() != 0).sum())}
+
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -244,6 +283,7 @@ def main():
     ap.add_argument("--cpu-frac", type=float, default=0.5, help="share of context tokens in the CPU sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-variants", action="store_true", help="skip the BF16 / tag-off comparisons")
+    ap.add_argument("--no-latent", action="store_true", help="skip the latent-stream measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -394,6 +434,13 @@ def main():
         extra["bf16_cache"] = {"us_per_decode": ms_bf * 1e3, "kv_gbs": bf_bytes / (ms_bf * 1e-3) / 1e9,
                                "hbm_frac": bf_bytes / (ms_bf * 1e-3) / 1e9 / peak,
                                "fp8_speedup_per_call": ms_bf / ms_dec}
+
+    # ---- latent-shared stream (64 heads over one 576-wide FP8 stream, batch 64)
+    if not args.no_latent:
+        del caches
+        torch.cuda.empty_cache()
+        extra["latent"] = bench_latent(abi, synth.latent(), dev, i32, bf16, capture, time_graph, peak,
+                                       max(3, K // 5))
 
     # ---- end to end: per-step inputs from pinned host memory, results back to host
     h_q = torch.from_numpy(np.ascontiguousarray(w.q_steps).view(np.int16)).view(torch.bfloat16).pin_memory()
