@@ -461,16 +461,20 @@ __global__ void __launch_bounds__(kLThreads, 1) latent_split_kernel(const Decode
       if (d.nb == 1) {
         float *o0 = a.out + ((size_t)d.b * a.Hq + h0) * kLDv + dbase;
         float *o1 = o0 + 8 * kLDv;
-        const float g0 = item_st ? 0.f : f0 / L0, g1 = item_st ? 0.f : f1 / L1;
+        // an aborted request's rows are zero, whatever the never-fetched pages held
+        const float g0 = f0 / L0, g1 = f1 / L1;
+        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < 2; ++e)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int nt = 4 * q4;
             *reinterpret_cast<float4 *>(o0 + 16 * e + nt) =
-                make_float4(o[nt][e] * g0, o[nt + 1][e] * g0, o[nt + 2][e] * g0, o[nt + 3][e] * g0);
+                item_st ? zero4 : make_float4(o[nt][e] * g0, o[nt + 1][e] * g0, o[nt + 2][e] * g0, o[nt + 3][e] * g0);
             *reinterpret_cast<float4 *>(o1 + 16 * e + nt) =
-                make_float4(o[nt][2 + e] * g1, o[nt + 1][2 + e] * g1, o[nt + 2][2 + e] * g1, o[nt + 3][2 + e] * g1);
+                item_st ? zero4
+                        : make_float4(o[nt][2 + e] * g1, o[nt + 1][2 + e] * g1, o[nt + 2][2 + e] * g1,
+                                      o[nt + 3][2 + e] * g1);
           }
         if (t == 0 && item_st) atomicOr(&a.status[d.b], item_st);
       } else {
