@@ -90,7 +90,7 @@ __device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t 
   o[3] = prmt(t1, t3, 0x7632u);
 }
 
-__global__ void __launch_bounds__(kLThreads, 1) latent_split_kernel(const DecodeArgs a, const int nst) {
+__global__ void __launch_bounds__(kLThreads, 2) latent_split_kernel(const DecodeArgs a, const int nst) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const LatSmem sp = lat_smem(nst);
@@ -309,16 +309,24 @@ __global__ void __launch_bounds__(kLThreads, 1) latent_split_kernel(const Decode
         const uint32_t scl = kst + kPageBytes + (uint32_t)((warp & 1) * 32) * 4;
         float z[4][4], zv[4][4];
         float mz0 = kNegInf, mz1 = kNegInf, mzv0 = kNegInf, mzv1 = kNegInf;
+        float tsc[4][2], tlg[4][2];  // this thread's 8 tokens: scale and its log2
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint2 v = live ? lds64(scl + 4 * (8 * j + 2 * tq)) : make_uint2(0x3f800000u, 0x3f800000u);
+          tsc[j][0] = __uint_as_float(v.x);
+          tsc[j][1] = __uint_as_float(v.y);
+          tlg[j][0] = fast_log2(tsc[j][0]);
+          tlg[j][1] = fast_log2(tsc[j][1]);
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int tk = 8 * j + 2 * tq + (c & 1);
             const bool ok_tok = live && tok0 + tk < d.L;
-            const float sc = ok_tok ? lds_f32(scl + 4 * tk) : 1.f;
-            const float zz = ok_tok ? acc[j][c] * ((c < 2) ? rs0 : rs1) * sc : kNegInf;
+            const float zz = ok_tok ? acc[j][c] * ((c < 2) ? rs0 : rs1) * tsc[j][c & 1] : kNegInf;
             z[j][c] = zz;
-            zv[j][c] = ok_tok ? zz + fast_log2(sc) : kNegInf;
+            zv[j][c] = ok_tok ? zz + tlg[j][c & 1] : kNegInf;
             if (c < 2) { mz0 = fmaxf(mz0, zz); mzv0 = fmaxf(mzv0, zv[j][c]); }
             else { mz1 = fmaxf(mz1, zz); mzv1 = fmaxf(mzv1, zv[j][c]); }
           }
@@ -512,7 +520,7 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   DecodeArgs a = a0;
   a.Hkv = kLGroups;
   a.G = kLHG;
-  static int nst = 4;
+  static int nst = 2;  // one pair of pages: two CTAs share an SM and hide each other's copies
   static uint32_t smem = 0;
   static int grid = 0;
   static std::mutex mu;
