@@ -283,11 +283,9 @@ __global__ void __launch_bounds__(kLThreads, 2) latent_split_kernel(const Decode
         const bool live = (kpage == 0 || has2) && tok0 < d.L;
         const uint32_t kst = s_base + stg[kpage] * kStageBytes;
         const uint32_t krow = kst + (uint32_t)((warp & 1) * 32) * kLD;
-        float acc[4][4], acc1[4][4], acc2[4][4];  // one accumulator per query term: shorter MMA chains
+        float acc[4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[j][c] = acc1[j][c] = acc2[j][c] = 0.f;
+        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
         if (live) {
 #pragma unroll 1
           for (int s2 = 0; s2 < kDSteps / 2; ++s2) {
@@ -302,17 +300,11 @@ __global__ void __launch_bounds__(kLThreads, 2) latent_split_kernel(const Decode
                 const uint4 av = lds128(q_base + (uint32_t)(((i * kDSteps + s) * 32 + lane) * 16));
                 const uint32_t af[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  mma_e4m3(i == 0 ? acc[j] : (i == 1 ? acc1[j] : acc2[j]), af, h2 ? kb[j].z : kb[j].x,
-                           h2 ? kb[j].w : kb[j].y);
+                for (int j = 0; j < 4; ++j) mma_e4m3(acc[j], af, h2 ? kb[j].z : kb[j].x, h2 ? kb[j].w : kb[j].y);
               }
             }
           }
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[j][c] += acc1[j][c] + acc2[j][c];
         // ---- scores (log2 domain); value weights carry log2 of the token scale
         const uint32_t scl = kst + kPageBytes + (uint32_t)((warp & 1) * 32) * 4;
         float z[4][4], zv[4][4];
