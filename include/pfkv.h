@@ -212,6 +212,24 @@ int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, const void 
                                             uint32_t *status, void *stream);
 
 /*
+ * handoff_bf16_to_fp8 -- quantize whole pages of a BF16 cache into an FP8
+ * cache ("Quantizing the KV cache": prefill keeps BF16 because it is
+ * compute-bound, the decode pool stores FP8 e4m3; a request moving between
+ * the two has its pages converted).
+ *   src : BF16 cache; dst : FP8 cache with the same num_kv_heads, page_size,
+ *         head_dim, v_head_dim and kv_shared.
+ *   src_pages, dst_pages : int32 [n_pages]; page src_pages[i] of src becomes
+ *         page dst_pages[i] of dst (every head, every slot, K and V).
+ *   page_status : uint32 [n_pages]; PFKV_ST_PAGE_OOB when either id is outside
+ *         its pool (that pair is skipped), else 0.
+ * Codes as in kv_append_quantize: e4m3(fp32(x)/s), s = dst's per-head scale,
+ * or (PER_TOKEN) amax/448 of each (token, head) row, stored in dst's scales.
+ * Destination pages must be distinct.
+ */
+int pfkv_handoff_bf16_to_fp8(const pfkv_cache *src, const pfkv_cache *dst, const int32_t *src_pages,
+                             const int32_t *dst_pages, int32_t n_pages, uint32_t *page_status, void *stream);
+
+/*
  * calibrate_scales -- per-head FP8 scales s[h] = fp32(amax/448) over
  * rows[n_rows][num_heads][head_dim] (bf16); s[h] = 1 when the head's rows
  * are all zero.  This is the "scale = amax / 448" convention of an e4m3 cache

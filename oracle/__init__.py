@@ -94,6 +94,8 @@ def lib():
             L.orc_calibrate_per_head.argtypes = [P, i64, i32, i32, P]
             L.orc_append.restype = None
             L.orc_append.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, u32, P]
+            L.orc_handoff.restype = None
+            L.orc_handoff.argtypes = [P, P, P, P, i32, P]
             L.orc_decode.restype = None
             L.orc_decode.argtypes = [P, P, i32, P, P, P, i32, i32, ctypes.c_double, u32, P, P, i32]
             _lib = L
@@ -225,6 +227,15 @@ class Cache:
         lib().orc_decode(ctypes.byref(cs), _ptr(qq), Hq, _ptr(lens), _ptr(bt), _ptr(tags), B, bt.shape[1],
                          float(softmax_scale), flags, _ptr(out), _ptr(status), threads)
         return out, status
+
+    def handoff_from(self, src: "Cache", src_pages, dst_pages):
+        """Quantize pages of a BF16 oracle cache into this FP8 cache; returns page status."""
+        sp = _c(src_pages, np.int32)
+        dp = _c(dst_pages, np.int32)
+        st = np.zeros(sp.shape[0], dtype=np.uint32)
+        cs, cd = src._struct(), self._struct()
+        lib().orc_handoff(ctypes.byref(cs), ctypes.byref(cd), _ptr(sp), _ptr(dp), sp.shape[0], _ptr(st))
+        return st
 
     # views for comparison
     def k_rows(self):

@@ -340,6 +340,33 @@ void orc_append(const orc_cache *c, const uint16_t *k_new, const uint16_t *v_new
   }
 }
 
+/*
+ * Hand-off of whole pages from a BF16 cache to an FP8 cache ("Quantizing the
+ * KV cache": prefill keeps BF16, decode stores FP8).  Page src_pages[i] of
+ * src becomes page dst_pages[i] of dst, each (head, slot) row quantized as an
+ * appended row would be.  page_status[i] gets PAGE_OOB for an id outside its
+ * pool (nothing written for that pair).
+ */
+void orc_handoff(const orc_cache *src, const orc_cache *dst, const int32_t *src_pages, const int32_t *dst_pages,
+                 int32_t n_pages, uint32_t *page_status) {
+  const int32_t H = dst->num_kv_heads, S = dst->page_size, D = dst->head_dim, Dv = dst->v_head_dim;
+  for (int32_t i = 0; i < n_pages; ++i) {
+    const int32_t sp = src_pages[i], dp = dst_pages[i];
+    if (sp < 0 || sp >= src->num_pages || dp < 0 || dp >= dst->num_pages) {
+      page_status[i] = ORC_ST_PAGE_OOB;
+      continue;
+    }
+    page_status[i] = 0;
+    for (int32_t h = 0; h < H; ++h)
+      for (int32_t slot = 0; slot < S; ++slot) {
+        const int64_t r = row_index(src, sp, h, slot);
+        put_row(dst, dst->k_pool, dst->k_scale, (const uint16_t *)src->k_pool + r * D, D, dp, h, slot);
+        if (!dst->kv_shared)
+          put_row(dst, dst->v_pool, dst->v_scale, (const uint16_t *)src->v_pool + r * Dv, Dv, dp, h, slot);
+      }
+  }
+}
+
 /* ------------------------------------------------------------------ */
 /* Decode attention                                                     */
 /* ------------------------------------------------------------------ */

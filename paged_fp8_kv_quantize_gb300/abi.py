@@ -31,6 +31,7 @@ EXPORTS = (
     "pfkv_paged_decode_attention_fp8",
     "pfkv_paged_decode_attention_bf16",
     "pfkv_paged_decode_attention_fp8_noalloc",
+    "pfkv_handoff_bf16_to_fp8",
     "pfkv_calibrate_scales",
     "pfkv_e4m3_encode",
     "pfkv_strerror",
@@ -81,6 +82,8 @@ def _load():
     L.pfkv_paged_decode_attention_fp8_noalloc.restype = ctypes.c_int
     L.pfkv_paged_decode_attention_fp8_noalloc.argtypes = [cp, P, i32, P, P, P, i32, i32, ctypes.c_float, u32, i32,
                                                           P, P, P]
+    L.pfkv_handoff_bf16_to_fp8.restype = ctypes.c_int
+    L.pfkv_handoff_bf16_to_fp8.argtypes = [cp, cp, P, P, i32, P, P]
     L.pfkv_calibrate_scales.restype = ctypes.c_int
     L.pfkv_calibrate_scales.argtypes = [P, i64, i32, i32, P, P]
     L.pfkv_e4m3_encode.restype = ctypes.c_int
@@ -263,6 +266,20 @@ def paged_decode_attention(cache, *args, **kw):
     """Dispatch on the cache dtype to the FP8 or BF16 entry point."""
     f = paged_decode_attention_fp8 if cache.dtype == DTYPE_FP8_E4M3 else paged_decode_attention_bf16
     return f(cache, *args, **kw)
+
+
+def handoff_bf16_to_fp8(src: PagedCache, dst: PagedCache, src_pages, dst_pages, page_status=None, stream=None):
+    """Quantize pages src_pages[i] of a BF16 cache into pages dst_pages[i] of an FP8 cache."""
+    n = src_pages.shape[0]
+    if page_status is None:
+        page_status = torch.empty(n, dtype=torch.int32, device=src_pages.device)
+    ds, dd = src.desc(), dst.desc()
+    rc = lib.pfkv_handoff_bf16_to_fp8(ctypes.byref(ds), ctypes.byref(dd),
+                                      _ptr(_dev(src_pages, "src_pages", torch.int32)),
+                                      _ptr(_dev(dst_pages, "dst_pages", torch.int32)), n,
+                                      _ptr(_dev(page_status, "page_status", torch.int32)), _stream(stream))
+    _check("pfkv_handoff_bf16_to_fp8", rc)
+    return page_status
 
 
 def calibrate_scales(rows, scale=None, stream=None):

@@ -197,6 +197,22 @@ int pfkv_paged_decode_attention_bf16(const pfkv_cache *cache, const void *q, int
                        softmax_scale, flags, max_splits, workspace, workspace_bytes, out, status, stream);
 }
 
+int pfkv_handoff_bf16_to_fp8(const pfkv_cache *src, const pfkv_cache *dst, const int32_t *src_pages,
+                             const int32_t *dst_pages, int32_t n_pages, uint32_t *page_status, void *stream) {
+  int rc = check_cache(src);
+  if (rc) return rc;
+  rc = check_cache(dst);
+  if (rc) return rc;
+  if (src->dtype != PFKV_DTYPE_BF16 || dst->dtype != PFKV_DTYPE_FP8_E4M3) return PFKV_ERR_DTYPE;
+  if (src->num_kv_heads != dst->num_kv_heads || src->page_size != dst->page_size ||
+      src->head_dim != dst->head_dim || src->v_head_dim != dst->v_head_dim || src->kv_shared != dst->kv_shared)
+    return PFKV_ERR_SHAPE;
+  if (n_pages < 0) return PFKV_ERR_SHAPE;
+  if (n_pages == 0) return PFKV_OK;
+  if (!src_pages || !dst_pages || !page_status) return PFKV_ERR_NULL;
+  return launch_handoff(*src, *dst, src_pages, dst_pages, n_pages, page_status, static_cast<cudaStream_t>(stream));
+}
+
 int pfkv_calibrate_scales(const void *rows, int64_t n_rows, int32_t num_heads, int32_t head_dim, float *scale,
                           void *stream) {
   if (n_rows < 0 || num_heads < 1 || head_dim < 1 || num_heads > 65535) return PFKV_ERR_SHAPE;

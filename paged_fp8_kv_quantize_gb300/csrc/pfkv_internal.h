@@ -65,6 +65,8 @@ int launch_latent_decode(const DecodeArgs &a, cudaStream_t s);
 int launch_append(const pfkv_cache &c, const void *k_new, const void *v_new, int n_rows, const int *row_req,
                   const int *positions, const int *block_table, const uint32_t *block_tags, int batch,
                   int max_pages, uint32_t flags, uint32_t *status, cudaStream_t s);
+int launch_handoff(const pfkv_cache &src, const pfkv_cache &dst, const int *src_pages, const int *dst_pages,
+                   int n_pages, uint32_t *page_status, cudaStream_t s);
 int launch_calibrate(const void *rows, int64_t n_rows, int heads, int dim, float *scale, cudaStream_t s);
 int launch_encode(const float *x, uint8_t *codes, int64_t n, cudaStream_t s);
 
