@@ -35,6 +35,9 @@ FLAG_TAG_CHECK = 1
 ST_STALE_TAG = 1
 ST_PAGE_OOB = 2
 ST_BAD_LEN = 4
+ST_NO_PAGES = 16
+ST_NOT_HELD = 32
+ST_DUPLICATE = 64
 
 
 def build(force: bool = False) -> str:
@@ -96,6 +99,14 @@ def lib():
             L.orc_append.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, u32, P]
             L.orc_handoff.restype = None
             L.orc_handoff.argtypes = [P, P, P, P, i32, P]
+            L.orc_alloc_init.restype = None
+            L.orc_alloc_init.argtypes = [P, P, P, i32, P, i32]
+            L.orc_page_alloc.restype = None
+            L.orc_page_alloc.argtypes = [P, P, P, P, i32, P, P, P]
+            L.orc_page_free.restype = None
+            L.orc_page_free.argtypes = [P, P, P, i32, P, i32, P]
+            L.orc_page_realloc.restype = None
+            L.orc_page_realloc.argtypes = [P, i32, P, P, i32, P, P]
             L.orc_decode.restype = None
             L.orc_decode.argtypes = [P, P, i32, P, P, P, i32, i32, ctypes.c_double, u32, P, P, i32]
             _lib = L
@@ -243,3 +254,49 @@ class Cache:
 
     def v_rows(self):
         return None if self.v_pool is None else self.v_pool.reshape(self.P, self.H, self.S, self.Dv)
+
+
+# ---------------------------------------------------------------- page allocator
+
+
+class Allocator:
+    """The oracle's sequential page allocator over a tag array it does not own."""
+
+    def __init__(self, num_pages, page_tags, held_pages=()):
+        self.P = int(num_pages)
+        self.page_tags = page_tags  # uint32 [P], updated in place
+        assert self.page_tags.dtype == np.uint32 and self.page_tags.flags.c_contiguous
+        self.stack = np.zeros(self.P, dtype=np.int32)
+        self.held = np.zeros(self.P, dtype=np.uint8)
+        self.count = np.zeros(1, dtype=np.int32)
+        hp = _c(np.asarray(held_pages, dtype=np.int64), np.int32)
+        lib().orc_alloc_init(_ptr(self.stack), _ptr(self.held), _ptr(self.count), self.P, _ptr(hp), hp.size)
+
+    @property
+    def free_count(self):
+        return int(self.count[0])
+
+    def free_list(self):
+        """Free ids, bottom of the stack first."""
+        return self.stack[: self.free_count].copy()
+
+    def alloc(self, n):
+        pages = np.zeros(n, dtype=np.int32)
+        tags = np.zeros(n, dtype=np.uint32)
+        st = np.zeros(1, dtype=np.uint32)
+        lib().orc_page_alloc(_ptr(self.stack), _ptr(self.held), _ptr(self.count), _ptr(self.page_tags), int(n),
+                             _ptr(pages), _ptr(tags), _ptr(st))
+        return pages, tags, int(st[0])
+
+    def free(self, pages):
+        pg = _c(pages, np.int32)
+        st = np.zeros(pg.size, dtype=np.uint32)
+        lib().orc_page_free(_ptr(self.stack), _ptr(self.held), _ptr(self.count), self.P, _ptr(pg), pg.size, _ptr(st))
+        return st
+
+    def realloc(self, pages):
+        pg = _c(pages, np.int32)
+        tags = np.zeros(pg.size, dtype=np.uint32)
+        st = np.zeros(pg.size, dtype=np.uint32)
+        lib().orc_page_realloc(_ptr(self.held), self.P, _ptr(self.page_tags), _ptr(pg), pg.size, _ptr(tags), _ptr(st))
+        return tags, st

@@ -35,6 +35,10 @@
  *  R7  the append also checks its destination page and writes nothing on
  *      a bad page.
  *  R8  attention output is fp32 [batch][q_heads][v_dim] (here fp64).
+ *  R13 a page's tag advances by one (mod 2^32) each time the page is handed
+ *      to an owner: at allocation and at a move to a new owner; freeing
+ *      leaves it.  A fresh allocator hands out pages in increasing id order
+ *      and reuses the most recently freed page first (a stack).
  *  NaN input encodes as 0x7F; +-inf saturates like any large value.
  *
  * Build: gcc -O2 -std=c11 -fPIC -shared -pthread pfkv_oracle.c -lm
@@ -55,6 +59,9 @@
 #define ORC_ST_STALE_TAG 1u
 #define ORC_ST_PAGE_OOB 2u
 #define ORC_ST_BAD_LEN 4u
+#define ORC_ST_NO_PAGES 16u
+#define ORC_ST_NOT_HELD 32u
+#define ORC_ST_DUPLICATE 64u
 
 typedef struct {
   int32_t num_pages, page_size, num_kv_heads, head_dim, v_head_dim;
@@ -364,6 +371,100 @@ void orc_handoff(const orc_cache *src, const orc_cache *dst, const int32_t *src_
         if (!dst->kv_shared)
           put_row(dst, dst->v_pool, dst->v_scale, (const uint16_t *)src->v_pool + r * Dv, Dv, dp, h, slot);
       }
+  }
+}
+
+/* ------------------------------------------------------------------ */
+/* Page allocator (the producer side of the tags)                      */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Same post, cache-protection passage: the tag of a page changes each time
+ * the page is reallocated, so a request still holding the old mapping (and
+ * the old tag) fails the check.  The allocator below is the plain sequential
+ * model: a stack of free page ids, a held flag per page, the tag bumped when
+ * a page is given to an owner (R13).  Every call is all-or-nothing per
+ * element and processes its list in order.
+ *   stack[0 .. *free_count) : free ids; the top (the end) is popped first.
+ */
+void orc_alloc_init(int32_t *stack, uint8_t *held, int32_t *free_count, int32_t num_pages,
+                    const int32_t *held_pages, int32_t n_held) {
+  memset(held, 0, (size_t)num_pages);
+  for (int32_t i = 0; i < n_held; ++i)
+    if (held_pages[i] >= 0 && held_pages[i] < num_pages) held[held_pages[i]] = 1;
+  int32_t n = 0;
+  for (int32_t p = num_pages - 1; p >= 0; --p) /* smallest free id on top */
+    if (!held[p]) stack[n++] = p;
+  *free_count = n;
+}
+
+/* Take n pages.  Not enough free pages: nothing is taken, pages_out = -1,
+ * tags_out = 0, *status = NO_PAGES. */
+void orc_page_alloc(int32_t *stack, uint8_t *held, int32_t *free_count, uint32_t *page_tags, int32_t n,
+                    int32_t *pages_out, uint32_t *tags_out, uint32_t *status) {
+  if (n > *free_count) {
+    for (int32_t i = 0; i < n; ++i) {
+      pages_out[i] = -1;
+      tags_out[i] = 0;
+    }
+    *status = ORC_ST_NO_PAGES;
+    return;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t p = stack[--*free_count];
+    held[p] = 1;
+    page_tags[p] += 1u;
+    pages_out[i] = p;
+    tags_out[i] = page_tags[p];
+  }
+  *status = 0;
+}
+
+/* Give pages back.  An id outside the pool: PAGE_OOB; a page that is not
+ * held (never taken, or already given back, earlier in this list too):
+ * NOT_HELD.  Either way that entry is skipped. */
+void orc_page_free(int32_t *stack, uint8_t *held, int32_t *free_count, int32_t num_pages, const int32_t *pages,
+                   int32_t n, uint32_t *page_status) {
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t p = pages[i];
+    if (p < 0 || p >= num_pages) {
+      page_status[i] = ORC_ST_PAGE_OOB;
+    } else if (!held[p]) {
+      page_status[i] = ORC_ST_NOT_HELD;
+    } else {
+      held[p] = 0;
+      stack[(*free_count)++] = p;
+      page_status[i] = 0;
+    }
+  }
+}
+
+/* Move held pages to new owners without a trip through the free list: each
+ * listed page's tag advances by one and the new tag is returned.  A page
+ * listed twice is moved once; the later entries get DUPLICATE (tag_out 0),
+ * as do entries that are OOB or NOT_HELD. */
+void orc_page_realloc(const uint8_t *held, int32_t num_pages, uint32_t *page_tags, const int32_t *pages, int32_t n,
+                      uint32_t *tags_out, uint32_t *page_status) {
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t p = pages[i];
+    tags_out[i] = 0;
+    if (p < 0 || p >= num_pages) {
+      page_status[i] = ORC_ST_PAGE_OOB;
+      continue;
+    }
+    if (!held[p]) {
+      page_status[i] = ORC_ST_NOT_HELD;
+      continue;
+    }
+    int seen = 0;
+    for (int32_t j = 0; j < i && !seen; ++j) seen = pages[j] == p;
+    if (seen) {
+      page_status[i] = ORC_ST_DUPLICATE;
+      continue;
+    }
+    page_tags[p] += 1u;
+    tags_out[i] = page_tags[p];
+    page_status[i] = 0;
   }
 }
 
