@@ -57,8 +57,11 @@ enum {
   PFKV_ST_PAGE_OOB = 2u,  /* a page id is outside [0, num_pages)          */
   PFKV_ST_BAD_LEN = 4u,   /* length < 1 or beyond max_pages * page_size,
                              or an append position outside the table      */
-  PFKV_ST_TIMEOUT = 8u    /* a pipeline wait inside the kernel gave up;
+  PFKV_ST_TIMEOUT = 8u,   /* a pipeline wait inside the kernel gave up;
                              the output of the call is not valid          */
+  PFKV_ST_NO_PAGES = 16u, /* page allocator: fewer free pages than asked  */
+  PFKV_ST_NOT_HELD = 32u, /* page allocator: the page is not handed out   */
+  PFKV_ST_DUPLICATE = 64u /* page allocator: id listed twice in one call  */
 };
 
 /* Return codes. */
@@ -228,6 +231,54 @@ int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, const void 
  */
 int pfkv_handoff_bf16_to_fp8(const pfkv_cache *src, const pfkv_cache *dst, const int32_t *src_pages,
                              const int32_t *dst_pages, int32_t n_pages, uint32_t *page_status, void *stream);
+
+/*
+ * Page allocator -- the producer side of the page tags (cache-protection
+ * passage: each page's tag changes whenever the page is reallocated, so a
+ * request that still holds the old mapping fails the tag check).  A free
+ * list that lives in device memory, so a step can take and return pages
+ * without a host round trip.  Every hand-out of a page to an owner (alloc,
+ * realloc) advances page_tags[p] by one, modulo 2^32; freeing leaves it.
+ *
+ * State (caller-owned device memory, pfkv_page_allocator_bytes(num_pages)
+ * bytes, 256-byte aligned):
+ *   bytes [0, 4)     int32 num_pages
+ *   bytes [4, 8)     int32 free_count
+ *   bytes [256, ...) int32 stack[num_pages]: stack[0 .. free_count) are the
+ *                    free ids, the last one is handed out first
+ *   followed by per-page bookkeeping (a held flag and a scratch word).
+ * A fresh state hands out pages in increasing id order; freed pages are
+ * reused last-in first-out.  Calls on one state must be ordered (one stream,
+ * or events): each call is one kernel that owns the state while it runs.
+ * Lists are processed as if in order (first occurrence wins); results are
+ * deterministic.
+ */
+size_t pfkv_page_allocator_bytes(int32_t num_pages);
+
+/* Make every page free except held_pages[0 .. n_held) (ids outside the pool
+ * and repeats are ignored; held_pages may be NULL when n_held == 0).
+ * Returns PFKV_ERR_WORKSPACE when state_bytes is too small. */
+int pfkv_page_allocator_init(void *state, size_t state_bytes, int32_t num_pages, const int32_t *held_pages,
+                             int32_t n_held, void *stream);
+
+/* Take n pages: pages_out[i], their new tags tags_out[i] (to be stored in
+ * the owner's block_tags).  All or nothing: with fewer than n free pages
+ * nothing is taken, pages_out = -1, tags_out = 0 and *status = NO_PAGES;
+ * else *status = 0.  page_tags: the cache's tag array [num_pages]. */
+int pfkv_page_alloc(void *state, uint32_t *page_tags, int32_t n, int32_t *pages_out, uint32_t *tags_out,
+                    uint32_t *status, void *stream);
+
+/* Give pages back.  page_status[i]: 0, PAGE_OOB (id outside the pool) or
+ * NOT_HELD (not handed out, or already given back earlier in the list);
+ * flagged entries are skipped. */
+int pfkv_page_free(void *state, const int32_t *pages, int32_t n, uint32_t *page_status, void *stream);
+
+/* Move held pages to new owners without a trip through the free list: each
+ * listed page's tag advances once and is returned in tags_out[i].
+ * page_status[i]: 0, PAGE_OOB, NOT_HELD, or DUPLICATE for a repeat of an
+ * earlier entry; flagged entries get tags_out 0 and change nothing. */
+int pfkv_page_realloc(void *state, uint32_t *page_tags, const int32_t *pages, int32_t n, uint32_t *tags_out,
+                      uint32_t *page_status, void *stream);
 
 /*
  * calibrate_scales -- per-head FP8 scales s[h] = fp32(amax/448) over

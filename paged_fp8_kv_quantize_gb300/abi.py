@@ -24,6 +24,9 @@ ST_STALE_TAG = 1
 ST_PAGE_OOB = 2
 ST_BAD_LEN = 4
 ST_TIMEOUT = 8
+ST_NO_PAGES = 16
+ST_NOT_HELD = 32
+ST_DUPLICATE = 64
 
 EXPORTS = (
     "pfkv_kv_append_quantize",
@@ -32,6 +35,11 @@ EXPORTS = (
     "pfkv_paged_decode_attention_bf16",
     "pfkv_paged_decode_attention_fp8_noalloc",
     "pfkv_handoff_bf16_to_fp8",
+    "pfkv_page_allocator_bytes",
+    "pfkv_page_allocator_init",
+    "pfkv_page_alloc",
+    "pfkv_page_free",
+    "pfkv_page_realloc",
     "pfkv_calibrate_scales",
     "pfkv_e4m3_encode",
     "pfkv_strerror",
@@ -84,6 +92,16 @@ def _load():
                                                           P, P, P]
     L.pfkv_handoff_bf16_to_fp8.restype = ctypes.c_int
     L.pfkv_handoff_bf16_to_fp8.argtypes = [cp, cp, P, P, i32, P, P]
+    L.pfkv_page_allocator_bytes.restype = sz
+    L.pfkv_page_allocator_bytes.argtypes = [i32]
+    L.pfkv_page_allocator_init.restype = ctypes.c_int
+    L.pfkv_page_allocator_init.argtypes = [P, sz, i32, P, i32, P]
+    L.pfkv_page_alloc.restype = ctypes.c_int
+    L.pfkv_page_alloc.argtypes = [P, P, i32, P, P, P, P]
+    L.pfkv_page_free.restype = ctypes.c_int
+    L.pfkv_page_free.argtypes = [P, P, i32, P, P]
+    L.pfkv_page_realloc.restype = ctypes.c_int
+    L.pfkv_page_realloc.argtypes = [P, P, P, i32, P, P, P]
     L.pfkv_calibrate_scales.restype = ctypes.c_int
     L.pfkv_calibrate_scales.argtypes = [P, i64, i32, i32, P, P]
     L.pfkv_e4m3_encode.restype = ctypes.c_int
@@ -280,6 +298,64 @@ def handoff_bf16_to_fp8(src: PagedCache, dst: PagedCache, src_pages, dst_pages, 
                                       _ptr(_dev(page_status, "page_status", torch.int32)), _stream(stream))
     _check("pfkv_handoff_bf16_to_fp8", rc)
     return page_status
+
+
+class PageAllocator:
+    """Device-resident free list over num_pages pages (pfkv_page_allocator_*).
+
+    Every hand-out (alloc, realloc) advances the page's tag in the cache's
+    page_tags; the returned tags go into the new owner's block_tags."""
+
+    def __init__(self, num_pages, held_pages=None, device="cuda", stream=None):
+        self.num_pages = int(num_pages)
+        nbytes = lib.pfkv_page_allocator_bytes(self.num_pages)
+        if nbytes == 0:
+            raise PfkvError("pfkv_page_allocator_bytes", -2)
+        self.state = torch.empty(nbytes, dtype=torch.uint8, device=device)  # torch blocks are 512-byte aligned
+        n_held, hp = 0, None
+        if held_pages is not None:
+            hp = _dev(held_pages, "held_pages", torch.int32)
+            n_held = hp.numel()
+        rc = lib.pfkv_page_allocator_init(_ptr(self.state), nbytes, self.num_pages, _ptr(hp) if n_held else None,
+                                          n_held, _stream(stream))
+        _check("pfkv_page_allocator_init", rc)
+
+    def alloc(self, n, page_tags, stream=None):
+        """-> (pages int32 [n], tags int32 [n] (uint32 bits), status int32 [1]) on the device."""
+        dev = self.state.device
+        pages = torch.empty(max(n, 1), dtype=torch.int32, device=dev)[:n]
+        tags = torch.empty(max(n, 1), dtype=torch.int32, device=dev)[:n]
+        status = torch.empty(1, dtype=torch.int32, device=dev)
+        rc = lib.pfkv_page_alloc(_ptr(self.state), _ptr(_dev(page_tags, "page_tags", torch.int32)), int(n),
+                                 _ptr(pages) if n else None, _ptr(tags) if n else None, _ptr(status), _stream(stream))
+        _check("pfkv_page_alloc", rc)
+        return pages, tags, status
+
+    def free(self, pages, stream=None):
+        pages = _dev(pages, "pages", torch.int32)
+        st = torch.zeros(pages.numel(), dtype=torch.int32, device=self.state.device)
+        rc = lib.pfkv_page_free(_ptr(self.state), _ptr(pages), pages.numel(), _ptr(st), _stream(stream))
+        _check("pfkv_page_free", rc)
+        return st
+
+    def realloc(self, pages, page_tags, stream=None):
+        pages = _dev(pages, "pages", torch.int32)
+        n = pages.numel()
+        tags = torch.zeros(n, dtype=torch.int32, device=self.state.device)
+        st = torch.zeros(n, dtype=torch.int32, device=self.state.device)
+        rc = lib.pfkv_page_realloc(_ptr(self.state), _ptr(_dev(page_tags, "page_tags", torch.int32)), _ptr(pages), n,
+                                   _ptr(tags), _ptr(st), _stream(stream))
+        _check("pfkv_page_realloc", rc)
+        return tags, st
+
+    def free_count(self):
+        """Reads the state's free count (synchronises with the device)."""
+        return int(self.state[4:8].view(torch.int32).item())
+
+    def free_list(self):
+        """Free ids, bottom of the stack first (synchronises with the device)."""
+        fc = self.free_count()
+        return self.state[256:256 + 4 * self.num_pages].view(torch.int32)[:fc].clone()
 
 
 def calibrate_scales(rows, scale=None, stream=None):

@@ -213,6 +213,48 @@ int pfkv_handoff_bf16_to_fp8(const pfkv_cache *src, const pfkv_cache *dst, const
   return launch_handoff(*src, *dst, src_pages, dst_pages, n_pages, page_status, static_cast<cudaStream_t>(stream));
 }
 
+size_t pfkv_page_allocator_bytes(int32_t num_pages) { return alloc_state_bytes(num_pages); }
+
+static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+int pfkv_page_allocator_init(void *state, size_t state_bytes, int32_t num_pages, const int32_t *held_pages,
+                             int32_t n_held, void *stream) {
+  if (!state) return PFKV_ERR_NULL;
+  if (num_pages < 1 || n_held < 0) return PFKV_ERR_SHAPE;
+  if (n_held > 0 && !held_pages) return PFKV_ERR_NULL;
+  if (state_bytes < alloc_state_bytes(num_pages)) return PFKV_ERR_WORKSPACE;
+  if (!aligned256(state)) return PFKV_ERR_ALIGN;
+  return launch_alloc_init(state, num_pages, held_pages, n_held, static_cast<cudaStream_t>(stream));
+}
+
+int pfkv_page_alloc(void *state, uint32_t *page_tags, int32_t n, int32_t *pages_out, uint32_t *tags_out,
+                    uint32_t *status, void *stream) {
+  if (!state || !page_tags || !status) return PFKV_ERR_NULL;
+  if (n < 0) return PFKV_ERR_SHAPE;
+  if (n > 0 && (!pages_out || !tags_out)) return PFKV_ERR_NULL;
+  if (!aligned256(state)) return PFKV_ERR_ALIGN;
+  return launch_page_alloc(state, page_tags, n, pages_out, tags_out, status, static_cast<cudaStream_t>(stream));
+}
+
+int pfkv_page_free(void *state, const int32_t *pages, int32_t n, uint32_t *page_status, void *stream) {
+  if (!state) return PFKV_ERR_NULL;
+  if (n < 0) return PFKV_ERR_SHAPE;
+  if (n == 0) return PFKV_OK;
+  if (!pages || !page_status) return PFKV_ERR_NULL;
+  if (!aligned256(state)) return PFKV_ERR_ALIGN;
+  return launch_page_free(state, pages, n, page_status, static_cast<cudaStream_t>(stream));
+}
+
+int pfkv_page_realloc(void *state, uint32_t *page_tags, const int32_t *pages, int32_t n, uint32_t *tags_out,
+                      uint32_t *page_status, void *stream) {
+  if (!state || !page_tags) return PFKV_ERR_NULL;
+  if (n < 0) return PFKV_ERR_SHAPE;
+  if (n == 0) return PFKV_OK;
+  if (!pages || !tags_out || !page_status) return PFKV_ERR_NULL;
+  if (!aligned256(state)) return PFKV_ERR_ALIGN;
+  return launch_page_realloc(state, page_tags, pages, n, tags_out, page_status, static_cast<cudaStream_t>(stream));
+}
+
 int pfkv_calibrate_scales(const void *rows, int64_t n_rows, int32_t num_heads, int32_t head_dim, float *scale,
                           void *stream) {
   if (n_rows < 0 || num_heads < 1 || head_dim < 1 || num_heads > 65535) return PFKV_ERR_SHAPE;

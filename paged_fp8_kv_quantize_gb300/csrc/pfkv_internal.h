@@ -67,6 +67,13 @@ int launch_append(const pfkv_cache &c, const void *k_new, const void *v_new, int
                   int max_pages, uint32_t flags, uint32_t *status, cudaStream_t s);
 int launch_handoff(const pfkv_cache &src, const pfkv_cache &dst, const int *src_pages, const int *dst_pages,
                    int n_pages, uint32_t *page_status, cudaStream_t s);
+size_t alloc_state_bytes(int num_pages);
+int launch_alloc_init(void *state, int num_pages, const int *held_pages, int n_held, cudaStream_t s);
+int launch_page_alloc(void *state, uint32_t *page_tags, int n, int *pages_out, uint32_t *tags_out, uint32_t *status,
+                      cudaStream_t s);
+int launch_page_free(void *state, const int *pages, int n, uint32_t *page_status, cudaStream_t s);
+int launch_page_realloc(void *state, uint32_t *page_tags, const int *pages, int n, uint32_t *tags_out,
+                        uint32_t *page_status, cudaStream_t s);
 int launch_calibrate(const void *rows, int64_t n_rows, int heads, int dim, float *scale, cudaStream_t s);
 int launch_encode(const float *x, uint8_t *codes, int64_t n, cudaStream_t s);
 

@@ -53,3 +53,22 @@ def test_argument_errors_return_before_any_cuda_call():
     assert f(ctypes.byref(unal), *args_tail) == -6  # misaligned pool
     g = abi.lib.pfkv_kv_append_quantize
     assert g(None, None, None, 0, None, None, None, None, 1, 1, 0, None, None) == -1
+
+
+def test_page_allocator_host_checks():
+    L = abi.lib
+    n = L.pfkv_page_allocator_bytes(1000)
+    # header + stack + scratch word + held flag per page + chunk counts
+    assert 256 + 9 * 1000 <= n < 256 + 9 * 1000 + 4 * 256 + 64
+    assert L.pfkv_page_allocator_bytes(0) == 0
+    assert L.pfkv_page_allocator_init(None, n, 1000, None, 0, None) == -1
+    assert L.pfkv_page_allocator_init(256, n, 0, None, 0, None) == -2
+    assert L.pfkv_page_allocator_init(256, n - 1, 1000, None, 0, None) == -5
+    assert L.pfkv_page_allocator_init(256, n, 1000, None, 3, None) == -1  # held ids missing
+    assert L.pfkv_page_allocator_init(272, n, 1000, None, 0, None) == -6  # state not 256-byte aligned
+    assert L.pfkv_page_alloc(256, 256, -1, None, None, 256, None) == -2
+    assert L.pfkv_page_alloc(256, 256, 4, None, None, 256, None) == -1
+    assert L.pfkv_page_free(256, None, 0, None, None) == 0  # nothing to do, nothing launched
+    assert L.pfkv_page_free(256, None, 2, None, None) == -1
+    assert L.pfkv_page_realloc(256, 256, None, 0, None, None, None) == 0
+    assert L.pfkv_page_realloc(256, None, None, 1, None, None, None) == -1
