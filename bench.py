@@ -350,10 +350,20 @@ def main():
     FLAGS = abi.FLAG_TAG_CHECK
 
     def step(cache, j, flags=FLAGS, do_append=True):
+        """One decode step: the fused call (new tokens appended by the plan grid, then attention)."""
         j %= T
         if do_append:
-            abi.kv_append_quantize(cache, k_steps[j], v_steps[j], pos_steps[j], table, tags, flags=flags,
-                                   status=st_app)
+            abi.paged_decode_step(cache, k_steps[j], v_steps[j], q_steps[j], len_steps[j], table, tags,
+                                  w.softmax_scale, flags=flags, max_splits=max_splits, workspace=ws, out=out,
+                                  status=st_dec)
+        else:
+            abi.paged_decode_attention(cache, q_steps[j], len_steps[j], table, tags, w.softmax_scale, flags=flags,
+                                       max_splits=max_splits, workspace=ws, out=out, status=st_dec)
+
+    def step_unfused(cache, j, flags=FLAGS):
+        """The same step as two calls: kv_append_quantize, then paged decode attention."""
+        j %= T
+        abi.kv_append_quantize(cache, k_steps[j], v_steps[j], pos_steps[j], table, tags, flags=flags, status=st_app)
         abi.paged_decode_attention(cache, q_steps[j], len_steps[j], table, tags, w.softmax_scale, flags=flags,
                                    max_splits=max_splits, workspace=ws, out=out, status=st_dec)
 
@@ -426,6 +436,11 @@ def main():
                                        "on_us_per_call": statistics.median(on_ms) / K * 1e3,
                                        "off_us_per_call": statistics.median(off_ms) / K * 1e3, "alternations": 11,
                                        "tags": "all valid in both arms"}
+        g_unf = capture(lambda j: step_unfused(fp8, j), K)
+        g_unf.replay()
+        ms_unf = time_graph(g_unf) / K
+        extra["unfused_step"] = {"us_per_step": ms_unf * 1e3, "fused_us_per_step": ms_per_step * 1e3,
+                                 "what": "kv_append_quantize + paged_decode_attention as two calls"}
         bf = caches["bf16"]
         g_bf = capture(lambda j: step(bf, j, do_append=False), K)
         g_bf.replay()
@@ -446,23 +461,20 @@ def main():
     h_q = torch.from_numpy(np.ascontiguousarray(w.q_steps).view(np.int16)).view(torch.bfloat16).pin_memory()
     h_k = torch.from_numpy(np.ascontiguousarray(w.k_steps).view(np.int16)).view(torch.bfloat16).pin_memory()
     h_v = torch.from_numpy(np.ascontiguousarray(w.v_steps).view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_pos = torch.from_numpy(np.stack([lens0 + j for j in range(T)]).astype(np.int32)).pin_memory()
     h_len = torch.from_numpy(np.stack([lens0 + j + 1 for j in range(T)]).astype(np.int32)).pin_memory()
     h_out = torch.empty(B, Hq, D, dtype=torch.float32).pin_memory()
     h_st = torch.empty(B, dtype=torch.int32).pin_memory()
     d_q, d_k, d_v = torch.empty_like(q_steps[0]), torch.empty_like(k_steps[0]), torch.empty_like(v_steps[0])
-    d_pos, d_len = torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev)
+    d_len = torch.empty(B, dtype=torch.int32, device=dev)
 
     def e2e_step(j):
         j %= T
         d_q.copy_(h_q[j], non_blocking=True)
         d_k.copy_(h_k[j], non_blocking=True)
         d_v.copy_(h_v[j], non_blocking=True)
-        d_pos.copy_(h_pos[j], non_blocking=True)
         d_len.copy_(h_len[j], non_blocking=True)
-        abi.kv_append_quantize(fp8, d_k, d_v, d_pos, table, tags, flags=FLAGS, status=st_app)
-        abi.paged_decode_attention(fp8, d_q, d_len, table, tags, w.softmax_scale, flags=FLAGS,
-                                   max_splits=max_splits, workspace=ws, out=out, status=st_dec)
+        abi.paged_decode_step(fp8, d_k, d_v, d_q, d_len, table, tags, w.softmax_scale, flags=FLAGS,
+                              max_splits=max_splits, workspace=ws, out=out, status=st_dec)
         h_out.copy_(out, non_blocking=True)
         h_st.copy_(st_dec, non_blocking=True)
 
@@ -470,7 +482,7 @@ def main():
     g_e2e.replay()
     ms_e2e = time_graph(g_e2e)
     e2e_val = job_throughput(sum(step_bytes), world, ms_e2e) / 1e9
-    h2d = h_q[0].numel() * 2 + h_k[0].numel() * 2 + h_v[0].numel() * 2 + 2 * B * 4
+    h2d = h_q[0].numel() * 2 + h_k[0].numel() * 2 + h_v[0].numel() * 2 + B * 4
     d2h = h_out.numel() * 4 + B * 4
 
     # ---- the CPU oracle on the host cores (rank 0, N=1 only)
@@ -484,7 +496,7 @@ def main():
                "seconds": dt}
 
     st_final = st_dec.cpu().numpy()
-    launches_per_step = 4  # append kernel; decode: plan + split + merge kernels
+    launches_per_step = 3  # plan (+ append blocks), split, merge kernels
     mean_lens = lens0 + (K - 1) % T + 1
     res = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,

@@ -215,6 +215,32 @@ int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, const void 
                                             uint32_t *status, void *stream);
 
 /*
+ * paged_decode_step -- one decode step of the paged cache: every request's
+ * new token is written into the cache (as pfkv_kv_append_quantize would,
+ * quantized on the way in for an FP8 cache) and then attended over, together
+ * with the rest of its context, as pfkv_paged_decode_attention_* does.  The
+ * post's two halves of the decode pool ("Quantizing the KV cache": rows are
+ * stored as FP8 and converted as they are read) in one call, so the new rows
+ * are written by the same launch that plans the attention.
+ *   k_new, v_new : bf16 [batch][num_kv_heads][head_dim]; row b goes to
+ *                  logical position seq_lens[b] - 1 (seq_lens counts the new
+ *                  token); v_new is ignored (may be NULL) for a kv_shared
+ *                  cache.  16-byte aligned.
+ *   The other arguments, the workspace and the outputs are those of
+ *   pfkv_paged_decode_attention_fp8 / _bf16; the cache's dtype selects the
+ *   variant, with the same supported shapes.
+ * status[b] is the attention's status.  It covers every refusal of the
+ * write: the write targets logical page (seq_lens[b] - 1) / page_size,
+ * which the attention inspects under the same rules, and a refused row
+ * writes nothing.  Distinct requests must not share a destination slot.
+ */
+int pfkv_paged_decode_step(const pfkv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                           int32_t num_q_heads, const int32_t *seq_lens, const int32_t *block_table,
+                           const uint32_t *block_tags, int32_t batch, int32_t max_pages, float softmax_scale,
+                           uint32_t flags, int32_t max_splits, void *workspace, size_t workspace_bytes, float *out,
+                           uint32_t *status, void *stream);
+
+/*
  * handoff_bf16_to_fp8 -- quantize whole pages of a BF16 cache into an FP8
  * cache ("Quantizing the KV cache": prefill keeps BF16 because it is
  * compute-bound, the decode pool stores FP8 e4m3; a request moving between

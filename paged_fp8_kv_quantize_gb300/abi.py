@@ -34,6 +34,7 @@ EXPORTS = (
     "pfkv_paged_decode_attention_fp8",
     "pfkv_paged_decode_attention_bf16",
     "pfkv_paged_decode_attention_fp8_noalloc",
+    "pfkv_paged_decode_step",
     "pfkv_handoff_bf16_to_fp8",
     "pfkv_page_allocator_bytes",
     "pfkv_page_allocator_init",
@@ -90,6 +91,9 @@ def _load():
     L.pfkv_paged_decode_attention_fp8_noalloc.restype = ctypes.c_int
     L.pfkv_paged_decode_attention_fp8_noalloc.argtypes = [cp, P, i32, P, P, P, i32, i32, ctypes.c_float, u32, i32,
                                                           P, P, P]
+    L.pfkv_paged_decode_step.restype = ctypes.c_int
+    L.pfkv_paged_decode_step.argtypes = [cp, P, P, P, i32, P, P, P, i32, i32, ctypes.c_float, u32, i32, P, sz, P, P,
+                                         P]
     L.pfkv_handoff_bf16_to_fp8.restype = ctypes.c_int
     L.pfkv_handoff_bf16_to_fp8.argtypes = [cp, cp, P, P, i32, P, P]
     L.pfkv_page_allocator_bytes.restype = sz
@@ -251,6 +255,31 @@ def paged_decode_attention_bf16(cache, q, seq_lens, block_table, block_tags, sof
                                 workspace=None, out=None, status=None, stream=None):
     return _decode("pfkv_paged_decode_attention_bf16", cache, q, seq_lens, block_table, block_tags, softmax_scale,
                    flags, max_splits, workspace, out, status, stream)
+
+
+def paged_decode_step(cache, k_new, v_new, q, seq_lens, block_table, block_tags, softmax_scale, flags=0,
+                      max_splits=64, workspace=None, out=None, status=None, stream=None):
+    """Append each request's new token (k_new/v_new bf16 [B][Hkv][D], position
+    seq_lens[b] - 1) and attend, in one call (pfkv_paged_decode_step)."""
+    B, Hq, D = q.shape
+    MP = block_table.shape[1]
+    dev = q.device
+    if workspace is None:
+        workspace = torch.empty(decode_workspace_bytes(cache, B, Hq, max_splits), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty(B, Hq, cache.Dv, dtype=torch.float32, device=dev)
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    d = cache.desc()
+    rc = lib.pfkv_paged_decode_step(
+        ctypes.byref(d), _ptr(_dev(k_new, "k_new", torch.bfloat16)),
+        _ptr(_dev(v_new, "v_new", torch.bfloat16)) if v_new is not None else None, _ptr(_dev(q, "q", torch.bfloat16)),
+        Hq, _ptr(_dev(seq_lens, "seq_lens", torch.int32)), _ptr(_dev(block_table, "block_table", torch.int32)),
+        _ptr(_dev(block_tags, "block_tags", torch.int32)), B, MP, float(softmax_scale), int(flags), int(max_splits),
+        _ptr(workspace), workspace.numel(), _ptr(_dev(out, "out", torch.float32)),
+        _ptr(_dev(status, "status", torch.int32)), _stream(stream))
+    _check("pfkv_paged_decode_step", rc)
+    return out, status
 
 
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # PFKV_NOALLOC_SCRATCH_BYTES

@@ -83,7 +83,8 @@ static int check_cache(const pfkv_cache *c) {
 static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int32_t Hq, const int32_t *seq_lens,
                          const int32_t *block_table, const uint32_t *block_tags, int32_t batch, int32_t max_pages,
                          float softmax_scale, uint32_t flags, int32_t max_splits, void *ws, size_t ws_bytes,
-                         float *out, uint32_t *status, void *stream) {
+                         float *out, uint32_t *status, void *stream, const void *k_new = nullptr,
+                         const void *v_new = nullptr) {
   int rc = check_cache(c);
   if (rc) return rc;
   if (c->dtype != want_dtype) return PFKV_ERR_DTYPE;
@@ -117,6 +118,10 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.part_ml = reinterpret_cast<float2 *>(w + L.part_ml);
   a.part_o = reinterpret_cast<float *>(w + L.part_o);
   a.out = out; a.status = status;
+  a.append = k_new != nullptr;
+  a.k_new = static_cast<const uint16_t *>(k_new);
+  a.v_new = static_cast<const uint16_t *>(v_new);
+  a.cache = *c;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (c->kv_shared) {
     if (!is_latent(c) || Hq != 64 || c->dtype != PFKV_DTYPE_FP8_E4M3 || c->scale_mode != PFKV_SCALE_PER_TOKEN ||
@@ -195,6 +200,21 @@ int pfkv_paged_decode_attention_bf16(const pfkv_cache *cache, const void *q, int
                                      size_t workspace_bytes, float *out, uint32_t *status, void *stream) {
   return decode_common(PFKV_DTYPE_BF16, cache, q, num_q_heads, seq_lens, block_table, block_tags, batch, max_pages,
                        softmax_scale, flags, max_splits, workspace, workspace_bytes, out, status, stream);
+}
+
+int pfkv_paged_decode_step(const pfkv_cache *cache, const void *k_new, const void *v_new, const void *q,
+                           int32_t num_q_heads, const int32_t *seq_lens, const int32_t *block_table,
+                           const uint32_t *block_tags, int32_t batch, int32_t max_pages, float softmax_scale,
+                           uint32_t flags, int32_t max_splits, void *workspace, size_t workspace_bytes, float *out,
+                           uint32_t *status, void *stream) {
+  if (!cache) return PFKV_ERR_NULL;
+  if (batch > 0) {
+    if (!k_new || (!cache->kv_shared && !v_new)) return PFKV_ERR_NULL;
+    if (!aligned16(k_new) || (!cache->kv_shared && !aligned16(v_new))) return PFKV_ERR_ALIGN;
+  }
+  return decode_common(cache->dtype, cache, q, num_q_heads, seq_lens, block_table, block_tags, batch, max_pages,
+                       softmax_scale, flags, max_splits, workspace, workspace_bytes, out, status, stream,
+                       batch > 0 ? k_new : nullptr, cache->kv_shared ? nullptr : v_new);
 }
 
 int pfkv_handoff_bf16_to_fp8(const pfkv_cache *src, const pfkv_cache *dst, const int32_t *src_pages,

@@ -2,15 +2,10 @@
 // calibration and a bulk e4m3 encoder.
 //
 // "Smaller, faster, safer: running Kimi and GLM at scale", section
-// "Quantizing the KV cache": the decode pool stores K and V as FP8 e4m3.
-// A new row x (bf16) becomes codes e4m3(fp32(x) / s): IEEE fp32 division,
-// round to nearest even, saturating at +-448; s is the head's calibrated
-// scale amax/448, or, in per-token mode, the row's own amax/448.  The
-// destination page is bounds- and (optionally) tag-checked first, as the
-// post's cache-protection passage does before a read; a refused row writes
-// nothing.
-#include "pfkv_device.cuh"
-#include "pfkv_internal.h"
+// "Quantizing the KV cache": the decode pool stores K and V as FP8 e4m3;
+// a new row is quantized as it is written (append_device.cuh holds the
+// per-row work and the destination check).
+#include "append_device.cuh"
 
 namespace pfkv {
 
@@ -30,67 +25,15 @@ __global__ void __launch_bounds__(128) append_kernel(pfkv_cache c, const uint16_
   const int b = row_req ? row_req[row] : row;
   if (b < 0 || b >= batch) return;
   const int pos = positions[row];
-  const int S = c.page_size;
-  uint32_t bad = 0;
   int page = -1;
-  if (pos < 0 || (long long)pos >= (long long)max_pages * S) {
-    bad = PFKV_ST_BAD_LEN;
-  } else {
-    const int i = pos / S;
-    page = block_table[(size_t)b * max_pages + i];
-    if (page < 0 || page >= c.num_pages) bad = PFKV_ST_PAGE_OOB;
-    else if ((flags & PFKV_FLAG_TAG_CHECK) && c.page_tags[page] != block_tags[(size_t)b * max_pages + i])
-      bad = PFKV_ST_STALE_TAG;
-  }
+  const uint32_t bad = append_target(c, b, pos, block_table, block_tags, max_pages, flags, &page);
   if (bad) {
     if (unit == 0 && lane == 0) atomicOr(&status[b], bad);
     return;
   }
   if (unit >= parts * c.num_kv_heads) return;
   const int part = unit / c.num_kv_heads, h = unit - part * c.num_kv_heads;
-  const int D = part ? c.v_head_dim : c.head_dim;
-  const uint16_t *src = (part ? v_new : k_new) + ((size_t)row * c.num_kv_heads + h) * D;
-  const size_t dst_row = ((size_t)page * c.num_kv_heads + h) * S + (pos % S);
-  if constexpr (!kFp8) {
-    uint16_t *dst = reinterpret_cast<uint16_t *>(part ? c.v_pool : c.k_pool) + dst_row * D;
-    for (int k = lane * 8; k < D; k += 256)
-      *reinterpret_cast<uint4 *>(dst + k) = *reinterpret_cast<const uint4 *>(src + k);
-  } else {
-    uint8_t *dst = reinterpret_cast<uint8_t *>(part ? c.v_pool : c.k_pool) + dst_row * D;
-    float *scale_arr = part ? c.v_scale : c.k_scale;
-    float s;
-    if (c.scale_mode == PFKV_SCALE_PER_TOKEN) {
-      float amax = 0.f;
-      for (int k = lane * 8; k < D; k += 256) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(src + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
-          amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
-        }
-      }
-      for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-      if (lane == 0) scale_arr[dst_row] = s;
-    } else {
-      s = scale_arr[h];
-    }
-    for (int k = lane * 8; k < D; k += 256) {
-      const uint4 v = *reinterpret_cast<const uint4 *>(src + k);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t out[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[2 * j] << 16), s),
-                                            __fdiv_rn(__uint_as_float(w[2 * j] & 0xffff0000u), s));
-        const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[2 * j + 1] << 16), s),
-                                            __fdiv_rn(__uint_as_float(w[2 * j + 1] & 0xffff0000u), s));
-        out[j] = lo | (hi << 16);
-      }
-      *reinterpret_cast<uint2 *>(dst + k) = make_uint2(out[0], out[1]);
-    }
-  }
+  append_row_warp<kFp8>(c, k_new, v_new, row, part, h, page, pos, lane);
 }
 
 // amax per head into scale[] (as fp32 bits, non-negative floats order like uints)

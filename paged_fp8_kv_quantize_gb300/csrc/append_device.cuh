@@ -1,0 +1,88 @@
+// append_device.cuh -- one warp writes one (row, K|V, head) of a new token
+// into the paged cache.  Used by the stand-alone append kernel and by the
+// decode step, whose plan grid appends the step's new tokens beside the
+// planning block.
+//
+// "Smaller, faster, safer: running Kimi and GLM at scale", section
+// "Quantizing the KV cache": the decode pool stores K and V as FP8 e4m3.
+// A new row x (bf16) becomes codes e4m3(fp32(x) / s): IEEE fp32 division,
+// round to nearest even, saturating at +-448; s is the head's calibrated
+// scale amax/448, or, in per-token mode, the row's own amax/448 (1 for an
+// all-zero row).  A BF16 cache takes the bits as they are.  The destination
+// page is bounds- and (optionally) tag-checked first, as the post's
+// cache-protection passage does before a read; a refused row writes nothing.
+#pragma once
+
+#include "pfkv_device.cuh"
+#include "pfkv_internal.h"
+
+namespace pfkv {
+
+// Destination check of an append at logical position pos of request b.
+// Returns 0 or the PFKV_ST_* bit; *page gets the physical page when 0.
+__device__ __forceinline__ uint32_t append_target(const pfkv_cache &c, int b, int pos, const int *block_table,
+                                                  const uint32_t *block_tags, int max_pages, uint32_t flags,
+                                                  int *page) {
+  const int S = c.page_size;
+  if (pos < 0 || (long long)pos >= (long long)max_pages * S) return PFKV_ST_BAD_LEN;
+  const int i = pos / S;
+  const int p = block_table[(size_t)b * max_pages + i];
+  if (p < 0 || p >= c.num_pages) return PFKV_ST_PAGE_OOB;
+  if ((flags & PFKV_FLAG_TAG_CHECK) && c.page_tags[p] != block_tags[(size_t)b * max_pages + i])
+    return PFKV_ST_STALE_TAG;
+  *page = p;
+  return 0u;
+}
+
+// Writes row `row` of k_new / v_new ([rows][num_kv_heads][dim] bf16), part
+// (0 = K, 1 = V) and head h, to slot pos % S of `page`.  Whole warp.
+template <bool kFp8>
+__device__ __forceinline__ void append_row_warp(const pfkv_cache &c, const uint16_t *k_new, const uint16_t *v_new,
+                                                int row, int part, int h, int page, int pos, int lane) {
+  const int S = c.page_size;
+  const int D = part ? c.v_head_dim : c.head_dim;
+  const uint16_t *src = (part ? v_new : k_new) + ((size_t)row * c.num_kv_heads + h) * D;
+  const size_t dst_row = ((size_t)page * c.num_kv_heads + h) * S + (pos % S);
+  if constexpr (!kFp8) {
+    uint16_t *dst = reinterpret_cast<uint16_t *>(part ? c.v_pool : c.k_pool) + dst_row * D;
+    for (int k = lane * 8; k < D; k += 256)
+      *reinterpret_cast<uint4 *>(dst + k) = *reinterpret_cast<const uint4 *>(src + k);
+  } else {
+    uint8_t *dst = reinterpret_cast<uint8_t *>(part ? c.v_pool : c.k_pool) + dst_row * D;
+    float *scale_arr = part ? c.v_scale : c.k_scale;
+    float s;
+    if (c.scale_mode == PFKV_SCALE_PER_TOKEN) {
+      float amax = 0.f;
+      for (int k = lane * 8; k < D; k += 256) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(src + k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+        }
+      }
+      for (int off = 16; off; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      if (lane == 0) scale_arr[dst_row] = s;
+    } else {
+      s = scale_arr[h];
+    }
+    for (int k = lane * 8; k < D; k += 256) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(src + k);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t out[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[2 * j] << 16), s),
+                                            __fdiv_rn(__uint_as_float(w[2 * j] & 0xffff0000u), s));
+        const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(__uint_as_float(w[2 * j + 1] << 16), s),
+                                            __fdiv_rn(__uint_as_float(w[2 * j + 1] & 0xffff0000u), s));
+        out[j] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint2 *>(dst + k) = make_uint2(out[0], out[1]);
+    }
+  }
+}
+
+}  // namespace pfkv

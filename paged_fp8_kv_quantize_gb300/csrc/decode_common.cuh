@@ -6,6 +6,7 @@
 
 #include <math.h>
 
+#include "append_device.cuh"
 #include "pfkv_device.cuh"
 #include "pfkv_internal.h"
 
@@ -25,8 +26,43 @@ struct ItemDesc {
 
 constexpr int kSortMax = 2048;  // requests ordered by length when the batch is at most this
 
+// Blocks after the first (decode step only): one warp per (request, K|V,
+// head) writes the step's new token at position seq_lens[b] - 1.  The split
+// kernel's grid-dependency wait covers this whole grid, so its page reads
+// see the new rows.  Status is the planning block's: the attention inspects
+// the same destination page under the same rules, so every refusal here is
+// also a status bit there.
+__device__ __forceinline__ void plan_append(const DecodeArgs &a) {
+  // heads of the cache itself (a work-item view such as the latent kernel's
+  // head groups may use another Hkv in the rest of DecodeArgs)
+  const int H = a.cache.num_kv_heads;
+  const int units = (a.cache.kv_shared ? 1 : 2) * H;
+  const int gw = (int)(blockIdx.x - 1) * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5);
+  const int b = gw / units, unit = gw - b * units;
+  if (b >= a.B) return;
+  const int pos = a.seq_lens[b] - 1;
+  int page = -1;
+  if (append_target(a.cache, b, pos, a.block_table, a.block_tags, a.MP, a.flags, &page)) return;
+  const int part = unit / H, h = unit - part * H;
+  if (a.cache.dtype == PFKV_DTYPE_FP8_E4M3)
+    append_row_warp<true>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, threadIdx.x & 31);
+  else
+    append_row_warp<false>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, threadIdx.x & 31);
+}
+
+// Number of plan-grid blocks: the planning block plus the append blocks.
+inline int plan_blocks(const DecodeArgs &a) {
+  if (!a.append) return 1;
+  const long long warps = (long long)a.B * (a.cache.kv_shared ? 1 : 2) * a.cache.num_kv_heads;
+  return 1 + (int)((warps + 31) / 32);
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
   pdl_launch_dependents();  // the split kernel waits for this grid's results before reading them
+  if (blockIdx.x > 0) {
+    plan_append(a);
+    return;
+  }
   __shared__ long long s_red[32];
   __shared__ int s_scan[32];
   __shared__ int s_carry;

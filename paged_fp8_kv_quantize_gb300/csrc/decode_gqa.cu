@@ -701,7 +701,7 @@ int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const 
       cache[slot] = sh;
     }
   }
-  plan_kernel<<<1, 1024, 0, s>>>(a, sh.grid * 8, (1024 + a.S - 1) / a.S);
+  plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, sh.grid * 8, (1024 + a.S - 1) / a.S);
   int rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
   if (rc) return rc;
   // The split kernel may start while the plan kernel runs; it waits for the

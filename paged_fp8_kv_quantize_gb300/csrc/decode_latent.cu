@@ -537,7 +537,7 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
       grid = num_sms() * per_sm;
     }
   }
-  plan_kernel<<<1, 1024, 0, s>>>(a, grid * 8, (1024 + kLS - 1) / kLS);
+  plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, grid * 8, (1024 + kLS - 1) / kLS);
   int rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
   if (rc) return rc;
   cudaLaunchAttribute attr[1];

@@ -49,6 +49,12 @@ struct DecodeArgs {
   float *part_o;
   float *out;
   uint32_t *status;
+  // decode step only (append == 1): new rows k_new / v_new [B][Hkv][D] bf16
+  // go to position seq_lens[b] - 1 of each request before attention; the
+  // plan grid writes them through `cache` (the same pools, writable).
+  int append;
+  const uint16_t *k_new, *v_new;
+  pfkv_cache cache;
 };
 
 // Tensor-map encoder obtained from the driver without linking libcuda.
