@@ -38,7 +38,7 @@ int num_sms() {
 
 static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool latent) {
   WsLayout w;
   const size_t slots = (size_t)batch * max_splits * q_heads;
   w.hdr = 0;
@@ -47,7 +47,9 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
   w.chunk_info = w.split_count + up256(sizeof(int) * (size_t)batch);
   w.part_ml = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
   w.part_o = w.part_ml + up256(sizeof(float2) * slots);
-  w.total = w.part_o + up256(sizeof(float) * slots * v_dim);
+  w.qterms = w.part_o + up256(sizeof(float) * slots * v_dim);
+  w.qfac = w.qterms + (latent ? up256(kLatentQTermBytes * (size_t)batch) : 0);
+  w.total = w.qfac + (latent ? up256(sizeof(float) * (size_t)batch * q_heads) : 0);
   return w;
 }
 
@@ -96,7 +98,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   if (Hq % c->num_kv_heads) return PFKV_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(out)) return PFKV_ERR_ALIGN;
   if (c->page_size % 16 || c->page_size > 256) return PFKV_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(batch, Hq, c->v_head_dim, max_splits);
+  const WsLayout L = ws_layout(batch, Hq, c->v_head_dim, max_splits, is_latent(c));
   if (ws_bytes < L.total) return PFKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return PFKV_ERR_ALIGN;
 
@@ -122,6 +124,9 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.k_new = static_cast<const uint16_t *>(k_new);
   a.v_new = static_cast<const uint16_t *>(v_new);
   a.cache = *c;
+  a.qprep = 0;
+  a.qterms = w + L.qterms;
+  a.qfac = reinterpret_cast<float *>(w + L.qfac);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (c->kv_shared) {
     if (!is_latent(c) || Hq != 64 || c->dtype != PFKV_DTYPE_FP8_E4M3 || c->scale_mode != PFKV_SCALE_PER_TOKEN ||
@@ -181,7 +186,7 @@ int pfkv_kv_append_quantize(const pfkv_cache *cache, const void *k_new, const vo
 
 size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32_t num_q_heads, int32_t max_splits) {
   if (!cache || batch < 0 || num_q_heads < 1 || max_splits < 1) return 0;
-  return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits).total;
+  return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits, is_latent(cache)).total;
 }
 
 int pfkv_paged_decode_attention_fp8(const pfkv_cache *cache, const void *q, int32_t num_q_heads,

@@ -4,6 +4,7 @@
 // linkage.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "append_device.cuh"
@@ -50,17 +51,86 @@ __device__ __forceinline__ void plan_append(const DecodeArgs &a) {
     append_row_warp<false>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, threadIdx.x & 31);
 }
 
-// Number of plan-grid blocks: the planning block plus the append blocks.
-inline int plan_blocks(const DecodeArgs &a) {
-  if (!a.append) return 1;
+// Append blocks of the plan grid (decode step only).
+__host__ __device__ inline int plan_append_blocks(const DecodeArgs &a) {
+  if (!a.append) return 0;
   const long long warps = (long long)a.B * (a.cache.kv_shared ? 1 : 2) * a.cache.num_kv_heads;
-  return 1 + (int)((warps + 31) / 32);
+  return (int)((warps + 31) / 32);
+}
+
+// Number of plan-grid blocks: the planning block, the append blocks, and
+// (latent stream) one query-term block per request.
+__host__ __device__ inline int plan_blocks(const DecodeArgs &a) { return 1 + plan_append_blocks(a) + (a.qprep ? a.B : 0); }
+
+// Query terms of request b for the latent-stream kernel.  Head h's bf16 row
+// q (576 values) is scaled by 2^-e_h, e_h = the exponent that puts max|q| in
+// [128, 256), and written as T1 = e4m3(q 2^-e_h), T2 = e4m3(q 2^-e_h - T1):
+// T1 + T2 equals the scaled row exactly for every element of magnitude at
+// least 2^-2 (a bf16 significand has 8 bits, each term carries 4), the
+// rest to within 2^-10.  The terms are stored as the kernel's shared-memory
+// image of 128-byte column blocks with the 128-byte swizzle (row h, 16-byte
+// chunk j at h*128 + 16*(j ^ (h & 7))): blocks 0-3 hold columns 0-511 of T1,
+// blocks 4-7 the same of T2, block 8 columns 512-575 of T1 in its chunks
+// 0-3 and of T2 in chunks 4-7.  qfac[h] = softmax scale * log2(e) * 2^e_h.
+__device__ __forceinline__ void plan_qprep(const DecodeArgs &a, int b) {
+  __shared__ float s_qinv[64];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint16_t *q = static_cast<const uint16_t *>(a.q) + (size_t)b * 64 * 576;
+  for (int h = warp; h < 64; h += (int)(blockDim.x >> 5)) {
+    float m = 0.f;
+    for (int k = lane; k < 576; k += 32) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)q[h * 576 + k] << 16)));
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) {
+      int e = 8;
+      if (m > 0.f) frexpf(m, &e);  // m = f 2^e, f in [0.5, 1)
+      s_qinv[h] = ldexpf(1.f, 8 - e);
+      a.qfac[(size_t)b * 64 + h] = a.sm_scale_log2 * ldexpf(1.f, e - 8);
+    }
+  }
+  __syncthreads();
+  uint8_t *dst = a.qterms + (size_t)b * kLatentQTermBytes;
+  for (int u = tid; u < 64 * 36; u += (int)blockDim.x) {
+    const int h = u / 36, r = u % 36;
+    const int k0 = 16 * r;  // 16 columns starting here (r < 36 covers all 576)
+    size_t off1, off2;
+    if (r < 32) {
+      const int c = r / 8, j = r % 8;
+      off1 = (size_t)c * 8192 + h * 128 + 16 * (j ^ (h & 7));
+      off2 = off1 + 4 * 8192;
+    } else {
+      const int j = r - 32;
+      off1 = (size_t)8 * 8192 + h * 128 + 16 * (j ^ (h & 7));
+      off2 = (size_t)8 * 8192 + h * 128 + 16 * ((j + 4) ^ (h & 7));
+    }
+    uint32_t t1[4], t2[4];
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>(q + h * 576 + k0);
+      const uint4 v0 = src[0], v1 = src[1];
+      const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      const float inv = s_qinv[h];
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const float x0 = __uint_as_float(wv[i] << 16) * inv, x1 = __uint_as_float(wv[i] & 0xffff0000u) * inv;
+        const float x2 = __uint_as_float(wv[i + 1] << 16) * inv, x3 = __uint_as_float(wv[i + 1] & 0xffff0000u) * inv;
+        const uint32_t a01 = f32x2_to_e4m3x2(x0, x1), a23 = f32x2_to_e4m3x2(x2, x3);
+        const uint32_t h01 = e4m3x2_to_f16x2(a01), h23 = e4m3x2_to_f16x2(a23);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+        t1[i / 2] = a01 | (a23 << 16);
+        t2[i / 2] = f32x2_to_e4m3x2(x0 - f01.x, x1 - f01.y) | (f32x2_to_e4m3x2(x2 - f23.x, x3 - f23.y) << 16);
+      }
+    }
+    *reinterpret_cast<uint4 *>(dst + off1) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
+    *reinterpret_cast<uint4 *>(dst + off2) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
+  }
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
   pdl_launch_dependents();  // the split kernel waits for this grid's results before reading them
   if (blockIdx.x > 0) {
-    plan_append(a);
+    const int nab = plan_append_blocks(a);
+    if ((int)blockIdx.x <= nab) plan_append(a);
+    else plan_qprep(a, (int)blockIdx.x - 1 - nab);
     return;
   }
   __shared__ long long s_red[32];

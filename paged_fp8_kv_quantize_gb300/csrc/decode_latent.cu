@@ -1,35 +1,36 @@
-// decode_latent.cu -- decode attention over a latent-shared FP8 stream:
-// 64 query heads read one 576-wide stream per token (512 latent + 64 rotary
-// values); V is the first 512 values of the same row; one fp32 scale per
-// cached token; pages of 64 tokens.
+// decode_latent.cu -- decode attention over a latent-shared FP8 stream on the
+// fifth-generation tensor cores: 64 query heads read one 576-wide stream per
+// token (512 latent + 64 rotary values); V is the first 512 values of the
+// same row; one fp32 scale per cached token; pages of 64 tokens.
 //
 // "Smaller, faster, safer: running Kimi and GLM at scale", section
 // "Quantizing the KV cache": the cache is FP8 e4m3 and is converted as it is
-// read.  Here the conversion is folded into the tensor cores: both
-// contractions run on FP8 (e4m3 x e4m3 -> fp32) register-operand MMA, with
-// the higher-precision operand written as a sum of e4m3 terms that share one
-// scale and are stacked along the contraction:
-//   QK^T: a bf16 query row q/2^e = T1 + T2 + T3 (three e4m3 terms; a bf16
-//         significand has 8 bits, each term carries 4, so the sum is exact
-//         except far below the row's largest element), contracted against the
-//         cached codes as they arrived in shared memory -- no conversion.
-//   PV:   the probabilities, with the per-token scale folded in through a
-//         second running maximum (log2 s_t is added to the score), are
-//         written as P1 + P2 (two e4m3 terms, about 8 bits), contracted
-//         against the cached codes of the first 512 values.
-// The softmax normaliser l is summed from the exact fp32 probabilities.
+// read.  With 64 heads on one stream the step is a dense contraction
+// (about 240 flop per cached byte), so both products run as tcgen05 MMAs of
+// kind f8f6f4 (e4m3 x e4m3 -> fp32 in tensor memory), straight from the
+// codes the TMA engine landed in shared memory:
+//   S^T = K . Q^T   M = 64 tokens (one page), N = 64 heads, K = 576.  The
+//        bf16 query of head h is q_h = 2^e_h (T1 + T2), two e4m3 terms with
+//        one power-of-two scale; T1 + T2 is exact for every element within
+//        2^10 of the row's largest, so the term split adds no error that
+//        matters.  Terms are prepared once per request by the plan grid.
+//   O^T += V^T . P^T   M = 128 values (four chunks of the 512), N = 64
+//        heads, K = 64 tokens.  V^T is the page itself read MN-major.  The
+//        probabilities, with the token's scale folded in relative to a
+//        running reference scale, are written as P1 + P2 + P3 (three e4m3
+//        terms, about 12 significant bits) by the softmax warps.
+// The softmax normaliser l is summed from the fp32 probabilities.
 //
-// Work item = (split of a request, group of 16 heads).  A CTA has one
-// producer warp (bulk copies of whole pages plus their scales into a ring,
-// page ids bounds-checked and tags compared beside the copies, as in the
-// grouped kernel) and four consumer warps.  Per pair of pages (128 tokens):
-// warp w computes S for the 16 heads x 32 tokens of k-block w; the four
-// warps agree on the running maxima through shared memory; each writes its
-// block's P terms as MMA operand fragments; then warp w accumulates
-// O[16 heads x 128 values] for its quarter of V over all 128 tokens.  The
-// QK^T accumulator layout is, token for token, the layout of the PV operand,
-// so no shuffles are needed between the two.  Partials are merged by the
+// One CTA per SM, persistent, work item = (request, split of its pages),
+// all 64 heads.  Warp 0 loads pages (TMA, 128-byte swizzle, bounds and tag
+// checks beside the copies) and the query terms; warp 1 owns tensor memory
+// and issues the MMAs (one thread); warps 2-5 read S^T from tensor memory,
+// run the online softmax (running maxima move only when they grow by more
+// than 2x, and only then is O^T rescaled in tensor memory), write P^T, and
+// write the item's partial or final output.  Partials are merged by the
 // shared log-sum-exp merge kernel.
+#include <cuda_fp16.h>
+
 #include <mutex>
 
 #include "decode_common.cuh"
@@ -38,527 +39,616 @@ namespace pfkv {
 
 namespace {
 
-constexpr int kLD = 576;                         // stream width
-constexpr int kLDv = 512;                        // V = leading values
-constexpr int kLS = 64;                          // tokens per page
-constexpr int kLHG = 16;                         // heads per work item
-constexpr int kLGroups = 4;                      // head groups of 64 heads
-constexpr int kLNCW = 4;                         // consumer warps
-constexpr int kQT = 3;                           // e4m3 terms of the query
-constexpr int kPT = 2;                           // e4m3 terms of the probabilities
-constexpr int kDSteps = kLD / 32;                // 18 contraction steps of 32
-constexpr uint32_t kPageBytes = kLS * kLD;       // 36864
-constexpr uint32_t kStageBytes = kPageBytes + kLS * 4;  // + per-token scales
-constexpr int kLThreads = (kLNCW + 1) * 32;
-constexpr float kPScaleL = 256.f;                // probabilities in [0, 1] -> [0, 256]
+constexpr int kTD = 576;                      // stream width
+constexpr int kTDv = 512;                     // V = leading values
+constexpr int kTS = 64;                       // tokens per page
+constexpr int kTH = 64;                       // query heads
+constexpr int kTBlocks = 5;                   // 128-byte column blocks of a row (the last one half used)
+constexpr uint32_t kBlk = kTS * 128;          // 8192: one column block of a page or of a query term
+constexpr uint32_t kPageSm = kTBlocks * kBlk;  // 40960
+// Query terms: blocks 0-3 of T1, blocks 0-3 of T2, then one block whose
+// rows hold the last 64 columns of T1 (bytes 0-63) and of T2 (64-127).
+constexpr uint32_t kQBytes = 9 * kBlk;        // 73728
+constexpr uint32_t kQTail = 8 * kBlk;
+constexpr int kPT = 3;                        // e4m3 terms of the probabilities
+constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
+constexpr uint32_t kPBuf = kPT * kPTerm;      // 12288
+constexpr int kNst = 3;                       // pages in flight per CTA
+constexpr int kTThreads = 192;                // producer, MMA, four softmax warps
+constexpr uint32_t kTmemCols = 512;           // S^T x2 (64 columns each), O^T (4 x 64)
+constexpr uint32_t kColS = 0, kColO = 128;
+constexpr float kPExp = 6.75f;                // P'' = p (s_t / s_ref) 2^kPExp <= 2 * 2 * 2^6.75 < 448
+constexpr float kTheta = 1.f;                 // log2 growth of a running max that triggers a rescale
+constexpr uint32_t kIdQK = umma_idesc_e4m3(64, 64, 0, 0);
+constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 64, 1, 1);
 
-struct LatSmem {
-  uint32_t stages_off, qfrag_off, pfrag_off, exch_off, bars_off, items_off, total;
+struct TcSmem {
+  uint32_t ring, q, p, scales, wg, bars, items, total;
 };
 
-__host__ __device__ inline LatSmem lat_smem(int nst) {
-  LatSmem p;
-  p.stages_off = 0;
-  p.qfrag_off = p.stages_off + kStageBytes * nst;                  // [term][step][lane] x 16 B
-  p.pfrag_off = p.qfrag_off + kQT * kDSteps * 32 * 16;             // [kblock][term][lane] x 16 B
-  p.exch_off = p.pfrag_off + kLNCW * kPT * 32 * 16;                // maxima, sums, query scales
-  p.bars_off = p.exch_off + 4 * (2 * kLNCW * kLHG + kLNCW * kLHG + kLHG + 16);
-  p.bars_off = (p.bars_off + 15u) & ~15u;
-  p.items_off = p.bars_off + 8u * (2 * nst + 3 * kNIQ) + 16u;
-  p.total = p.items_off + (sizeof(ItemDesc) + 4u) * kNIQ + 128u;
-  return p;
+__host__ __device__ constexpr TcSmem tc_smem() {
+  TcSmem s{};
+  s.ring = 0;                                  // kNst pages, each 5 column blocks (1024-aligned)
+  s.q = s.ring + kNst * kPageSm;               // 2 query terms x 5 blocks
+  s.p = s.q + kQBytes;                         // 2 buffers x kPT P^T terms
+  s.scales = s.p + 2 * kPBuf;                  // kNst x 64 per-token scales
+  s.wg = s.scales + kNst * kTS * 4;            // softmax-warp scratch (see below)
+  s.bars = s.wg + 4 * (64 * 4 + 4 * 64 + 8);   // cq, m, alpha, beta | ex[4][64] | ex_s[4], misc
+  s.items = s.bars + 8 * (2 * kNst + 12 + 3 * kNIQ);
+  s.total = s.items + (sizeof(ItemDesc) + 4) * kNIQ + 16;
+  return s;
+}
+static_assert(tc_smem().total + 1024 <= 232448, "shared memory plan exceeds one SM");
+
+// Softmax-warp scratch, floats: cq[64] | m[64] | alpha[64] | beta[64] | ex[4][64] | ex_s[4] | pad
+constexpr int kWgCq = 0, kWgM = 64, kWgAlpha = 128, kWgBeta = 192, kWgEx = 256, kWgExS = 512;
+
+// Bounded wait that ignores the abort flag: used on the way out, so that a
+// block that gave up still lets its own copies and MMAs land before it exits.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
 }
 
-// Physical column of the stream for contraction step s, logical index k
-// (0..31) of thread quad position tq: each thread's bytes for steps 2s',
-// 2s'+1 are 16 contiguous bytes at 64 s' + 16 tq.
-__device__ __forceinline__ int qk_col(int s, int tq, int half, int j) {
-  return 64 * (s >> 1) + 16 * tq + 8 * (s & 1) + 4 * half + j;
+struct Bars {
+  uint64_t *full, *empty, *s_full, *s_empty, *p_full, *p_empty, *q_full, *q_empty, *o_empty, *drain;
+  uint64_t *item_full, *item_empty, *item_done;
+};
+
+__device__ __forceinline__ Bars bars_at(uint8_t *base) {
+  uint64_t *b = reinterpret_cast<uint64_t *>(base);
+  Bars r;
+  r.full = b; b += kNst;
+  r.empty = b; b += kNst;
+  r.s_full = b; b += 2;
+  r.s_empty = b; b += 2;
+  r.p_full = b; b += 2;
+  r.p_empty = b; b += 2;
+  r.q_full = b; b += 1;
+  r.q_empty = b; b += 1;
+  r.o_empty = b; b += 1;
+  r.drain = b; b += 1;
+  r.item_full = b; b += kNIQ;
+  r.item_empty = b; b += kNIQ;
+  r.item_done = b;
+  return r;
 }
 
-__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
-  return f32x2_to_e4m3x2(a, b) | (f32x2_to_e4m3x2(c, d) << 16);
-}
+// ---------------------------------------------------------------- producer (warp 0)
 
-// 4x4 byte transpose: out[x] = byte x of r0..r3.
-__device__ __forceinline__ void transpose4x4(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3, uint32_t (&o)[4]) {
-  const uint32_t t0 = prmt(r0, r1, 0x5140u), t1 = prmt(r0, r1, 0x7362u);
-  const uint32_t t2 = prmt(r2, r3, 0x5140u), t3 = prmt(r2, r3, 0x7362u);
-  o[0] = prmt(t0, t2, 0x5410u);
-  o[1] = prmt(t0, t2, 0x7632u);
-  o[2] = prmt(t1, t3, 0x5410u);
-  o[3] = prmt(t1, t3, 0x7632u);
-}
-
-__global__ void __launch_bounds__(kLThreads, 2) latent_split_kernel(const DecodeArgs a, const int nst) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const LatSmem sp = lat_smem(nst);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + sp.bars_off);
-  uint64_t *empty = full + nst;
-  uint64_t *item_full = empty + nst;
-  uint64_t *item_empty = item_full + kNIQ;
-  uint64_t *item_done = item_empty + kNIQ;
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(item_done + kNIQ);
-  ItemDesc *items = reinterpret_cast<ItemDesc *>(smem + sp.items_off);
-  uint32_t *item_status = reinterpret_cast<uint32_t *>(items + kNIQ);
-  float *ex_m = reinterpret_cast<float *>(smem + sp.exch_off);  // [warp][head] score maxima
-  float *ex_mv = ex_m + kLNCW * kLHG;                            // [warp][head] value-weight maxima
-  float *ex_l = ex_mv + kLNCW * kLHG;                            // [warp][head] sums
-  float *sq_scale = ex_l + kLNCW * kLHG;                         // [head] query scale 2^e
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < nst; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kLNCW);
+__device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorMap &map, uint8_t *smem,
+                                            const Bars &B, ItemDesc *items, uint32_t *item_status,
+                                            volatile int *abort_flag) {
+  const TcSmem sp = tc_smem();
+  const int lane = threadIdx.x & 31;
+  const int n_items = a.hdr->n_items;
+  const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
+  uint32_t g = 0;  // pages issued by this CTA
+  uint32_t it = 0, q_loads = 0;
+  bool ok = true;
+  for (;; ++it) {
+    int item = 0;
+    if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    const uint32_t slot = it % kNIQ;
+    bool w = true;
+    if (lane == 0) w = mbar_wait(&B.item_empty[slot], ((it / kNIQ) & 1u) ^ 1u, abort_flag);
+    if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+    if (item >= n_items) {
+      if (lane == 0) {
+        items[slot].b = -1;
+        mbar_arrive(&B.item_full[slot]);
+      }
+      break;
     }
+    const int4 info = a.chunk_info[2 * item], info2 = a.chunk_info[2 * item + 1];
+    const int b = info.x, p0 = info.y, p1 = info.z;
+    if (lane == 0) {
+      ItemDesc d;
+      d.b = b; d.cg = item; d.g = 0; d.p0 = p0; d.p1 = p1; d.L = info.w; d.ring = g; d.nb = info2.x;
+      items[slot] = d;
+      mbar_arrive(&B.item_full[slot]);
+      // the request's query terms, once the previous item's last QK^T is done
+      if (mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag)) {
+        mbar_arrive_expect_tx(B.q_full, kQBytes);
+        const uint8_t *src = a.qterms + (size_t)b * kQBytes;
+        for (uint32_t o = 0; o < kQBytes; o += kBlk) bulk_load(smem + sp.q + o, src + o, kBlk, B.q_full);
+        ++q_loads;
+      }
+    }
+    const int *trow = a.block_table + (size_t)b * a.MP;
+    const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
+    uint32_t st_bits = 0;
+    for (int i0 = p0; i0 < p1 && ok; i0 += kNst) {
+      const int i = i0 + lane;
+      const bool valid = lane < kNst && i < p1;
+      const int pid = valid ? __ldg(&trow[i]) : 0;
+      const bool oob = valid && (pid < 0 || pid >= a.P);
+      uint32_t page_tag = 0, want_tag = 0;
+      if (tag_check && valid && !oob) {  // loads issued now, compared after the copies
+        page_tag = __ldg(&a.page_tags[pid]);
+        want_tag = __ldg(&tagrow[i]);
+      }
+      bool lane_ok = true;
+      if (valid) {
+        const uint32_t r = g + (uint32_t)lane;
+        const uint32_t st = r % kNst;
+        lane_ok = mbar_wait(&B.empty[st], ((r / kNst) & 1u) ^ 1u, abort_flag);
+        if (lane_ok) {
+          if (oob) {
+            mbar_arrive(&B.full[st]);  // never fetched; the request is aborted
+          } else {
+            mbar_arrive_expect_tx(&B.full[st], kPageSm + kTS * 4);
+            uint8_t *stage = smem + sp.ring + st * kPageSm;
+#pragma unroll
+            for (int c = 0; c < kTBlocks; ++c) tma_load_3d(stage + c * kBlk, &map, &B.full[st], 128 * c, 0, pid);
+            bulk_load(smem + sp.scales + st * (kTS * 4), a.k_scale + (size_t)pid * kTS, kTS * 4, &B.full[st]);
+          }
+        }
+      }
+      g += (uint32_t)min(kNst, p1 - i0);
+      ok = __all_sync(0xffffffffu, lane_ok);
+      if (__any_sync(0xffffffffu, oob)) st_bits |= PFKV_ST_PAGE_OOB;
+      if (__any_sync(0xffffffffu, page_tag != want_tag)) st_bits |= PFKV_ST_STALE_TAG;
+    }
+    if (lane == 0) {
+      item_status[slot] = st_bits;
+      if (st_bits) atomicOr(&a.status[b], st_bits);
+      mbar_arrive(&B.item_done[slot]);
+    }
+    if (!ok) break;
+  }
+  // Copies still in flight land before the block may exit: the last pages
+  // issued and the last query load.
+  if (lane == 0) {
+    for (uint32_t k = g > kNst ? g - kNst : 0; k < g; ++k) drain_wait(&B.full[k % kNst], (k / kNst) & 1u);
+    if (q_loads) drain_wait(B.q_full, (q_loads - 1) & 1u);
+  }
+}
+
+// ---------------------------------------------------------------- MMA issuer (warp 1, one thread)
+
+__device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const Bars &B, const ItemDesc *items,
+                                       uint32_t tmem, volatile int *abort_flag) {
+  const TcSmem sp = tc_smem();
+  const uint32_t s_ring = smem_addr(smem + sp.ring), s_q = smem_addr(smem + sp.q), s_p = smem_addr(smem + sp.p);
+  uint32_t g = 0;   // pages consumed
+  uint32_t it = 0;  // items
+  bool ok = true;
+  // PV of page gp (j-th page of its item): O^T[c] (+)= V^T_c . (P1 + P2)^T
+  auto pv = [&](uint32_t gp, bool first) -> bool {
+    const uint32_t pb = gp & 1u;
+    if (!mbar_wait(&B.p_full[pb], (gp >> 1) & 1u, abort_flag)) return false;
+    tc_fence_after();
+    const uint32_t st = gp % kNst;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int t = 0; t < kPT; ++t)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + ks * 4096, 8192, 1024, 2);
+          const uint64_t db = umma_sdesc(s_p + pb * kPBuf + t * kPTerm + ks * 512, 128, 1024, 0);
+          umma_e4m3(tmem + kColO + 64 * c, da, db, kIdPV, (first && t == 0 && ks == 0) ? 0u : 1u);
+        }
+    umma_commit(&B.empty[st]);
+    umma_commit(&B.p_empty[pb]);
+    return true;
+  };
+  for (;; ++it) {
+    const uint32_t slot = it % kNIQ;
+    if (!mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag)) break;
+    const ItemDesc d = items[slot];
+    mbar_arrive(&B.item_empty[slot]);
+    if (d.b < 0) break;
+    const uint32_t n = (uint32_t)(d.p1 - d.p0);
+    if (!mbar_wait(B.q_full, it & 1u, abort_flag)) break;
+    for (uint32_t j = 0; j < n && ok; ++j) {
+      const uint32_t gp = g + j, st = gp % kNst, sb = gp & 1u;
+      if (!mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
+          !mbar_wait(&B.s_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // S^T[sb] = K_page . (T1 + T2)^T over the 576 columns (18 steps of 32 per term)
+      uint32_t acc = 0;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int c = 0; c < kTBlocks; ++c)
+#pragma unroll
+          for (int kk = 0; kk < (c < 4 ? 4 : 2); ++kk) {
+            const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + kk * 32, 16, 1024, 2);
+            const uint32_t qb = c < 4 ? (uint32_t)(4 * t + c) * kBlk + kk * 32 : kQTail + (uint32_t)(2 * t + kk) * 32;
+            const uint64_t db = umma_sdesc(s_q + qb, 16, 1024, 2);
+            umma_e4m3(tmem + kColS + 64 * sb, da, db, kIdQK, acc);
+            acc = 1u;
+          }
+      umma_commit(&B.s_full[sb]);
+      if (j + 1 == n) umma_commit(B.q_empty);  // the query terms may be replaced
+      if (j > 0) {
+        if (j == 1 && !mbar_wait(B.o_empty, (it & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+        if (!pv(gp - 1, j == 1)) { ok = false; break; }
+      }
+    }
+    if (!ok) break;
+    if (n == 1 && !mbar_wait(B.o_empty, (it & 1u) ^ 1u, abort_flag)) break;
+    if (!pv(g + n - 1, n == 1)) break;
+    g += n;
+  }
+  // every MMA issued above has completed before tensor memory is released
+  umma_commit(B.drain);
+  drain_wait(B.drain, 0);
+}
+
+
+// ---------------------------------------------------------------- softmax warps (warps 2-5)
+
+// Barrier of the four softmax warps that also ORs a flag over them.
+__device__ __forceinline__ bool wg_bar_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0u;
+}
+
+// e4m3 pair of x and the exact fp32 values the two codes stand for.
+__device__ __forceinline__ uint32_t e4m3_pair(float x0, float x1, float &v0, float &v1) {
+  const uint32_t c = f32x2_to_e4m3x2(x0, x1);
+  const uint32_t hv = e4m3x2_to_f16x2(c);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
+  v0 = f.x;
+  v1 = f.y;
+  return c;
+}
+
+// Three e4m3 terms of four non-negative floats: t1 = e4m3(x), t2 = e4m3(x -
+// t1), t3 = e4m3(x - t1 - t2) (each difference is exact in fp32).
+__device__ __forceinline__ void three_terms4(float x0, float x1, float x2, float x3, uint32_t &t1, uint32_t &t2,
+                                             uint32_t &t3) {
+  float a0, a1, a2, a3;
+  t1 = e4m3_pair(x0, x1, a0, a1) | (e4m3_pair(x2, x3, a2, a3) << 16);
+  x0 -= a0; x1 -= a1; x2 -= a2; x3 -= a3;
+  t2 = e4m3_pair(x0, x1, a0, a1) | (e4m3_pair(x2, x3, a2, a3) << 16);
+  t3 = f32x2_to_e4m3x2(x0 - a0, x1 - a1) | (f32x2_to_e4m3x2(x2 - a2, x3 - a3) << 16);
+}
+
+__device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, const Bars &B, const ItemDesc *items,
+                                           const uint32_t *item_status, uint32_t tmem, volatile int *abort_flag) {
+  const TcSmem sp = tc_smem();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp - 2;          // 0..3 among the softmax warps
+  const int gq = warp & 3;          // tensor-memory lane quarter this warp may access
+  const int wt = threadIdx.x - 64;  // 0..127
+  float *wg = reinterpret_cast<float *>(smem + sp.wg);
+  float *s_cq = wg + kWgCq, *s_m = wg + kWgM, *s_alpha = wg + kWgAlpha, *s_beta = wg + kWgBeta;
+  float *s_ex = wg + kWgEx, *s_exs = wg + kWgExS;
+  const float *scales = reinterpret_cast<const float *>(smem + sp.scales);
+  uint8_t *pbase = smem + sp.p;
+  const uint32_t tq = tmem + ((uint32_t)(32 * gq) << 16);  // this warp's lanes
+  // S^T row i (token i of the page) sits in lane 32 (i / 16) + i % 16: this
+  // warp holds tokens 16 gq .. 16 gq + 15 in its lanes 0-15.
+  const int t = 16 * gq + (lane & 15);
+  const bool tok_lane = lane < 16;
+  uint32_t g = 0;
+  for (uint32_t it = 0;; ++it) {
+    const uint32_t slot = it % kNIQ;
+    bool fail = !mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag);
+    if (wg_bar_or(fail)) break;
+    const ItemDesc d = items[slot];
+    if (d.b < 0) break;
+    const uint32_t n = (uint32_t)(d.p1 - d.p0);
+    if (wt < kTH) {
+      s_cq[wt] = __ldg(&a.qfac[(size_t)d.b * kTH + wt]);
+      s_m[wt] = kNegInf;
+    }
+    float s_ref = 0.f;
+    float lp[kTH];
+#pragma unroll
+    for (int h = 0; h < kTH; ++h) lp[h] = 0.f;
+    named_bar_sync(1, 128);
+    bool dead = false;
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t gp = g + j, sb = gp & 1u, st = gp % kNst;
+      fail = fail || !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
+             !mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
+             !mbar_wait(&B.p_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag);
+      float y[kTH];
+      {
+        tc_fence_after();
+        uint32_t r[32];
+        tmem_ld32(tq + kColS + 64 * sb, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(r[i]);
+        tmem_ld32(tq + kColS + 64 * sb + 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) y[32 + i] = __uint_as_float(r[i]);
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.s_empty[sb]);
+      const bool valid = tok_lane && (d.p0 + (int)j) * kTS + t < d.L;
+      const float s_t = valid ? scales[st * kTS + t] : 0.f;
+      // z (log2 units) = S * (tau log2(e) 2^e_h) * s_t; padding and spare lanes -> -inf
+#pragma unroll
+      for (int h = 0; h < kTH; h += 4) {
+        const float4 c4 = *reinterpret_cast<const float4 *>(&s_cq[h]);
+        y[h] = valid ? y[h] * c4.x * s_t : kNegInf;
+        y[h + 1] = valid ? y[h + 1] * c4.y * s_t : kNegInf;
+        y[h + 2] = valid ? y[h + 2] * c4.z * s_t : kNegInf;
+        y[h + 3] = valid ? y[h + 3] * c4.w * s_t : kNegInf;
+      }
+      // per-head maxima over the page: warp maxima, then over the four warps
+      float mine0 = kNegInf, mine1 = kNegInf;
+#pragma unroll
+      for (int h = 0; h < kTH; ++h) {
+        const float r = warp_max_f32(y[h]);
+        if (lane == (h & 31)) {
+          if (h < 32) mine0 = r;
+          else mine1 = r;
+        }
+      }
+      const float smx = warp_max_f32(s_t);
+      s_ex[wq * kTH + lane] = mine0;
+      s_ex[wq * kTH + 32 + lane] = mine1;
+      if (lane == 0) s_exs[wq] = smx;
+      if (wg_bar_or(fail)) {
+        dead = true;
+        break;
+      }
+      const float sm = fmaxf(fmaxf(s_exs[0], s_exs[1]), fmaxf(s_exs[2], s_exs[3]));
+      const float s_old = s_ref;
+      const float s_new = sm > 2.f * s_old ? sm : s_old;
+      bool resc = s_new != s_old;
+      if (wt < kTH) {
+        const float tm = fmaxf(fmaxf(s_ex[wt], s_ex[kTH + wt]), fmaxf(s_ex[2 * kTH + wt], s_ex[3 * kTH + wt]));
+        const float m_old = s_m[wt];
+        const float m_new = tm > m_old + kTheta ? tm : m_old;
+        const float alpha = fast_exp2(m_old - m_new);
+        s_m[wt] = m_new;
+        s_alpha[wt] = alpha;
+        s_beta[wt] = alpha * (s_old / s_new);
+        resc = resc || m_new != m_old;
+      }
+      s_ref = s_new;
+      resc = wg_bar_or(resc) && j > 0;
+      if (resc) {
+        // O^T so far holds the earlier pages: every head column h scaled by beta_h
+        // once the previous page's PV has landed; l by alpha_h.
+        fail = fail || !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag);
+        if (!fail) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[32];
+            const uint32_t ta = tq + kColO + 32 * c;
+            tmem_ld32(ta, r);
+            const float *bt = s_beta + 32 * (c & 1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bt[i]);
+            tmem_st32(ta, r);
+          }
+          tmem_wait_st();
+        }
+#pragma unroll
+        for (int h = 0; h < kTH; ++h) lp[h] *= s_alpha[h];
+      }
+      // P'' = p (s_t / s_ref) 2^kPExp as three e4m3 terms; p = 2^(z - m) summed into l
+      const float kt = valid ? fast_log2(s_t / s_ref) + kPExp : 0.f;
+      const float rt = fast_exp2(-kt);
+      // P^T, MN-major without swizzle: head chunks of 16 bytes, token rows 16 bytes apart
+      uint8_t *pt = pbase + sb * kPBuf + (t & 7) * 16 + (t >> 3) * 128;
+#pragma unroll
+      for (int hc = 0; hc < 4; ++hc) {
+        uint32_t w1[4], w2[4], w3[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int h = 16 * hc + 4 * q4;
+          const float4 m4 = *reinterpret_cast<const float4 *>(&s_m[h]);
+          const float p0 = fast_exp2(y[h] - m4.x + kt), p1 = fast_exp2(y[h + 1] - m4.y + kt);
+          const float p2 = fast_exp2(y[h + 2] - m4.z + kt), p3 = fast_exp2(y[h + 3] - m4.w + kt);
+          lp[h] += p0 * rt;
+          lp[h + 1] += p1 * rt;
+          lp[h + 2] += p2 * rt;
+          lp[h + 3] += p3 * rt;
+          three_terms4(p0, p1, p2, p3, w1[q4], w2[q4], w3[q4]);
+        }
+        if (tok_lane && !fail) {
+          *reinterpret_cast<uint4 *>(pt + hc * 1024) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+          *reinterpret_cast<uint4 *>(pt + kPTerm + hc * 1024) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+          *reinterpret_cast<uint4 *>(pt + 2 * kPTerm + hc * 1024) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.p_full[sb]);
+    }
+    if (dead) break;
+    // ---- the item's result: wait for its last PV and its status
+    const uint32_t gl = g + n - 1;
+    fail = fail || !mbar_wait(&B.p_empty[gl & 1u], (gl >> 1) & 1u, abort_flag) ||
+           !mbar_wait(&B.item_done[slot], (it / kNIQ) & 1u, abort_flag);
+    // l per head: over the 16 token lanes, then over the four warps
+#pragma unroll
+    for (int h = 0; h < kTH; ++h) {
+      float v = lp[h];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      if (lane == (h & 15)) s_ex[wq * kTH + h] = v;
+    }
+    if (wg_bar_or(fail)) break;
+    if (wt < kTH) s_alpha[wt] = s_ex[wt] + s_ex[kTH + wt] + s_ex[2 * kTH + wt] + s_ex[3 * kTH + wt];
+    named_bar_sync(1, 128);
+    tc_fence_after();
+    const uint32_t stv = item_status[slot];
+    const float oscale = s_ref * exp2f(-kPExp);  // O^T accumulates p (s_t / s_ref) 2^kPExp * code
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tq + kColO + 32 * c, r);
+      const int dd = 128 * (c >> 1) + 32 * gq + lane;  // value index of this thread's row
+      const int h0 = 32 * (c & 1);
+      if (d.nb == 1) {
+        float *o = a.out + (size_t)d.b * kTH * kTDv + dd;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          o[(size_t)(h0 + i) * kTDv] = stv ? 0.f : __uint_as_float(r[i]) * oscale / s_alpha[h0 + i];
+      } else {
+        float *o = a.part_o + (size_t)d.cg * kTH * kTDv + dd;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[(size_t)(h0 + i) * kTDv] = __uint_as_float(r[i]) * oscale;
+      }
+    }
+    if (d.nb != 1 && wt < kTH) a.part_ml[(size_t)d.cg * kTH + wt] = make_float2(s_m[wt], s_alpha[wt]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.o_empty);
+    named_bar_sync(1, 128);  // the scratch is reused by the next item
+    if (wt == 0) mbar_arrive(&B.item_empty[slot]);
+    g += n;
+  }
+}
+
+
+__global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_constant__ CUtensorMap map,
+                                                                 const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const TcSmem sp = tc_smem();
+  const Bars B = bars_at(smem + sp.bars);
+  ItemDesc *items = reinterpret_cast<ItemDesc *>(smem + sp.items);
+  uint32_t *item_status = reinterpret_cast<uint32_t *>(items + kNIQ);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(item_status + kNIQ);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(item_status + kNIQ + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNst; ++i) {
+      mbar_init(&B.full[i], 1);
+      mbar_init(&B.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.s_full[i], 1);
+      mbar_init(&B.s_empty[i], 4);
+      mbar_init(&B.p_full[i], 4);
+      mbar_init(&B.p_empty[i], 1);
+    }
+    mbar_init(B.q_full, 1);
+    mbar_init(B.q_empty, 1);
+    mbar_init(B.o_empty, 4);
+    mbar_init(B.drain, 1);
     for (int i = 0; i < kNIQ; ++i) {
-      mbar_init(&item_full[i], 1);
-      mbar_init(&item_empty[i], 1);
-      mbar_init(&item_done[i], 1);
+      mbar_init(&B.item_full[i], 1);
+      mbar_init(&B.item_empty[i], 2);  // the MMA thread and the softmax warps
+      mbar_init(&B.item_done[i], 1);
     }
     *abort_flag = 0;
     mbar_init_fence();
   }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   pdl_wait();
   pdl_launch_dependents();
-
-  if (warp == kLNCW) {
-    // ------------------------------------------------------------ producer
-    const int n_items = a.hdr->n_items;
-    const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
-    const int batch_pages = min(32, nst);
-    uint32_t ring = 0;
-    int item = 0, item_next = 0;
-    if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
-    item = __shfl_sync(0xffffffffu, item, 0);
-    int4 info = make_int4(0, 0, 0, 0), info2 = make_int4(0, 0, 0, 0);
-    if (item < n_items) {
-      info = a.chunk_info[2 * (item / kLGroups)];
-      info2 = a.chunk_info[2 * (item / kLGroups) + 1];
-    }
-    for (uint32_t iq = 0;; ++iq) {
-      if (lane == 0) item_next = (int)atomicAdd(&a.hdr->work, 1u);
-      const uint32_t slot = iq % kNIQ;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&item_empty[slot], ((iq / kNIQ) & 1u) ^ 1u, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (item >= n_items) {
-        if (lane == 0) {
-          items[slot].b = -1;
-          mbar_arrive(&item_full[slot]);
-        }
-        break;
-      }
-      const int cg = item / kLGroups, g = item - cg * kLGroups;
-      const int b = info.x, p0 = info.y, p1 = info.z, L = info.w;
-      if (lane == 0) {
-        ItemDesc d;
-        d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = info2.x;
-        items[slot] = d;
-        mbar_arrive(&item_full[slot]);
-      }
-      item_next = __shfl_sync(0xffffffffu, item_next, 0);
-      int4 info_next = make_int4(0, 0, 0, 0), info2_next = make_int4(0, 0, 0, 0);
-      if (item_next < n_items) {
-        info_next = a.chunk_info[2 * (item_next / kLGroups)];
-        info2_next = a.chunk_info[2 * (item_next / kLGroups) + 1];
-      }
-      const int *trow = a.block_table + (size_t)b * a.MP;
-      const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
-      uint32_t st_bits = 0;
-      for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages) {
-        const int i = i0 + lane;
-        const bool valid = lane < batch_pages && i < p1;
-        const int pid = valid ? __ldg(&trow[i]) : 0;
-        const bool oob = valid && (pid < 0 || pid >= a.P);
-        uint32_t page_tag = 0, want_tag = 0;
-        if (tag_check && valid && !oob) {
-          page_tag = __ldg(&a.page_tags[pid]);
-          want_tag = __ldg(&tagrow[i]);
-        }
-        bool lane_ok = true;
-        if (valid) {
-          const uint32_t r = ring + (uint32_t)lane;
-          const uint32_t st = r % (uint32_t)nst;
-          lane_ok = mbar_wait(&empty[st], ((r / (uint32_t)nst) & 1u) ^ 1u, abort_flag);
-          if (lane_ok) {
-            uint8_t *stage = smem + sp.stages_off + (size_t)st * kStageBytes;
-            if (oob) {
-              mbar_arrive(&full[st]);  // never fetched; the request is aborted
-            } else {
-              mbar_arrive_expect_tx(&full[st], kStageBytes);
-              bulk_load(stage, reinterpret_cast<const uint8_t *>(a.k_pool) + (size_t)pid * kPageBytes, kPageBytes,
-                        &full[st]);
-              bulk_load(stage + kPageBytes, a.k_scale + (size_t)pid * kLS, kLS * 4u, &full[st]);
-            }
-          }
-        }
-        ring += (uint32_t)min(batch_pages, p1 - i0);
-        ok = __all_sync(0xffffffffu, lane_ok);
-        if (__any_sync(0xffffffffu, oob)) st_bits |= PFKV_ST_PAGE_OOB;
-        if (__any_sync(0xffffffffu, page_tag != want_tag)) st_bits |= PFKV_ST_STALE_TAG;
-      }
-      if (lane == 0) {
-        item_status[slot] = st_bits;
-        mbar_arrive(&item_done[slot]);
-      }
-      if (!ok) break;
-      item = item_next;
-      info = info_next;
-      info2 = info2_next;
-    }
+  if (warp == 0) {
+    if (lane == 0) tma_prefetch_desc(&map);
+    tc_producer(a, map, smem, B, items, item_status, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) tc_mma(a, smem, B, items, tmem, abort_flag);
+    __syncwarp();
   } else {
-    // ------------------------------------------------------------ consumers
-    const int gid = lane >> 2, tq = lane & 3, t = threadIdx.x;
-    constexpr int kCT = kLNCW * 32;
-    const uint32_t s_base = smem_addr(smem + sp.stages_off);
-    const uint32_t q_base = smem_addr(smem + sp.qfrag_off);
-    const uint32_t p_base = smem_addr(smem + sp.pfrag_off);
-    uint32_t *qfrag = reinterpret_cast<uint32_t *>(smem + sp.qfrag_off);
-    uint32_t *pfrag = reinterpret_cast<uint32_t *>(smem + sp.pfrag_off);
-    for (uint32_t iq = 0;; ++iq) {
-      const uint32_t slot = iq % kNIQ;
-      if (!mbar_wait(&item_full[slot], (iq / kNIQ) & 1u, abort_flag)) break;
-      const ItemDesc d = items[slot];
-      if (d.b < 0) break;
-      const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(a.q) +
-                                  ((size_t)d.b * a.Hq + d.g * kLHG) * kLD;
-      // ---- query terms: per head scale 2^e with max|q| / 2^e in [128, 256)
-      for (int h = warp * 4; h < warp * 4 + 4; ++h) {
-        float mx = 0.f;
-        for (int k = lane; k < kLD; k += 32) mx = fmaxf(mx, fabsf(__bfloat162float(qrow[h * kLD + k])));
-        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) {
-          int k2 = 0;
-          if (mx > 0.f) frexpf(mx, &k2);
-          sq_scale[h] = mx > 0.f ? ldexpf(1.f, k2 - 8) : 1.f;
-        }
-      }
-      named_bar_sync(1, kCT);
-      // fragment word (term i, step s, lane ln, register r): 4 consecutive columns
-      for (int wd = t; wd < kQT * kDSteps * 32 * 4; wd += kCT) {
-        const int r = wd & 3, ln = (wd >> 2) & 31, rest = wd >> 7;
-        const int s = rest % kDSteps, i = rest / kDSteps;
-        const int row = (ln >> 2) + 8 * (r & 1), c0 = qk_col(s, ln & 3, r >> 1, 0);
-        const float inv = 1.f / sq_scale[row];
-        float v[4], term[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = __bfloat162float(qrow[row * kLD + c0 + j]) * inv;  // exact (power of 2)
-        for (int k = 0; k <= i; ++k) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            term[j] = e4m3_to_f32(f32x2_to_e4m3x2(v[j], 0.f));
-            v[j] -= term[j];  // exact: the residual of a round to nearest
-          }
-        }
-        qfrag[wd] = pack4_e4m3(term[0], term[1], term[2], term[3]);
-      }
-      named_bar_sync(1, kCT);
-      const float rs0 = sq_scale[gid] * a.sm_scale_log2, rs1 = sq_scale[gid + 8] * a.sm_scale_log2;
-
-      float m[2] = {kNegInf, kNegInf}, mv[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
-      float o[16][4];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-      const int n_pages = d.p1 - d.p0;
-      bool alive = true;
-      for (int pr = 0; 2 * pr < n_pages; ++pr) {
-        const bool has2 = 2 * pr + 1 < n_pages;
-        uint32_t stg[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const uint32_t rp = d.ring + (uint32_t)(2 * pr + k);
-          stg[k] = rp % (uint32_t)nst;
-          if ((k == 0 || has2) && !mbar_wait(&full[stg[k]], (rp / (uint32_t)nst) & 1u, abort_flag)) alive = false;
-        }
-        if (!alive) break;
-        const int tok_pair = (d.p0 + 2 * pr) * kLS;  // token index of the pair's first row
-        // ---- S = Q K^T for k-block `warp` (32 tokens)
-        const int kpage = warp >> 1;
-        const int tok0 = tok_pair + warp * 32;
-        const bool live = (kpage == 0 || has2) && tok0 < d.L;
-        const uint32_t kst = s_base + stg[kpage] * kStageBytes;
-        const uint32_t krow = kst + (uint32_t)((warp & 1) * 32) * kLD;
-        float acc[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        if (live) {
-#pragma unroll 1
-          for (int s2 = 0; s2 < kDSteps / 2; ++s2) {
-            uint4 kb[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) kb[j] = lds128(krow + (uint32_t)(8 * j + gid) * kLD + 64 * s2 + 16 * tq);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int s = 2 * s2 + h2;
-#pragma unroll
-              for (int i = 0; i < kQT; ++i) {
-                const uint4 av = lds128(q_base + (uint32_t)(((i * kDSteps + s) * 32 + lane) * 16));
-                const uint32_t af[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) mma_e4m3(acc[j], af, h2 ? kb[j].z : kb[j].x, h2 ? kb[j].w : kb[j].y);
-              }
-            }
-          }
-        }
-        // ---- scores (log2 domain); value weights carry log2 of the token scale
-        const uint32_t scl = kst + kPageBytes + (uint32_t)((warp & 1) * 32) * 4;
-        float z[4][4], zv[4][4];
-        float mz0 = kNegInf, mz1 = kNegInf, mzv0 = kNegInf, mzv1 = kNegInf;
-        float tsc[4][2], tlg[4][2];  // this thread's 8 tokens: scale and its log2
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint2 v = live ? lds64(scl + 4 * (8 * j + 2 * tq)) : make_uint2(0x3f800000u, 0x3f800000u);
-          tsc[j][0] = __uint_as_float(v.x);
-          tsc[j][1] = __uint_as_float(v.y);
-          tlg[j][0] = fast_log2(tsc[j][0]);
-          tlg[j][1] = fast_log2(tsc[j][1]);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int tk = 8 * j + 2 * tq + (c & 1);
-            const bool ok_tok = live && tok0 + tk < d.L;
-            const float zz = ok_tok ? acc[j][c] * ((c < 2) ? rs0 : rs1) * tsc[j][c & 1] : kNegInf;
-            z[j][c] = zz;
-            zv[j][c] = ok_tok ? zz + tlg[j][c & 1] : kNegInf;
-            if (c < 2) { mz0 = fmaxf(mz0, zz); mzv0 = fmaxf(mzv0, zv[j][c]); }
-            else { mz1 = fmaxf(mz1, zz); mzv1 = fmaxf(mzv1, zv[j][c]); }
-          }
-#pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
-          mz0 = fmaxf(mz0, __shfl_xor_sync(0xffffffffu, mz0, off));
-          mz1 = fmaxf(mz1, __shfl_xor_sync(0xffffffffu, mz1, off));
-          mzv0 = fmaxf(mzv0, __shfl_xor_sync(0xffffffffu, mzv0, off));
-          mzv1 = fmaxf(mzv1, __shfl_xor_sync(0xffffffffu, mzv1, off));
-        }
-        if (tq == 0) {
-          ex_m[warp * kLHG + gid] = mz0;
-          ex_m[warp * kLHG + gid + 8] = mz1;
-          ex_mv[warp * kLHG + gid] = mzv0;
-          ex_mv[warp * kLHG + gid + 8] = mzv1;
-        }
-        named_bar_sync(1, kCT);
-        float M0 = m[0], M1 = m[1], MV0 = mv[0], MV1 = mv[1];
-#pragma unroll
-        for (int w = 0; w < kLNCW; ++w) {
-          M0 = fmaxf(M0, ex_m[w * kLHG + gid]);
-          M1 = fmaxf(M1, ex_m[w * kLHG + gid + 8]);
-          MV0 = fmaxf(MV0, ex_mv[w * kLHG + gid]);
-          MV1 = fmaxf(MV1, ex_mv[w * kLHG + gid + 8]);
-        }
-        const float al0 = fast_exp2(m[0] - M0), al1 = fast_exp2(m[1] - M1);
-        const float av0 = fast_exp2(mv[0] - MV0), av1 = fast_exp2(mv[1] - MV1);
-        m[0] = M0; m[1] = M1; mv[0] = MV0; mv[1] = MV1;
-        float ls0 = 0.f, ls1 = 0.f;
-        float pv[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const float p = fast_exp2(z[j][c] - ((c < 2) ? M0 : M1));
-            if (c < 2) ls0 += p; else ls1 += p;
-            pv[j][c] = fast_exp2(zv[j][c] - ((c < 2) ? MV0 : MV1)) * kPScaleL;
-          }
-        l[0] = l[0] * al0 + ls0;
-        l[1] = l[1] * al1 + ls1;
-        if (av0 != 1.f || av1 != 1.f) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            o[i][0] *= av0; o[i][1] *= av0; o[i][2] *= av1; o[i][3] *= av1;
-          }
-        }
-        // ---- this k-block's P as PV operand fragments: term 1 then the residual term
-        {
-          uint32_t fr[kPT][4];
-          // register r: row (gid | gid+8) = r & 1, k half = r >> 1 -> n-tiles 2*(r>>1), 2*(r>>1)+1
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int cc = (r & 1) * 2, ja = 2 * (r >> 1);
-            float v4[4] = {pv[ja][cc], pv[ja][cc + 1], pv[ja + 1][cc], pv[ja + 1][cc + 1]};
-#pragma unroll
-            for (int i = 0; i < kPT; ++i) {
-              float tm[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                tm[j] = (i + 1 < kPT) ? e4m3_to_f32(f32x2_to_e4m3x2(v4[j], 0.f)) : v4[j];
-                v4[j] -= tm[j];
-              }
-              fr[i][r] = pack4_e4m3(tm[0], tm[1], tm[2], tm[3]);
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < kPT; ++i)
-            *reinterpret_cast<uint4 *>(pfrag + ((warp * kPT + i) * 32 + lane) * 4) =
-                make_uint4(fr[i][0], fr[i][1], fr[i][2], fr[i][3]);
-        }
-        named_bar_sync(1, kCT);
-        // ---- O[16 heads x 128 values of quarter `warp`] += P V over the pair's k-blocks
-#pragma unroll 1
-        for (int kbk = 0; kbk < kLNCW; ++kbk) {
-          const int vpage = kbk >> 1;
-          if (!((vpage == 0 || has2) && tok_pair + kbk * 32 < d.L)) continue;
-          uint32_t af[kPT][4];
-#pragma unroll
-          for (int i = 0; i < kPT; ++i) {
-            const uint4 v = lds128(p_base + (uint32_t)(((kbk * kPT + i) * 32 + lane) * 16));
-            af[i][0] = v.x; af[i][1] = v.y; af[i][2] = v.z; af[i][3] = v.w;
-          }
-          const uint32_t vrow = s_base + stg[vpage] * kStageBytes + (uint32_t)((kbk & 1) * 32) * kLD + warp * 128 +
-                                16 * gid;
-          uint32_t bq[2][16];  // [b0|b1][n-tile]
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            uint4 rv[4];
-            const int tks[4] = {16 * hb + 2 * tq, 16 * hb + 2 * tq + 1, 16 * hb + 8 + 2 * tq, 16 * hb + 9 + 2 * tq};
-#pragma unroll
-            for (int x = 0; x < 4; ++x) rv[x] = lds128(vrow + (uint32_t)tks[x] * kLD);
-            const uint32_t w0[4] = {rv[0].x, rv[0].y, rv[0].z, rv[0].w}, w1[4] = {rv[1].x, rv[1].y, rv[1].z, rv[1].w};
-            const uint32_t w2[4] = {rv[2].x, rv[2].y, rv[2].z, rv[2].w}, w3[4] = {rv[3].x, rv[3].y, rv[3].z, rv[3].w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint32_t tr[4];
-              transpose4x4(w0[u], w1[u], w2[u], w3[u], tr);
-#pragma unroll
-              for (int x = 0; x < 4; ++x) bq[hb][4 * u + x] = tr[x];
-            }
-          }
-#pragma unroll
-          for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-            for (int i = 0; i < kPT; ++i) mma_e4m3(o[nt], af[i], bq[0][nt], bq[1][nt]);
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&empty[stg[0]]);
-          if (has2) mbar_arrive(&empty[stg[1]]);
-        }
-      }
-      // ---- item epilogue: total l over the warps, then this warp's quarter of O
-#pragma unroll
-      for (int off = 1; off < 4; off <<= 1) {
-        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
-        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
-      }
-      if (tq == 0) {
-        ex_l[warp * kLHG + gid] = l[0];
-        ex_l[warp * kLHG + gid + 8] = l[1];
-      }
-      if (t == 0) {
-        uint32_t stv = PFKV_ST_TIMEOUT;
-        if (mbar_wait(&item_done[slot], (iq / kNIQ) & 1u, abort_flag)) stv = item_status[slot];
-        ex_l[kLNCW * kLHG + kLHG] = __uint_as_float(stv);  // broadcast word after sq_scale
-      }
-      named_bar_sync(1, kCT);
-      const uint32_t item_st = __float_as_uint(ex_l[kLNCW * kLHG + kLHG]);
-      float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-      for (int w = 0; w < kLNCW; ++w) {
-        L0 += ex_l[w * kLHG + gid];
-        L1 += ex_l[w * kLHG + gid + 8];
-      }
-      // O holds 256 * sum p' v with p' relative to mv; rebase to m
-      const float f0 = fast_exp2(mv[0] - m[0]) / kPScaleL, f1 = fast_exp2(mv[1] - m[1]) / kPScaleL;
-      const int h0 = d.g * kLHG + gid;
-      const int dbase = warp * 128 + 32 * tq;  // this thread's 32 output values (n-tile nt -> dbase + nt, +16)
-      if (d.nb == 1) {
-        float *o0 = a.out + ((size_t)d.b * a.Hq + h0) * kLDv + dbase;
-        float *o1 = o0 + 8 * kLDv;
-        // an aborted request's rows are zero, whatever the never-fetched pages held
-        const float g0 = f0 / L0, g1 = f1 / L1;
-        const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int nt = 4 * q4;
-            *reinterpret_cast<float4 *>(o0 + 16 * e + nt) =
-                item_st ? zero4 : make_float4(o[nt][e] * g0, o[nt + 1][e] * g0, o[nt + 2][e] * g0, o[nt + 3][e] * g0);
-            *reinterpret_cast<float4 *>(o1 + 16 * e + nt) =
-                item_st ? zero4
-                        : make_float4(o[nt][2 + e] * g1, o[nt + 1][2 + e] * g1, o[nt + 2][2 + e] * g1,
-                                      o[nt + 3][2 + e] * g1);
-          }
-        if (t == 0 && item_st) atomicOr(&a.status[d.b], item_st);
-      } else {
-        float *o0 = a.part_o + ((size_t)d.cg * a.Hq + h0) * kLDv + dbase;
-        float *o1 = o0 + 8 * kLDv;
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int nt = 4 * q4;
-            *reinterpret_cast<float4 *>(o0 + 16 * e + nt) =
-                make_float4(o[nt][e] * f0, o[nt + 1][e] * f0, o[nt + 2][e] * f0, o[nt + 3][e] * f0);
-            *reinterpret_cast<float4 *>(o1 + 16 * e + nt) =
-                make_float4(o[nt][2 + e] * f1, o[nt + 1][2 + e] * f1, o[nt + 2][2 + e] * f1, o[nt + 3][2 + e] * f1);
-          }
-        if (warp == 0 && tq == 0) {
-          a.part_ml[(size_t)d.cg * a.Hq + h0] = make_float2(m[0], L0);
-          a.part_ml[(size_t)d.cg * a.Hq + h0 + 8] = make_float2(m[1], L1);
-        }
-        if (t == 0 && item_st) atomicOr(&a.status[d.b], item_st);
-      }
-      named_bar_sync(1, kCT);
-      if (t == 0) mbar_arrive(&item_empty[slot]);
-      if (!alive) break;
-    }
+    tc_softmax(a, smem, B, items, item_status, tmem, abort_flag);
   }
-  if (lane == 0 && *abort_flag)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  // A wait gave up somewhere in this block: every request of the call is
+  // reported as timed out (its output is not valid).
+  if (threadIdx.x == 0 && *abort_flag)
     for (int b = 0; b < a.B; ++b) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
 }
 
 }  // namespace
 
+// Tensor map over the stream pool viewed as [page][slot][576 bytes]; a box
+// is one 128-byte column block of a page (the fifth box reads 64 bytes past
+// the row end, which the copy fills with zeros).
+static int make_stream_map(CUtensorMap *map, const void *pool, int P) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
+  cuuint64_t dims[3] = {(cuuint64_t)kTD, (cuuint64_t)kTS, (cuuint64_t)P};
+  cuuint64_t strides[2] = {(cuuint64_t)kTD, (cuuint64_t)kTD * kTS};
+  cuuint32_t box[3] = {128, (cuuint32_t)kTS, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (stream)");
+  return PFKV_OK;
+}
+
 int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
-  // head groups play the role of KV heads for the split plan and the merge
+  // Work items are splits of a request, all 64 heads each.
   DecodeArgs a = a0;
-  a.Hkv = kLGroups;
-  a.G = kLHG;
-  static int nst = 2;  // one pair of pages: two CTAs share an SM and hide each other's copies
-  static uint32_t smem = 0;
-  static int grid = 0;
+  a.Hkv = 1;
+  a.G = kTH;
+  a.qprep = 1;
+  CUtensorMap map;
+  int rc = make_stream_map(&map, a.k_pool, a.P);
+  if (rc) return rc;
+  const uint32_t smem = tc_smem().total + 1024;
   static std::mutex mu;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (!smem) {
-      smem = lat_smem(nst).total;
-      cudaError_t e = cudaFuncSetAttribute(latent_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (dev >= 64 || !attr_set[dev]) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(latent_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(latent kernel)");
-      int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, latent_split_kernel, kLThreads, smem);
-      if (e != cudaSuccess) return cuda_fail(e, "occupancy query (latent kernel)");
-      if (per_sm < 1) return cuda_fail(cudaErrorInvalidConfiguration, "latent kernel does not fit on an SM");
-      grid = num_sms() * per_sm;
+      if (dev < 64) attr_set[dev] = true;
     }
   }
-  plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, grid * 8, (1024 + kLS - 1) / kLS);
-  int rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
+  const int grid = num_sms();
+  plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, grid * 2, 8);
+  rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
   if (rc) return rc;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kLThreads);
+  cfg.blockDim = dim3(kTThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  rc = cuda_ok(cudaLaunchKernelEx(&cfg, latent_split_kernel, a, nst), "latent kernel launch");
+  rc = cuda_ok(cudaLaunchKernelEx(&cfg, latent_tc_kernel, map, a), "latent kernel launch");
   if (rc) return rc;
+  // merge in blocks of 16 heads
+  DecodeArgs m = a;
+  m.Hkv = kTH / 16;
+  m.G = 16;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(a.B * kLGroups);
+  mcfg.gridDim = dim3(a.B * m.Hkv);
   mcfg.blockDim = dim3(256);
   mcfg.stream = s;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&mcfg, merge_kernel<kLDv, kLHG>, a), "merge kernel launch (latent)");
+  return cuda_ok(cudaLaunchKernelEx(&mcfg, merge_kernel<kTDv, 16>, m), "merge kernel launch");
 }
 
 }  // namespace pfkv

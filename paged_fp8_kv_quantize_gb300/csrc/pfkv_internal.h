@@ -22,9 +22,13 @@ struct WsHeader {
 
 // Decode workspace carve-up.
 struct WsLayout {
-  size_t hdr, split_first, split_count, chunk_info, part_ml, part_o, total;
+  size_t hdr, split_first, split_count, chunk_info, part_ml, part_o, qterms, qfac, total;
 };
-WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits);
+// latent: the latent-stream path also keeps each request's query as two e4m3
+// terms in the shared-memory image its kernel copies (qterms, 72 KB per
+// request) and one factor per head (qfac).
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool latent);
+constexpr size_t kLatentQTermBytes = 9 * 64 * 128;  // nine 128-byte column blocks x 64 heads
 
 struct DecodeArgs {
   // cache
@@ -55,6 +59,11 @@ struct DecodeArgs {
   int append;
   const uint16_t *k_new, *v_new;
   pfkv_cache cache;
+  // latent-stream path only (qprep == 1): the plan grid writes the query
+  // terms and per-head factors of every request here
+  int qprep;
+  uint8_t *qterms;
+  float *qfac;
 };
 
 // Tensor-map encoder obtained from the driver without linking libcuda.
