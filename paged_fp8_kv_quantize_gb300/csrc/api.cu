@@ -45,7 +45,8 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool laten
   w.split_first = up256(sizeof(WsHeader));
   w.split_count = w.split_first + up256(sizeof(int) * ((size_t)batch + 1));
   w.chunk_info = w.split_count + up256(sizeof(int) * (size_t)batch);
-  w.part_ml = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
+  w.cta_first = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
+  w.part_ml = w.cta_first + up256(sizeof(int) * (kMaxRanges + 1));
   w.part_o = w.part_ml + up256(sizeof(float2) * slots);
   w.qterms = w.part_o + up256(sizeof(float) * slots * v_dim);
   w.qfac = w.qterms + (latent ? up256(kLatentQTermBytes * (size_t)batch) : 0);
@@ -125,6 +126,8 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.v_new = static_cast<const uint16_t *>(v_new);
   a.cache = *c;
   a.qprep = 0;
+  a.balanced = 0;
+  a.cta_first = reinterpret_cast<int *>(w + L.cta_first);
   a.qterms = w + L.qterms;
   a.qfac = reinterpret_cast<float *>(w + L.qfac);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -68,10 +68,12 @@ __host__ __device__ inline int plan_blocks(const DecodeArgs &a) { return 1 + pla
 // T1 + T2 equals the scaled row exactly for every element of magnitude at
 // least 2^-2 (a bf16 significand has 8 bits, each term carries 4), the
 // rest to within 2^-10.  The terms are stored as the kernel's shared-memory
-// image of 128-byte column blocks with the 128-byte swizzle (row h, 16-byte
-// chunk j at h*128 + 16*(j ^ (h & 7))): blocks 0-3 hold columns 0-511 of T1,
-// blocks 4-7 the same of T2, block 8 columns 512-575 of T1 in its chunks
-// 0-3 and of T2 in chunks 4-7.  qfac[h] = softmax scale * log2(e) * 2^e_h.
+// image of one 128-row operand (row R < 64: T1 of head R; R >= 64: T2 of
+// head R - 64): columns 0-511 in four 16 KB blocks of 128-byte rows with the
+// 128-byte swizzle (16-byte chunk j of row R at c*16384 + R*128 +
+// 16*(j ^ (R & 7))), columns 512-575 in one 8 KB block of 64-byte rows with
+// the 64-byte swizzle (chunk j at 65536 + R*64 + 16*(j ^ ((R >> 1) & 3))).
+// qfac[h] = softmax scale * log2(e) * 2^e_h.
 __device__ __forceinline__ void plan_qprep(const DecodeArgs &a, int b) {
   __shared__ float s_qinv[64];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -92,15 +94,15 @@ __device__ __forceinline__ void plan_qprep(const DecodeArgs &a, int b) {
   for (int u = tid; u < 64 * 36; u += (int)blockDim.x) {
     const int h = u / 36, r = u % 36;
     const int k0 = 16 * r;  // 16 columns starting here (r < 36 covers all 576)
-    size_t off1, off2;
+    size_t off1, off2;  // T1 row h, T2 row 64 + h (same swizzle phase)
     if (r < 32) {
       const int c = r / 8, j = r % 8;
-      off1 = (size_t)c * 8192 + h * 128 + 16 * (j ^ (h & 7));
-      off2 = off1 + 4 * 8192;
+      off1 = (size_t)c * 16384 + h * 128 + 16 * (j ^ (h & 7));
+      off2 = off1 + 64 * 128;
     } else {
       const int j = r - 32;
-      off1 = (size_t)8 * 8192 + h * 128 + 16 * (j ^ (h & 7));
-      off2 = (size_t)8 * 8192 + h * 128 + 16 * ((j + 4) ^ (h & 7));
+      off1 = (size_t)65536 + h * 64 + 16 * (j ^ ((h >> 1) & 3));
+      off2 = off1 + 64 * 64;
     }
     uint32_t t1[4], t2[4];
     {
@@ -125,12 +127,135 @@ __device__ __forceinline__ void plan_qprep(const DecodeArgs &a, int b) {
   }
 }
 
+// Exclusive prefix over the block (1024 threads) of one int64 per thread;
+// returns this thread's prefix, the block total in *total.  s_w: 33 entries.
+__device__ __forceinline__ long long block_excl_scan(long long v, long long *s_w, long long *total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  long long x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_w[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    long long w = lane < (int)(blockDim.x >> 5) ? s_w[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_w[lane] = w;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const long long r = (wid ? s_w[wid - 1] : 0) + x - v;
+  *total = s_w[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return r;
+}
+
+// Balanced plan: the requests' pages, concatenated in request order (T in
+// all), are cut into R ranges [floor(kT/R), floor((k+1)T/R)), one per CTA;
+// an item is the part of one request inside one range.  Every CTA gets the
+// same number of pages to within one, and at most R + B - 1 partial results
+// are written.  R <= ranges, R <= T, and R is small enough that no request
+// is cut into more than max_splits pieces (a request of p pages meets at
+// most ceil(p R / T) + 1 ranges).
+__device__ void plan_balanced(const DecodeArgs &a, int ranges) {
+  __shared__ long long s_w[33];
+  __shared__ long long s_tot, s_max, s_pcarry, s_icarry;
+  const int tid = threadIdx.x;
+  const int S = a.S;
+  const long long max_len = (long long)a.MP * S;
+  long long tot = 0, mx = 0;
+  for (int b = tid; b < a.B; b += blockDim.x) {
+    const int L = a.seq_lens[b];
+    const bool bad = L < 1 || (long long)L > max_len;
+    a.status[b] = bad ? PFKV_ST_BAD_LEN : 0u;
+    const long long p = bad ? 0 : (L + S - 1) / S;
+    tot += p;
+    mx = p > mx ? p : mx;
+  }
+  for (int o = 16; o; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const long long y = __shfl_xor_sync(0xffffffffu, mx, o);
+    mx = y > mx ? y : mx;
+  }
+  if (tid == 0) { s_tot = 0; s_max = 0; s_pcarry = 0; s_icarry = 0; }
+  __syncthreads();
+  if ((tid & 31) == 0) {
+    atomicAdd(reinterpret_cast<unsigned long long *>(&s_tot), (unsigned long long)tot);
+    atomicMax(reinterpret_cast<unsigned long long *>(&s_max), (unsigned long long)mx);
+  }
+  __syncthreads();
+  const long long T = s_tot, pmax = s_max;
+  long long R = ranges;
+  if (R > T) R = T;
+  if (pmax > 0) {
+    const long long cap = (long long)(a.max_splits - 2) * T / pmax;
+    if (R > cap) R = cap;
+  }
+  if (R > kMaxRanges) R = kMaxRanges;
+  if (R < 1) R = 1;
+  if (tid == 0 && T == 0) a.cta_first[0] = 0;
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int b = base + tid;
+    long long pages = 0;
+    int L = 0;
+    if (b < a.B) {
+      L = a.seq_lens[b];
+      pages = (L < 1 || (long long)L > max_len) ? 0 : (L + S - 1) / S;
+    }
+    long long ptot;
+    const long long off = s_pcarry + block_excl_scan(pages, s_w, &ptot);
+    long long kf = 0, kl = -1;
+    if (pages > 0) {
+      kf = ((off + 1) * R - 1) / T;          // range holding the first page
+      kl = ((off + pages) * R - 1) / T;      // range holding the last page
+    }
+    const long long n = pages > 0 ? kl - kf + 1 : 0;
+    long long itot;
+    const long long first = s_icarry + block_excl_scan(n, s_w, &itot);
+    if (b < a.B) {
+      a.split_first[b] = (int)first;
+      a.split_count[b] = (int)n;
+      for (long long j = 0; j < n; ++j) {
+        const long long k = kf + j;
+        const long long r0 = k * T / R, r1 = (k + 1) * T / R;
+        const long long p0 = (r0 > off ? r0 : off) - off, p1 = (r1 < off + pages ? r1 : off + pages) - off;
+        a.chunk_info[2 * (first + j)] = make_int4(b, (int)p0, (int)p1, L);
+        a.chunk_info[2 * (first + j) + 1] = make_int4((int)n, (int)j, (int)k, 0);
+        if (j > 0 || off == r0) a.cta_first[k] = (int)(first + j);  // first item of range k
+      }
+      if (n == 0)  // bad length: no item writes this request's rows
+        for (size_t k = 0; k < (size_t)a.Hq * a.Dv; ++k) a.out[(size_t)b * a.Hq * a.Dv + k] = 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      s_pcarry += ptot;
+      s_icarry += itot;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    a.cta_first[R] = (int)s_icarry;
+    a.hdr->n_chunks = (int)s_icarry;
+    a.hdr->n_items = (int)s_icarry;
+    a.hdr->work = 0u;
+    a.hdr->err = 0u;
+    a.hdr->chunk_pages = (int)R;  // number of ranges
+  }
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
   pdl_launch_dependents();  // the split kernel waits for this grid's results before reading them
   if (blockIdx.x > 0) {
     const int nab = plan_append_blocks(a);
     if ((int)blockIdx.x <= nab) plan_append(a);
     else plan_qprep(a, (int)blockIdx.x - 1 - nab);
+    return;
+  }
+  if (a.balanced > 0) {
+    plan_balanced(a, a.balanced);
     return;
   }
   __shared__ long long s_red[32];

@@ -24,11 +24,12 @@
 // One CTA per SM, persistent, work item = (request, split of its pages),
 // all 64 heads.  Warp 0 loads pages (TMA, 128-byte swizzle, bounds and tag
 // checks beside the copies) and the query terms; warp 1 owns tensor memory
-// and issues the MMAs (one thread); warps 2-5 read S^T from tensor memory,
-// run the online softmax (running maxima move only when they grow by more
-// than 2x, and only then is O^T rescaled in tensor memory), write P^T, and
-// write the item's partial or final output.  Partials are merged by the
-// shared log-sum-exp merge kernel.
+// and issues the MMAs (one thread); warps 2-9, two groups of four with 32
+// heads each, read S^T from tensor memory (every lane holds two tokens x
+// eight heads), run the online softmax (running maxima move only when they
+// grow by more than 8x, and only then is the group's part of O^T rescaled
+// in tensor memory), write P^T, and write the item's partial or final
+// output.  Partials are merged by the shared log-sum-exp merge kernel.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -43,23 +44,27 @@ constexpr int kTD = 576;                      // stream width
 constexpr int kTDv = 512;                     // V = leading values
 constexpr int kTS = 64;                       // tokens per page
 constexpr int kTH = 64;                       // query heads
-constexpr int kTBlocks = 5;                   // 128-byte column blocks of a row (the last one half used)
-constexpr uint32_t kBlk = kTS * 128;          // 8192: one column block of a page or of a query term
-constexpr uint32_t kPageSm = kTBlocks * kBlk;  // 40960
-// Query terms: blocks 0-3 of T1, blocks 0-3 of T2, then one block whose
-// rows hold the last 64 columns of T1 (bytes 0-63) and of T2 (64-127).
-constexpr uint32_t kQBytes = 9 * kBlk;        // 73728
-constexpr uint32_t kQTail = 8 * kBlk;
+constexpr uint32_t kBlk = kTS * 128;          // 8192: one 128-byte column block of a page
+// A page in shared memory: columns 0-511 as four 128-byte blocks (128-byte
+// swizzle), columns 512-575 as one 64-byte block (64-byte swizzle).
+constexpr uint32_t kPageTail = 4 * kBlk;      // 32768
+constexpr uint32_t kPageSm = kPageTail + kTS * 64;  // 36864
+// Query terms as one 128-row operand (rows 0-63: T1 of heads 0-63, rows
+// 64-127: T2): four 128-byte column blocks of 16 KB, then the 64-byte tail.
+constexpr uint32_t kQBlk = 2 * kBlk;          // 16384
+constexpr uint32_t kQTail = 4 * kQBlk;        // 65536
+constexpr uint32_t kQBytes = kQTail + 2 * kTH * 64;  // 73728
 constexpr int kPT = 3;                        // e4m3 terms of the probabilities
 constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
 constexpr uint32_t kPBuf = kPT * kPTerm;      // 12288
 constexpr int kNst = 3;                       // pages in flight per CTA
-constexpr int kTThreads = 192;                // producer, MMA, four softmax warps
-constexpr uint32_t kTmemCols = 512;           // S^T x2 (64 columns each), O^T (4 x 64)
-constexpr uint32_t kColS = 0, kColO = 128;
-constexpr float kPExp = 6.75f;                // P'' = p (s_t / s_ref) 2^kPExp <= 2 * 2 * 2^6.75 < 448
-constexpr float kTheta = 1.f;                 // log2 growth of a running max that triggers a rescale
-constexpr uint32_t kIdQK = umma_idesc_e4m3(64, 64, 0, 0);
+constexpr int kPrefetch = 6;                  // pages pulled into L2 ahead of their copy
+constexpr int kTThreads = 320;                // producer, MMA, two groups of four softmax warps
+constexpr uint32_t kTmemCols = 512;           // S^T x2 (128 columns each: T1 | T2 parts), O^T (4 x 64)
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr float kTheta = 3.f;                 // log2 growth of a running max that triggers a rescale
+constexpr float kPExp = 4.75f;                // P'' = p (s_t / s_ref) 2^kPExp <= 2^kTheta * 2 * 2^4.75 < 448
+constexpr uint32_t kIdQK = umma_idesc_e4m3(64, 128, 0, 0);
 constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 64, 1, 1);
 
 struct TcSmem {
@@ -69,18 +74,18 @@ struct TcSmem {
 __host__ __device__ constexpr TcSmem tc_smem() {
   TcSmem s{};
   s.ring = 0;                                  // kNst pages, each 5 column blocks (1024-aligned)
-  s.q = s.ring + kNst * kPageSm;               // 2 query terms x 5 blocks
+  s.q = s.ring + kNst * kPageSm;               // query terms (kQBytes)
   s.p = s.q + kQBytes;                         // 2 buffers x kPT P^T terms
   s.scales = s.p + 2 * kPBuf;                  // kNst x 64 per-token scales
   s.wg = s.scales + kNst * kTS * 4;            // softmax-warp scratch (see below)
-  s.bars = s.wg + 4 * (64 * 4 + 4 * 64 + 8);   // cq, m, alpha, beta | ex[4][64] | ex_s[4], misc
+  s.bars = s.wg + 4 * (64 * 4 + 2 * 4 * 32 + 2 * 4);  // cq, m, alpha, beta | ex[2][4][32] | ex_s[2][4]
   s.items = s.bars + 8 * (2 * kNst + 12 + 3 * kNIQ);
   s.total = s.items + (sizeof(ItemDesc) + 4) * kNIQ + 16;
   return s;
 }
 static_assert(tc_smem().total + 1024 <= 232448, "shared memory plan exceeds one SM");
 
-// Softmax-warp scratch, floats: cq[64] | m[64] | alpha[64] | beta[64] | ex[4][64] | ex_s[4] | pad
+// Softmax-warp scratch, floats: cq[64] | m[64] | alpha[64] | beta[64] | ex[group][warp][32] | ex_s[group][warp]
 constexpr int kWgCq = 0, kWgM = 64, kWgAlpha = 128, kWgBeta = 192, kWgEx = 256, kWgExS = 512;
 
 // Bounded wait that ignores the abort flag: used on the way out, so that a
@@ -117,7 +122,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
 
 // ---------------------------------------------------------------- producer (warp 0)
 
-__device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorMap &map, uint8_t *smem,
+__device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorMap &map, const CUtensorMap &map_tail,
+                                            uint8_t *smem,
                                             const Bars &B, ItemDesc *items, uint32_t *item_status,
                                             volatile int *abort_flag) {
   const TcSmem sp = tc_smem();
@@ -127,10 +133,21 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
   uint32_t g = 0;  // pages issued by this CTA
   uint32_t it = 0, q_loads = 0;
   bool ok = true;
+  // balanced plan: this CTA's items are a fixed run; otherwise items are
+  // taken from a shared counter
+  int next = 0, last = 0;
+  if (a.balanced > 0 && (int)blockIdx.x < a.hdr->chunk_pages) {
+    next = a.cta_first[blockIdx.x];
+    last = a.cta_first[blockIdx.x + 1];
+  }
   for (;; ++it) {
     int item = 0;
-    if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
-    item = __shfl_sync(0xffffffffu, item, 0);
+    if (a.balanced > 0) {
+      item = next < last ? next++ : n_items;
+    } else {
+      if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
+      item = __shfl_sync(0xffffffffu, item, 0);
+    }
     const uint32_t slot = it % kNIQ;
     bool w = true;
     if (lane == 0) w = mbar_wait(&B.item_empty[slot], ((it / kNIQ) & 1u) ^ 1u, abort_flag);
@@ -154,15 +171,18 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
         mbar_arrive_expect_tx(B.q_full, kQBytes);
         const uint8_t *src = a.qterms + (size_t)b * kQBytes;
         for (uint32_t o = 0; o < kQBytes; o += kBlk) bulk_load(smem + sp.q + o, src + o, kBlk, B.q_full);
+        static_assert(kQBytes % kBlk == 0, "query image is copied in 8 KB pieces");
         ++q_loads;
       }
     }
     const int *trow = a.block_table + (size_t)b * a.MP;
     const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
     uint32_t st_bits = 0;
-    for (int i0 = p0; i0 < p1 && ok; i0 += kNst) {
+    // Table entries 32 at a time (one round trip per 32 pages, hidden behind
+    // the pages in flight); pages issued one by one as ring slots free up.
+    for (int i0 = p0; i0 < p1 && ok; i0 += 32) {
       const int i = i0 + lane;
-      const bool valid = lane < kNst && i < p1;
+      const bool valid = i < p1;
       const int pid = valid ? __ldg(&trow[i]) : 0;
       const bool oob = valid && (pid < 0 || pid >= a.P);
       uint32_t page_tag = 0, want_tag = 0;
@@ -170,25 +190,48 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
         page_tag = __ldg(&a.page_tags[pid]);
         want_tag = __ldg(&tagrow[i]);
       }
-      bool lane_ok = true;
-      if (valid) {
-        const uint32_t r = g + (uint32_t)lane;
-        const uint32_t st = r % kNst;
-        lane_ok = mbar_wait(&B.empty[st], ((r / kNst) & 1u) ^ 1u, abort_flag);
-        if (lane_ok) {
-          if (oob) {
-            mbar_arrive(&B.full[st]);  // never fetched; the request is aborted
-          } else {
-            mbar_arrive_expect_tx(&B.full[st], kPageSm + kTS * 4);
-            uint8_t *stage = smem + sp.ring + st * kPageSm;
+      const int cnt = min(32, p1 - i0);
+      // pages kPrefetch ahead of the copies are pulled into L2, so that a copy
+      // issued when a ring slot frees up finds its page there
+      auto prefetch = [&](int k) {
+        const int pk = __shfl_sync(0xffffffffu, pid, k);
+        const bool bad = __shfl_sync(0xffffffffu, oob, k);
+        if (lane == 0 && !bad) {
 #pragma unroll
-            for (int c = 0; c < kTBlocks; ++c) tma_load_3d(stage + c * kBlk, &map, &B.full[st], 128 * c, 0, pid);
-            bulk_load(smem + sp.scales + st * (kTS * 4), a.k_scale + (size_t)pid * kTS, kTS * 4, &B.full[st]);
+          for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&map, 128 * c, 0, pk);
+          tma_prefetch_l2_3d(&map_tail, 512, 0, pk);
+          bulk_prefetch_l2(a.k_scale + (size_t)pk * kTS, kTS * 4);
+        }
+      };
+      for (int k = 0; k < min(kPrefetch, cnt); ++k) prefetch(k);
+      for (int k = 0; k < cnt; ++k) {
+        if (k + kPrefetch < cnt) prefetch(k + kPrefetch);
+        const int pk = __shfl_sync(0xffffffffu, pid, k);
+        const bool ok_k = __shfl_sync(0xffffffffu, oob, k);
+        bool w = true;
+        if (lane == 0) {
+          const uint32_t r = g + (uint32_t)k, st = r % kNst;
+          w = mbar_wait(&B.empty[st], ((r / kNst) & 1u) ^ 1u, abort_flag);
+          if (w) {
+            if (ok_k) {
+              mbar_arrive(&B.full[st]);  // never fetched; the request is aborted
+            } else {
+              mbar_arrive_expect_tx(&B.full[st], kPageSm + kTS * 4);
+              uint8_t *stage = smem + sp.ring + st * kPageSm;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) tma_load_3d(stage + c * kBlk, &map, &B.full[st], 128 * c, 0, pk);
+              tma_load_3d(stage + kPageTail, &map_tail, &B.full[st], 512, 0, pk);
+              bulk_load(smem + sp.scales + st * (kTS * 4), a.k_scale + (size_t)pk * kTS, kTS * 4, &B.full[st]);
+            }
           }
         }
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          g += (uint32_t)k;  // pages issued so far in this batch
+          break;
+        }
       }
-      g += (uint32_t)min(kNst, p1 - i0);
-      ok = __all_sync(0xffffffffu, lane_ok);
+      if (ok) g += (uint32_t)cnt;
       if (__any_sync(0xffffffffu, oob)) st_bits |= PFKV_ST_PAGE_OOB;
       if (__any_sync(0xffffffffu, page_tag != want_tag)) st_bits |= PFKV_ST_STALE_TAG;
     }
@@ -213,30 +256,9 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
                                        uint32_t tmem, volatile int *abort_flag) {
   const TcSmem sp = tc_smem();
   const uint32_t s_ring = smem_addr(smem + sp.ring), s_q = smem_addr(smem + sp.q), s_p = smem_addr(smem + sp.p);
-  uint32_t g = 0;   // pages consumed
-  uint32_t it = 0;  // items
+  uint32_t g = 0;  // pages consumed before the current item
   bool ok = true;
-  // PV of page gp (j-th page of its item): O^T[c] (+)= V^T_c . (P1 + P2)^T
-  auto pv = [&](uint32_t gp, bool first) -> bool {
-    const uint32_t pb = gp & 1u;
-    if (!mbar_wait(&B.p_full[pb], (gp >> 1) & 1u, abort_flag)) return false;
-    tc_fence_after();
-    const uint32_t st = gp % kNst;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-      for (int t = 0; t < kPT; ++t)
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + ks * 4096, 8192, 1024, 2);
-          const uint64_t db = umma_sdesc(s_p + pb * kPBuf + t * kPTerm + ks * 512, 128, 1024, 0);
-          umma_e4m3(tmem + kColO + 64 * c, da, db, kIdPV, (first && t == 0 && ks == 0) ? 0u : 1u);
-        }
-    umma_commit(&B.empty[st]);
-    umma_commit(&B.p_empty[pb]);
-    return true;
-  };
-  for (;; ++it) {
+  for (uint32_t it = 0; ok; ++it) {
     const uint32_t slot = it % kNIQ;
     if (!mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag)) break;
     const ItemDesc d = items[slot];
@@ -244,38 +266,75 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
     if (!mbar_wait(B.q_full, it & 1u, abort_flag)) break;
-    for (uint32_t j = 0; j < n && ok; ++j) {
-      const uint32_t gp = g + j, st = gp % kNst, sb = gp & 1u;
-      if (!mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
-          !mbar_wait(&B.s_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // S^T[sb] = K_page . (T1 + T2)^T over the 576 columns (18 steps of 32 per term)
-      uint32_t acc = 0;
+    // Issue each MMA group as soon as its inputs are ready: QK^T of page nq
+    // (page landed, its S^T buffer read by the softmax warps) or PV of page
+    // np (P^T written; for the item's first page, O^T read out).  A PV never
+    // waits behind the next page's copy.
+    uint32_t nq = 0, np = 0;
+    bool o_free = false;
+    uint64_t t_last = 0;  // start of the current stretch without progress
+    while (np < n) {
+      bool did = false;
+      if (nq < n) {
+        const uint32_t gp = g + nq, st = gp % kNst, sb = gp & 1u;
+        if (mbar_test(&B.full[st], (gp / kNst) & 1u) && mbar_test(&B.s_empty[sb], ((gp >> 1) & 1u) ^ 1u)) {
+          tc_fence_after();
+          // S^T[sb] = K_page . [T1; T2]^T: 64 tokens x 128 columns (heads of T1,
+          // then of T2) over the 576 columns, 18 steps of 32
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
+          for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int c = 0; c < kTBlocks; ++c)
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + kk * 32, 16, 1024, 2);
+              const uint64_t db = umma_sdesc(s_q + c * kQBlk + kk * 32, 16, 1024, 2);
+              umma_e4m3(tmem + kColS + 128 * sb, da, db, kIdQK, (c | kk) ? 1u : 0u);
+            }
 #pragma unroll
-          for (int kk = 0; kk < (c < 4 ? 4 : 2); ++kk) {
-            const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + kk * 32, 16, 1024, 2);
-            const uint32_t qb = c < 4 ? (uint32_t)(4 * t + c) * kBlk + kk * 32 : kQTail + (uint32_t)(2 * t + kk) * 32;
-            const uint64_t db = umma_sdesc(s_q + qb, 16, 1024, 2);
-            umma_e4m3(tmem + kColS + 64 * sb, da, db, kIdQK, acc);
-            acc = 1u;
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t da = umma_sdesc(s_ring + st * kPageSm + kPageTail + kk * 32, 16, 512, 4);
+            const uint64_t db = umma_sdesc(s_q + kQTail + kk * 32, 16, 512, 4);
+            umma_e4m3(tmem + kColS + 128 * sb, da, db, kIdQK, 1u);
           }
-      umma_commit(&B.s_full[sb]);
-      if (j + 1 == n) umma_commit(B.q_empty);  // the query terms may be replaced
-      if (j > 0) {
-        if (j == 1 && !mbar_wait(B.o_empty, (it & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-        if (!pv(gp - 1, j == 1)) { ok = false; break; }
+          umma_commit(&B.s_full[sb]);
+          if (nq + 1 == n) umma_commit(B.q_empty);  // the query terms may be replaced
+          ++nq;
+          did = true;
+        }
+      }
+      if (np < nq) {
+        const uint32_t gp = g + np, st = gp % kNst, pb = gp & 1u;
+        if (np == 0 && !o_free) o_free = mbar_test(B.o_empty, (it & 1u) ^ 1u);
+        if ((np > 0 || o_free) && mbar_test(&B.p_full[pb], (gp >> 1) & 1u)) {
+          tc_fence_after();
+          // O^T[c] (+)= V^T_c . (P1 + P2 + P3)^T
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int t = 0; t < kPT; ++t)
+#pragma unroll
+              for (int ks = 0; ks < 2; ++ks) {
+                const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + ks * 4096, 8192, 1024, 2);
+                const uint64_t db = umma_sdesc(s_p + pb * kPBuf + t * kPTerm + ks * 512, 128, 1024, 0);
+                umma_e4m3(tmem + kColO + 64 * c, da, db, kIdPV, (np == 0 && t == 0 && ks == 0) ? 0u : 1u);
+              }
+          umma_commit(&B.empty[st]);
+          umma_commit(&B.p_empty[pb]);
+          ++np;
+          did = true;
+        }
+      }
+      if (did) {
+        t_last = 0;
+      } else {
+        const uint64_t now = global_timer_ns();
+        if (t_last == 0) t_last = now;
+        if (*abort_flag || now - t_last > kWaitLimitNs) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
       }
     }
-    if (!ok) break;
-    if (n == 1 && !mbar_wait(B.o_empty, (it & 1u) ^ 1u, abort_flag)) break;
-    if (!pv(g + n - 1, n == 1)) break;
     g += n;
   }
   // every MMA issued above has completed before tensor memory is released
@@ -283,121 +342,145 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
   drain_wait(B.drain, 0);
 }
 
+// ---------------------------------------------------------------- softmax warps (warps 2-9)
 
-// ---------------------------------------------------------------- softmax warps (warps 2-5)
-
-// Barrier of the four softmax warps that also ORs a flag over them.
-__device__ __forceinline__ bool wg_bar_or(bool v) {
+// Barrier of one softmax warpgroup (id 1 + wg, 128 threads) that also ORs a
+// flag over it.
+__device__ __forceinline__ bool wg_bar_or(int id, bool v) {
   uint32_t r;
   asm volatile(
-      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "r"(id)
       : "memory");
   return r != 0u;
 }
 
-// e4m3 pair of x and the exact fp32 values the two codes stand for.
-__device__ __forceinline__ uint32_t e4m3_pair(float x0, float x1, float &v0, float &v1) {
-  const uint32_t c = f32x2_to_e4m3x2(x0, x1);
-  const uint32_t hv = e4m3x2_to_f16x2(c);
-  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hv));
-  v0 = f.x;
-  v1 = f.y;
-  return c;
+// Whole warp: 16 lanes from taddr's lane, 32 columns, in the register-MMA
+// accumulator layout: thread t gets rows t/4 and t/4 + 8; for column group k
+// (8 columns) r[4k..4k+3] = (row t/4, col 8k + 2(t%4)), (.., +1),
+// (row t/4 + 8, 8k + 2(t%4)), (.., +1).
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
 }
 
-// Three e4m3 terms of four non-negative floats: t1 = e4m3(x), t2 = e4m3(x -
-// t1), t3 = e4m3(x - t1 - t2) (each difference is exact in fp32).
-__device__ __forceinline__ void three_terms4(float x0, float x1, float x2, float x3, uint32_t &t1, uint32_t &t2,
-                                             uint32_t &t3) {
-  float a0, a1, a2, a3;
-  t1 = e4m3_pair(x0, x1, a0, a1) | (e4m3_pair(x2, x3, a2, a3) << 16);
-  x0 -= a0; x1 -= a1; x2 -= a2; x3 -= a3;
-  t2 = e4m3_pair(x0, x1, a0, a1) | (e4m3_pair(x2, x3, a2, a3) << 16);
-  t3 = f32x2_to_e4m3x2(x0 - a0, x1 - a1) | (f32x2_to_e4m3x2(x2 - a2, x3 - a3) << 16);
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
 }
 
+// Three e4m3 terms of a pair of non-negative floats (lo -> low byte), split
+// in f16: x = f16(x), t1 = e4m3(x), t2 = e4m3(x - t1), t3 = e4m3(x - t1 - t2);
+// each difference is exact in f16.
+__device__ __forceinline__ void three_terms2(float lo, float hi, uint32_t &t1, uint32_t &t2, uint32_t &t3) {
+  const __half2 x = __floats2half2_rn(lo, hi);
+  const uint32_t xb = *reinterpret_cast<const uint32_t *>(&x);
+  t1 = f16x2_to_e4m3x2(xb);
+  const uint32_t b1 = e4m3x2_to_f16x2(t1);
+  const __half2 r1 = __hsub2(x, *reinterpret_cast<const __half2 *>(&b1));
+  const uint32_t r1b = *reinterpret_cast<const uint32_t *>(&r1);
+  t2 = f16x2_to_e4m3x2(r1b);
+  const uint32_t b2 = e4m3x2_to_f16x2(t2);
+  const __half2 r2 = __hsub2(r1, *reinterpret_cast<const __half2 *>(&b2));
+  t3 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&r2));
+}
+
+// Softmax warpgroup wg (heads 32 wg .. 32 wg + 31).  Warp w of the group
+// reads the S^T rows of tensor-memory quarter w % 4: tokens 16 q .. 16 q + 15
+// of the page (the M = 64 accumulator keeps row i in lane 32 (i / 16) + i % 16).
 __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, const Bars &B, const ItemDesc *items,
                                            const uint32_t *item_status, uint32_t tmem, volatile int *abort_flag) {
   const TcSmem sp = tc_smem();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wq = warp - 2;          // 0..3 among the softmax warps
-  const int gq = warp & 3;          // tensor-memory lane quarter this warp may access
-  const int wt = threadIdx.x - 64;  // 0..127
-  float *wg = reinterpret_cast<float *>(smem + sp.wg);
-  float *s_cq = wg + kWgCq, *s_m = wg + kWgM, *s_alpha = wg + kWgAlpha, *s_beta = wg + kWgBeta;
-  float *s_ex = wg + kWgEx, *s_exs = wg + kWgExS;
+  const int wg = (warp - 2) >> 2;          // warpgroup: 0 or 1
+  const int wq = (warp - 2) & 3;           // warp within the group
+  const int gq = warp & 3;                 // tensor-memory lane quarter
+  const int wt = threadIdx.x - 64 - 128 * wg;  // 0..127 within the group
+  const int bar_id = 1 + wg;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int hb = 32 * wg;                  // first head of the group
+  float *wsc = reinterpret_cast<float *>(smem + sp.wg);
+  float *s_cq = wsc + kWgCq, *s_m = wsc + kWgM, *s_alpha = wsc + kWgAlpha, *s_beta = wsc + kWgBeta;
+  float *s_ex = wsc + kWgEx + wg * 128;     // [warp][32 heads]
+  float *s_exs = wsc + kWgExS + wg * 4;     // [warp]
   const float *scales = reinterpret_cast<const float *>(smem + sp.scales);
   uint8_t *pbase = smem + sp.p;
-  const uint32_t tq = tmem + ((uint32_t)(32 * gq) << 16);  // this warp's lanes
-  // S^T row i (token i of the page) sits in lane 32 (i / 16) + i % 16: this
-  // warp holds tokens 16 gq .. 16 gq + 15 in its lanes 0-15.
-  const int t = 16 * gq + (lane & 15);
-  const bool tok_lane = lane < 16;
+  const uint32_t tq = tmem + ((uint32_t)(32 * gq) << 16);
+  const int t0 = 16 * gq + gid, t1 = t0 + 8;  // this thread's two tokens of the page
   uint32_t g = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
     bool fail = !mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag);
-    if (wg_bar_or(fail)) break;
+    if (wg_bar_or(bar_id, fail)) break;
     const ItemDesc d = items[slot];
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
-    if (wt < kTH) {
-      s_cq[wt] = __ldg(&a.qfac[(size_t)d.b * kTH + wt]);
-      s_m[wt] = kNegInf;
+    if (wt < 32) {
+      s_cq[hb + wt] = __ldg(&a.qfac[(size_t)d.b * kTH + hb + wt]);
+      s_m[hb + wt] = kNegInf;
     }
     float s_ref = 0.f;
-    float lp[kTH];
+    float lp[8];  // l of heads hb + 8k + 2 tig + e, index 2k + e
 #pragma unroll
-    for (int h = 0; h < kTH; ++h) lp[h] = 0.f;
-    named_bar_sync(1, 128);
+    for (int i = 0; i < 8; ++i) lp[i] = 0.f;
+    named_bar_sync(bar_id, 128);
+    float cq[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 c2 = *reinterpret_cast<const float2 *>(&s_cq[hb + 8 * k + 2 * tig]);
+      cq[2 * k] = c2.x;
+      cq[2 * k + 1] = c2.y;
+    }
     bool dead = false;
     for (uint32_t j = 0; j < n; ++j) {
       const uint32_t gp = g + j, sb = gp & 1u, st = gp % kNst;
       fail = fail || !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
              !mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
              !mbar_wait(&B.p_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag);
-      float y[kTH];
+      float y[16];  // [k][row][e] -> 4k + 2 row + e
       {
         tc_fence_after();
-        uint32_t r[32];
-        tmem_ld32(tq + kColS + 64 * sb, r);
+        uint32_t r[16], r2[16];
+        tmem_ld16x256_x4(tq + kColS + 128 * sb + hb, r);        // K . T1
+        tmem_ld16x256_x4(tq + kColS + 128 * sb + 64 + hb, r2);  // K . T2
 #pragma unroll
-        for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(r[i]);
-        tmem_ld32(tq + kColS + 64 * sb + 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) y[32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 16; ++i) y[i] = __uint_as_float(r[i]) + __uint_as_float(r2[i]);
         tc_fence_before();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.s_empty[sb]);
-      const bool valid = tok_lane && (d.p0 + (int)j) * kTS + t < d.L;
-      const float s_t = valid ? scales[st * kTS + t] : 0.f;
-      // z (log2 units) = S * (tau log2(e) 2^e_h) * s_t; padding and spare lanes -> -inf
+      const int tok0 = (d.p0 + (int)j) * kTS;
+      const bool v0 = tok0 + t0 < d.L, v1 = tok0 + t1 < d.L;
+      const float s0 = v0 ? scales[st * kTS + t0] : 0.f, s1 = v1 ? scales[st * kTS + t1] : 0.f;
+      float mx[8];
 #pragma unroll
-      for (int h = 0; h < kTH; h += 4) {
-        const float4 c4 = *reinterpret_cast<const float4 *>(&s_cq[h]);
-        y[h] = valid ? y[h] * c4.x * s_t : kNegInf;
-        y[h + 1] = valid ? y[h + 1] * c4.y * s_t : kNegInf;
-        y[h + 2] = valid ? y[h + 2] * c4.z * s_t : kNegInf;
-        y[h + 3] = valid ? y[h + 3] * c4.w * s_t : kNegInf;
-      }
-      // per-head maxima over the page: warp maxima, then over the four warps
-      float mine0 = kNegInf, mine1 = kNegInf;
+      for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int h = 0; h < kTH; ++h) {
-        const float r = warp_max_f32(y[h]);
-        if (lane == (h & 31)) {
-          if (h < 32) mine0 = r;
-          else mine1 = r;
+        for (int e = 0; e < 2; ++e) {
+          float &ya = y[4 * k + e], &yb = y[4 * k + 2 + e];
+          ya = v0 ? ya * cq[2 * k + e] * s0 : kNegInf;
+          yb = v1 ? yb * cq[2 * k + e] * s1 : kNegInf;
+          float m = fmaxf(ya, yb);
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          mx[2 * k + e] = m;
         }
+      const float smx = warp_max_f32(fmaxf(s0, s1));
+      if (gid == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<float2 *>(&s_ex[wq * 32 + 8 * k + 2 * tig]) = make_float2(mx[2 * k], mx[2 * k + 1]);
       }
-      const float smx = warp_max_f32(s_t);
-      s_ex[wq * kTH + lane] = mine0;
-      s_ex[wq * kTH + 32 + lane] = mine1;
       if (lane == 0) s_exs[wq] = smx;
-      if (wg_bar_or(fail)) {
+      if (wg_bar_or(bar_id, fail)) {
         dead = true;
         break;
       }
@@ -405,63 +488,69 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       const float s_old = s_ref;
       const float s_new = sm > 2.f * s_old ? sm : s_old;
       bool resc = s_new != s_old;
-      if (wt < kTH) {
-        const float tm = fmaxf(fmaxf(s_ex[wt], s_ex[kTH + wt]), fmaxf(s_ex[2 * kTH + wt], s_ex[3 * kTH + wt]));
-        const float m_old = s_m[wt];
+      if (wt < 32) {
+        const int h = hb + wt;
+        const float tm = fmaxf(fmaxf(s_ex[wt], s_ex[32 + wt]), fmaxf(s_ex[64 + wt], s_ex[96 + wt]));
+        const float m_old = s_m[h];
         const float m_new = tm > m_old + kTheta ? tm : m_old;
         const float alpha = fast_exp2(m_old - m_new);
-        s_m[wt] = m_new;
-        s_alpha[wt] = alpha;
-        s_beta[wt] = alpha * (s_old / s_new);
+        s_m[h] = m_new;
+        s_alpha[h] = alpha;
+        s_beta[h] = alpha * (s_old / s_new);
         resc = resc || m_new != m_old;
       }
       s_ref = s_new;
-      resc = wg_bar_or(resc) && j > 0;
+      resc = wg_bar_or(bar_id, resc) && j > 0;
       if (resc) {
-        // O^T so far holds the earlier pages: every head column h scaled by beta_h
-        // once the previous page's PV has landed; l by alpha_h.
+        // this group's columns of O^T hold the earlier pages: scale head h by
+        // beta_h once the previous page's PV has landed; l by alpha_h
         fail = fail || !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag);
         if (!fail) {
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
-            const uint32_t ta = tq + kColO + 32 * c;
+            const uint32_t ta = tq + kColO + 64 * c + hb;
             tmem_ld32(ta, r);
-            const float *bt = s_beta + 32 * (c & 1);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bt[i]);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * s_beta[hb + i]);
             tmem_st32(ta, r);
           }
           tmem_wait_st();
         }
 #pragma unroll
-        for (int h = 0; h < kTH; ++h) lp[h] *= s_alpha[h];
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) lp[2 * k + e] *= s_alpha[hb + 8 * k + 2 * tig + e];
       }
       // P'' = p (s_t / s_ref) 2^kPExp as three e4m3 terms; p = 2^(z - m) summed into l
-      const float kt = valid ? fast_log2(s_t / s_ref) + kPExp : 0.f;
-      const float rt = fast_exp2(-kt);
-      // P^T, MN-major without swizzle: head chunks of 16 bytes, token rows 16 bytes apart
-      uint8_t *pt = pbase + sb * kPBuf + (t & 7) * 16 + (t >> 3) * 128;
+      const float kt0 = v0 ? fast_log2(s0 / s_ref) + kPExp : 0.f;
+      const float kt1 = v1 ? fast_log2(s1 / s_ref) + kPExp : 0.f;
+      const float rt0 = fast_exp2(-kt0), rt1 = fast_exp2(-kt1);
+      // P^T, MN-major without swizzle: byte (head h, token t) at
+      // (h % 16) + (h / 16) * 1024 + (t % 8) * 16 + (t / 8) * 128
+      uint8_t *pt = pbase + sb * kPBuf;
 #pragma unroll
-      for (int hc = 0; hc < 4; ++hc) {
-        uint32_t w1[4], w2[4], w3[4];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int h = 16 * hc + 4 * q4;
-          const float4 m4 = *reinterpret_cast<const float4 *>(&s_m[h]);
-          const float p0 = fast_exp2(y[h] - m4.x + kt), p1 = fast_exp2(y[h + 1] - m4.y + kt);
-          const float p2 = fast_exp2(y[h + 2] - m4.z + kt), p3 = fast_exp2(y[h + 3] - m4.w + kt);
-          lp[h] += p0 * rt;
-          lp[h + 1] += p1 * rt;
-          lp[h + 2] += p2 * rt;
-          lp[h + 3] += p3 * rt;
-          three_terms4(p0, p1, p2, p3, w1[q4], w2[q4], w3[q4]);
-        }
-        if (tok_lane && !fail) {
-          *reinterpret_cast<uint4 *>(pt + hc * 1024) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-          *reinterpret_cast<uint4 *>(pt + kPTerm + hc * 1024) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-          *reinterpret_cast<uint4 *>(pt + 2 * kPTerm + hc * 1024) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+      for (int k = 0; k < 4; ++k) {
+        const int h = hb + 8 * k + 2 * tig;
+        const float2 m2 = *reinterpret_cast<const float2 *>(&s_m[h]);
+        const float pa0 = fast_exp2(y[4 * k] - m2.x + kt0), pa1 = fast_exp2(y[4 * k + 1] - m2.y + kt0);
+        const float pb0 = fast_exp2(y[4 * k + 2] - m2.x + kt1), pb1 = fast_exp2(y[4 * k + 3] - m2.y + kt1);
+        lp[2 * k] += pa0 * rt0 + pb0 * rt1;
+        lp[2 * k + 1] += pa1 * rt0 + pb1 * rt1;
+        uint32_t a1, a2, a3, b1, b2, b3;
+        three_terms2(pa0, pa1, a1, a2, a3);
+        three_terms2(pb0, pb1, b1, b2, b3);
+        if (!fail) {
+          const int hoff = (h & 15) + (h >> 4) * 1024;
+          uint8_t *q0 = pt + hoff + (t0 & 7) * 16 + (t0 >> 3) * 128;
+          uint8_t *q1 = pt + hoff + (t1 & 7) * 16 + (t1 >> 3) * 128;
+          *reinterpret_cast<uint16_t *>(q0) = (uint16_t)a1;
+          *reinterpret_cast<uint16_t *>(q0 + kPTerm) = (uint16_t)a2;
+          *reinterpret_cast<uint16_t *>(q0 + 2 * kPTerm) = (uint16_t)a3;
+          *reinterpret_cast<uint16_t *>(q1) = (uint16_t)b1;
+          *reinterpret_cast<uint16_t *>(q1 + kPTerm) = (uint16_t)b2;
+          *reinterpret_cast<uint16_t *>(q1 + 2 * kPTerm) = (uint16_t)b3;
         }
       }
       fence_async_smem();
@@ -474,51 +563,55 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     const uint32_t gl = g + n - 1;
     fail = fail || !mbar_wait(&B.p_empty[gl & 1u], (gl >> 1) & 1u, abort_flag) ||
            !mbar_wait(&B.item_done[slot], (it / kNIQ) & 1u, abort_flag);
-    // l per head: over the 16 token lanes, then over the four warps
+    // l per head: over the eight threads that share a head, then the four warps
 #pragma unroll
-    for (int h = 0; h < kTH; ++h) {
-      float v = lp[h];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
+    for (int i = 0; i < 8; ++i) {
+      float v = lp[i];
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 8);
-      if (lane == (h & 15)) s_ex[wq * kTH + h] = v;
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      lp[i] = v;
     }
-    if (wg_bar_or(fail)) break;
-    if (wt < kTH) s_alpha[wt] = s_ex[wt] + s_ex[kTH + wt] + s_ex[2 * kTH + wt] + s_ex[3 * kTH + wt];
-    named_bar_sync(1, 128);
+    if (gid == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<float2 *>(&s_ex[wq * 32 + 8 * k + 2 * tig]) = make_float2(lp[2 * k], lp[2 * k + 1]);
+    }
+    if (wg_bar_or(bar_id, fail)) break;
+    if (wt < 32) s_alpha[hb + wt] = s_ex[wt] + s_ex[32 + wt] + s_ex[64 + wt] + s_ex[96 + wt];
+    named_bar_sync(bar_id, 128);
     tc_fence_after();
     const uint32_t stv = item_status[slot];
     const float oscale = s_ref * exp2f(-kPExp);  // O^T accumulates p (s_t / s_ref) 2^kPExp * code
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
       uint32_t r[32];
-      tmem_ld32(tq + kColO + 32 * c, r);
-      const int dd = 128 * (c >> 1) + 32 * gq + lane;  // value index of this thread's row
-      const int h0 = 32 * (c & 1);
+      tmem_ld32(tq + kColO + 64 * c + hb, r);
+      const int dd = 128 * c + 32 * gq + lane;  // value index of this thread's row
       if (d.nb == 1) {
-        float *o = a.out + (size_t)d.b * kTH * kTDv + dd;
+        float *o = a.out + ((size_t)d.b * kTH + hb) * kTDv + dd;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          o[(size_t)(h0 + i) * kTDv] = stv ? 0.f : __uint_as_float(r[i]) * oscale / s_alpha[h0 + i];
+          o[(size_t)i * kTDv] = stv ? 0.f : __uint_as_float(r[i]) * oscale / s_alpha[hb + i];
       } else {
-        float *o = a.part_o + (size_t)d.cg * kTH * kTDv + dd;
+        float *o = a.part_o + ((size_t)d.cg * kTH + hb) * kTDv + dd;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[(size_t)(h0 + i) * kTDv] = __uint_as_float(r[i]) * oscale;
+        for (int i = 0; i < 32; ++i) o[(size_t)i * kTDv] = __uint_as_float(r[i]) * oscale;
       }
     }
-    if (d.nb != 1 && wt < kTH) a.part_ml[(size_t)d.cg * kTH + wt] = make_float2(s_m[wt], s_alpha[wt]);
+    if (d.nb != 1 && wt < 32)
+      a.part_ml[(size_t)d.cg * kTH + hb + wt] = make_float2(s_m[hb + wt], s_alpha[hb + wt]);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(B.o_empty);
-    named_bar_sync(1, 128);  // the scratch is reused by the next item
+    named_bar_sync(bar_id, 128);  // the scratch is reused by the next item
     if (wt == 0) mbar_arrive(&B.item_empty[slot]);
     g += n;
   }
 }
 
-
 __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_constant__ CUtensorMap map,
+                                                                 const __grid_constant__ CUtensorMap map_tail,
                                                                  const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -536,17 +629,17 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.s_empty[i], 4);
-      mbar_init(&B.p_full[i], 4);
+      mbar_init(&B.s_empty[i], 8);
+      mbar_init(&B.p_full[i], 8);
       mbar_init(&B.p_empty[i], 1);
     }
     mbar_init(B.q_full, 1);
     mbar_init(B.q_empty, 1);
-    mbar_init(B.o_empty, 4);
+    mbar_init(B.o_empty, 8);
     mbar_init(B.drain, 1);
     for (int i = 0; i < kNIQ; ++i) {
       mbar_init(&B.item_full[i], 1);
-      mbar_init(&B.item_empty[i], 2);  // the MMA thread and the softmax warps
+      mbar_init(&B.item_empty[i], 3);  // the MMA thread and the two softmax groups
       mbar_init(&B.item_done[i], 1);
     }
     *abort_flag = 0;
@@ -560,8 +653,11 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
   pdl_wait();
   pdl_launch_dependents();
   if (warp == 0) {
-    if (lane == 0) tma_prefetch_desc(&map);
-    tc_producer(a, map, smem, B, items, item_status, abort_flag);
+    if (lane == 0) {
+      tma_prefetch_desc(&map);
+      tma_prefetch_desc(&map_tail);
+    }
+    tc_producer(a, map, map_tail, smem, B, items, item_status, abort_flag);
   } else if (warp == 1) {
     if (lane == 0) tc_mma(a, smem, B, items, tmem, abort_flag);
     __syncwarp();
@@ -582,19 +678,19 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
 
 }  // namespace
 
-// Tensor map over the stream pool viewed as [page][slot][576 bytes]; a box
-// is one 128-byte column block of a page (the fifth box reads 64 bytes past
-// the row end, which the copy fills with zeros).
-static int make_stream_map(CUtensorMap *map, const void *pool, int P) {
+// Tensor maps over the stream pool viewed as [page][slot][576 bytes]: boxes
+// of one page x 128 bytes (128-byte swizzle) for columns 0-511, and one page
+// x 64 bytes (64-byte swizzle) for columns 512-575.
+static int make_stream_map(CUtensorMap *map, const void *pool, int P, uint32_t box_bytes, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
   cuuint64_t dims[3] = {(cuuint64_t)kTD, (cuuint64_t)kTS, (cuuint64_t)P};
   cuuint64_t strides[2] = {(cuuint64_t)kTD, (cuuint64_t)kTD * kTS};
-  cuuint32_t box[3] = {128, (cuuint32_t)kTS, 1};
+  cuuint32_t box[3] = {box_bytes, (cuuint32_t)kTS, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (stream)");
   return PFKV_OK;
 }
@@ -605,8 +701,10 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   a.Hkv = 1;
   a.G = kTH;
   a.qprep = 1;
-  CUtensorMap map;
-  int rc = make_stream_map(&map, a.k_pool, a.P);
+  CUtensorMap map, map_tail;
+  int rc = make_stream_map(&map, a.k_pool, a.P, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  rc = make_stream_map(&map_tail, a.k_pool, a.P, 64, CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
   const uint32_t smem = tc_smem().total + 1024;
   static std::mutex mu;
@@ -623,6 +721,9 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
     }
   }
   const int grid = num_sms();
+  // one equal page range per CTA when requests may be cut into 3 or more
+  // pieces; otherwise longest-first items from a shared counter
+  a.balanced = a.max_splits >= 3 ? (grid < kMaxRanges ? grid : kMaxRanges) : 0;
   plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, grid * 2, 8);
   rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
   if (rc) return rc;
@@ -636,7 +737,7 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  rc = cuda_ok(cudaLaunchKernelEx(&cfg, latent_tc_kernel, map, a), "latent kernel launch");
+  rc = cuda_ok(cudaLaunchKernelEx(&cfg, latent_tc_kernel, map, map_tail, a), "latent kernel launch");
   if (rc) return rc;
   // merge in blocks of 16 heads
   DecodeArgs m = a;

@@ -22,8 +22,9 @@ struct WsHeader {
 
 // Decode workspace carve-up.
 struct WsLayout {
-  size_t hdr, split_first, split_count, chunk_info, part_ml, part_o, qterms, qfac, total;
+  size_t hdr, split_first, split_count, chunk_info, cta_first, part_ml, part_o, qterms, qfac, total;
 };
+constexpr int kMaxRanges = 1024;  // balanced plan: at most this many page ranges (one per CTA)
 // latent: the latent-stream path also keeps each request's query as two e4m3
 // terms in the shared-memory image its kernel copies (qterms, 72 KB per
 // request) and one factor per head (qfac).
@@ -64,6 +65,11 @@ struct DecodeArgs {
   int qprep;
   uint8_t *qterms;
   float *qfac;
+  // balanced plan (balanced > 0: at most that many ranges): the concatenated
+  // page list of all requests is cut into equal ranges, one per CTA; CTA c
+  // processes items cta_first[c] .. cta_first[c + 1] - 1
+  int balanced;
+  int *cta_first;
 };
 
 // Tensor-map encoder obtained from the driver without linking libcuda.

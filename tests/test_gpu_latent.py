@@ -37,7 +37,7 @@ def test_latent_small_ragged():
     _check(_lat(500, [1, 63, 64, 65, 127, 129, 300, 1000]))
 
 
-@pytest.mark.parametrize("max_splits", [1, 2, 64])
+@pytest.mark.parametrize("max_splits", [1, 2, 3, 5, 64])
 def test_latent_splits(max_splits):
     _check(_lat(501, [5000, 2100, 77]), max_splits=max_splits)
 
