@@ -67,13 +67,12 @@ __host__ __device__ inline int plan_blocks(const DecodeArgs &a) { return 1 + pla
 // [128, 256), and written as T1 = e4m3(q 2^-e_h), T2 = e4m3(q 2^-e_h - T1):
 // T1 + T2 equals the scaled row exactly for every element of magnitude at
 // least 2^-2 (a bf16 significand has 8 bits, each term carries 4), the
-// rest to within 2^-10.  The terms are stored as the kernel's shared-memory
-// image of one 128-row operand (row R < 64: T1 of head R; R >= 64: T2 of
-// head R - 64): columns 0-511 in four 16 KB blocks of 128-byte rows with the
-// 128-byte swizzle (16-byte chunk j of row R at c*16384 + R*128 +
-// 16*(j ^ (R & 7))), columns 512-575 in one 8 KB block of 64-byte rows with
-// the 64-byte swizzle (chunk j at 65536 + R*64 + 16*(j ^ ((R >> 1) & 3))).
-// qfac[h] = softmax scale * log2(e) * 2^e_h.
+// rest to within 2^-10.  The terms form one 128-row operand: row
+// R = 32 (h / 16) + 16 t + h % 16 holds term t of head h.  Columns 0-511 of
+// row R are stored as 512 plain bytes at R * 512 (loaded into tensor memory
+// by the kernel), columns 512-575 as the 64-byte-swizzled shared-memory
+// image at 65536: 16-byte chunk j of row R at 65536 + R * 64 +
+// 16 (j ^ ((R >> 1) & 3)).  qfac[h] = softmax scale * log2(e) * 2^e_h.
 __device__ __forceinline__ void plan_qprep(const DecodeArgs &a, int b) {
   __shared__ float s_qinv[64];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -94,15 +93,15 @@ __device__ __forceinline__ void plan_qprep(const DecodeArgs &a, int b) {
   for (int u = tid; u < 64 * 36; u += (int)blockDim.x) {
     const int h = u / 36, r = u % 36;
     const int k0 = 16 * r;  // 16 columns starting here (r < 36 covers all 576)
-    size_t off1, off2;  // T1 row h, T2 row 64 + h (same swizzle phase)
+    const int R1 = 32 * (h >> 4) + (h & 15), R2 = R1 + 16;  // rows of T1 and T2 of head h
+    size_t off1, off2;
     if (r < 32) {
-      const int c = r / 8, j = r % 8;
-      off1 = (size_t)c * 16384 + h * 128 + 16 * (j ^ (h & 7));
-      off2 = off1 + 64 * 128;
+      off1 = (size_t)R1 * 512 + 16 * r;
+      off2 = (size_t)R2 * 512 + 16 * r;
     } else {
       const int j = r - 32;
-      off1 = (size_t)65536 + h * 64 + 16 * (j ^ ((h >> 1) & 3));
-      off2 = off1 + 64 * 64;
+      off1 = (size_t)65536 + R1 * 64 + 16 * (j ^ ((R1 >> 1) & 3));
+      off2 = (size_t)65536 + R2 * 64 + 16 * (j ^ ((R2 >> 1) & 3));
     }
     uint32_t t1[4], t2[4];
     {

@@ -9,11 +9,13 @@
 // (about 240 flop per cached byte), so both products run as tcgen05 MMAs of
 // kind f8f6f4 (e4m3 x e4m3 -> fp32 in tensor memory), straight from the
 // codes the TMA engine landed in shared memory:
-//   S^T = K . Q^T   M = 64 tokens (one page), N = 64 heads, K = 576.  The
-//        bf16 query of head h is q_h = 2^e_h (T1 + T2), two e4m3 terms with
-//        one power-of-two scale; T1 + T2 is exact for every element within
-//        2^10 of the row's largest, so the term split adds no error that
-//        matters.  Terms are prepared once per request by the plan grid.
+//   S = Q . K^T   M = 128 query rows, N = 64 tokens (one page), K = 576.
+//        The bf16 query of head h is q_h = 2^e_h (T1 + T2), two e4m3 terms
+//        with one power-of-two scale (exact for every element within 2^10
+//        of the row's largest); both terms are rows of A, so one MMA per K
+//        step gives T1.k and T2.k, which the softmax warps add.  A lives in
+//        tensor memory (columns 0-511 of the query) and, for the last 64
+//        columns, in shared memory; it is loaded once per work item.
 //   O^T += V^T . P^T   M = 128 values (four chunks of the 512), N = 64
 //        heads, K = 64 tokens.  V^T is the page itself read MN-major.  The
 //        probabilities, with the token's scale folded in relative to a
@@ -21,15 +23,17 @@
 //        terms, about 12 significant bits) by the softmax warps.
 // The softmax normaliser l is summed from the fp32 probabilities.
 //
-// One CTA per SM, persistent, work item = (request, split of its pages),
-// all 64 heads.  Warp 0 loads pages (TMA, 128-byte swizzle, bounds and tag
-// checks beside the copies) and the query terms; warp 1 owns tensor memory
-// and issues the MMAs (one thread); warps 2-9, two groups of four with 32
-// heads each, read S^T from tensor memory (every lane holds two tokens x
-// eight heads), run the online softmax (running maxima move only when they
-// grow by more than 8x, and only then is the group's part of O^T rescaled
-// in tensor memory), write P^T, and write the item's partial or final
-// output.  Partials are merged by the shared log-sum-exp merge kernel.
+// One CTA per SM, persistent; work item = (request, range of its pages), all
+// 64 heads.  Warp 0 loads pages into a five-page ring (TMA, bounds and tag
+// checks beside the copies); warp 1 owns tensor memory and issues the MMAs
+// (one thread, each MMA group as soon as its inputs are ready); warps 2-5
+// run the softmax: warp w reads tensor-memory quarter w % 4, i.e. heads
+// 16 q .. 16 q + 15, each lane one head and 32 of the page's tokens, so the
+// running maxima and sums are per thread.  A running maximum moves only when
+// it grows by more than 8x; O^T, whose columns are heads and whose lanes
+// are values, is then rescaled by all four warps before the page's PV, a
+// hand-off that costs nothing on the pages that need none.  Partials are
+// merged by the shared log-sum-exp merge kernel.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -49,44 +53,45 @@ constexpr uint32_t kBlk = kTS * 128;          // 8192: one 128-byte column block
 // swizzle), columns 512-575 as one 64-byte block (64-byte swizzle).
 constexpr uint32_t kPageTail = 4 * kBlk;      // 32768
 constexpr uint32_t kPageSm = kPageTail + kTS * 64;  // 36864
-// Query terms as one 128-row operand (rows 0-63: T1 of heads 0-63, rows
-// 64-127: T2): four 128-byte column blocks of 16 KB, then the 64-byte tail.
-constexpr uint32_t kQBlk = 2 * kBlk;          // 16384
-constexpr uint32_t kQTail = 4 * kQBlk;        // 65536
-constexpr uint32_t kQBytes = kQTail + 2 * kTH * 64;  // 73728
+// Query image per request (written by the plan grid): 128 rows x 512 bytes
+// for tensor memory, then the 64-byte-swizzled 128 x 64 tail.  Row r of the
+// operand is term r / 16 % 2 of head 16 (r / 32) + r % 16.
+constexpr uint32_t kQMainBytes = 128 * 512;   // 65536
+constexpr uint32_t kQTailBytes = 128 * 64;    // 8192
+static_assert(kQMainBytes + kQTailBytes == kLatentQTermBytes, "query image size");
 constexpr int kPT = 3;                        // e4m3 terms of the probabilities
 constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
 constexpr uint32_t kPBuf = kPT * kPTerm;      // 12288
-constexpr int kNst = 3;                       // pages in flight per CTA
+constexpr int kNst = 5;                       // pages in flight per CTA
 constexpr int kPrefetch = 6;                  // pages pulled into L2 ahead of their copy
-constexpr int kTThreads = 320;                // producer, MMA, two groups of four softmax warps
-constexpr uint32_t kTmemCols = 512;           // S^T x2 (128 columns each: T1 | T2 parts), O^T (4 x 64)
-constexpr uint32_t kColS = 0, kColO = 256;
+constexpr int kTThreads = 192;                // producer, MMA, four softmax warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;  // Q (128) | S x2 (64 each) | O^T (4 x 64)
 constexpr float kTheta = 3.f;                 // log2 growth of a running max that triggers a rescale
 constexpr float kPExp = 4.75f;                // P'' = p (s_t / s_ref) 2^kPExp <= 2^kTheta * 2 * 2^4.75 < 448
-constexpr uint32_t kIdQK = umma_idesc_e4m3(64, 128, 0, 0);
-constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 64, 1, 1);
+constexpr uint32_t kIdQK = umma_idesc_e4m3(128, 64, 0, 0);
+constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 64, 1, 0);
 
 struct TcSmem {
-  uint32_t ring, q, p, scales, wg, bars, items, total;
+  uint32_t ring, qtail, p, scales, wg, bars, items, total;
 };
 
 __host__ __device__ constexpr TcSmem tc_smem() {
   TcSmem s{};
-  s.ring = 0;                                  // kNst pages, each 5 column blocks (1024-aligned)
-  s.q = s.ring + kNst * kPageSm;               // query terms (kQBytes)
-  s.p = s.q + kQBytes;                         // 2 buffers x kPT P^T terms
+  s.ring = 0;                                  // kNst pages (1024-aligned)
+  s.qtail = s.ring + kNst * kPageSm;           // query tail (A of the last two QK^T steps)
+  s.p = s.qtail + kQTailBytes;                 // 2 buffers x kPT P^T terms
   s.scales = s.p + 2 * kPBuf;                  // kNst x 64 per-token scales
   s.wg = s.scales + kNst * kTS * 4;            // softmax-warp scratch (see below)
-  s.bars = s.wg + 4 * (64 * 4 + 2 * 4 * 32 + 2 * 4);  // cq, m, alpha, beta | ex[2][4][32] | ex_s[2][4]
-  s.items = s.bars + 8 * (2 * kNst + 12 + 3 * kNIQ);
+  s.bars = s.wg + 4 * (2 * 64 + 3 * 64 + 4);   // beta[2][64] | l, m, cq-unused[64] | tags[2], pad
+  s.items = s.bars + 8 * (2 * kNst + 14 + 3 * kNIQ);
   s.total = s.items + (sizeof(ItemDesc) + 4) * kNIQ + 16;
   return s;
 }
 static_assert(tc_smem().total + 1024 <= 232448, "shared memory plan exceeds one SM");
 
-// Softmax-warp scratch, floats: cq[64] | m[64] | alpha[64] | beta[64] | ex[group][warp][32] | ex_s[group][warp]
-constexpr int kWgCq = 0, kWgM = 64, kWgAlpha = 128, kWgBeta = 192, kWgEx = 256, kWgExS = 512;
+// Softmax-warp scratch, floats: beta[2][64] | l[64] | m[64] | spare[64] | resc_tag[2] (uint32) | pad
+constexpr int kWgBeta = 0, kWgL = 128, kWgM = 192, kWgTag = 320;
 
 // Bounded wait that ignores the abort flag: used on the way out, so that a
 // block that gave up still lets its own copies and MMAs land before it exits.
@@ -97,7 +102,8 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 struct Bars {
-  uint64_t *full, *empty, *s_full, *s_empty, *p_full, *p_empty, *q_full, *q_empty, *o_empty, *drain;
+  uint64_t *full, *empty, *s_full, *s_empty, *p_full, *p_empty, *q_full, *q_empty, *q_tfull, *o_empty, *r_done,
+      *drain;
   uint64_t *item_full, *item_empty, *item_done;
 };
 
@@ -112,7 +118,9 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
   r.p_empty = b; b += 2;
   r.q_full = b; b += 1;
   r.q_empty = b; b += 1;
+  r.q_tfull = b; b += 1;
   r.o_empty = b; b += 1;
+  r.r_done = b; b += 1;
   r.drain = b; b += 1;
   r.item_full = b; b += kNIQ;
   r.item_empty = b; b += kNIQ;
@@ -166,12 +174,11 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
       d.b = b; d.cg = item; d.g = 0; d.p0 = p0; d.p1 = p1; d.L = info.w; d.ring = g; d.nb = info2.x;
       items[slot] = d;
       mbar_arrive(&B.item_full[slot]);
-      // the request's query terms, once the previous item's last QK^T is done
+      // the last 64 columns of the request's query terms (the A operand of
+      // the last two QK^T steps), once the previous item's last QK^T is done
       if (mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag)) {
-        mbar_arrive_expect_tx(B.q_full, kQBytes);
-        const uint8_t *src = a.qterms + (size_t)b * kQBytes;
-        for (uint32_t o = 0; o < kQBytes; o += kBlk) bulk_load(smem + sp.q + o, src + o, kBlk, B.q_full);
-        static_assert(kQBytes % kBlk == 0, "query image is copied in 8 KB pieces");
+        mbar_arrive_expect_tx(B.q_full, kQTailBytes);
+        bulk_load(smem + sp.qtail, a.qterms + (size_t)b * kLatentQTermBytes + kQMainBytes, kQTailBytes, B.q_full);
         ++q_loads;
       }
     }
@@ -252,11 +259,21 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
 
 // ---------------------------------------------------------------- MMA issuer (warp 1, one thread)
 
-__device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const Bars &B, const ItemDesc *items,
-                                       uint32_t tmem, volatile int *abort_flag) {
+__device__ __forceinline__ void tc_mma(uint8_t *smem, const Bars &B, const ItemDesc *items, uint32_t tmem,
+                                       volatile int *abort_flag) {
   const TcSmem sp = tc_smem();
-  const uint32_t s_ring = smem_addr(smem + sp.ring), s_q = smem_addr(smem + sp.q), s_p = smem_addr(smem + sp.p);
-  uint32_t g = 0;  // pages consumed before the current item
+  const uint32_t s_ring = smem_addr(smem + sp.ring), s_qt = smem_addr(smem + sp.qtail), s_p = smem_addr(smem + sp.p);
+  // Shared-memory descriptors built once; an MMA adds its operand's byte
+  // offset / 16 to the start-address field (addresses stay below 256 KB, so
+  // the 14-bit field never carries).
+  const uint64_t d_page = umma_sdesc(s_ring, 16, 1024, 2);             // B of QK^T: page rows, 128-byte swizzle
+  const uint64_t d_page_tail = umma_sdesc(s_ring + kPageTail, 16, 512, 4);  // B of the tail steps
+  const uint64_t d_qtail = umma_sdesc(s_qt, 16, 512, 4);               // A of the tail steps
+  const uint64_t d_vt = umma_sdesc(s_ring, 8192, 1024, 2);             // A of PV: V^T, MN-major
+  const uint64_t d_pt = umma_sdesc(s_p, 128, 512, 0);                  // B of PV: P^T, K-major
+  const volatile uint32_t *resc_tag = reinterpret_cast<const uint32_t *>(smem + sp.wg) + kWgTag;
+  uint32_t g = 0;       // pages consumed before the current item
+  uint32_t n_resc = 0;  // rescale hand-offs so far
   bool ok = true;
   for (uint32_t it = 0; ok; ++it) {
     const uint32_t slot = it % kNIQ;
@@ -265,11 +282,11 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
     mbar_arrive(&B.item_empty[slot]);
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
-    if (!mbar_wait(B.q_full, it & 1u, abort_flag)) break;
+    if (!mbar_wait(B.q_full, it & 1u, abort_flag) || !mbar_wait(B.q_tfull, it & 1u, abort_flag)) break;
     // Issue each MMA group as soon as its inputs are ready: QK^T of page nq
-    // (page landed, its S^T buffer read by the softmax warps) or PV of page
-    // np (P^T written; for the item's first page, O^T read out).  A PV never
-    // waits behind the next page's copy.
+    // (page landed, its S buffer read by the softmax warps) or PV of page np
+    // (P^T written; O^T read out for the item's first page, rescaled when
+    // the softmax warps asked for it).
     uint32_t nq = 0, np = 0;
     bool o_free = false;
     uint64_t t_last = 0;  // start of the current stretch without progress
@@ -279,24 +296,18 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
         const uint32_t gp = g + nq, st = gp % kNst, sb = gp & 1u;
         if (mbar_test(&B.full[st], (gp / kNst) & 1u) && mbar_test(&B.s_empty[sb], ((gp >> 1) & 1u) ^ 1u)) {
           tc_fence_after();
-          // S^T[sb] = K_page . [T1; T2]^T: 64 tokens x 128 columns (heads of T1,
-          // then of T2) over the 576 columns, 18 steps of 32
+          // S[sb] = [T1; T2 rows] . K_page^T: 128 x 64, K = 576 in 18 steps of 32
+          const uint64_t pg = (uint64_t)((st * kPageSm) >> 4);
+          const uint32_t d_s = tmem + kColS + 64 * sb;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int kk = 0; kk < 16; ++kk)
+            umma_e4m3_ts(d_s, tmem + kColQ + 8 * kk, d_page + pg + (uint64_t)(((kk >> 2) * kBlk + (kk & 3) * 32) >> 4),
+                         kIdQK, kk ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + kk * 32, 16, 1024, 2);
-              const uint64_t db = umma_sdesc(s_q + c * kQBlk + kk * 32, 16, 1024, 2);
-              umma_e4m3(tmem + kColS + 128 * sb, da, db, kIdQK, (c | kk) ? 1u : 0u);
-            }
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t da = umma_sdesc(s_ring + st * kPageSm + kPageTail + kk * 32, 16, 512, 4);
-            const uint64_t db = umma_sdesc(s_q + kQTail + kk * 32, 16, 512, 4);
-            umma_e4m3(tmem + kColS + 128 * sb, da, db, kIdQK, 1u);
-          }
+          for (int kk = 0; kk < 2; ++kk)
+            umma_e4m3(d_s, d_qtail + (uint64_t)(2 * kk), d_page_tail + pg + (uint64_t)(2 * kk), kIdQK, 1u);
           umma_commit(&B.s_full[sb]);
-          if (nq + 1 == n) umma_commit(B.q_empty);  // the query terms may be replaced
+          if (nq + 1 == n) umma_commit(B.q_empty);  // the query operand may be replaced
           ++nq;
           did = true;
         }
@@ -304,19 +315,24 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
       if (np < nq) {
         const uint32_t gp = g + np, st = gp % kNst, pb = gp & 1u;
         if (np == 0 && !o_free) o_free = mbar_test(B.o_empty, (it & 1u) ^ 1u);
-        if ((np > 0 || o_free) && mbar_test(&B.p_full[pb], (gp >> 1) & 1u)) {
+        bool ready = (np > 0 || o_free) && mbar_test(&B.p_full[pb], (gp >> 1) & 1u);
+        const bool resc = ready && np > 0 && resc_tag[pb] == gp + 1u;
+        if (resc) ready = mbar_test(B.r_done, n_resc & 1u);
+        if (ready) {
+          if (resc) ++n_resc;
           tc_fence_after();
           // O^T[c] (+)= V^T_c . (P1 + P2 + P3)^T
+          const uint64_t pg = (uint64_t)((st * kPageSm) >> 4), pp = (uint64_t)((pb * kPBuf) >> 4);
+          const uint32_t first = np == 0 ? 0u : 1u;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int t = 0; t < kPT; ++t)
 #pragma unroll
-              for (int ks = 0; ks < 2; ++ks) {
-                const uint64_t da = umma_sdesc(s_ring + st * kPageSm + c * kBlk + ks * 4096, 8192, 1024, 2);
-                const uint64_t db = umma_sdesc(s_p + pb * kPBuf + t * kPTerm + ks * 512, 128, 1024, 0);
-                umma_e4m3(tmem + kColO + 64 * c, da, db, kIdPV, (np == 0 && t == 0 && ks == 0) ? 0u : 1u);
-              }
+              for (int ks = 0; ks < 2; ++ks)
+                umma_e4m3(tmem + kColO + 64 * c, d_vt + pg + (uint64_t)((c * kBlk + ks * 4096) >> 4),
+                          d_pt + pp + (uint64_t)((t * kPTerm + ks * 256) >> 4), kIdPV,
+                          (t == 0 && ks == 0) ? first : 1u);
           umma_commit(&B.empty[st]);
           umma_commit(&B.p_empty[pb]);
           ++np;
@@ -326,6 +342,9 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
       if (did) {
         t_last = 0;
       } else {
+        // nothing ready: back off briefly, leaving this scheduler's issue slots
+        // to the softmax warp that shares it
+        __nanosleep(64);
         const uint64_t now = global_timer_ns();
         if (t_last == 0) t_last = now;
         if (*abort_flag || now - t_last > kWaitLimitNs) {
@@ -342,32 +361,17 @@ __device__ __forceinline__ void tc_mma(const DecodeArgs &a, uint8_t *smem, const
   drain_wait(B.drain, 0);
 }
 
-// ---------------------------------------------------------------- softmax warps (warps 2-9)
+// ---------------------------------------------------------------- softmax warps (warps 2-5)
 
-// Barrier of one softmax warpgroup (id 1 + wg, 128 threads) that also ORs a
-// flag over it.
-__device__ __forceinline__ bool wg_bar_or(int id, bool v) {
+// Barrier of the four softmax warps (id 1) that also ORs a flag over them.
+__device__ __forceinline__ bool wg_bar_or(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v), "r"(id)
+      : "r"((uint32_t)v)
       : "memory");
   return r != 0u;
-}
-
-// Whole warp: 16 lanes from taddr's lane, 32 columns, in the register-MMA
-// accumulator layout: thread t gets rows t/4 and t/4 + 8; for column group k
-// (8 columns) r[4k..4k+3] = (row t/4, col 8k + 2(t%4)), (.., +1),
-// (row t/4 + 8, 8k + 2(t%4)), (.., +1).
-__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
 }
 
 __device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
@@ -392,219 +396,199 @@ __device__ __forceinline__ void three_terms2(float lo, float hi, uint32_t &t1, u
   t3 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&r2));
 }
 
-// Softmax warpgroup wg (heads 32 wg .. 32 wg + 31).  Warp w of the group
-// reads the S^T rows of tensor-memory quarter w % 4: tokens 16 q .. 16 q + 15
-// of the page (the M = 64 accumulator keeps row i in lane 32 (i / 16) + i % 16).
+// Warp w reads tensor-memory quarter q = w % 4: rows 32 q .. 32 q + 31 of S,
+// i.e. T1 (lanes 0-15) and T2 (lanes 16-31) of heads 16 q .. 16 q + 15.
+// After adding the two halves, lane l holds head 16 q + l % 16 and tokens
+// 32 (l / 16) .. 32 (l / 16) + 31 of the page.
 __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, const Bars &B, const ItemDesc *items,
                                            const uint32_t *item_status, uint32_t tmem, volatile int *abort_flag) {
   const TcSmem sp = tc_smem();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wg = (warp - 2) >> 2;          // warpgroup: 0 or 1
-  const int wq = (warp - 2) & 3;           // warp within the group
-  const int gq = warp & 3;                 // tensor-memory lane quarter
-  const int wt = threadIdx.x - 64 - 128 * wg;  // 0..127 within the group
-  const int bar_id = 1 + wg;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int hb = 32 * wg;                  // first head of the group
+  const int q = warp & 3;                 // tensor-memory lane quarter
+  const int wt = threadIdx.x - 64;        // 0..127
+  const int half = lane >> 4;             // token half, and the term of this lane's S row
+  const int h = 16 * q + (lane & 15);     // head of this thread
   float *wsc = reinterpret_cast<float *>(smem + sp.wg);
-  float *s_cq = wsc + kWgCq, *s_m = wsc + kWgM, *s_alpha = wsc + kWgAlpha, *s_beta = wsc + kWgBeta;
-  float *s_ex = wsc + kWgEx + wg * 128;     // [warp][32 heads]
-  float *s_exs = wsc + kWgExS + wg * 4;     // [warp]
+  float *s_beta = wsc + kWgBeta, *s_l = wsc + kWgL, *s_m = wsc + kWgM;
+  volatile uint32_t *resc_tag = reinterpret_cast<uint32_t *>(wsc + kWgTag);
   const float *scales = reinterpret_cast<const float *>(smem + sp.scales);
   uint8_t *pbase = smem + sp.p;
-  const uint32_t tq = tmem + ((uint32_t)(32 * gq) << 16);
-  const int t0 = 16 * gq + gid, t1 = t0 + 8;  // this thread's two tokens of the page
-  uint32_t g = 0;
+  const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+  // P^T (K-major, no swizzle): byte (head, token) at (head % 8) * 16 + (head / 8) * 512 +
+  // (token / 16) * 128 + token % 16; this thread writes 16-token chunks 2 half and 2 half + 1
+  const uint32_t p_off = (h & 7) * 16 + (h >> 3) * 512 + (2 * half) * 128;
+  uint32_t g = 0, n_resc = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
     bool fail = !mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag);
-    if (wg_bar_or(bar_id, fail)) break;
+    if (wg_bar_or(fail)) break;
     const ItemDesc d = items[slot];
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
-    if (wt < 32) {
-      s_cq[hb + wt] = __ldg(&a.qfac[(size_t)d.b * kTH + hb + wt]);
-      s_m[hb + wt] = kNegInf;
-    }
-    float s_ref = 0.f;
-    float lp[8];  // l of heads hb + 8k + 2 tig + e, index 2k + e
+    // this item's query rows into tensor memory, once the previous item's
+    // last QK^T is done with them
+    fail = !mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag);
+    if (!fail) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.qterms + (size_t)d.b * kLatentQTermBytes +
+                                                         (size_t)(32 * q + lane) * 512);
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        uint32_t r[32];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) lp[i] = 0.f;
-    named_bar_sync(bar_id, 128);
-    float cq[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 c2 = *reinterpret_cast<const float2 *>(&s_cq[hb + 8 * k + 2 * tig]);
-      cq[2 * k] = c2.x;
-      cq[2 * k + 1] = c2.y;
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = __ldg(src + 8 * k + i);
+          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+        }
+        tmem_st32(tq + kColQ + 32 * k, r);
+      }
+      tmem_wait_st();
     }
-    bool dead = false;
-    for (uint32_t j = 0; j < n; ++j) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(B.q_tfull);
+    const float cq = __ldg(&a.qfac[(size_t)d.b * kTH + h]);
+    float m = kNegInf, l = 0.f, s_ref = 0.f;
+    for (uint32_t j = 0; j < n && !fail; ++j) {
       const uint32_t gp = g + j, sb = gp & 1u, st = gp % kNst;
-      fail = fail || !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
+      fail = !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
              !mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
              !mbar_wait(&B.p_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag);
-      float y[16];  // [k][row][e] -> 4k + 2 row + e
+      if (fail) break;
+      float v[32];
       {
         tc_fence_after();
-        uint32_t r[16], r2[16];
-        tmem_ld16x256_x4(tq + kColS + 128 * sb + hb, r);        // K . T1
-        tmem_ld16x256_x4(tq + kColS + 128 * sb + 64 + hb, r2);  // K . T2
-#pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] = __uint_as_float(r[i]) + __uint_as_float(r2[i]);
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tq + kColS + 64 * sb, r0);       // tokens 0-31 of this lane's row
+        tmem_ld32(tq + kColS + 64 * sb + 32, r1);  // tokens 32-63
         tc_fence_before();
+        // T1 + T2: the partner lane (l ^ 16) holds the other term of the same head
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t give = half ? r0[i] : r1[i];
+          const uint32_t take = __shfl_xor_sync(0xffffffffu, give, 16);
+          v[i] = __uint_as_float(half ? r1[i] : r0[i]) + __uint_as_float(take);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.s_empty[sb]);
-      const int tok0 = (d.p0 + (int)j) * kTS;
-      const bool v0 = tok0 + t0 < d.L, v1 = tok0 + t1 < d.L;
-      const float s0 = v0 ? scales[st * kTS + t0] : 0.f, s1 = v1 ? scales[st * kTS + t1] : 0.f;
-      float mx[8];
+      const int tok0 = (d.p0 + (int)j) * kTS + 32 * half;
+      float sv[32];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+      for (int i = 0; i < 32; i += 4) {
+        const float4 s4 = *reinterpret_cast<const float4 *>(&scales[st * kTS + 32 * half + i]);
+        sv[i] = s4.x; sv[i + 1] = s4.y; sv[i + 2] = s4.z; sv[i + 3] = s4.w;
+      }
+      float mt = kNegInf, smx = 0.f;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float &ya = y[4 * k + e], &yb = y[4 * k + 2 + e];
-          ya = v0 ? ya * cq[2 * k + e] * s0 : kNegInf;
-          yb = v1 ? yb * cq[2 * k + e] * s1 : kNegInf;
-          float m = fmaxf(ya, yb);
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-          mx[2 * k + e] = m;
-        }
-      const float smx = warp_max_f32(fmaxf(s0, s1));
-      if (gid == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<float2 *>(&s_ex[wq * 32 + 8 * k + 2 * tig]) = make_float2(mx[2 * k], mx[2 * k + 1]);
+      for (int i = 0; i < 32; ++i) {
+        const bool valid = tok0 + i < d.L;
+        if (!valid) sv[i] = 0.f;
+        v[i] = valid ? v[i] * cq * sv[i] : kNegInf;  // z in log2 units
+        mt = fmaxf(mt, v[i]);
+        smx = fmaxf(smx, sv[i]);
       }
-      if (lane == 0) s_exs[wq] = smx;
-      if (wg_bar_or(bar_id, fail)) {
-        dead = true;
-        break;
-      }
-      const float sm = fmaxf(fmaxf(s_exs[0], s_exs[1]), fmaxf(s_exs[2], s_exs[3]));
-      const float s_old = s_ref;
-      const float s_new = sm > 2.f * s_old ? sm : s_old;
-      bool resc = s_new != s_old;
-      if (wt < 32) {
-        const int h = hb + wt;
-        const float tm = fmaxf(fmaxf(s_ex[wt], s_ex[32 + wt]), fmaxf(s_ex[64 + wt], s_ex[96 + wt]));
-        const float m_old = s_m[h];
-        const float m_new = tm > m_old + kTheta ? tm : m_old;
-        const float alpha = fast_exp2(m_old - m_new);
-        s_m[h] = m_new;
-        s_alpha[h] = alpha;
-        s_beta[h] = alpha * (s_old / s_new);
-        resc = resc || m_new != m_old;
-      }
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+      smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, 16));
+      const float s_new = smx > 2.f * s_ref ? smx : s_ref;
+      const float m_new = mt > m + kTheta ? mt : m;
+      const float alpha = fast_exp2(m - m_new);
+      const bool resc = j > 0 && (m_new != m || s_new != s_ref);
+      if (j > 0 && lane < 16) s_beta[sb * kTH + h] = alpha * (s_ref / s_new);
+      if (__any_sync(0xffffffffu, resc) && lane == 0) resc_tag[sb] = gp + 1u;
+      l *= alpha;
+      m = m_new;
       s_ref = s_new;
-      resc = wg_bar_or(bar_id, resc) && j > 0;
-      if (resc) {
-        // this group's columns of O^T hold the earlier pages: scale head h by
-        // beta_h once the previous page's PV has landed; l by alpha_h
-        fail = fail || !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag);
-        if (!fail) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            const uint32_t ta = tq + kColO + 64 * c + hb;
-            tmem_ld32(ta, r);
+      // P'' = 2^(z - m) (s_t / s_ref) 2^kPExp as three e4m3 terms; l sums 2^(z - m)
+      const float w = exp2f(kPExp) / s_ref;
+      uint32_t t1[16], t2[16], t3[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * s_beta[hb + i]);
-            tmem_st32(ta, r);
-          }
-          tmem_wait_st();
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) lp[2 * k + e] *= s_alpha[hb + 8 * k + 2 * tig + e];
+      for (int i = 0; i < 32; i += 2) {
+        const float e0 = fast_exp2(v[i] - m), e1 = fast_exp2(v[i + 1] - m);
+        l += e0 + e1;
+        three_terms2(e0 * sv[i] * w, e1 * sv[i + 1] * w, t1[i / 2], t2[i / 2], t3[i / 2]);
       }
-      // P'' = p (s_t / s_ref) 2^kPExp as three e4m3 terms; p = 2^(z - m) summed into l
-      const float kt0 = v0 ? fast_log2(s0 / s_ref) + kPExp : 0.f;
-      const float kt1 = v1 ? fast_log2(s1 / s_ref) + kPExp : 0.f;
-      const float rt0 = fast_exp2(-kt0), rt1 = fast_exp2(-kt1);
-      // P^T, MN-major without swizzle: byte (head h, token t) at
-      // (h % 16) + (h / 16) * 1024 + (t % 8) * 16 + (t / 8) * 128
-      uint8_t *pt = pbase + sb * kPBuf;
+      uint8_t *pt = pbase + sb * kPBuf + p_off;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int h = hb + 8 * k + 2 * tig;
-        const float2 m2 = *reinterpret_cast<const float2 *>(&s_m[h]);
-        const float pa0 = fast_exp2(y[4 * k] - m2.x + kt0), pa1 = fast_exp2(y[4 * k + 1] - m2.y + kt0);
-        const float pb0 = fast_exp2(y[4 * k + 2] - m2.x + kt1), pb1 = fast_exp2(y[4 * k + 3] - m2.y + kt1);
-        lp[2 * k] += pa0 * rt0 + pb0 * rt1;
-        lp[2 * k + 1] += pa1 * rt0 + pb1 * rt1;
-        uint32_t a1, a2, a3, b1, b2, b3;
-        three_terms2(pa0, pa1, a1, a2, a3);
-        three_terms2(pb0, pb1, b1, b2, b3);
-        if (!fail) {
-          const int hoff = (h & 15) + (h >> 4) * 1024;
-          uint8_t *q0 = pt + hoff + (t0 & 7) * 16 + (t0 >> 3) * 128;
-          uint8_t *q1 = pt + hoff + (t1 & 7) * 16 + (t1 >> 3) * 128;
-          *reinterpret_cast<uint16_t *>(q0) = (uint16_t)a1;
-          *reinterpret_cast<uint16_t *>(q0 + kPTerm) = (uint16_t)a2;
-          *reinterpret_cast<uint16_t *>(q0 + 2 * kPTerm) = (uint16_t)a3;
-          *reinterpret_cast<uint16_t *>(q1) = (uint16_t)b1;
-          *reinterpret_cast<uint16_t *>(q1 + kPTerm) = (uint16_t)b2;
-          *reinterpret_cast<uint16_t *>(q1 + 2 * kPTerm) = (uint16_t)b3;
-        }
+      for (int c = 0; c < 2; ++c) {
+        const int o = 8 * c;  // 16-bit words of this 16-token chunk
+        *reinterpret_cast<uint4 *>(pt + c * 128) = make_uint4(t1[o] | (t1[o + 1] << 16), t1[o + 2] | (t1[o + 3] << 16),
+                                                              t1[o + 4] | (t1[o + 5] << 16), t1[o + 6] | (t1[o + 7] << 16));
+        *reinterpret_cast<uint4 *>(pt + kPTerm + c * 128) =
+            make_uint4(t2[o] | (t2[o + 1] << 16), t2[o + 2] | (t2[o + 3] << 16), t2[o + 4] | (t2[o + 5] << 16),
+                       t2[o + 6] | (t2[o + 7] << 16));
+        *reinterpret_cast<uint4 *>(pt + 2 * kPTerm + c * 128) =
+            make_uint4(t3[o] | (t3[o + 1] << 16), t3[o + 2] | (t3[o + 3] << 16), t3[o + 4] | (t3[o + 5] << 16),
+                       t3[o + 6] | (t3[o + 7] << 16));
       }
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.p_full[sb]);
+      if (j > 0) {
+        // Rescale hand-off: once every warp's P^T and scale factors for this
+        // page are in, if any head asked for it, scale this warp's lanes of
+        // O^T (values 32 q .. 32 q + 31 of each chunk) by beta_h per head
+        // column, after the previous page's PV and before this page's.
+        fail = !mbar_wait(&B.p_full[sb], (gp >> 1) & 1u, abort_flag);
+        if (!fail && resc_tag[sb] == gp + 1u) {
+          fail = !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag);
+          if (!fail) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t r[32];
+              const uint32_t ta = tq + kColO + 32 * c;
+              tmem_ld32(ta, r);
+              const float *bt = s_beta + sb * kTH + 32 * (c & 1);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bt[i]);
+              tmem_st32(ta, r);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(B.r_done);
+          ++n_resc;
+        }
+      }
     }
-    if (dead) break;
+    if (wg_bar_or(fail)) break;
     // ---- the item's result: wait for its last PV and its status
     const uint32_t gl = g + n - 1;
-    fail = fail || !mbar_wait(&B.p_empty[gl & 1u], (gl >> 1) & 1u, abort_flag) ||
+    fail = !mbar_wait(&B.p_empty[gl & 1u], (gl >> 1) & 1u, abort_flag) ||
            !mbar_wait(&B.item_done[slot], (it / kNIQ) & 1u, abort_flag);
-    // l per head: over the eight threads that share a head, then the four warps
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float v = lp[i];
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      lp[i] = v;
+    const float l_tot = l + __shfl_xor_sync(0xffffffffu, l, 16);
+    if (lane < 16) {
+      s_l[h] = l_tot;
+      s_m[h] = m;
     }
-    if (gid == 0) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        *reinterpret_cast<float2 *>(&s_ex[wq * 32 + 8 * k + 2 * tig]) = make_float2(lp[2 * k], lp[2 * k + 1]);
-    }
-    if (wg_bar_or(bar_id, fail)) break;
-    if (wt < 32) s_alpha[hb + wt] = s_ex[wt] + s_ex[32 + wt] + s_ex[64 + wt] + s_ex[96 + wt];
-    named_bar_sync(bar_id, 128);
+    if (wg_bar_or(fail)) break;
     tc_fence_after();
     const uint32_t stv = item_status[slot];
-    const float oscale = s_ref * exp2f(-kPExp);  // O^T accumulates p (s_t / s_ref) 2^kPExp * code
+    const float oscale = s_ref * exp2f(-kPExp);  // O^T accumulates 2^(z - m) (s_t / s_ref) 2^kPExp * code
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
       uint32_t r[32];
-      tmem_ld32(tq + kColO + 64 * c + hb, r);
-      const int dd = 128 * c + 32 * gq + lane;  // value index of this thread's row
+      tmem_ld32(tq + kColO + 32 * c, r);
+      const int dd = 128 * (c >> 1) + 32 * q + lane;  // value index of this thread's row
+      const int h0 = 32 * (c & 1);
       if (d.nb == 1) {
-        float *o = a.out + ((size_t)d.b * kTH + hb) * kTDv + dd;
+        float *o = a.out + ((size_t)d.b * kTH + h0) * kTDv + dd;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          o[(size_t)i * kTDv] = stv ? 0.f : __uint_as_float(r[i]) * oscale / s_alpha[hb + i];
+          o[(size_t)i * kTDv] = stv ? 0.f : __uint_as_float(r[i]) * oscale / s_l[h0 + i];
       } else {
-        float *o = a.part_o + ((size_t)d.cg * kTH + hb) * kTDv + dd;
+        float *o = a.part_o + ((size_t)d.cg * kTH + h0) * kTDv + dd;
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[(size_t)i * kTDv] = __uint_as_float(r[i]) * oscale;
       }
     }
-    if (d.nb != 1 && wt < 32)
-      a.part_ml[(size_t)d.cg * kTH + hb + wt] = make_float2(s_m[hb + wt], s_alpha[hb + wt]);
+    if (d.nb != 1 && wt < kTH) a.part_ml[(size_t)d.cg * kTH + wt] = make_float2(s_m[wt], s_l[wt]);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(B.o_empty);
-    named_bar_sync(bar_id, 128);  // the scratch is reused by the next item
+    named_bar_sync(1, 128);  // the scratch is reused by the next item
     if (wt == 0) mbar_arrive(&B.item_empty[slot]);
     g += n;
   }
@@ -629,19 +613,23 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.s_empty[i], 8);
-      mbar_init(&B.p_full[i], 8);
+      mbar_init(&B.s_empty[i], 4);
+      mbar_init(&B.p_full[i], 4);
       mbar_init(&B.p_empty[i], 1);
     }
     mbar_init(B.q_full, 1);
     mbar_init(B.q_empty, 1);
-    mbar_init(B.o_empty, 8);
+    mbar_init(B.q_tfull, 4);
+    mbar_init(B.o_empty, 4);
+    mbar_init(B.r_done, 4);
     mbar_init(B.drain, 1);
     for (int i = 0; i < kNIQ; ++i) {
       mbar_init(&B.item_full[i], 1);
-      mbar_init(&B.item_empty[i], 3);  // the MMA thread and the two softmax groups
+      mbar_init(&B.item_empty[i], 2);  // the MMA thread and the softmax warps
       mbar_init(&B.item_done[i], 1);
     }
+    uint32_t *tag = reinterpret_cast<uint32_t *>(smem + sp.wg) + kWgTag;
+    tag[0] = tag[1] = 0u;
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -659,7 +647,7 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
     }
     tc_producer(a, map, map_tail, smem, B, items, item_status, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) tc_mma(a, smem, B, items, tmem, abort_flag);
+    if (lane == 0) tc_mma(smem, B, items, tmem, abort_flag);
     __syncwarp();
   } else {
     tc_softmax(a, smem, B, items, item_status, tmem, abort_flag);

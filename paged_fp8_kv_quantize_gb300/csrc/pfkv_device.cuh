@@ -298,6 +298,17 @@ __device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t 
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T (A rows in tensor-memory lanes, four e4m3
+// codes per 32-bit column, 8 columns per K step of 32); one thread issues.
+__device__ __forceinline__ void umma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // Arrive once on bar when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))

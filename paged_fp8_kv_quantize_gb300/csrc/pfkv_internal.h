@@ -26,10 +26,10 @@ struct WsLayout {
 };
 constexpr int kMaxRanges = 1024;  // balanced plan: at most this many page ranges (one per CTA)
 // latent: the latent-stream path also keeps each request's query as two e4m3
-// terms in the shared-memory image its kernel copies (qterms, 72 KB per
-// request) and one factor per head (qfac).
+// terms in the operand image its kernel loads (qterms, 72 KB per request)
+// and one factor per head (qfac).
 WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool latent);
-constexpr size_t kLatentQTermBytes = 9 * 64 * 128;  // nine 128-byte column blocks x 64 heads
+constexpr size_t kLatentQTermBytes = 128 * 576;  // 128 operand rows (two terms x 64 heads) x 576 codes
 
 struct DecodeArgs {
   // cache
