@@ -274,6 +274,74 @@ def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
 
 
 
+def bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls, dtype, num_pages=None):
+    """Decode-only timing of one workload (all rows appended first)."""
+    import torch
+
+    fp8 = dtype == abi.DTYPE_FP8_E4M3
+    P = w.num_pages if num_pages is None else num_pages
+    cache = abi.PagedCache(P, w.page_size, w.kv_heads, w.head_dim, dtype=dtype, device=dev, fill=0)
+    cache.page_tags.copy_(i32(w.page_tags))
+    table, tags, lens = i32(w.block_table), i32(w.block_tags), i32(w.seq_lens)
+    k, v = bf16(w.k_rows), bf16(w.v_rows)
+    if fp8:
+        abi.calibrate_scales(k, cache.k_scale)
+        abi.calibrate_scales(v, cache.v_scale)
+    abi.kv_append_quantize(cache, k, v, i32(w.row_pos), table, tags, row_req=i32(w.row_req), batch=w.batch)
+    del k, v
+    q = bf16(w.q)
+    ws = torch.empty(abi.decode_workspace_bytes(cache, w.batch, w.q_heads, w.max_splits), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty(w.batch, w.q_heads, w.head_dim, dtype=torch.float32, device=dev)
+    st = torch.empty(w.batch, dtype=torch.int32, device=dev)
+
+    def call(_):
+        abi.paged_decode_attention(cache, q, lens, table, tags, w.softmax_scale, flags=abi.FLAG_TAG_CHECK,
+                                   max_splits=w.max_splits, workspace=ws, out=out, status=st)
+
+    for _ in range(3):
+        call(0)
+    g = capture(call, n_calls)
+    g.replay()
+    ms = time_graph(g) / n_calls
+    nbytes = decode_alg_bytes(w.seq_lens, w.kv_heads, w.head_dim, w.page_size, w.q_heads, w.head_dim, fp8=fp8)
+    res = {"us_per_call": ms * 1e3, "kv_gbs": nbytes / (ms * 1e-3) / 1e9,
+           "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak, "alg_bytes_per_call": nbytes,
+           "aborted_requests": int((st.cpu().numpy() != 0).sum()), "pool_pages": P}
+    del cache, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_configs(abi, dev, i32, bf16, capture, time_graph, peak, n_calls):
+    """The other shapes of the benchmark table: the grouped-query batch and the long-context batch."""
+    import torch
+
+    res = {}
+    w = synth.gqa()
+    res["gqa"] = {"workload": "batch 32, lengths U[1024, 8192], 32 q / 8 KV heads, head_dim 128, page 16, "
+                              "1% outliers x20, tag check on",
+                  "fp8": bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
+                                             abi.DTYPE_FP8_E4M3),
+                  "bf16": bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
+                                              abi.DTYPE_BF16)}
+    del w
+    # long contexts, pages scattered over a pool of half the free device memory (FP8 K + V)
+    free, _ = torch.cuda.mem_get_info(dev)
+    big = int(0.5 * free) // (2 * 64 * 128)
+    w = synth.long_ctx(num_pages=big)
+    res["long"] = {"workload": f"batch 8 x 131072 tokens, 8 q / 1 KV head, head_dim 128, page 64, pages scattered "
+                               f"over a pool of {big} pages (half the free device memory), tag check on",
+                   "fp8": bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
+                                              abi.DTYPE_FP8_E4M3, num_pages=big)}
+    del w
+    w = synth.long_ctx()
+    res["long"]["bf16"] = bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
+                                              abi.DTYPE_BF16)
+    res["long"]["bf16"]["pool"] = "1.25x the pages needed"
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,6 +517,10 @@ def main():
         extra["bf16_cache"] = {"us_per_decode": ms_bf * 1e3, "kv_gbs": bf_bytes / (ms_bf * 1e-3) / 1e9,
                                "hbm_frac": bf_bytes / (ms_bf * 1e-3) / 1e9 / peak,
                                "fp8_speedup_per_call": ms_bf / ms_dec}
+
+    # ---- the other benchmark shapes (grouped-query batch, long contexts)
+    if not args.no_variants:
+        extra["configs"] = bench_configs(abi, dev, i32, bf16, capture, time_graph, peak, max(3, K // 5))
 
     # ---- latent-shared stream (64 heads over one 576-wide FP8 stream, batch 64)
     if not args.no_latent:

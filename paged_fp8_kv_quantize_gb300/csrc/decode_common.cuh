@@ -362,6 +362,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
 
 // ---------------------------------------------------------------- merge
 
+// Blocks needed along y to cover a group's kG * kD / 4 float4 columns.
+template <int kD, int kG>
+constexpr int merge_col_blocks() { return (kG * kD / 4 + 255) / 256; }
+
 template <int kD, int kG>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   __shared__ float s_w[256 * kG];  // per (split, head): m, then the split's weight (splits <= 256)
@@ -374,8 +378,12 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   if (nb <= 1) return;  // finished by the split kernel (or zeroed by the plan kernel)
   const int t = threadIdx.x, c0 = a.split_first[b];
   float *out_bg = a.out + ((size_t)b * a.Hq + g * kG) * kD;
+  constexpr int kCols = kG * kD / 4;  // float4 columns of the group's rows
+  // columns of this block: 256 float4 columns per blockIdx.y (all of them
+  // when the group's rows are narrower)
+  const int col_lo = (int)blockIdx.y * 256, col_hi = kCols < 256 ? kCols : min(kCols, col_lo + 256);
   if (__ldcg(&a.status[b]) != 0u) {
-    for (int i = t; i < kG * kD; i += 256) out_bg[i] = 0.f;
+    for (int i = 4 * col_lo + t; i < 4 * col_hi; i += 256) out_bg[i] = 0.f;
     return;
   }
   for (int i = t; i < nb * kG; i += 256) {
@@ -401,11 +409,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   for (int i = t; i < nb * kG; i += 256) s_w[i] = fast_exp2(s_w[i] - s_M[i % kG]);
   __syncthreads();
   // thread = (float4 column, group of splits); wide rows loop over columns
-  constexpr int kCols = kG * kD / 4;
   constexpr int kGroups = kCols >= 256 ? 1 : 256 / kCols;
   const size_t cstride = (size_t)a.Hq * kD / 4;
   const float4 *pbase = reinterpret_cast<const float4 *>(a.part_o + ((size_t)c0 * a.Hq + g * kG) * kD);
-  for (int col0 = 0; col0 < kCols; col0 += 256) {
+  for (int col0 = col_lo; col0 < col_hi; col0 += 256) {
     const int col = col0 + t % (kCols < 256 ? kCols : 256), grp = kCols < 256 ? t / kCols : 0;
     const int jh = (col * 4) / kD;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);

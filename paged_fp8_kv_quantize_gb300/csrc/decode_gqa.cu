@@ -719,7 +719,7 @@ int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const 
   rc = cuda_ok(cudaLaunchKernelEx(&cfg, kern, mk, mv, a, sh.nst), "split kernel launch");
   if (rc) return rc;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(a.B * a.Hkv);
+  mcfg.gridDim = dim3(a.B * a.Hkv, merge_col_blocks<kD, kG>());
   mcfg.blockDim = dim3(256);
   mcfg.stream = s;
   mcfg.attrs = attr;

@@ -732,7 +732,7 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   m.Hkv = kTH / 16;
   m.G = 16;
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(a.B * m.Hkv);
+  mcfg.gridDim = dim3(a.B * m.Hkv, merge_col_blocks<kTDv, 16>());
   mcfg.blockDim = dim3(256);
   mcfg.stream = s;
   mcfg.attrs = attr;
