@@ -22,6 +22,11 @@ __global__ void __launch_bounds__(128) append_kernel(pfkv_cache c, const uint16_
   const int unit = blockIdx.y * 4 + (threadIdx.x >> 5);  // (part, head)
   const int parts = c.kv_shared ? 1 : 2;
   if (row >= n_rows) return;
+  const bool mine = unit < parts * c.num_kv_heads;  // this warp writes a (part, head) of the row
+  const int part = unit / c.num_kv_heads, h = unit - part * c.num_kv_heads;
+  const bool regs = append_row_fits(c);
+  AppendRow r;
+  if (mine && regs) r = append_row_load<kFp8>(c, k_new, v_new, row, part, h, lane);  // overlaps the lookups
   const int b = row_req ? row_req[row] : row;
   if (b < 0 || b >= batch) return;
   const int pos = positions[row];
@@ -31,9 +36,11 @@ __global__ void __launch_bounds__(128) append_kernel(pfkv_cache c, const uint16_
     if (unit == 0 && lane == 0) atomicOr(&status[b], bad);
     return;
   }
-  if (unit >= parts * c.num_kv_heads) return;
-  const int part = unit / c.num_kv_heads, h = unit - part * c.num_kv_heads;
-  append_row_warp<kFp8>(c, k_new, v_new, row, part, h, page, pos, lane);
+  if (!mine) return;
+  if (regs)
+    append_row_store<kFp8>(c, r, part, h, page, pos, lane);
+  else
+    append_row_wide<kFp8>(c, k_new, v_new, row, part, h, page, pos, lane);
 }
 
 // amax per head into scale[] (as fp32 bits, non-negative floats order like uints)

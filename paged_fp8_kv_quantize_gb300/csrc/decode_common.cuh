@@ -41,14 +41,23 @@ __device__ __forceinline__ void plan_append(const DecodeArgs &a) {
   const int gw = (int)(blockIdx.x - 1) * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5);
   const int b = gw / units, unit = gw - b * units;
   if (b >= a.B) return;
+  const int part = unit / H, h = unit - part * H, lane = threadIdx.x & 31;
+  const bool fp8 = a.cache.dtype == PFKV_DTYPE_FP8_E4M3;
+  const bool regs = append_row_fits(a.cache);
+  AppendRow r;
+  if (regs)  // the row and its scale load while the destination is looked up
+    r = fp8 ? append_row_load<true>(a.cache, a.k_new, a.v_new, b, part, h, lane)
+            : append_row_load<false>(a.cache, a.k_new, a.v_new, b, part, h, lane);
   const int pos = a.seq_lens[b] - 1;
   int page = -1;
   if (append_target(a.cache, b, pos, a.block_table, a.block_tags, a.MP, a.flags, &page)) return;
-  const int part = unit / H, h = unit - part * H;
-  if (a.cache.dtype == PFKV_DTYPE_FP8_E4M3)
-    append_row_warp<true>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, threadIdx.x & 31);
-  else
-    append_row_warp<false>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, threadIdx.x & 31);
+  if (regs) {
+    if (fp8) append_row_store<true>(a.cache, r, part, h, page, pos, lane);
+    else append_row_store<false>(a.cache, r, part, h, page, pos, lane);
+  } else {
+    if (fp8) append_row_wide<true>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, lane);
+    else append_row_wide<false>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, lane);
+  }
 }
 
 // Append blocks of the plan grid (decode step only).
@@ -158,11 +167,16 @@ __device__ __forceinline__ long long block_excl_scan(long long v, long long *s_w
 // same number of pages to within one, and at most R + B - 1 partial results
 // are written.  R <= ranges, R <= T, and R is small enough that no request
 // is cut into more than max_splits pieces (a request of p pages meets at
-// most ceil(p R / T) + 1 ranges).
-__device__ void plan_balanced(const DecodeArgs &a, int ranges) {
+// most ceil(p R / T) + 1 ranges).  Returns false, having written nothing
+// but status, when those caps leave fewer than 3/4 of `ranges`.
+__device__ bool plan_balanced(const DecodeArgs &a, int ranges) {
   __shared__ long long s_w[33];
   __shared__ long long s_tot, s_max, s_pcarry, s_icarry;
-  const int tid = threadIdx.x;
+  // one pass of up to 1024 requests, handed from the thread that sized a
+  // request to the warp that writes its chunks (one chunk per lane)
+  __shared__ long long s_off[1024];
+  __shared__ int s_np[1024], s_kf[1024], s_n[1024], s_first[1024];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int S = a.S;
   const long long max_len = (long long)a.MP * S;
   long long tot = 0, mx = 0;
@@ -195,6 +209,7 @@ __device__ void plan_balanced(const DecodeArgs &a, int ranges) {
   }
   if (R > kMaxRanges) R = kMaxRanges;
   if (R < 1) R = 1;
+  if (T > 0 && 4 * R < 3 * (long long)ranges) return false;
   if (tid == 0 && T == 0) a.cta_first[0] = 0;
   for (int base = 0; base < a.B; base += blockDim.x) {
     const int b = base + tid;
@@ -217,16 +232,31 @@ __device__ void plan_balanced(const DecodeArgs &a, int ranges) {
     if (b < a.B) {
       a.split_first[b] = (int)first;
       a.split_count[b] = (int)n;
-      for (long long j = 0; j < n; ++j) {
-        const long long k = kf + j;
-        const long long r0 = k * T / R, r1 = (k + 1) * T / R;
-        const long long p0 = (r0 > off ? r0 : off) - off, p1 = (r1 < off + pages ? r1 : off + pages) - off;
-        a.chunk_info[2 * (first + j)] = make_int4(b, (int)p0, (int)p1, L);
-        a.chunk_info[2 * (first + j) + 1] = make_int4((int)n, (int)j, (int)k, 0);
-        if (j > 0 || off == r0) a.cta_first[k] = (int)(first + j);  // first item of range k
+    }
+    s_off[tid] = off;
+    s_np[tid] = (int)pages;
+    s_kf[tid] = (int)kf;
+    s_n[tid] = b < a.B ? (int)n : 0;
+    s_first[tid] = (int)first;
+    __syncthreads();
+    // chunk descriptors: warp per request, lane per chunk
+    const int in_pass = min((int)blockDim.x, a.B - base);
+    for (int i = wid; i < in_pass; i += (int)(blockDim.x >> 5)) {
+      const int bi = base + i, ni = s_n[i], fi = s_first[i];
+      const long long oi = s_off[i], pi = s_np[i];
+      if (ni == 0) {  // bad length: no item writes this request's rows
+        for (size_t k = lane; k < (size_t)a.Hq * a.Dv; k += 32) a.out[(size_t)bi * a.Hq * a.Dv + k] = 0.f;
+        continue;
       }
-      if (n == 0)  // bad length: no item writes this request's rows
-        for (size_t k = 0; k < (size_t)a.Hq * a.Dv; ++k) a.out[(size_t)b * a.Hq * a.Dv + k] = 0.f;
+      const int Li = a.seq_lens[bi];
+      for (int j = lane; j < ni; j += 32) {
+        const long long k = s_kf[i] + j;
+        const long long r0 = k * T / R, r1 = (k + 1) * T / R;
+        const long long p0 = (r0 > oi ? r0 : oi) - oi, p1 = (r1 < oi + pi ? r1 : oi + pi) - oi;
+        a.chunk_info[2 * (fi + j)] = make_int4(bi, (int)p0, (int)p1, Li);
+        a.chunk_info[2 * (fi + j) + 1] = make_int4(ni, j, (int)k, 0);
+        if (j > 0 || oi == r0) a.cta_first[k] = fi + j;  // first item of range k
+      }
     }
     __syncthreads();
     if (tid == 0) {
@@ -238,11 +268,13 @@ __device__ void plan_balanced(const DecodeArgs &a, int ranges) {
   if (tid == 0) {
     a.cta_first[R] = (int)s_icarry;
     a.hdr->n_chunks = (int)s_icarry;
-    a.hdr->n_items = (int)s_icarry;
+    a.hdr->n_items = (int)s_icarry * a.Hkv;
     a.hdr->work = 0u;
     a.hdr->err = 0u;
-    a.hdr->chunk_pages = (int)R;  // number of ranges
+    a.hdr->chunk_pages = (int)R;
+    a.hdr->n_ranges = (int)R;
   }
+  return true;
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
@@ -253,10 +285,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
     else plan_qprep(a, (int)blockIdx.x - 1 - nab);
     return;
   }
-  if (a.balanced > 0) {
-    plan_balanced(a, a.balanced);
-    return;
-  }
+  if (a.balanced > 0 && plan_balanced(a, a.balanced)) return;
   __shared__ long long s_red[32];
   __shared__ int s_scan[32];
   __shared__ int s_carry;
@@ -357,20 +386,37 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
     a.hdr->work = 0u;
     a.hdr->err = 0u;
     a.hdr->chunk_pages = (int)cp;
+    a.hdr->n_ranges = 0;
   }
 }
 
 // ---------------------------------------------------------------- merge
 
-// Blocks needed along y to cover a group's kG * kD / 4 float4 columns.
+// Merge launch shape: a block takes kW float4 columns of one (request, KV
+// head)'s group rows (kG heads x kD values) and spreads the splits over
+// 256 / kW thread groups; gridDim.y = kBlocks.
 template <int kD, int kG>
-constexpr int merge_col_blocks() { return (kG * kD / 4 + 255) / 256; }
+struct MergeShape {
+  static constexpr int kCols = kG * kD / 4;               // float4 columns of the group
+  // float4 columns per block: 64, so that the splits of a column spread
+  // over 4 thread groups; very wide groups (the latent stream's 16 x 512)
+  // take 256 per block, which keeps the block count down
+  static constexpr int kW = kCols < 64 ? kCols : (kCols >= 1024 ? 256 : 64);
+  static constexpr int kGroups = 256 / kW;                // split groups per column
+  static constexpr int kBlocks = kCols / kW;
+  static constexpr int kNH = kW * 4 / kD > 0 ? kW * 4 / kD : 1;  // heads a block touches
+  static_assert(kCols % kW == 0 && 256 % kW == 0, "merge columns");
+};
+
+template <int kD, int kG>
+constexpr int merge_col_blocks() { return MergeShape<kD, kG>::kBlocks; }
 
 template <int kD, int kG>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
-  __shared__ float s_w[256 * kG];  // per (split, head): m, then the split's weight (splits <= 256)
-  __shared__ float s_l[256 * kG];
-  __shared__ float s_M[kG], s_W[kG];
+  using M = MergeShape<kD, kG>;
+  __shared__ float s_w[256 * M::kNH];  // per (split, head of this block): m, then the split's weight (splits <= 256)
+  __shared__ float s_l[256 * M::kNH];
+  __shared__ float s_M[M::kNH], s_W[M::kNH];
   __shared__ float4 s_acc[256];
   pdl_wait();  // partials and status of the split kernel are visible from here on
   const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
@@ -378,65 +424,56 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   if (nb <= 1) return;  // finished by the split kernel (or zeroed by the plan kernel)
   const int t = threadIdx.x, c0 = a.split_first[b];
   float *out_bg = a.out + ((size_t)b * a.Hq + g * kG) * kD;
-  constexpr int kCols = kG * kD / 4;  // float4 columns of the group's rows
-  // columns of this block: 256 float4 columns per blockIdx.y (all of them
-  // when the group's rows are narrower)
-  const int col_lo = (int)blockIdx.y * 256, col_hi = kCols < 256 ? kCols : min(kCols, col_lo + 256);
+  const int col_lo = (int)blockIdx.y * M::kW;
   if (__ldcg(&a.status[b]) != 0u) {
-    for (int i = 4 * col_lo + t; i < 4 * col_hi; i += 256) out_bg[i] = 0.f;
+    for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
     return;
   }
-  for (int i = t; i < nb * kG; i += 256) {
-    const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / kG) * a.Hq + g * kG + i % kG]);
+  const int h_lo = col_lo * 4 / kD;  // first head of this block's columns
+  for (int i = t; i < nb * M::kNH; i += 256) {
+    const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / M::kNH) * a.Hq + g * kG + h_lo + i % M::kNH]);
     s_w[i] = ml.x;
     s_l[i] = ml.y;
   }
   __syncthreads();
   const int warp = t >> 5, lane = t & 31;
-  for (int hh = warp; hh < kG; hh += 8) {  // 8 warps cover the group's heads
-    float M = -INFINITY;
-    for (int c = lane; c < nb; c += 32) M = fmaxf(M, s_w[c * kG + hh]);
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (warp < M::kNH) {
+    const int hh = warp;
+    float Mx = -INFINITY;
+    for (int c = lane; c < nb; c += 32) Mx = fmaxf(Mx, s_w[c * M::kNH + hh]);
+    for (int o = 16; o; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
     float W = 0.f;
-    for (int c = lane; c < nb; c += 32) W += s_l[c * kG + hh] * fast_exp2(s_w[c * kG + hh] - M);
+    for (int c = lane; c < nb; c += 32) W += s_l[c * M::kNH + hh] * fast_exp2(s_w[c * M::kNH + hh] - Mx);
     for (int o = 16; o; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
     if (lane == 0) {
-      s_M[hh] = M;
+      s_M[hh] = Mx;
       s_W[hh] = W;
     }
   }
   __syncthreads();
-  for (int i = t; i < nb * kG; i += 256) s_w[i] = fast_exp2(s_w[i] - s_M[i % kG]);
+  for (int i = t; i < nb * M::kNH; i += 256) s_w[i] = fast_exp2(s_w[i] - s_M[i % M::kNH]);
   __syncthreads();
-  // thread = (float4 column, group of splits); wide rows loop over columns
-  constexpr int kGroups = kCols >= 256 ? 1 : 256 / kCols;
+  // thread = (float4 column, group of splits)
   const size_t cstride = (size_t)a.Hq * kD / 4;
-  const float4 *pbase = reinterpret_cast<const float4 *>(a.part_o + ((size_t)c0 * a.Hq + g * kG) * kD);
-  for (int col0 = col_lo; col0 < col_hi; col0 += 256) {
-    const int col = col0 + t % (kCols < 256 ? kCols : 256), grp = kCols < 256 ? t / kCols : 0;
-    const int jh = (col * 4) / kD;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (grp < kGroups && col < kCols) {
-      const float4 *po = pbase + col;
-#pragma unroll 8
-      for (int c = grp; c < nb; c += kGroups) {
-        const float w = s_w[c * kG + jh];
-        const float4 v = __ldcg(po + (size_t)c * cstride);
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-      }
+  const int col = col_lo + t % M::kW, grp = t / M::kW;
+  const int jh = col * 4 / kD - h_lo;
+  const float4 *po = reinterpret_cast<const float4 *>(a.part_o + ((size_t)c0 * a.Hq + g * kG) * kD) + col;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int c = grp; c < nb; c += M::kGroups) {
+    const float w = s_w[c * M::kNH + jh];
+    const float4 v = __ldcg(po + (size_t)c * cstride);
+    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  }
+  s_acc[t] = acc;
+  __syncthreads();
+  if (t < M::kW) {
+    for (int k = 1; k < M::kGroups; ++k) {
+      const float4 v = s_acc[t + k * M::kW];
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    if (kGroups > 1) {
-      s_acc[t] = acc;
-      __syncthreads();
-    }
-    if (t < (kCols < 256 ? kCols : 256) && col < kCols) {
-      for (int k = 1; k < kGroups; ++k) {
-        const float4 v = s_acc[t + k * kCols];
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      const float inv = 1.f / s_W[jh];
-      reinterpret_cast<float4 *>(out_bg)[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
+    const float inv = 1.f / s_W[jh];
+    reinterpret_cast<float4 *>(out_bg)[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
 }
 

@@ -12,8 +12,10 @@
 //                request into page-aligned chunks (flash-decoding) and
 //                writes the chunk prefix into the workspace.
 //   2. split  -- persistent CTAs, one producer warp + NCW consumer warps.
-//                The producer takes work items (request, chunk, KV head)
-//                from a device counter, walks the chunk's page-table
+//                The producer takes work items (request, chunk, KV head):
+//                under the balanced plan the chunks of one equal page
+//                range for one KV head, otherwise from a device counter
+//                (longest request first).  It walks the chunk's page-table
 //                entries 32 at a time, bounds-checks every page id before
 //                any fetch, compares tags off the critical path (the tag
 //                load is issued next to the page copy; a mismatch only sets
@@ -25,13 +27,13 @@
 //                An item that covers a whole request writes its output
 //                directly; otherwise it leaves an unnormalised partial
 //                (m, l, O).
-//   3. merge  -- one CTA per (request, KV head) with more than one split:
-//                log-sum-exp merge of the partials, split weights staged in
-//                shared memory and splits spread over thread groups.
+//   3. merge  -- one CTA per (request, KV head, block of 64 float4
+//                columns) with more than one split: log-sum-exp merge of
+//                the partials, split weights staged in shared memory and
+//                splits spread over thread groups.
 //   A request with any status bit gets zero output.  The split and merge
 //   kernels are programmatic dependents of the kernel before them, so their
-//   launch and prologue overlap it.  Splits are ordered longest request
-//   first, which balances the dynamic schedule.
+//   launch and prologue overlap it.
 #include <math.h>
 
 #include <mutex>
@@ -151,8 +153,23 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     uint32_t ring = 0;
     // Work items are claimed one ahead: the id and the split descriptor of
     // the next item are in flight while the current item's pages go out.
+    // Balanced plan: CTA r * Hkv + h walks range r's chunks for KV head h;
+    // otherwise items come from the shared counter.  Lane 0 claims.
+    const int n_ranges = a.hdr->n_ranges;
+    int run_next = n_items, run_end = n_items;
+    if (n_ranges > 0 && (int)blockIdx.x < n_ranges * a.Hkv) {
+      const int r = (int)blockIdx.x / a.Hkv, h = (int)blockIdx.x - r * a.Hkv;
+      run_next = a.cta_first[r] * a.Hkv + h;
+      run_end = a.cta_first[r + 1] * a.Hkv;
+    }
+    auto claim = [&]() -> int {
+      if (n_ranges == 0) return (int)atomicAdd(&a.hdr->work, 1u);
+      const int v = run_next < run_end ? run_next : n_items;
+      run_next += a.Hkv;
+      return v;
+    };
     int item = 0, item_next = 0;
-    if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
+    if (lane == 0) item = claim();
     item = __shfl_sync(0xffffffffu, item, 0);
     int4 info = make_int4(0, 0, 0, 0), info2 = make_int4(0, 0, 0, 0);
     if (item < n_items) {
@@ -160,7 +177,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       info2 = a.chunk_info[2 * (item / a.Hkv) + 1];
     }
     for (uint32_t iq = 0;; ++iq) {
-      if (lane == 0) item_next = (int)atomicAdd(&a.hdr->work, 1u);
+      if (lane == 0) item_next = claim();
       const uint32_t slot = iq % kNIQ;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&item_empty[slot], ((iq / kNIQ) & 1u) ^ 1u, abort_flag);
@@ -655,8 +672,9 @@ struct SplitShape {
 };
 
 template <bool kFp8, int kD, int kG>
-int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const CUtensorMap &mv) {
+int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, const CUtensorMap &mv) {
   using C = Cfg<kFp8, kD, kG, kNCW>;
+  DecodeArgs a = a_in;
   const bool per_token = kFp8 && a.scale_mode == PFKV_SCALE_PER_TOKEN;
   auto kern = gqa_split_kernel<kFp8, kD, kG, kNCW>;
   static SplitShape cache[4];
@@ -701,6 +719,10 @@ int run_split(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const 
       cache[slot] = sh;
     }
   }
+  // one equal page range per (CTA / Hkv) when requests may be cut into 3 or
+  // more pieces (the plan falls back to longest-first items when the caps
+  // leave too few ranges)
+  a.balanced = a.max_splits >= 3 ? min(sh.grid / a.Hkv, kMaxRanges) : 0;
   plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, sh.grid * 8, (1024 + a.S - 1) / a.S);
   int rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
   if (rc) return rc;

@@ -143,14 +143,15 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
   bool ok = true;
   // balanced plan: this CTA's items are a fixed run; otherwise items are
   // taken from a shared counter
+  const int n_ranges = a.hdr->n_ranges;
   int next = 0, last = 0;
-  if (a.balanced > 0 && (int)blockIdx.x < a.hdr->chunk_pages) {
+  if (n_ranges > 0 && (int)blockIdx.x < n_ranges) {
     next = a.cta_first[blockIdx.x];
     last = a.cta_first[blockIdx.x + 1];
   }
   for (;; ++it) {
     int item = 0;
-    if (a.balanced > 0) {
+    if (n_ranges > 0) {
       item = next < last ? next++ : n_items;
     } else {
       if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);

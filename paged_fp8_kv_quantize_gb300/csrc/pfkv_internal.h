@@ -16,8 +16,9 @@ struct WsHeader {
   int n_items;      // n_chunks * num_kv_heads
   unsigned work;    // dynamic work counter
   unsigned err;     // nonzero: a kernel wait timed out
-  int chunk_pages;  // pages per split target
-  int pad[59];
+  int chunk_pages;  // pages per split target (balanced plan: number of ranges)
+  int n_ranges;     // > 0: balanced plan with this many ranges; 0: items from the work counter
+  int pad[58];
 };
 
 // Decode workspace carve-up.
@@ -66,8 +67,11 @@ struct DecodeArgs {
   uint8_t *qterms;
   float *qfac;
   // balanced plan (balanced > 0: at most that many ranges): the concatenated
-  // page list of all requests is cut into equal ranges, one per CTA; CTA c
-  // processes items cta_first[c] .. cta_first[c + 1] - 1
+  // page list of all requests is cut into equal ranges; range r covers
+  // chunks cta_first[r] .. cta_first[r + 1] - 1, taken for KV head h by CTA
+  // r * Hkv + h.  The plan falls back to longest-first items from the work
+  // counter when fewer than 3/4 of the ranges survive its caps; the header's
+  // n_ranges says which plan was made.
   int balanced;
   int *cta_first;
 };

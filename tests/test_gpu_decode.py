@@ -54,10 +54,20 @@ def test_decode_shapes(dtype, si):
     _check(_work(300 + si, G=G, Hkv=Hkv, D=D, S=S, lens=lens), dtype)
 
 
-@pytest.mark.parametrize("max_splits", [1, 3, 64, 256])
+@pytest.mark.parametrize("max_splits", [1, 2, 3, 64, 256])
 def test_split_counts(max_splits):
+    # 1, 2: longest-first plan; 3: the balanced plan's cap leaves too few
+    # ranges and it falls back to longest-first; 64, 256: balanced ranges
     w = _work(400, G=4, Hkv=8, D=128, S=16, lens=[7, 1000, 4097, 20000])
     _check(w, FP8, max_splits=max_splits)
+
+
+@pytest.mark.parametrize("lens", [[16384] * 8, [16384] * 7 + [100]])
+def test_balanced_ranges_cross_requests(lens):
+    # one KV head: every CTA owns a range, and a request meets more ranges
+    # than a warp has lanes (the plan writes its chunks in two lane passes)
+    w = _work(403, G=8, Hkv=1, D=128, S=64, lens=lens)
+    _check(w, FP8, max_splits=64)
 
 
 def test_per_token_scales_gqa():
