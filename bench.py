@@ -314,10 +314,15 @@ def bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_cal
 
 
 def bench_configs(abi, dev, i32, bf16, capture, time_graph, peak, n_calls):
-    """The other shapes of the benchmark table: the grouped-query batch and the long-context batch."""
+    """The other shapes of the benchmark table: the tiny batch, the grouped-query batch and the long-context batch."""
     import torch
 
     res = {}
+    w = synth.tiny()
+    res["tiny"] = {"workload": "batch 2, lengths 37 and 100, 4 q / 1 KV head, head_dim 64, page 16, pool of 32, "
+                               "one stale entry, tag check on (launch-bound)",
+                   "fp8": bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
+                                              abi.DTYPE_FP8_E4M3)}
     w = synth.gqa()
     res["gqa"] = {"workload": "batch 32, lengths U[1024, 8192], 32 q / 8 KV heads, head_dim 128, page 16, "
                               "1% outliers x20, tag check on",

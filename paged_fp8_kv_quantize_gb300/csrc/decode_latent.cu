@@ -428,7 +428,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
     // this item's query rows into tensor memory, once the previous item's
     // last QK^T is done with them
-    fail = !mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag);
+    fail = __any_sync(0xffffffffu, !mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag));  // warp-uniform
     if (!fail) {
       const uint4 *src = reinterpret_cast<const uint4 *>(a.qterms + (size_t)d.b * kLatentQTermBytes +
                                                          (size_t)(32 * q + lane) * 512);
@@ -454,6 +454,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       fail = !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
              !mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
              !mbar_wait(&B.p_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag);
+      fail = __any_sync(0xffffffffu, fail);  // the warp-wide tensor-memory loads below need every lane
       if (fail) break;
       float v[32];
       {
@@ -530,9 +531,9 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
         // page are in, if any head asked for it, scale this warp's lanes of
         // O^T (values 32 q .. 32 q + 31 of each chunk) by beta_h per head
         // column, after the previous page's PV and before this page's.
-        fail = !mbar_wait(&B.p_full[sb], (gp >> 1) & 1u, abort_flag);
+        fail = __any_sync(0xffffffffu, !mbar_wait(&B.p_full[sb], (gp >> 1) & 1u, abort_flag));
         if (!fail && resc_tag[sb] == gp + 1u) {
-          fail = !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag);
+          fail = __any_sync(0xffffffffu, !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag));
           if (!fail) {
             tc_fence_after();
 #pragma unroll 1
