@@ -278,7 +278,12 @@ __device__ bool plan_balanced(const DecodeArgs &a, int ranges) {
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
-  pdl_launch_dependents();  // the split kernel waits for this grid's results before reading them
+  // Launched as a programmatic dependent: the stream's earlier work is
+  // complete from here.  Only then may the split kernel launch (it waits for
+  // this grid's results before reading them): its CTAs must not take SMs
+  // while the previous call's merge still runs.
+  pdl_wait();
+  pdl_launch_dependents();
   if (blockIdx.x > 0) {
     const int nab = plan_append_blocks(a);
     if ((int)blockIdx.x <= nab) plan_append(a);
@@ -390,6 +395,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_ite
   }
 }
 
+// The plan grid, launched as a programmatic dependent of the stream's
+// previous kernel: its launch overlaps that kernel's tail, and it waits for
+// it (griddepcontrol.wait) before touching memory.
+inline cudaError_t launch_plan(const DecodeArgs &a, cudaStream_t s, int target_items, int min_chunk_pages) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan_blocks(a));
+  cfg.blockDim = dim3(1024);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, a, target_items, min_chunk_pages);
+}
+
 // ---------------------------------------------------------------- merge
 
 // Merge launch shape: a block takes kW float4 columns of one (request, KV
@@ -418,6 +439,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   __shared__ float s_l[256 * M::kNH];
   __shared__ float s_M[M::kNH], s_W[M::kNH];
   __shared__ float4 s_acc[256];
+  pdl_launch_dependents();  // the next call's plan grid may launch; it waits for this grid to finish
   pdl_wait();  // partials and status of the split kernel are visible from here on
   const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
   const int nb = a.split_count[b];

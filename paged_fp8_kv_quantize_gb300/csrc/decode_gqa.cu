@@ -723,8 +723,7 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
   // more pieces (the plan falls back to longest-first items when the caps
   // leave too few ranges)
   a.balanced = a.max_splits >= 3 ? min(sh.grid / a.Hkv, kMaxRanges) : 0;
-  plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, sh.grid * 8, (1024 + a.S - 1) / a.S);
-  int rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
+  int rc = cuda_ok(launch_plan(a, s, sh.grid * 8, (1024 + a.S - 1) / a.S), "plan kernel launch");
   if (rc) return rc;
   // The split kernel may start while the plan kernel runs; it waits for the
   // plan's results (griddepcontrol.wait) before it reads them.

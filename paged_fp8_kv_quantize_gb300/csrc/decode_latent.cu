@@ -714,8 +714,7 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   // one equal page range per CTA when requests may be cut into 3 or more
   // pieces; otherwise longest-first items from a shared counter
   a.balanced = a.max_splits >= 3 ? (grid < kMaxRanges ? grid : kMaxRanges) : 0;
-  plan_kernel<<<plan_blocks(a), 1024, 0, s>>>(a, grid * 2, 8);
-  rc = cuda_ok(cudaGetLastError(), "plan kernel launch");
+  rc = cuda_ok(launch_plan(a, s, grid * 2, 8), "plan kernel launch");
   if (rc) return rc;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
