@@ -25,8 +25,9 @@
 //
 // One CTA per SM, persistent; work item = (request, range of its pages), all
 // 64 heads.  Warp 0 loads pages into a five-page ring (TMA, bounds and tag
-// checks beside the copies); warp 1 owns tensor memory and issues the MMAs
-// (one thread, each MMA group as soon as its inputs are ready); warps 2-5
+// checks beside the copies); warp 1 owns tensor memory and issues the QK^T
+// MMAs and warp 6 the PV MMAs (one thread each, so that the two instruction
+// streams overlap on the tensor pipe); warps 2-5
 // run the softmax: warp w reads tensor-memory quarter w % 4, i.e. heads
 // 16 q .. 16 q + 15, each lane one head and 32 of the page's tokens, so the
 // running maxima and sums are per thread.  A running maximum moves only when
@@ -64,7 +65,7 @@ constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
 constexpr uint32_t kPBuf = kPT * kPTerm;      // 12288
 constexpr int kNst = 5;                       // pages in flight per CTA
 constexpr int kPrefetch = 6;                  // pages pulled into L2 ahead of their copy
-constexpr int kTThreads = 192;                // producer, MMA, four softmax warps
+constexpr int kTThreads = 224;                // producer, QK issuer, four softmax warps, PV issuer
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;  // Q (128) | S x2 (64 each) | O^T (4 x 64)
 constexpr float kTheta = 3.f;                 // log2 growth of a running max that triggers a rescale
@@ -258,25 +259,35 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
   }
 }
 
-// ---------------------------------------------------------------- MMA issuer (warp 1, one thread)
+// ---------------------------------------------------------------- MMA issuers (warps 1 and 6, one thread each)
 
-__device__ __forceinline__ void tc_mma(uint8_t *smem, const Bars &B, const ItemDesc *items, uint32_t tmem,
-                                       volatile int *abort_flag) {
+// Shared-memory descriptors, built once; an MMA adds its operand's byte
+// offset / 16 to the start-address field (addresses stay below 256 KB, so
+// the 14-bit field never carries).
+struct TcDesc {
+  uint64_t page, page_tail, qtail, vt, pt;
+};
+
+__device__ __forceinline__ TcDesc tc_desc(uint8_t *smem) {
   const TcSmem sp = tc_smem();
   const uint32_t s_ring = smem_addr(smem + sp.ring), s_qt = smem_addr(smem + sp.qtail), s_p = smem_addr(smem + sp.p);
-  // Shared-memory descriptors built once; an MMA adds its operand's byte
-  // offset / 16 to the start-address field (addresses stay below 256 KB, so
-  // the 14-bit field never carries).
-  const uint64_t d_page = umma_sdesc(s_ring, 16, 1024, 2);             // B of QK^T: page rows, 128-byte swizzle
-  const uint64_t d_page_tail = umma_sdesc(s_ring + kPageTail, 16, 512, 4);  // B of the tail steps
-  const uint64_t d_qtail = umma_sdesc(s_qt, 16, 512, 4);               // A of the tail steps
-  const uint64_t d_vt = umma_sdesc(s_ring, 8192, 1024, 2);             // A of PV: V^T, MN-major
-  const uint64_t d_pt = umma_sdesc(s_p, 128, 512, 0);                  // B of PV: P^T, K-major
-  const volatile uint32_t *resc_tag = reinterpret_cast<const uint32_t *>(smem + sp.wg) + kWgTag;
-  uint32_t g = 0;       // pages consumed before the current item
-  uint32_t n_resc = 0;  // rescale hand-offs so far
-  bool ok = true;
-  for (uint32_t it = 0; ok; ++it) {
+  TcDesc d;
+  d.page = umma_sdesc(s_ring, 16, 1024, 2);                // B of QK^T: page rows, 128-byte swizzle
+  d.page_tail = umma_sdesc(s_ring + kPageTail, 16, 512, 4);  // B of the tail steps
+  d.qtail = umma_sdesc(s_qt, 16, 512, 4);                   // A of the tail steps
+  d.vt = umma_sdesc(s_ring, 8192, 1024, 2);                 // A of PV: V^T, MN-major
+  d.pt = umma_sdesc(s_p, 128, 512, 0);                      // B of PV: P^T, K-major
+  return d;
+}
+
+// QK^T issuer (warp 1): S[sb] = [T1; T2 rows] . K_page^T for every page in
+// order, as soon as the page has landed and the softmax warps have read the
+// S buffer's previous page.
+__device__ __forceinline__ void tc_mma_qk(uint8_t *smem, const Bars &B, const ItemDesc *items, uint32_t tmem,
+                                          volatile int *abort_flag) {
+  const TcDesc dd = tc_desc(smem);
+  uint32_t g = 0;  // pages consumed before the current item
+  for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
     if (!mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag)) break;
     const ItemDesc d = items[slot];
@@ -284,80 +295,85 @@ __device__ __forceinline__ void tc_mma(uint8_t *smem, const Bars &B, const ItemD
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
     if (!mbar_wait(B.q_full, it & 1u, abort_flag) || !mbar_wait(B.q_tfull, it & 1u, abort_flag)) break;
-    // Issue each MMA group as soon as its inputs are ready: QK^T of page nq
-    // (page landed, its S buffer read by the softmax warps) or PV of page np
-    // (P^T written; O^T read out for the item's first page, rescaled when
-    // the softmax warps asked for it).
-    uint32_t nq = 0, np = 0;
-    bool o_free = false;
-    uint64_t t_last = 0;  // start of the current stretch without progress
-    while (np < n) {
-      bool did = false;
-      if (nq < n) {
-        const uint32_t gp = g + nq, st = gp % kNst, sb = gp & 1u;
-        if (mbar_test(&B.full[st], (gp / kNst) & 1u) && mbar_test(&B.s_empty[sb], ((gp >> 1) & 1u) ^ 1u)) {
-          tc_fence_after();
-          // S[sb] = [T1; T2 rows] . K_page^T: 128 x 64, K = 576 in 18 steps of 32
-          const uint64_t pg = (uint64_t)((st * kPageSm) >> 4);
-          const uint32_t d_s = tmem + kColS + 64 * sb;
-#pragma unroll
-          for (int kk = 0; kk < 16; ++kk)
-            umma_e4m3_ts(d_s, tmem + kColQ + 8 * kk, d_page + pg + (uint64_t)(((kk >> 2) * kBlk + (kk & 3) * 32) >> 4),
-                         kIdQK, kk ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            umma_e4m3(d_s, d_qtail + (uint64_t)(2 * kk), d_page_tail + pg + (uint64_t)(2 * kk), kIdQK, 1u);
-          umma_commit(&B.s_full[sb]);
-          if (nq + 1 == n) umma_commit(B.q_empty);  // the query operand may be replaced
-          ++nq;
-          did = true;
-        }
+    bool ok = true;
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t gp = g + j, st = gp % kNst, sb = gp & 1u;
+      if (!mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
+          !mbar_wait(&B.s_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag)) {
+        ok = false;
+        break;
       }
-      if (np < nq) {
-        const uint32_t gp = g + np, st = gp % kNst, pb = gp & 1u;
-        if (np == 0 && !o_free) o_free = mbar_test(B.o_empty, (it & 1u) ^ 1u);
-        bool ready = (np > 0 || o_free) && mbar_test(&B.p_full[pb], (gp >> 1) & 1u);
-        const bool resc = ready && np > 0 && resc_tag[pb] == gp + 1u;
-        if (resc) ready = mbar_test(B.r_done, n_resc & 1u);
-        if (ready) {
-          if (resc) ++n_resc;
-          tc_fence_after();
-          // O^T[c] (+)= V^T_c . (P1 + P2 + P3)^T
-          const uint64_t pg = (uint64_t)((st * kPageSm) >> 4), pp = (uint64_t)((pb * kPBuf) >> 4);
-          const uint32_t first = np == 0 ? 0u : 1u;
+      tc_fence_after();
+      // 128 x 64, K = 576 in 18 steps of 32
+      const uint64_t pg = (uint64_t)((st * kPageSm) >> 4);
+      const uint32_t d_s = tmem + kColS + 64 * sb;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+      for (int kk = 0; kk < 16; ++kk)
+        umma_e4m3_ts(d_s, tmem + kColQ + 8 * kk, dd.page + pg + (uint64_t)(((kk >> 2) * kBlk + (kk & 3) * 32) >> 4),
+                     kIdQK, kk ? 1u : 0u);
 #pragma unroll
-            for (int t = 0; t < kPT; ++t)
-#pragma unroll
-              for (int ks = 0; ks < 2; ++ks)
-                umma_e4m3(tmem + kColO + 64 * c, d_vt + pg + (uint64_t)((c * kBlk + ks * 4096) >> 4),
-                          d_pt + pp + (uint64_t)((t * kPTerm + ks * 256) >> 4), kIdPV,
-                          (t == 0 && ks == 0) ? first : 1u);
-          umma_commit(&B.empty[st]);
-          umma_commit(&B.p_empty[pb]);
-          ++np;
-          did = true;
-        }
+      for (int kk = 0; kk < 2; ++kk)
+        umma_e4m3(d_s, dd.qtail + (uint64_t)(2 * kk), dd.page_tail + pg + (uint64_t)(2 * kk), kIdQK, 1u);
+      umma_commit(&B.s_full[sb]);
+    }
+    if (!ok) break;
+    umma_commit(B.q_empty);  // the query operand may be replaced
+    g += n;
+  }
+  // every MMA issued here has completed before tensor memory is released
+  umma_commit(B.drain);
+  drain_wait(B.drain, 0);
+}
+
+// PV issuer (warp 6): O^T[c] (+)= V^T_c . (P1 + P2 + P3)^T for every page
+// in order, once its P^T is written (and, for an item's first page, the
+// previous item's O^T has been read out; after a rescale hand-off, once the
+// softmax warps have scaled O^T).  Frees the page's ring slot and P buffer.
+__device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const ItemDesc *items, uint32_t tmem,
+                                          volatile int *abort_flag) {
+  const TcSmem sp = tc_smem();
+  const TcDesc dd = tc_desc(smem);
+  const volatile uint32_t *resc_tag = reinterpret_cast<const uint32_t *>(smem + sp.wg) + kWgTag;
+  uint32_t g = 0, n_resc = 0;
+  for (uint32_t it = 0;; ++it) {
+    const uint32_t slot = it % kNIQ;
+    if (!mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag)) break;
+    const ItemDesc d = items[slot];
+    mbar_arrive(&B.item_empty[slot]);
+    if (d.b < 0) break;
+    const uint32_t n = (uint32_t)(d.p1 - d.p0);
+    if (!mbar_wait(B.o_empty, (it & 1u) ^ 1u, abort_flag)) break;
+    bool ok = true;
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t gp = g + j, st = gp % kNst, pb = gp & 1u;
+      if (!mbar_wait(&B.p_full[pb], (gp >> 1) & 1u, abort_flag)) {
+        ok = false;
+        break;
       }
-      if (did) {
-        t_last = 0;
-      } else {
-        // nothing ready: back off briefly, leaving this scheduler's issue slots
-        // to the softmax warp that shares it
-        __nanosleep(64);
-        const uint64_t now = global_timer_ns();
-        if (t_last == 0) t_last = now;
-        if (*abort_flag || now - t_last > kWaitLimitNs) {
-          *abort_flag = 1;
+      if (j > 0 && resc_tag[pb] == gp + 1u) {
+        if (!mbar_wait(B.r_done, n_resc & 1u, abort_flag)) {
           ok = false;
           break;
         }
+        ++n_resc;
       }
+      tc_fence_after();
+      const uint64_t pg = (uint64_t)((st * kPageSm) >> 4), pp = (uint64_t)((pb * kPBuf) >> 4);
+      const uint32_t first = j == 0 ? 0u : 1u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int t = 0; t < kPT; ++t)
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks)
+            umma_e4m3(tmem + kColO + 64 * c, dd.vt + pg + (uint64_t)((c * kBlk + ks * 4096) >> 4),
+                      dd.pt + pp + (uint64_t)((t * kPTerm + ks * 256) >> 4), kIdPV, (t == 0 && ks == 0) ? first : 1u);
+      umma_commit(&B.empty[st]);
+      umma_commit(&B.p_empty[pb]);
     }
+    if (!ok) break;
     g += n;
   }
-  // every MMA issued above has completed before tensor memory is released
   umma_commit(B.drain);
   drain_wait(B.drain, 0);
 }
@@ -624,10 +640,10 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
     mbar_init(B.q_tfull, 4);
     mbar_init(B.o_empty, 4);
     mbar_init(B.r_done, 4);
-    mbar_init(B.drain, 1);
+    mbar_init(B.drain, 2);  // one commit from each MMA issuer
     for (int i = 0; i < kNIQ; ++i) {
       mbar_init(&B.item_full[i], 1);
-      mbar_init(&B.item_empty[i], 2);  // the MMA thread and the softmax warps
+      mbar_init(&B.item_empty[i], 3);  // the two MMA threads and the softmax warps
       mbar_init(&B.item_done[i], 1);
     }
     uint32_t *tag = reinterpret_cast<uint32_t *>(smem + sp.wg) + kWgTag;
@@ -649,7 +665,10 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
     }
     tc_producer(a, map, map_tail, smem, B, items, item_status, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) tc_mma(smem, B, items, tmem, abort_flag);
+    if (lane == 0) tc_mma_qk(smem, B, items, tmem, abort_flag);
+    __syncwarp();
+  } else if (warp == 6) {
+    if (lane == 0) tc_mma_pv(smem, B, items, tmem, abort_flag);
     __syncwarp();
   } else {
     tc_softmax(a, smem, B, items, item_status, tmem, abort_flag);
