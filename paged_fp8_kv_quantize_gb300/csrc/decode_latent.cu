@@ -26,8 +26,8 @@
 // One CTA per SM, persistent; work item = (request, range of its pages), all
 // 64 heads.  Warp 0 loads pages into a five-page ring (TMA, bounds and tag
 // checks beside the copies); warp 1 owns tensor memory and issues the QK^T
-// MMAs and warp 6 the PV MMAs (one thread each, so that the two instruction
-// streams overlap on the tensor pipe); warps 2-5
+// MMAs and warps 6 and 7 the PV MMAs of two value chunks each (one thread
+// each, so that the instruction streams overlap on the tensor pipe); warps 2-5
 // run the softmax: warp w reads tensor-memory quarter w % 4, i.e. heads
 // 16 q .. 16 q + 15, each lane one head and 32 of the page's tokens, so the
 // running maxima and sums are per thread.  A running maximum moves only when
@@ -65,7 +65,7 @@ constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
 constexpr uint32_t kPBuf = kPT * kPTerm;      // 12288
 constexpr int kNst = 5;                       // pages in flight per CTA
 constexpr int kPrefetch = 6;                  // pages pulled into L2 ahead of their copy
-constexpr int kTThreads = 224;                // producer, QK issuer, four softmax warps, PV issuer
+constexpr int kTThreads = 256;                // producer, QK issuer, four softmax warps, two PV issuers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;  // Q (128) | S x2 (64 each) | O^T (4 x 64)
 constexpr float kTheta = 3.f;                 // log2 growth of a running max that triggers a rescale
@@ -325,12 +325,13 @@ __device__ __forceinline__ void tc_mma_qk(uint8_t *smem, const Bars &B, const It
   drain_wait(B.drain, 0);
 }
 
-// PV issuer (warp 6): O^T[c] (+)= V^T_c . (P1 + P2 + P3)^T for every page
-// in order, once its P^T is written (and, for an item's first page, the
+// PV issuers (warps 6 and 7, value chunks 2 h and 2 h + 1 for h = warp - 6):
+// O^T[c] (+)= V^T_c . (P1 + P2 + P3)^T for every page in order, once its
+// P^T is written (and, for an item's first page, the
 // previous item's O^T has been read out; after a rescale hand-off, once the
 // softmax warps have scaled O^T).  Frees the page's ring slot and P buffer.
 __device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const ItemDesc *items, uint32_t tmem,
-                                          volatile int *abort_flag) {
+                                          volatile int *abort_flag, int half) {
   const TcSmem sp = tc_smem();
   const TcDesc dd = tc_desc(smem);
   const volatile uint32_t *resc_tag = reinterpret_cast<const uint32_t *>(smem + sp.wg) + kWgTag;
@@ -361,7 +362,7 @@ __device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const It
       const uint64_t pg = (uint64_t)((st * kPageSm) >> 4), pp = (uint64_t)((pb * kPBuf) >> 4);
       const uint32_t first = j == 0 ? 0u : 1u;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 2 * half; c < 2 * half + 2; ++c)
 #pragma unroll
         for (int t = 0; t < kPT; ++t)
 #pragma unroll
@@ -627,23 +628,23 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNst; ++i) {
       mbar_init(&B.full[i], 1);
-      mbar_init(&B.empty[i], 1);
+      mbar_init(&B.empty[i], 2);  // a commit from each PV issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
       mbar_init(&B.s_empty[i], 4);
       mbar_init(&B.p_full[i], 4);
-      mbar_init(&B.p_empty[i], 1);
+      mbar_init(&B.p_empty[i], 2);  // a commit from each PV issuer
     }
     mbar_init(B.q_full, 1);
     mbar_init(B.q_empty, 1);
     mbar_init(B.q_tfull, 4);
     mbar_init(B.o_empty, 4);
     mbar_init(B.r_done, 4);
-    mbar_init(B.drain, 2);  // one commit from each MMA issuer
+    mbar_init(B.drain, 3);  // one commit from each MMA issuer
     for (int i = 0; i < kNIQ; ++i) {
       mbar_init(&B.item_full[i], 1);
-      mbar_init(&B.item_empty[i], 3);  // the two MMA threads and the softmax warps
+      mbar_init(&B.item_empty[i], 4);  // the three MMA threads and the softmax warps
       mbar_init(&B.item_done[i], 1);
     }
     uint32_t *tag = reinterpret_cast<uint32_t *>(smem + sp.wg) + kWgTag;
@@ -667,8 +668,8 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
   } else if (warp == 1) {
     if (lane == 0) tc_mma_qk(smem, B, items, tmem, abort_flag);
     __syncwarp();
-  } else if (warp == 6) {
-    if (lane == 0) tc_mma_pv(smem, B, items, tmem, abort_flag);
+  } else if (warp >= 6) {
+    if (lane == 0) tc_mma_pv(smem, B, items, tmem, abort_flag, warp - 6);
     __syncwarp();
   } else {
     tc_softmax(a, smem, B, items, item_status, tmem, abort_flag);
