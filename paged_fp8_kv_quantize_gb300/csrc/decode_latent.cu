@@ -27,12 +27,14 @@
 // 64 heads.  Warp 0 loads pages into a five-page ring (TMA, bounds and tag
 // checks beside the copies); warp 1 owns tensor memory and issues the QK^T
 // MMAs and warps 6 and 7 the PV MMAs of two value chunks each (one thread
-// each, so that the instruction streams overlap on the tensor pipe); warps 2-5
-// run the softmax: warp w reads tensor-memory quarter w % 4, i.e. heads
-// 16 q .. 16 q + 15, each lane one head and 32 of the page's tokens, so the
-// running maxima and sums are per thread.  A running maximum moves only when
-// it grows by more than 8x; O^T, whose columns are heads and whose lanes
-// are values, is then rescaled by all four warps before the page's PV, a
+// each, so that the instruction streams overlap on the tensor pipe); warps
+// 2-5 and 8-11 run the softmax: warp w reads tensor-memory quarter w % 4,
+// i.e. heads 16 q .. 16 q + 15, and one half of the page's tokens, each
+// lane one head and 16 tokens; the two warps of a quarter agree on each
+// page's maximum through shared memory, so the running maxima are identical
+// in both and the sums are per thread.  A running maximum moves only when it
+// grows by more than 8x; O^T, whose columns are heads and whose lanes are
+// values, is then rescaled by the softmax warps before the page's PV, a
 // hand-off that costs nothing on the pages that need none.  Partials are
 // merged by the shared log-sum-exp merge kernel.
 #include <cuda_fp16.h>
@@ -65,13 +67,18 @@ constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
 constexpr uint32_t kPBuf = kPT * kPTerm;      // 12288
 constexpr int kNst = 5;                       // pages in flight per CTA
 constexpr int kPrefetch = 6;                  // pages pulled into L2 ahead of their copy
-constexpr int kTThreads = 256;                // producer, QK issuer, four softmax warps, two PV issuers
+constexpr int kTThreads = 384;                // producer, QK issuer, softmax x4, two PV issuers, softmax x4
+constexpr int kSmxThreads = 256;              // the eight softmax warps (2-5 and 8-11)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;  // Q (128) | S x2 (64 each) | O^T (4 x 64)
 constexpr float kTheta = 3.f;                 // log2 growth of a running max that triggers a rescale
 constexpr float kPExp = 4.75f;                // P'' = p (s_t / s_ref) 2^kPExp <= 2^kTheta * 2 * 2^4.75 < 448
 constexpr uint32_t kIdQK = umma_idesc_e4m3(128, 64, 0, 0);
 constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 64, 1, 0);
+
+// Softmax-warp scratch, floats: beta[2][64] | l[2 halves][64] | m[64] | resc_tag[2] (uint32) | pad |
+// page maxima exchanged by the two warps of a lane quarter, float2 [2 pages][2 halves][64]
+constexpr int kWgBeta = 0, kWgL = 128, kWgM = 256, kWgTag = 320, kWgX = 328, kWgFloats = kWgX + 2 * 2 * 2 * 64;
 
 struct TcSmem {
   uint32_t ring, qtail, p, scales, wg, bars, items, total;
@@ -84,15 +91,13 @@ __host__ __device__ constexpr TcSmem tc_smem() {
   s.p = s.qtail + kQTailBytes;                 // 2 buffers x kPT P^T terms
   s.scales = s.p + 2 * kPBuf;                  // kNst x 64 per-token scales
   s.wg = s.scales + kNst * kTS * 4;            // softmax-warp scratch (see below)
-  s.bars = s.wg + 4 * (2 * 64 + 3 * 64 + 4);   // beta[2][64] | l, m, cq-unused[64] | tags[2], pad
+  s.bars = s.wg + 4 * kWgFloats;               // softmax-warp scratch (layout above)
   s.items = s.bars + 8 * (2 * kNst + 14 + 3 * kNIQ);
   s.total = s.items + (sizeof(ItemDesc) + 4) * kNIQ + 16;
   return s;
 }
 static_assert(tc_smem().total + 1024 <= 232448, "shared memory plan exceeds one SM");
 
-// Softmax-warp scratch, floats: beta[2][64] | l[64] | m[64] | spare[64] | resc_tag[2] (uint32) | pad
-constexpr int kWgBeta = 0, kWgL = 128, kWgM = 192, kWgTag = 320;
 
 // Bounded wait that ignores the abort flag: used on the way out, so that a
 // block that gave up still lets its own copies and MMAs land before it exits.
@@ -381,16 +386,19 @@ __device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const It
 
 // ---------------------------------------------------------------- softmax warps (warps 2-5)
 
-// Barrier of the four softmax warps (id 1) that also ORs a flag over them.
-__device__ __forceinline__ bool wg_bar_or(bool v) {
+// Barrier `id` of `nthreads` threads that also ORs a flag over them.
+__device__ __forceinline__ bool bar_or(int id, int nthreads, bool v) {
   uint32_t r;
   asm volatile(
-      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %3, 0;\nbar.red.or.pred q, %1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v)
+      : "r"(id), "r"(nthreads), "r"((uint32_t)v)
       : "memory");
   return r != 0u;
 }
+
+// All softmax warps (barrier 1).
+__device__ __forceinline__ bool wg_bar_or(bool v) { return bar_or(1, kSmxThreads, v); }
 
 __device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
   uint16_t r;
@@ -414,27 +422,33 @@ __device__ __forceinline__ void three_terms2(float lo, float hi, uint32_t &t1, u
   t3 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&r2));
 }
 
-// Warp w reads tensor-memory quarter q = w % 4: rows 32 q .. 32 q + 31 of S,
-// i.e. T1 (lanes 0-15) and T2 (lanes 16-31) of heads 16 q .. 16 q + 15.
-// After adding the two halves, lane l holds head 16 q + l % 16 and tokens
-// 32 (l / 16) .. 32 (l / 16) + 31 of the page.
+// Softmax warp w (2-5 and 8-11) reads tensor-memory quarter q = w % 4, i.e.
+// rows 32 q .. 32 q + 31 of S: T1 (lanes 0-15) and T2 (lanes 16-31) of heads
+// 16 q .. 16 q + 15, and takes half x = (w >= 8) of the page's tokens.  After
+// adding the two terms, lane l holds head 16 q + l % 16 and tokens
+// 32 x + 16 (l / 16) .. + 15.  The two warps of a quarter agree on each
+// page's maximum through shared memory (barrier 2 + q, which also ORs their
+// failure flags, so both leave the page loop together).
 __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, const Bars &B, const ItemDesc *items,
                                            const uint32_t *item_status, uint32_t tmem, volatile int *abort_flag) {
   const TcSmem sp = tc_smem();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q = warp & 3;                 // tensor-memory lane quarter
-  const int wt = threadIdx.x - 64;        // 0..127
-  const int half = lane >> 4;             // token half, and the term of this lane's S row
-  const int h = 16 * q + (lane & 15);     // head of this thread
+  const int q = warp & 3;                       // tensor-memory lane quarter
+  const int x = warp >= 8 ? 1 : 0;              // token half of the page (and half of the O^T columns)
+  const int wt = (4 * x + (warp - 2 - 6 * x)) * 32 + lane;  // 0..255 over the softmax warps
+  const int half = lane >> 4;                   // term of this lane's S row; then the 16-token chunk
+  const int h = 16 * q + (lane & 15);           // head of this thread
+  const int tb = 32 * x + 16 * half;            // first token of the page this thread owns
   float *wsc = reinterpret_cast<float *>(smem + sp.wg);
   float *s_beta = wsc + kWgBeta, *s_l = wsc + kWgL, *s_m = wsc + kWgM;
+  float2 *s_x = reinterpret_cast<float2 *>(wsc + kWgX);
   volatile uint32_t *resc_tag = reinterpret_cast<uint32_t *>(wsc + kWgTag);
   const float *scales = reinterpret_cast<const float *>(smem + sp.scales);
   uint8_t *pbase = smem + sp.p;
   const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
   // P^T (K-major, no swizzle): byte (head, token) at (head % 8) * 16 + (head / 8) * 512 +
-  // (token / 16) * 128 + token % 16; this thread writes 16-token chunks 2 half and 2 half + 1
-  const uint32_t p_off = (h & 7) * 16 + (h >> 3) * 512 + (2 * half) * 128;
+  // (token / 16) * 128 + token % 16; this thread writes the 16-token chunk tb / 16
+  const uint32_t p_off = (h & 7) * 16 + (h >> 3) * 512 + (tb / 16) * 128;
   uint32_t g = 0, n_resc = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
@@ -443,14 +457,15 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     const ItemDesc d = items[slot];
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
-    // this item's query rows into tensor memory, once the previous item's
-    // last QK^T is done with them
+    // this item's query rows into tensor memory (this warp: columns 64 x ..
+    // 64 x + 63 of its quarter's rows), once the previous item's last QK^T
+    // is done with them
     fail = __any_sync(0xffffffffu, !mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag));  // warp-uniform
     if (!fail) {
       const uint4 *src = reinterpret_cast<const uint4 *>(a.qterms + (size_t)d.b * kLatentQTermBytes +
                                                          (size_t)(32 * q + lane) * 512);
 #pragma unroll 1
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 2 * x; k < 2 * x + 2; ++k) {
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -466,95 +481,99 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     if (lane == 0) mbar_arrive(B.q_tfull);
     const float cq = __ldg(&a.qfac[(size_t)d.b * kTH + h]);
     float m = kNegInf, l = 0.f, s_ref = 0.f;
-    for (uint32_t j = 0; j < n && !fail; ++j) {
+    for (uint32_t j = 0; j < n; ++j) {
       const uint32_t gp = g + j, sb = gp & 1u, st = gp % kNst;
-      fail = !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
-             !mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
-             !mbar_wait(&B.p_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag);
-      fail = __any_sync(0xffffffffu, fail);  // the warp-wide tensor-memory loads below need every lane
-      if (fail) break;
-      float v[32];
-      {
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tq + kColS + 64 * sb, r0);       // tokens 0-31 of this lane's row
-        tmem_ld32(tq + kColS + 64 * sb + 32, r1);  // tokens 32-63
-        tc_fence_before();
-        // T1 + T2: the partner lane (l ^ 16) holds the other term of the same head
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t give = half ? r0[i] : r1[i];
-          const uint32_t take = __shfl_xor_sync(0xffffffffu, give, 16);
-          v[i] = __uint_as_float(half ? r1[i] : r0[i]) + __uint_as_float(take);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B.s_empty[sb]);
-      const int tok0 = (d.p0 + (int)j) * kTS + 32 * half;
-      float sv[32];
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 s4 = *reinterpret_cast<const float4 *>(&scales[st * kTS + 32 * half + i]);
-        sv[i] = s4.x; sv[i + 1] = s4.y; sv[i + 2] = s4.z; sv[i + 3] = s4.w;
-      }
+      if (!fail)
+        fail = !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
+               !mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
+               !mbar_wait(&B.p_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag);
+      fail = __any_sync(0xffffffffu, fail);  // the warp-wide tensor-memory load below needs every lane
+      float v[16], sv[16];
       float mt = kNegInf, smx = 0.f;
+      if (!fail) {
+        {
+          tc_fence_after();
+          uint32_t r[32];
+          tmem_ld32(tq + kColS + 64 * sb + 32 * x, r);  // tokens 32 x .. 32 x + 31 of this lane's row
+          tc_fence_before();
+          // T1 + T2: the partner lane (l ^ 16) holds the other term of the same head
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const bool valid = tok0 + i < d.L;
-        if (!valid) sv[i] = 0.f;
-        v[i] = valid ? v[i] * cq * sv[i] : kNegInf;  // z in log2 units
-        mt = fmaxf(mt, v[i]);
-        smx = fmaxf(smx, sv[i]);
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t give = half ? r[i] : r[16 + i];
+            const uint32_t take = __shfl_xor_sync(0xffffffffu, give, 16);
+            v[i] = __uint_as_float(half ? r[16 + i] : r[i]) + __uint_as_float(take);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.s_empty[sb]);
+        const int tok0 = (d.p0 + (int)j) * kTS + tb;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) {
+          const float4 s4 = *reinterpret_cast<const float4 *>(&scales[st * kTS + tb + i]);
+          sv[i] = s4.x; sv[i + 1] = s4.y; sv[i + 2] = s4.z; sv[i + 3] = s4.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const bool valid = tok0 + i < d.L;
+          if (!valid) sv[i] = 0.f;
+          v[i] = valid ? v[i] * cq * sv[i] : kNegInf;  // z in log2 units
+          mt = fmaxf(mt, v[i]);
+          smx = fmaxf(smx, sv[i]);
+        }
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, 16));
+        if (lane < 16) s_x[(sb * 2 + x) * kTH + h] = make_float2(mt, smx);
       }
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-      smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, 16));
+      if (bar_or(2 + q, 64, fail)) {
+        fail = true;
+        break;
+      }
+      {
+        const float2 o = s_x[(sb * 2 + (x ^ 1)) * kTH + h];  // the other half of the page
+        mt = fmaxf(mt, o.x);
+        smx = fmaxf(smx, o.y);
+      }
       const float s_new = smx > 2.f * s_ref ? smx : s_ref;
       const float m_new = mt > m + kTheta ? mt : m;
       const float alpha = fast_exp2(m - m_new);
       const bool resc = j > 0 && (m_new != m || s_new != s_ref);
-      if (j > 0 && lane < 16) s_beta[sb * kTH + h] = alpha * (s_ref / s_new);
-      if (__any_sync(0xffffffffu, resc) && lane == 0) resc_tag[sb] = gp + 1u;
+      if (j > 0 && x == 0 && lane < 16) s_beta[sb * kTH + h] = alpha * (s_ref / s_new);
+      if (__any_sync(0xffffffffu, resc) && x == 0 && lane == 0) resc_tag[sb] = gp + 1u;
       l *= alpha;
       m = m_new;
       s_ref = s_new;
       // P'' = 2^(z - m) (s_t / s_ref) 2^kPExp as three e4m3 terms; l sums 2^(z - m)
       const float w = exp2f(kPExp) / s_ref;
-      uint32_t t1[16], t2[16], t3[16];
+      uint32_t t1[8], t2[8], t3[8];
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
+      for (int i = 0; i < 16; i += 2) {
         const float e0 = fast_exp2(v[i] - m), e1 = fast_exp2(v[i + 1] - m);
         l += e0 + e1;
         three_terms2(e0 * sv[i] * w, e1 * sv[i + 1] * w, t1[i / 2], t2[i / 2], t3[i / 2]);
       }
       uint8_t *pt = pbase + sb * kPBuf + p_off;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int o = 8 * c;  // 16-bit words of this 16-token chunk
-        *reinterpret_cast<uint4 *>(pt + c * 128) = make_uint4(t1[o] | (t1[o + 1] << 16), t1[o + 2] | (t1[o + 3] << 16),
-                                                              t1[o + 4] | (t1[o + 5] << 16), t1[o + 6] | (t1[o + 7] << 16));
-        *reinterpret_cast<uint4 *>(pt + kPTerm + c * 128) =
-            make_uint4(t2[o] | (t2[o + 1] << 16), t2[o + 2] | (t2[o + 3] << 16), t2[o + 4] | (t2[o + 5] << 16),
-                       t2[o + 6] | (t2[o + 7] << 16));
-        *reinterpret_cast<uint4 *>(pt + 2 * kPTerm + c * 128) =
-            make_uint4(t3[o] | (t3[o + 1] << 16), t3[o + 2] | (t3[o + 3] << 16), t3[o + 4] | (t3[o + 5] << 16),
-                       t3[o + 6] | (t3[o + 7] << 16));
-      }
+      *reinterpret_cast<uint4 *>(pt) =
+          make_uint4(t1[0] | (t1[1] << 16), t1[2] | (t1[3] << 16), t1[4] | (t1[5] << 16), t1[6] | (t1[7] << 16));
+      *reinterpret_cast<uint4 *>(pt + kPTerm) =
+          make_uint4(t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16), t2[4] | (t2[5] << 16), t2[6] | (t2[7] << 16));
+      *reinterpret_cast<uint4 *>(pt + 2 * kPTerm) =
+          make_uint4(t3[0] | (t3[1] << 16), t3[2] | (t3[3] << 16), t3[4] | (t3[5] << 16), t3[6] | (t3[7] << 16));
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.p_full[sb]);
       if (j > 0) {
         // Rescale hand-off: once every warp's P^T and scale factors for this
-        // page are in, if any head asked for it, scale this warp's lanes of
-        // O^T (values 32 q .. 32 q + 31 of each chunk) by beta_h per head
-        // column, after the previous page's PV and before this page's.
+        // page are in, if any head asked for it, scale this warp's share of
+        // O^T (its quarter's lanes, columns 128 x .. 128 x + 127) by beta_h
+        // per head column, after the previous page's PV and before this page's.
         fail = __any_sync(0xffffffffu, !mbar_wait(&B.p_full[sb], (gp >> 1) & 1u, abort_flag));
         if (!fail && resc_tag[sb] == gp + 1u) {
           fail = __any_sync(0xffffffffu, !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag));
           if (!fail) {
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 4 * x; c < 4 * x + 4; ++c) {
               uint32_t r[32];
               const uint32_t ta = tq + kColO + 32 * c;
               tmem_ld32(ta, r);
@@ -577,17 +596,17 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     const uint32_t gl = g + n - 1;
     fail = !mbar_wait(&B.p_empty[gl & 1u], (gl >> 1) & 1u, abort_flag) ||
            !mbar_wait(&B.item_done[slot], (it / kNIQ) & 1u, abort_flag);
-    const float l_tot = l + __shfl_xor_sync(0xffffffffu, l, 16);
+    const float l_half = l + __shfl_xor_sync(0xffffffffu, l, 16);
     if (lane < 16) {
-      s_l[h] = l_tot;
-      s_m[h] = m;
+      s_l[x * kTH + h] = l_half;
+      if (x == 0) s_m[h] = m;
     }
     if (wg_bar_or(fail)) break;
     tc_fence_after();
     const uint32_t stv = item_status[slot];
     const float oscale = s_ref * exp2f(-kPExp);  // O^T accumulates 2^(z - m) (s_t / s_ref) 2^kPExp * code
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 4 * x; c < 4 * x + 4; ++c) {
       uint32_t r[32];
       tmem_ld32(tq + kColO + 32 * c, r);
       const int dd = 128 * (c >> 1) + 32 * q + lane;  // value index of this thread's row
@@ -596,18 +615,18 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
         float *o = a.out + ((size_t)d.b * kTH + h0) * kTDv + dd;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          o[(size_t)i * kTDv] = stv ? 0.f : __uint_as_float(r[i]) * oscale / s_l[h0 + i];
+          o[(size_t)i * kTDv] = stv ? 0.f : __uint_as_float(r[i]) * oscale / (s_l[h0 + i] + s_l[kTH + h0 + i]);
       } else {
         float *o = a.part_o + ((size_t)d.cg * kTH + h0) * kTDv + dd;
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[(size_t)i * kTDv] = __uint_as_float(r[i]) * oscale;
       }
     }
-    if (d.nb != 1 && wt < kTH) a.part_ml[(size_t)d.cg * kTH + wt] = make_float2(s_m[wt], s_l[wt]);
+    if (d.nb != 1 && wt < kTH) a.part_ml[(size_t)d.cg * kTH + wt] = make_float2(s_m[wt], s_l[wt] + s_l[kTH + wt]);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(B.o_empty);
-    named_bar_sync(1, 128);  // the scratch is reused by the next item
+    named_bar_sync(1, kSmxThreads);  // the scratch is reused by the next item
     if (wt == 0) mbar_arrive(&B.item_empty[slot]);
     g += n;
   }
@@ -632,15 +651,15 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&B.s_full[i], 1);
-      mbar_init(&B.s_empty[i], 4);
-      mbar_init(&B.p_full[i], 4);
+      mbar_init(&B.s_empty[i], kSmxThreads / 32);
+      mbar_init(&B.p_full[i], kSmxThreads / 32);
       mbar_init(&B.p_empty[i], 2);  // a commit from each PV issuer
     }
     mbar_init(B.q_full, 1);
     mbar_init(B.q_empty, 1);
-    mbar_init(B.q_tfull, 4);
-    mbar_init(B.o_empty, 4);
-    mbar_init(B.r_done, 4);
+    mbar_init(B.q_tfull, kSmxThreads / 32);
+    mbar_init(B.o_empty, kSmxThreads / 32);
+    mbar_init(B.r_done, kSmxThreads / 32);
     mbar_init(B.drain, 3);  // one commit from each MMA issuer
     for (int i = 0; i < kNIQ; ++i) {
       mbar_init(&B.item_full[i], 1);
@@ -668,7 +687,7 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
   } else if (warp == 1) {
     if (lane == 0) tc_mma_qk(smem, B, items, tmem, abort_flag);
     __syncwarp();
-  } else if (warp >= 6) {
+  } else if (warp == 6 || warp == 7) {
     if (lane == 0) tc_mma_pv(smem, B, items, tmem, abort_flag, warp - 6);
     __syncwarp();
   } else {
