@@ -220,8 +220,10 @@ int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, const void 
  * quantized on the way in for an FP8 cache) and then attended over, together
  * with the rest of its context, as pfkv_paged_decode_attention_* does.  The
  * post's two halves of the decode pool ("Quantizing the KV cache": rows are
- * stored as FP8 and converted as they are read) in one call, so the new rows
- * are written by the same launch that plans the attention.
+ * stored as FP8 and converted as they are read) in one call: for the
+ * grouped-query layouts the attention kernel writes each (request, KV head)
+ * row itself, just before it copies the destination page; for the latent
+ * stream the launch that plans the attention writes them.
  *   k_new, v_new : bf16 [batch][num_kv_heads][head_dim]; row b goes to
  *                  logical position seq_lens[b] - 1 (seq_lens counts the new
  *                  token); v_new is ignored (may be NULL) for a kv_shared
@@ -232,7 +234,9 @@ int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, const void 
  * status[b] is the attention's status.  It covers every refusal of the
  * write: the write targets logical page (seq_lens[b] - 1) / page_size,
  * which the attention inspects under the same rules, and a refused row
- * writes nothing.  Distinct requests must not share a destination slot.
+ * writes nothing.  Distinct requests must not share a destination slot, and
+ * a request's destination page must not be read by another request of the
+ * same call (a page being appended to belongs to one request).
  */
 int pfkv_paged_decode_step(const pfkv_cache *cache, const void *k_new, const void *v_new, const void *q,
                            int32_t num_q_heads, const int32_t *seq_lens, const int32_t *block_table,

@@ -122,6 +122,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.part_o = reinterpret_cast<float *>(w + L.part_o);
   a.out = out; a.status = status;
   a.append = k_new != nullptr;
+  a.split_append = 0;
   a.k_new = static_cast<const uint16_t *>(k_new);
   a.v_new = static_cast<const uint16_t *>(v_new);
   a.cache = *c;

@@ -94,6 +94,39 @@ __device__ __forceinline__ float round16(float x) {
   else return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// Decode step, producer warp: the new token of (request, KV head g) goes to
+// slot `slot` of the page that lane `src` of the batch looked up, unless that
+// page is out of range or (tag check on) its tag does not match; the walk
+// reports those cases in the request's status as for any page.  Quantized
+// as the append does (x / s, RNE, satfinite; per-token s = amax / 448, or 1
+// for an all-zero row).  The stores are made visible to the tensor-copy
+// engine before the page is copied (proxy fence).
+template <bool kFp8, int kD>
+__device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, float s, bool has, int part, int k, int src,
+                                              int pid_lane, bool oob_lane, bool stale_lane, int g, int slot,
+                                              bool per_token) {
+  const int pid = __shfl_sync(0xffffffffu, pid_lane, src);
+  const bool refused = __shfl_sync(0xffffffffu, oob_lane || stale_lane, src);
+  if (refused) return;
+  const size_t row = ((size_t)pid * a.Hkv + g) * a.S + slot;
+  if constexpr (kFp8) {
+    if (per_token) {
+      float amax = amax8(v, 0.f);  // lanes without values hold zeros
+#pragma unroll
+      for (int o = 8; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+      if (has && k == 0) (part ? a.cache.v_scale : a.cache.k_scale)[row] = s;
+    }
+    if (has)
+      *reinterpret_cast<uint2 *>(reinterpret_cast<uint8_t *>(part ? a.cache.v_pool : a.cache.k_pool) + row * kD + k) =
+          e4m3x8(v, s);
+  } else {
+    if (has) *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(part ? a.cache.v_pool : a.cache.k_pool) + row * kD + k) = v;
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
 template <bool kFp8, int kD, int kG, int kNCW>
 __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, kD, kG, kNCW>::kMinBlocks)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -207,6 +240,20 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       const int *trow = a.block_table + (size_t)b * a.MP;
       const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
       uint32_t st_bits = 0;
+      // Decode step: the item holding the request's last page writes the new
+      // token's K and V rows of head g into that page before copying it.
+      // Lanes 0-15 hold 8 values each of the K row, lanes 16-31 of the V row,
+      // loaded now so that their latency hides behind the walk.
+      const int i_new = (L - 1) / S;
+      const bool has_new = a.split_append && p0 <= i_new && i_new < p1;
+      const int nv_part = lane >> 4, nv_k = (lane & 15) * 8;
+      const bool nv_lane = has_new && nv_k < kD;
+      uint4 nv = make_uint4(0u, 0u, 0u, 0u);
+      float nv_scale = 1.f;
+      if (nv_lane) {
+        nv = *reinterpret_cast<const uint4 *>((nv_part ? a.v_new : a.k_new) + ((size_t)b * a.Hkv + g) * kD + nv_k);
+        if (kFp8 && !per_token) nv_scale = __ldg(&(nv_part ? a.v_scale : a.k_scale)[g]);
+      }
       for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages) {
         const int i = i0 + lane;
         const bool valid = lane < batch_pages && i < p1;
@@ -217,6 +264,9 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           page_tag = __ldg(&a.page_tags[pid]);
           want_tag = __ldg(&tagrow[i]);
         }
+        if (has_new && i0 <= i_new && i_new < i0 + batch_pages)
+          write_new_row<kFp8, kD>(a, nv, nv_scale, nv_lane, nv_part, nv_k, i_new - i0, pid, oob,
+                                  page_tag != want_tag, g, (L - 1) % S, per_token);
         bool lane_ok = true;
         if (valid) {
           const uint32_t r = ring + (uint32_t)lane;
@@ -723,6 +773,11 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
   // more pieces (the plan falls back to longest-first items when the caps
   // leave too few ranges)
   a.balanced = a.max_splits >= 3 ? min(sh.grid / a.Hkv, kMaxRanges) : 0;
+  // decode step: the split kernel's producer writes the new tokens (the plan
+  // grid then needs no append blocks, which would hold SMs the split CTAs
+  // are waiting for)
+  a.split_append = a.append;
+  a.append = 0;
   int rc = cuda_ok(launch_plan(a, s, sh.grid * 8, (1024 + a.S - 1) / a.S), "plan kernel launch");
   if (rc) return rc;
   // The split kernel may start while the plan kernel runs; it waits for the

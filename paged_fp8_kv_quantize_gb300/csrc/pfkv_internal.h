@@ -55,10 +55,12 @@ struct DecodeArgs {
   float *part_o;
   float *out;
   uint32_t *status;
-  // decode step only (append == 1): new rows k_new / v_new [B][Hkv][D] bf16
-  // go to position seq_lens[b] - 1 of each request before attention; the
-  // plan grid writes them through `cache` (the same pools, writable).
-  int append;
+  // decode step only: new rows k_new / v_new [B][Hkv][D] bf16 go to
+  // position seq_lens[b] - 1 of each request before attention, through
+  // `cache` (the same pools, writable).  append == 1: the plan grid writes
+  // them; split_append == 1: the grouped-query split kernel's producer
+  // writes each (request, KV head)'s row just before it copies that page.
+  int append, split_append;
   const uint16_t *k_new, *v_new;
   pfkv_cache cache;
   // latent-stream path only (qprep == 1): the plan grid writes the query
