@@ -25,7 +25,7 @@ def _split(w):
     return ~last, k_new, v_new
 
 
-def _run(w, dtype, flags):
+def _run(w, dtype, flags, max_splits=None):
     hist, k_new, v_new = _split(w)
     mode = w.scale_mode if dtype == FP8 else synth.PER_HEAD
     # GPU: calibrate on all rows, append history, then the one-call step
@@ -39,7 +39,7 @@ def _run(w, dtype, flags):
                                run.table, run.tags, row_req=dev_i32(w.row_req[hist]), batch=w.batch)
     out, st = abi.paged_decode_step(run.cache, dev_bf16(k_new), None if v_new is None else dev_bf16(v_new), run.q,
                                     run.seq_lens, run.table, run.tags, w.softmax_scale, flags=flags,
-                                    max_splits=w.max_splits)
+                                    max_splits=w.max_splits if max_splits is None else max_splits)
     torch.cuda.synchronize()
     out = out.cpu().numpy().astype(np.float64)
     st = st.cpu().numpy().view(np.uint32)
@@ -86,6 +86,17 @@ def test_step_gqa(dtype, flags):
     st = _run(w, dtype, flags)
     if flags:
         assert st[2] == abi.ST_STALE_TAG and st[4] == abi.ST_STALE_TAG
+
+
+@pytest.mark.parametrize("max_splits", [1, 2])
+@pytest.mark.parametrize("dtype", [FP8, BF16])
+def test_step_gqa_longest_first_plan(dtype, max_splits):
+    # max_splits < 3: the longest-first plan, items from the work counter; the
+    # new rows are still written by the item that holds each last page
+    w = synth.make("step_lpt", 903, batch=len(LENS), q_heads=32, kv_heads=8, head_dim=128, page_size=16,
+                   seq_lens=LENS, stale_block_entries=[(2, 1)], outlier_p=0.01)
+    st = _run(w, dtype, abi.FLAG_TAG_CHECK, max_splits=max_splits)
+    assert st[2] == abi.ST_STALE_TAG
 
 
 def test_step_per_token_scales_and_oob_destination():
