@@ -92,3 +92,57 @@ def test_ragged_batch64_100_steps():
     assert aborted == stale_reqs
     assert np.array_equal(_pool_pages(run, used, "k").reshape(-1), c.k_pool.view(np.uint8))
     assert np.array_equal(_pool_pages(run, used, "v").reshape(-1), c.v_pool.view(np.uint8))
+
+
+def test_ragged_batch64_100_fused_steps():
+    """The benchmark's timed call: pfkv_paged_decode_step (the new token of
+    every request written by the attention kernel, then attention) for 100
+    steps; parity at steps 0, 1, 50 and 99, status of every checked step and
+    the final pool bytes bit-exact."""
+    w = synth.ragged()
+    run = GpuRun(w)
+    c, ctab, ctags, used = oracle_cache_subset(w, np.arange(w.batch))
+    B = w.batch
+    ws = torch.empty(abi.decode_workspace_bytes(run.cache, B, w.q_heads, w.max_splits), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(B, w.q_heads, w.head_dim, dtype=torch.float32, device="cuda")
+    st = torch.empty(B, dtype=torch.int32, device="cuda")
+    for j in range(w.steps):
+        pos = w.seq_lens.astype(np.int64) + j
+        abi.paged_decode_step(run.cache, dev_bf16(w.k_steps[j]), dev_bf16(w.v_steps[j]), dev_bf16(w.q_steps[j]),
+                              dev_i32(pos + 1), run.table, run.tags, w.softmax_scale, flags=FLAGS,
+                              max_splits=w.max_splits, workspace=ws, out=out, status=st)
+        c.append(w.k_steps[j], w.v_steps[j], pos, ctab, ctags, flags=oracle.FLAG_TAG_CHECK)
+        if j in (0, 1, 50, 99):
+            torch.cuda.synchronize()
+            o = out.cpu().numpy().astype(np.float64)
+            s = st.cpu().numpy().view(np.uint32)
+            o_ref, st_ref = c.decode(w.q_steps[j], pos + 1, ctab, ctags, w.softmax_scale,
+                                     flags=oracle.FLAG_TAG_CHECK, threads=16)
+            assert np.array_equal(s, st_ref), f"step status, step {j}"
+            assert not o[s != 0].any()
+            assert_close(o, o_ref, f"fused ragged step {j}")
+    torch.cuda.synchronize()
+    assert np.array_equal(_pool_pages(run, used, "k").reshape(-1), c.k_pool.view(np.uint8))
+    assert np.array_equal(_pool_pages(run, used, "v").reshape(-1), c.v_pool.view(np.uint8))
+
+
+def test_latent_full_size_sampled():
+    """The latent-stream workload at full size (64 requests, lengths
+    U[4096, 32768], 1.09 M tokens, per-token scales, tag check on), in the
+    benchmark's launch configuration: outputs of the two shortest and two
+    longest requests against the oracle, their pages' codes and per-token
+    scales bit-exact, no request aborted."""
+    w = synth.latent()
+    run = GpuRun(w)
+    out, st = run.decode(flags=FLAGS)
+    assert not st.any()
+    idx = _sample(w)
+    c, ctab, ctags, used = oracle_cache_subset(w, idx)
+    assert np.array_equal(_pool_pages(run, used, "k").reshape(-1), c.k_pool.view(np.uint8))
+    gsc = run.cache.k_scale.view(run.cache.P, run.cache.H, run.cache.S)[
+        torch.as_tensor(used, device="cuda", dtype=torch.long)].cpu().numpy().reshape(-1)
+    written = c.k_scale.reshape(-1) != 0
+    assert np.array_equal(gsc[written].view(np.uint32), c.k_scale.reshape(-1)[written].view(np.uint32))
+    o_ref, _ = c.decode(w.q[idx], w.seq_lens[idx], ctab, ctags, w.softmax_scale, flags=FLAGS, threads=16)
+    assert_close(out[idx], o_ref, "latent full size")
