@@ -98,7 +98,6 @@ __host__ __device__ constexpr TcSmem tc_smem() {
 }
 static_assert(tc_smem().total + 1024 <= 232448, "shared memory plan exceeds one SM");
 
-
 // Bounded wait that ignores the abort flag: used on the way out, so that a
 // block that gave up still lets its own copies and MMAs land before it exits.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
@@ -384,7 +383,7 @@ __device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const It
   drain_wait(B.drain, 0);
 }
 
-// ---------------------------------------------------------------- softmax warps (warps 2-5)
+// ---------------------------------------------------------------- softmax warps (warps 2-5 and 8-11)
 
 // Barrier `id` of `nthreads` threads that also ORs a flag over them.
 __device__ __forceinline__ bool bar_or(int id, int nthreads, bool v) {
