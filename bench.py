@@ -126,6 +126,16 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def fp8_dense_peak_tflops():
+    """Dense e4m3 tensor peak: the measured bf16 GEMM burst figure times the
+    nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s), or the fallback bf16 figure."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "measured bf16 x 2"
+    return 2.0 * 1900.0, "fallback bf16 x 2"
+
+
 def global_max(value, dist=None, device="cpu"):
     """Max of a per-rank float over all ranks (the job's time is its slowest rank)."""
     if dist is None:
@@ -266,11 +276,21 @@ def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
     pages = int(((wl.seq_lens.astype(np.int64) + S - 1) // S).sum())
     nbytes = tokens * (wl.head_dim + 4) + pages * 12 + q.numel() * 2 + out.numel() * 4
     flops = tokens * wl.q_heads * (wl.head_dim + wl.v_head_dim) * 2
+    # The tensor cores run e4m3 MMAs over whole pages: S = [T1; T2] K^T (two
+    # query terms, 128 rows x 576) and O^T += V^T (P1 + P2 + P3)^T (three
+    # probability terms, 512 values x 64 heads).
+    mma_flops = pages * S * (2 * 2 * wl.q_heads * wl.head_dim + 2 * 3 * wl.q_heads * wl.v_head_dim)
+    tpeak, tpeak_kind = fp8_dense_peak_tflops()
+    tach = mma_flops / (ms * 1e-3) / 1e12
     return {"workload": "latent-shared stream: batch 64, lengths U[4096, 32768], 64 q heads over one 576-wide "
                         "FP8 stream (V = first 512), per-token scales, page 64, tag check on",
             "us_per_call": ms * 1e3, "kv_gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak,
             "tflops": flops / (ms * 1e-3) / 1e12, "context_tokens": tokens, "alg_bytes_per_call": nbytes,
-            "decode_tokens_per_s": B / (ms * 1e-3), "aborted_requests": int((st.cpu().numpy() != 0).sum())}
+            "decode_tokens_per_s": B / (ms * 1e-3), "aborted_requests": int((st.cpu().numpy() != 0).sum()),
+            "roofline": {"bound": "tensor", "kernel": "latent_tc_kernel (plan + kernel + merge)", "achieved": tach,
+                         "peak": tpeak, "peak_kind": tpeak_kind, "unit": "TFLOP/s", "frac": tach / tpeak,
+                         "mma_flops_per_call": mma_flops,
+                         "what": "executed e4m3 MMA work (query terms x2, probability terms x3, whole pages)"}}
 
 
 
