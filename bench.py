@@ -581,7 +581,16 @@ def main():
         h_res.copy_(d_res, non_blocking=True)
 
     g_e2e = capture(e2e_step, K)
+    # the replayed graph must move the bytes: poison the device input and the
+    # host result, replay, and check both copies happened
+    d_in.fill_(0xFF)
+    h_res.zero_()
+    torch.cuda.synchronize()
     g_e2e.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(d_in.cpu(), h_in[(K - 1) % T]), "end-to-end graph did not copy the step inputs"
+    assert torch.equal(h_res, d_res.cpu()), "end-to-end graph did not copy the step results back"
+    assert h_res.any(), "end-to-end graph left the host result empty"
     ms_e2e = time_graph(g_e2e)
     e2e_val = job_throughput(sum(step_bytes), world, ms_e2e) / 1e9
     h2d = int(offs[-1])
