@@ -20,6 +20,7 @@ DTYPE_FP8_E4M3 = 1
 SCALE_PER_HEAD = 0
 SCALE_PER_TOKEN = 1
 FLAG_TAG_CHECK = 1
+FLAG_TEST_WITHHOLD = 0x80000000  # test hook: the grouped-query decode's abort path (see pfkv.h)
 ST_STALE_TAG = 1
 ST_PAGE_OOB = 2
 ST_BAD_LEN = 4

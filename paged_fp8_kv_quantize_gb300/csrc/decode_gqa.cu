@@ -127,6 +127,14 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, floa
   __syncwarp();
 }
 
+// Bounded wait that ignores the abort flag: the page loader's way out, so
+// that a block that gave up still lets its own copies land before it exits.
+__device__ __forceinline__ void drain_wait_full(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+}
+
 template <bool kFp8, int kD, int kG, int kNCW>
 __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, kD, kG, kNCW>::kMinBlocks)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -202,6 +210,10 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       return v;
     };
     int item = 0, item_next = 0;
+    // the last batch's first ring position, and whether this lane's page of
+    // it was issued (every page of earlier batches was)
+    uint32_t last_first = 0;
+    bool last_issued = false;
     if (lane == 0) item = claim();
     item = __shfl_sync(0xffffffffu, item, 0);
     int4 info = make_int4(0, 0, 0, 0), info2 = make_int4(0, 0, 0, 0);
@@ -225,11 +237,14 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       }
       const int cg = item / a.Hkv, g = item - cg * a.Hkv;
       const int b = info.x, p0 = info.y, p1 = info.z, L = info.w;
+      // test hook (PFKV_FLAG_TEST_WITHHOLD): the first CTA never hands its
+      // first item to the consumers, whose bounded wait then gives up
+      const bool withhold = (a.flags & PFKV_FLAG_TEST_WITHHOLD) && blockIdx.x == 0 && iq == 0;
       if (lane == 0) {
         ItemDesc d;
         d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = info2.x;
         items[slot] = d;
-        mbar_arrive(&item_full[slot]);
+        if (!withhold) mbar_arrive(&item_full[slot]);
       }
       item_next = __shfl_sync(0xffffffffu, item_next, 0);
       int4 info_next = make_int4(0, 0, 0, 0), info2_next = make_int4(0, 0, 0, 0);
@@ -255,6 +270,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         if (kFp8 && !per_token) nv_scale = __ldg(&(nv_part ? a.v_scale : a.k_scale)[g]);
       }
       for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages) {
+        last_first = ring;
         const int i = i0 + lane;
         const bool valid = lane < batch_pages && i < p1;
         const int pid = valid ? __ldg(&trow[i]) : 0;
@@ -294,6 +310,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           }
         }
         ring += (uint32_t)min(batch_pages, p1 - i0);
+        last_issued = valid && lane_ok;
         ok = __all_sync(0xffffffffu, lane_ok);
         if (__any_sync(0xffffffffu, oob)) st_bits |= PFKV_ST_PAGE_OOB;
         if (__any_sync(0xffffffffu, page_tag != want_tag)) st_bits |= PFKV_ST_STALE_TAG;
@@ -306,6 +323,16 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       item = item_next;
       info = info_next;
       info2 = info2_next;
+    }
+    // Copies still in flight land before the block may exit (the consumers
+    // wait for every page they use, but on the abort path they leave early):
+    // lane k waits for the k-th of the last nst pages issued.
+    if (__shfl_sync(0xffffffffu, (int)(*abort_flag != 0), 0)) {
+      const bool have = lane < nst && ring >= (uint32_t)(nst - lane);
+      const uint32_t r = ring - (uint32_t)nst + (uint32_t)lane;  // meaningful when have
+      const bool in_last = have && r >= last_first;            // then r - last_first < batch_pages
+      const bool src_issued = __shfl_sync(0xffffffffu, last_issued, in_last ? (int)(r - last_first) : 0);
+      if (have && (!in_last || src_issued)) drain_wait_full(&full[r % (uint32_t)nst], (r / (uint32_t)nst) & 1u);
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -338,7 +365,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
 
     for (uint32_t iq = 0;; ++iq) {
       const uint32_t slot = iq % kNIQ;
-      if (!mbar_wait(&item_full[slot], (iq / kNIQ) & 1u, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&item_full[slot], (iq / kNIQ) & 1u, abort_flag))) break;
       const ItemDesc d = items[slot];
       if (d.b < 0) break;
 
@@ -426,6 +453,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           live[t] = valid[t] && tok_base[t] < d.L;
           tbase[t] = smem_base + stg[t] * sp.stage_bytes + (uint32_t)(mt_in_page * 16 * C::kRowBytes);
         }
+        alive = __all_sync(0xffffffffu, alive);  // the whole warp leaves together
         if (!alive) break;
         // ---- S = K q^T for both tiles
         float z[2][4];
