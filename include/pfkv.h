@@ -48,10 +48,10 @@ enum { PFKV_DTYPE_BF16 = 0, PFKV_DTYPE_FP8_E4M3 = 1 };
 enum { PFKV_SCALE_PER_HEAD = 0, PFKV_SCALE_PER_TOKEN = 1 };
 
 /* Call flags.  TAG_CHECK enables the page-tag comparison; it is off unless
- * set, as in the post.  TEST_WITHHOLD is a test hook for the grouped-query
- * decode, never set in normal use: the first CTA's page loader withholds its
- * first work item from the compute warps, whose bounded wait then runs out
- * (about 2 s); every request of the call reports PFKV_ST_TIMEOUT and the
+ * set, as in the post.  TEST_WITHHOLD is a test hook for the decode
+ * kernels, never set in normal use: the first CTA's page loader withholds
+ * its first work item from the other warps, whose bounded wait then runs
+ * out (about 2 s); every request of the call reports PFKV_ST_TIMEOUT and the
  * context stays usable.  It exercises the abort path without a fault. */
 enum { PFKV_FLAG_TAG_CHECK = 1u, PFKV_FLAG_TEST_WITHHOLD = 0x80000000u };
 

@@ -228,18 +228,19 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       if (lane == 0) ok = mbar_wait(&item_empty[slot], ((iq / kNIQ) & 1u) ^ 1u, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      // test hook (PFKV_FLAG_TEST_WITHHOLD): the first CTA never hands its
+      // first item (or its end marker) to the consumers, whose bounded wait
+      // then gives up
+      const bool withhold = (a.flags & PFKV_FLAG_TEST_WITHHOLD) && blockIdx.x == 0 && iq == 0;
       if (item >= n_items) {
         if (lane == 0) {
           items[slot].b = -1;
-          mbar_arrive(&item_full[slot]);
+          if (!withhold) mbar_arrive(&item_full[slot]);
         }
         break;
       }
       const int cg = item / a.Hkv, g = item - cg * a.Hkv;
       const int b = info.x, p0 = info.y, p1 = info.z, L = info.w;
-      // test hook (PFKV_FLAG_TEST_WITHHOLD): the first CTA never hands its
-      // first item to the consumers, whose bounded wait then gives up
-      const bool withhold = (a.flags & PFKV_FLAG_TEST_WITHHOLD) && blockIdx.x == 0 && iq == 0;
       if (lane == 0) {
         ItemDesc d;
         d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = info2.x;

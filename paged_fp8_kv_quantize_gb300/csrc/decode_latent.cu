@@ -166,10 +166,14 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
     bool w = true;
     if (lane == 0) w = mbar_wait(&B.item_empty[slot], ((it / kNIQ) & 1u) ^ 1u, abort_flag);
     if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+    // test hook (PFKV_FLAG_TEST_WITHHOLD): the first CTA never hands its
+    // first item (or its end marker) to the other warps, whose bounded waits
+    // then give up
+    const bool withhold = (a.flags & PFKV_FLAG_TEST_WITHHOLD) && blockIdx.x == 0 && it == 0;
     if (item >= n_items) {
       if (lane == 0) {
         items[slot].b = -1;
-        mbar_arrive(&B.item_full[slot]);
+        if (!withhold) mbar_arrive(&B.item_full[slot]);
       }
       break;
     }
@@ -179,7 +183,7 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
       ItemDesc d;
       d.b = b; d.cg = item; d.g = 0; d.p0 = p0; d.p1 = p1; d.L = info.w; d.ring = g; d.nb = info2.x;
       items[slot] = d;
-      mbar_arrive(&B.item_full[slot]);
+      if (!withhold) mbar_arrive(&B.item_full[slot]);
       // the last 64 columns of the request's query terms (the A operand of
       // the last two QK^T steps), once the previous item's last QK^T is done
       if (mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag)) {
