@@ -126,23 +126,3 @@ def test_ragged_batch64_100_fused_steps():
     assert np.array_equal(_pool_pages(run, used, "k").reshape(-1), c.k_pool.view(np.uint8))
     assert np.array_equal(_pool_pages(run, used, "v").reshape(-1), c.v_pool.view(np.uint8))
 
-
-def test_latent_full_size_sampled():
-    """The latent-stream workload at full size (64 requests, lengths
-    U[4096, 32768], 1.09 M tokens, per-token scales, tag check on), in the
-    benchmark's launch configuration: outputs of the two shortest and two
-    longest requests against the oracle, their pages' codes and per-token
-    scales bit-exact, no request aborted."""
-    w = synth.latent()
-    run = GpuRun(w)
-    out, st = run.decode(flags=FLAGS)
-    assert not st.any()
-    idx = _sample(w)
-    c, ctab, ctags, used = oracle_cache_subset(w, idx)
-    assert np.array_equal(_pool_pages(run, used, "k").reshape(-1), c.k_pool.view(np.uint8))
-    gsc = run.cache.k_scale.view(run.cache.P, run.cache.H, run.cache.S)[
-        torch.as_tensor(used, device="cuda", dtype=torch.long)].cpu().numpy().reshape(-1)
-    written = c.k_scale.reshape(-1) != 0
-    assert np.array_equal(gsc[written].view(np.uint32), c.k_scale.reshape(-1)[written].view(np.uint32))
-    o_ref, _ = c.decode(w.q[idx], w.seq_lens[idx], ctab, ctags, w.softmax_scale, flags=FLAGS, threads=16)
-    assert_close(out[idx], o_ref, "latent full size")
