@@ -53,6 +53,11 @@ def test_argument_errors_return_before_any_cuda_call():
     assert f(ctypes.byref(unal), *args_tail) == -6  # misaligned pool
     g = abi.lib.pfkv_kv_append_quantize
     assert g(None, None, None, 0, None, None, None, None, 1, 1, 0, None, None) == -1
+    # an empty batch is a valid call that enqueues nothing (no CUDA call is made)
+    ok = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None)
+    empty_tail = [None, 32, None, None, None, 0, 8, 1.0, 0, 64, None, 0, None, None, None]
+    assert f(ctypes.byref(ok), *empty_tail) == 0
+    assert g(ctypes.byref(ok), None, None, 0, None, None, None, None, 0, 1, 0, None, None) == 0
 
 
 def test_page_allocator_host_checks():
