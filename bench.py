@@ -263,8 +263,8 @@ def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
     out = torch.empty(B, wl.q_heads, wl.v_head_dim, dtype=torch.float32, device=dev)
     st = torch.empty(B, dtype=torch.int32, device=dev)
 
-    def call(_):
-        abi.paged_decode_attention_fp8(cache, q, lens, table, tags, wl.softmax_scale, flags=abi.FLAG_TAG_CHECK,
+    def call(_, flags=abi.FLAG_TAG_CHECK):
+        abi.paged_decode_attention_fp8(cache, q, lens, table, tags, wl.softmax_scale, flags=flags,
                                        max_splits=wl.max_splits, workspace=ws, out=out, status=st)
 
     for _ in range(3):
@@ -272,6 +272,13 @@ def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
     g = capture(call, n_calls)
     g.replay()
     ms = time_graph(g) / n_calls
+    # tag check on / off, alternated (all tags valid)
+    g_off = capture(lambda j: call(j, flags=0), n_calls)
+    g_off.replay()
+    ratios = []
+    for _ in range(5):
+        a, b = time_graph(g), time_graph(g_off)
+        ratios.append(a / b)
     tokens = int(wl.seq_lens.astype(np.int64).sum())
     pages = int(((wl.seq_lens.astype(np.int64) + S - 1) // S).sum())
     nbytes = tokens * (wl.head_dim + 4) + pages * 12 + q.numel() * 2 + out.numel() * 4
@@ -287,6 +294,7 @@ def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
             "us_per_call": ms * 1e3, "kv_gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak,
             "tflops": flops / (ms * 1e-3) / 1e12, "context_tokens": tokens, "alg_bytes_per_call": nbytes,
             "decode_tokens_per_s": B / (ms * 1e-3), "aborted_requests": int((st.cpu().numpy() != 0).sum()),
+            "tag_check_ratio_on_over_off": statistics.median(ratios),
             "roofline": {"bound": "tensor", "kernel": "latent_tc_kernel (plan + kernel + merge)", "achieved": tach,
                          "peak": tpeak, "peak_kind": tpeak_kind, "unit": "TFLOP/s", "frac": tach / tpeak,
                          "mma_flops_per_call": mma_flops,
