@@ -484,6 +484,39 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     if (lane == 0) mbar_arrive(B.q_tfull);
     const float cq = __ldg(&a.qfac[(size_t)d.b * kTH + h]);
     float m = kNegInf, l = 0.f, s_ref = 0.f;
+    // Rescale hand-off for page gq (not an item's first page): once every
+    // warp's P^T and scale factors for it are in, if any head asked for it,
+    // scale this warp's share of O^T (its quarter's lanes, columns 128 x ..
+    // 128 x + 127) by beta_h per head column, after the previous page's PV
+    // and before this page's.  Checked one page late, so that the softmax
+    // warps need not wait for one another on every page: the PV of a page
+    // that needs it waits for this hand-off, and the buffers it reads are
+    // reused only after that PV.
+    auto rescale_check = [&](uint32_t gq, bool &fl) {
+      const uint32_t sq = gq & 1u;
+      if (fl) return;
+      fl = __any_sync(0xffffffffu, !mbar_wait(&B.p_full[sq], (gq >> 1) & 1u, abort_flag));
+      if (fl || resc_tag[sq] != gq + 1u) return;
+      fl = __any_sync(0xffffffffu, !mbar_wait(&B.p_empty[(gq - 1) & 1u], ((gq - 1) >> 1) & 1u, abort_flag));
+      if (!fl) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 4 * x; c < 4 * x + 4; ++c) {
+          uint32_t r[32];
+          const uint32_t ta = tq + kColO + 32 * c;
+          tmem_ld32(ta, r);
+          const float *bt = s_beta + sq * kTH + 32 * (c & 1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bt[i]);
+          tmem_st32(ta, r);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(B.r_done);
+      ++n_resc;
+    };
     for (uint32_t j = 0; j < n; ++j) {
       const uint32_t gp = g + j, sb = gp & 1u, st = gp % kNst;
       if (!fail)
@@ -565,35 +598,10 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.p_full[sb]);
-      if (j > 0) {
-        // Rescale hand-off: once every warp's P^T and scale factors for this
-        // page are in, if any head asked for it, scale this warp's share of
-        // O^T (its quarter's lanes, columns 128 x .. 128 x + 127) by beta_h
-        // per head column, after the previous page's PV and before this page's.
-        fail = __any_sync(0xffffffffu, !mbar_wait(&B.p_full[sb], (gp >> 1) & 1u, abort_flag));
-        if (!fail && resc_tag[sb] == gp + 1u) {
-          fail = __any_sync(0xffffffffu, !mbar_wait(&B.p_empty[(gp - 1) & 1u], ((gp - 1) >> 1) & 1u, abort_flag));
-          if (!fail) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 4 * x; c < 4 * x + 4; ++c) {
-              uint32_t r[32];
-              const uint32_t ta = tq + kColO + 32 * c;
-              tmem_ld32(ta, r);
-              const float *bt = s_beta + sb * kTH + 32 * (c & 1);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * bt[i]);
-              tmem_st32(ta, r);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(B.r_done);
-          ++n_resc;
-        }
-      }
+      // the previous page's rescale, now that this page's P^T is out
+      if (j > 1) rescale_check(g + j - 1, fail);
     }
+    if (n > 1) rescale_check(g + n - 1, fail);  // the item's last page
     if (wg_bar_or(fail)) break;
     // ---- the item's result: wait for its last PV and its status
     const uint32_t gl = g + n - 1;
