@@ -99,6 +99,19 @@ def test_step_gqa_longest_first_plan(dtype, max_splits):
     assert st[2] == abi.ST_STALE_TAG
 
 
+@pytest.mark.parametrize("dtype", [FP8, BF16])
+@pytest.mark.parametrize("shape", [(8, 1, 128, 64), (4, 2, 64, 16), (2, 4, 64, 32)])
+def test_step_other_shapes(dtype, shape):
+    # group sizes 8 and 2, head width 64, pages of 64 and 32 tokens: the new
+    # rows are written by the item holding each request's last page
+    G, Hkv, D, S = shape
+    lens = [1, S, S + 1, 3 * S - 1, 2000, 5000]
+    w = synth.make("step_shapes", 904 + G, batch=len(lens), q_heads=G * Hkv, kv_heads=Hkv, head_dim=D,
+                   page_size=S, seq_lens=lens, stale_block_entries=[(4, 1)], outlier_p=0.01)
+    st = _run(w, dtype, abi.FLAG_TAG_CHECK)
+    assert st[4] == abi.ST_STALE_TAG
+
+
 def test_step_per_token_scales_and_oob_destination():
     w = synth.make("step_tok", 901, batch=6, q_heads=16, kv_heads=2, head_dim=64, page_size=16,
                    seq_lens=[1, 65, 200, 1000, 16, 3000], scale_mode=synth.PER_TOKEN)
