@@ -383,6 +383,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-frac", type=float, default=0.5, help="share of context tokens in the CPU sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="minimum wall time of the CPU oracle leg (whole steps are repeated until it is reached)")
     ap.add_argument("--no-variants", action="store_true", help="skip the BF16 / tag-off comparisons")
     ap.add_argument("--no-latent", action="store_true", help="skip the latent-stream measurement")
     args = ap.parse_args()
@@ -609,10 +611,13 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         stepc, threads, desc, nb = oracle_step_sample(w, args.cpu_frac)
         t0 = time.perf_counter()
-        tot = stepc()
+        tot, n_cpu = 0, 0
+        while n_cpu == 0 or time.perf_counter() - t0 < args.cpu_seconds:
+            tot += stepc()
+            n_cpu += 1
         dt = time.perf_counter() - t0
-        cpu = {"value": tot / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
-               "seconds": dt}
+        cpu = {"value": tot / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n_cpu} consecutive steps over {desc}", "seconds": dt}
 
     st_final = st_dec.cpu().numpy()
     launches_per_step = 3  # plan (+ append blocks), split, merge kernels
