@@ -453,7 +453,7 @@ def main():
     FLAGS = abi.FLAG_TAG_CHECK
 
     def step(cache, j, flags=FLAGS, do_append=True):
-        """One decode step: the fused call (new tokens appended by the plan grid, then attention)."""
+        """One decode step: the fused call (new tokens written by the split kernel's page loader, then attention)."""
         j %= T
         if do_append:
             abi.paged_decode_step(cache, k_steps[j], v_steps[j], q_steps[j], len_steps[j], table, tags,
@@ -506,7 +506,7 @@ def main():
     value = job_throughput(sum(step_bytes), world, ms_step) / 1e9
     dec_bytes = [decode_alg_bytes(lens0 + j % T + 1, Hkv, D, S, Hq, D) for j in range(K)]
 
-    # ---- dominant kernel group: decode alone (plan + split + merge), same stream
+    # ---- dominant kernel group: decode alone (split + merge), same stream
     g_dec = capture(lambda j: step(fp8, j, do_append=False), K)
     g_dec.replay()
     ms_dec = time_graph(g_dec) / K
@@ -620,7 +620,7 @@ def main():
                "sample": f"{n_cpu} consecutive steps over {desc}", "seconds": dt}
 
     st_final = st_dec.cpu().numpy()
-    launches_per_step = 3  # plan (+ append blocks), split, merge kernels
+    launches_per_step = 2  # split (page loader also appends the new tokens), merge kernels
     mean_lens = lens0 + (K - 1) % T + 1
     res = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -633,7 +633,7 @@ def main():
         "kv_tokens_per_s": world * float(mean_lens.sum()) / (ms_per_step * 1e-3),
         "hbm_frac_step": value / world / peak,
         "aborted_requests": int((st_final != 0).sum()),
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention_fp8 (plan + split + merge kernels)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention_fp8 (split + merge kernels)",
                      "achieved": dec_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": dec_gbs / peak, "us_per_launch": ms_dec * 1e3,
                      "alg_bytes_per_launch": statistics.mean(dec_bytes), "traffic": recorded_traffic(),

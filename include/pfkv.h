@@ -26,7 +26,9 @@
  *  - Per-request data faults (stale tag, page id outside the pool, bad
  *    length) are reported in status[batch] (uint32 bit set, PFKV_ST_*), which
  *    every call overwrites.  They never trap on the device.
- *  - An aborted request's attention output rows are all zero.
+ *  - The attention output rows of a request with a data fault (STALE_TAG,
+ *    PAGE_OOB, BAD_LEN) are all zero; under TIMEOUT the output of the call
+ *    is not valid.
  *  - Results are deterministic for identical inputs.
  */
 #ifndef PFKV_H
@@ -162,7 +164,8 @@ size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32
  *   out[b][h] = sum_t p_t v^[g][t],  where k^, v^ are the dequantized rows
  *   (code value * scale for FP8).
  * Only logical pages i < ceil(L_b / page_size) are inspected.  A request
- * with any status bit gets zero output.  max_splits (1..256) bounds how many
+ * with a data-fault bit gets zero output.  batch * max_pages may not exceed
+ * 2^40 (PFKV_ERR_SHAPE).  max_splits (1..256) bounds how many
  * pieces one request's context is split into (flash-decoding); the pieces
  * are merged with the log-sum-exp rule.  workspace must hold
  * pfkv_decode_workspace_bytes(cache, batch, num_q_heads, max_splits) bytes;
@@ -205,10 +208,11 @@ int pfkv_paged_decode_attention_bf16(const pfkv_cache *cache, const void *q, int
  *  - The first call on each device looks up the buffer's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before any stream capture.
- *  - Every call shares the one buffer, which keeps the last call's contents;
- *    the kernels reset what must start at zero themselves.  Calls that
- *    overlap on the GPU (different streams, or different host threads, at
- *    the same time) race on the buffer and give wrong results.
+ *  - Every call shares the one buffer, which keeps the last call's
+ *    contents; every word a call reads back is written earlier in the same
+ *    call.  Calls that overlap on the GPU (different streams, or different
+ *    host threads, at the same time) race on the buffer and give wrong
+ *    results.
  */
 #define PFKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -48,7 +48,9 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool laten
   w.cta_first = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
   w.part_ml = w.cta_first + up256(sizeof(int) * (kMaxRanges + 1));
   w.part_o = w.part_ml + up256(sizeof(float2) * slots);
-  w.qterms = w.part_o + up256(sizeof(float) * slots * v_dim);
+  w.part_st = w.part_o + up256(sizeof(float) * slots * v_dim);
+  w.cta_abort = w.part_st + up256(sizeof(uint32_t) * (size_t)batch * max_splits);
+  w.qterms = w.cta_abort + up256(sizeof(int) * (size_t)kMaxCtas);
   w.qfac = w.qterms + (latent ? up256(kLatentQTermBytes * (size_t)batch) : 0);
   w.total = w.qfac + (latent ? up256(sizeof(float) * (size_t)batch * q_heads) : 0);
   return w;
@@ -92,6 +94,8 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   if (rc) return rc;
   if (c->dtype != want_dtype) return PFKV_ERR_DTYPE;
   if (batch < 0 || max_pages < 1 || Hq < 1 || max_splits < 1 || max_splits > 256) return PFKV_ERR_SHAPE;
+  // the kernels' page arithmetic assumes at most 2^40 pages in one call
+  if ((uint64_t)batch * (uint64_t)max_pages > (1ull << 40)) return PFKV_ERR_SHAPE;
   if (!isfinite(softmax_scale)) return PFKV_ERR_SHAPE;
   if (batch == 0) return PFKV_OK;
   if (!q || !seq_lens || !block_table || !out || !status || !ws) return PFKV_ERR_NULL;
@@ -129,6 +133,13 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.qprep = 0;
   a.balanced = 0;
   a.cta_first = reinterpret_cast<int *>(w + L.cta_first);
+  a.self_plan = 0;
+  a.ranges = 0;
+  a.target_items = 0;
+  a.min_chunk_pages = 1;
+  a.n_ctas = 0;
+  a.part_st = reinterpret_cast<uint32_t *>(w + L.part_st);
+  a.cta_abort = reinterpret_cast<int *>(w + L.cta_abort);
   a.qterms = w + L.qterms;
   a.qfac = reinterpret_cast<float *>(w + L.qfac);
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -7,33 +7,32 @@
 // page's tag is compared with the mapping's tag before its data may be
 // returned; a mismatch aborts the request.
 //
-// Kernels (all on the caller's stream):
-//   1. plan   -- one CTA: validates lengths, zeroes status, splits every
-//                request into page-aligned chunks (flash-decoding) and
-//                writes the chunk prefix into the workspace.
-//   2. split  -- persistent CTAs, one producer warp + NCW consumer warps.
-//                The producer takes work items (request, chunk, KV head):
-//                under the balanced plan the chunks of one equal page
-//                range for one KV head, otherwise from a device counter
-//                (longest request first).  It walks the chunk's page-table
-//                entries 32 at a time, bounds-checks every page id before
-//                any fetch, compares tags off the critical path (the tag
-//                load is issued next to the page copy; a mismatch only sets
-//                the request's status bit), and stages whole (page, head)
-//                K and V slices into a shared-memory ring with TMA tensor
-//                copies (128-byte swizzle).  Consumer warps take 16-token
-//                tiles: e4m3 -> f16 in registers (exact), QK^T and PV on
-//                register-operand tensor-core MMA, online softmax in fp32.
-//                An item that covers a whole request writes its output
-//                directly; otherwise it leaves an unnormalised partial
-//                (m, l, O).
-//   3. merge  -- one CTA per (request, KV head, block of 64 float4
-//                columns) with more than one split: log-sum-exp merge of
-//                the partials, split weights staged in shared memory and
-//                splits spread over thread groups.
-//   A request with any status bit gets zero output.  The split and merge
-//   kernels are programmatic dependents of the kernel before them, so their
-//   launch and prologue overlap it.
+// Kernels (both on the caller's stream; no plan kernel):
+//   1. split  -- persistent CTAs, one producer warp + NCW consumer warps.
+//                Each CTA works out its own pieces from the lengths (see
+//                "work split" below): CTA k * Hkv + h takes page range k of
+//                the requests' concatenated pages for KV head h.  The
+//                producer walks a piece's page-table entries 32 at a time,
+//                bounds-checks every page id before any fetch, compares tags
+//                off the critical path (the tag load is issued next to the
+//                page copy; a mismatch only sets the piece's status bits),
+//                and stages whole (page, head) K and V slices into a
+//                shared-memory ring with TMA tensor copies (128-byte
+//                swizzle).  Consumer warps take 16-token tiles: e4m3 -> f16
+//                in registers (exact), QK^T and PV on register-operand
+//                tensor-core MMA, online softmax in fp32.  A piece that
+//                covers a whole request writes its output directly;
+//                otherwise it leaves an unnormalised partial (m, l, O).
+//   2. merge  -- one CTA per (request, KV head, block of 64 float4
+//                columns): writes each request's status (the bits its
+//                pieces found, a bad length, or a timeout anywhere in the
+//                split grid), zeroes the rows of a faulted request, and
+//                merges the partials of a request cut into several pieces
+//                by the log-sum-exp rule, split weights staged in shared
+//                memory and splits spread over thread groups.
+//   A request with a data-fault bit gets zero output.  Each kernel is a
+//   programmatic dependent of the kernel before it, so its launch and
+//   prologue overlap that kernel's tail.
 #include <math.h>
 
 #include <mutex>
@@ -127,6 +126,229 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, floa
   __syncwarp();
 }
 
+// ---------------------------------------------------------------- work split
+//
+// There is no plan kernel on this path: every CTA works out its own share
+// from the lengths, and all CTAs reach the same answer.  The requests' pages,
+// concatenated in request order (T pages in all, a request with a bad length
+// counting none), are cut into R ranges [floor(kT/R), floor((k+1)T/R)); CTA
+// k * Hkv + h takes range k for KV head h.  Pieces of a request are numbered
+// consecutively in request order over the whole call (the merge finds a
+// request's pieces at split_first[b] .. + split_count[b]).  Two rules:
+//  - cut: a piece is the part of one request inside one range, so every
+//    CTA gets the same number of pages to within one.  R is capped so that
+//    no request is cut into more than max_splits pieces (a request of p
+//    pages meets at most ceil(p R / T) + 1 ranges); the rule is used when
+//    max_splits >= 3 and the caps leave at least 3/4 of the CTA groups.
+//  - chunk: each request is first cut into at most max_splits chunks of
+//    about cp pages; a range takes the chunks that start inside it.  Used
+//    for small batches (T below the number of CTA groups) and batches whose
+//    longest request the split cap would otherwise leave on few CTAs.
+struct WorkSplit {
+  long long T, R, r0, r1, cp, max_len;
+  int k, chunks;
+  // walk: next request to look at, its first page in the concatenation, the
+  // number of its first piece, and (chunk rule) its next chunk
+  int b;
+  long long off, first, c;
+};
+
+struct Piece {
+  int b, cg, p0, p1, L, nb;
+  bool lead;  // the request's first piece: its CTA of head 0 records the numbering
+};
+
+// floor(x / y) for 0 <= x < 2^53 and y >= 1, with no call to a 64-bit
+// division routine (the entry points bound batch * max_pages by 2^40, and
+// every dividend here is at most 2^12 times a page count).  A reciprocal
+// estimate (rcp.approx.f64) refined by two Newton-Raphson steps
+// r <- r (2 - y r) is close to full double precision, so x * r is within a
+// few units of the quotient; the exact integer remainder then corrects it.
+// The correction steps are bounded (16, against at most about 4 needed); a
+// result left wrong by a violated precondition is caught by the callers'
+// bounds checks rather than looping.
+__device__ __forceinline__ long long div_floor(long long x, long long y) {
+  const double yd = (double)y;
+  double r;
+  asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(yd));
+  r = fma(r, fma(-yd, r, 1.0), r);
+  r = fma(r, fma(-yd, r, 1.0), r);
+  long long q = (long long)((double)x * r);
+  long long rem = x - q * y;
+  for (int i = 0; i < 16 && rem < 0; ++i) {
+    --q;
+    rem += y;
+  }
+  for (int i = 0; i < 16 && rem >= y; ++i) {
+    ++q;
+    rem -= y;
+  }
+  return q;
+}
+
+__device__ __forceinline__ int ws_pages(const WorkSplit &w, int L, int S) {
+  return (L < 1 || (long long)L > w.max_len) ? 0 : (int)(((unsigned)L + (unsigned)S - 1u) / (unsigned)S);
+}
+
+// Pieces of a request of p > 0 pages whose first page is page `off` of the
+// concatenation; *ppc: chunk length (chunk rule only).
+__device__ __forceinline__ int ws_count(const WorkSplit &w, long long off, int p, int max_splits, int *ppc) {
+  if (!w.chunks) return (int)(div_floor((off + p) * w.R - 1, w.T) - div_floor((off + 1) * w.R - 1, w.T) + 1);
+  int nn = w.cp >= p ? 1 : (int)(((unsigned)p + (unsigned)w.cp - 1u) / (unsigned)w.cp);
+  if (nn > max_splits) nn = max_splits;
+  const int q = (int)(((unsigned)p + (unsigned)nn - 1u) / (unsigned)nn);
+  *ppc = q;
+  return (int)(((unsigned)p + (unsigned)q - 1u) / (unsigned)q);
+}
+
+// Warp-wide (all 32 lanes, same result in each): the rule, R and this CTA's
+// range, then the first request with a piece in it.
+__device__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
+  const int S = a.S;
+  w.max_len = (long long)a.MP * S;
+  long long tot = 0;
+  int mx = 0;
+  for (int b = lane; b < a.B; b += 32) {
+    const int p = ws_pages(w, __ldg(&a.seq_lens[b]), S);
+    tot += p;
+    mx = p > mx ? p : mx;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const long long T = tot, ranges = a.ranges;
+  long long R = ranges < T ? ranges : T;
+  if (mx > 0 && a.max_splits >= 3) {
+    const long long cap = div_floor((long long)(a.max_splits - 2) * T, mx);
+    if (R > cap) R = cap;
+  }
+  w.chunks = !(a.max_splits >= 3 && T > 0 && R >= 1 && 4 * R >= 3 * ranges);
+  if (w.chunks) {
+    R = ranges < T ? ranges : T;
+    const long long cp = div_floor(T * a.Hkv + a.target_items - 1, a.target_items);
+    w.cp = cp < a.min_chunk_pages ? a.min_chunk_pages : cp;
+  } else {
+    w.cp = 0;
+  }
+  w.T = T;
+  w.R = R < 1 ? 1 : R;
+  w.k = (int)blockIdx.x / a.Hkv;
+  w.b = a.B;  // no pieces unless found below
+  w.off = w.first = w.c = 0;
+  if (T == 0 || w.k >= w.R) return;
+  w.r0 = div_floor((long long)w.k * T, w.R);
+  w.r1 = div_floor((long long)(w.k + 1) * T, w.R);
+  long long off_c = 0, first_c = 0;  // totals of earlier passes
+  for (int base = 0; base < a.B; base += 32) {
+    const int b = base + lane;
+    const int p = b < a.B ? ws_pages(w, __ldg(&a.seq_lens[b]), S) : 0;
+    long long xp = p;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, xp, o);
+      if (lane >= o) xp += y;
+    }
+    const long long off = off_c + xp - p;
+    int ppc = 1, n = 0;
+    if (p > 0) n = ws_count(w, off, p, a.max_splits, &ppc);
+    long long xn = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, xn, o);
+      if (lane >= o) xn += y;
+    }
+    const long long first = first_c + xn - n;
+    bool has = false;
+    int c_lo = 0;
+    if (p > 0 && off < w.r1 && off + p > w.r0) {
+      if (!w.chunks) {
+        has = true;
+      } else {
+        // r0 - off < p here, so the chunk index fits an int
+        c_lo = off >= w.r0 ? 0 : (int)((unsigned)(w.r0 - off + ppc - 1) / (unsigned)ppc);
+        has = c_lo < n && off + (long long)c_lo * ppc < w.r1;
+      }
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, has);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      w.b = base + src;
+      w.off = __shfl_sync(0xffffffffu, off, src);
+      w.first = __shfl_sync(0xffffffffu, first, src);
+      w.c = __shfl_sync(0xffffffffu, c_lo, src);
+      return;
+    }
+    off_c += __shfl_sync(0xffffffffu, xp, 31);
+    first_c += __shfl_sync(0xffffffffu, xn, 31);
+  }
+}
+
+// The CTA's next piece, in request order (uniform across the warp); false
+// when the range has none left.  A piece that would break the workspace
+// bounds ends the walk instead of being used (it cannot occur when the
+// rules above hold).
+__device__ bool ws_next(WorkSplit &w, const DecodeArgs &a, Piece &pc) {
+  while (w.b < a.B) {
+    const int L = __ldg(&a.seq_lens[w.b]);
+    const int p = ws_pages(w, L, a.S);
+    if (p == 0) {
+      ++w.b;
+      continue;
+    }
+    if (w.off >= w.r1) return false;
+    int ppc = 1;
+    const int n = ws_count(w, w.off, p, a.max_splits, &ppc);
+    long long j, p0, p1;
+    if (!w.chunks) {
+      j = (long long)w.k - div_floor((w.off + 1) * w.R - 1, w.T);
+      p0 = (w.r0 > w.off ? w.r0 : w.off) - w.off;
+      p1 = (w.r1 < w.off + p ? w.r1 : w.off + p) - w.off;
+    } else {
+      if (w.c >= n) {
+        w.first += n;
+        w.off += p;
+        ++w.b;
+        w.c = 0;
+        continue;
+      }
+      if (w.off + w.c * ppc >= w.r1) return false;
+      j = w.c++;
+      p0 = j * ppc;
+      p1 = p0 + ppc < p ? p0 + ppc : p;
+    }
+    const long long cg = w.first + j;
+    if (j < 0 || j >= n || n > a.max_splits || p0 < 0 || p0 >= p1 || p1 > p || cg >= (long long)a.B * a.max_splits)
+      return false;
+    pc.b = w.b;
+    pc.cg = (int)cg;
+    pc.p0 = (int)p0;
+    pc.p1 = (int)p1;
+    pc.L = L;
+    pc.nb = n;
+    pc.lead = j == 0;
+    if (!w.chunks) {
+      w.first += n;
+      w.off += p;
+      ++w.b;
+    }
+    return true;
+  }
+  return false;
+}
+
+// ws_next on a state kept in shared memory (one copy per warp), so that it
+// holds no registers while the pages go out.
+__device__ __forceinline__ bool ws_next_shared(WorkSplit &s, const DecodeArgs &a, Piece &pc, int lane) {
+  WorkSplit w = s;
+  __syncwarp();
+  const bool r = ws_next(w, a, pc);
+  if (lane == 0) s = w;
+  __syncwarp();
+  return r;
+}
+
 // Bounded wait that ignores the abort flag: the page loader's way out, so
 // that a block that gave up still lets its own copies land before it exits.
 __device__ __forceinline__ void drain_wait_full(uint64_t *bar, uint32_t parity) {
@@ -175,7 +397,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     mbar_init_fence();
   }
   __syncthreads();
-  pdl_wait();  // the plan kernel's outputs (splits, status) are visible from here on
+  pdl_wait();  // the kernel before this one (the previous call's merge) is complete from here on
   pdl_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid to finish
 
   if (warp == kNCW) {
@@ -184,7 +406,6 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
     }
-    const int n_items = a.hdr->n_items;
     const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
     // Pages of one batch are issued by separate lanes at once.  A batch never
     // holds more pages than the ring has stages, so no two lanes of a batch
@@ -192,37 +413,23 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     // use only (no parity aliasing).
     const int batch_pages = min(32, nst);
     uint32_t ring = 0;
-    // Work items are claimed one ahead: the id and the split descriptor of
-    // the next item are in flight while the current item's pages go out.
-    // Balanced plan: CTA r * Hkv + h walks range r's chunks for KV head h;
-    // otherwise items come from the shared counter.  Lane 0 claims.
-    const int n_ranges = a.hdr->n_ranges;
-    int run_next = n_items, run_end = n_items;
-    if (n_ranges > 0 && (int)blockIdx.x < n_ranges * a.Hkv) {
-      const int r = (int)blockIdx.x / a.Hkv, h = (int)blockIdx.x - r * a.Hkv;
-      run_next = a.cta_first[r] * a.Hkv + h;
-      run_end = a.cta_first[r + 1] * a.Hkv;
+    // This CTA's pieces for KV head g, worked out from the lengths; the next
+    // piece is found once the current one's pages have gone out.
+    const int g = (int)blockIdx.x % a.Hkv;
+    __shared__ WorkSplit s_ws;
+    {
+      WorkSplit w;
+      ws_init(w, a, lane);
+      if (lane == 0) s_ws = w;
+      __syncwarp();
     }
-    auto claim = [&]() -> int {
-      if (n_ranges == 0) return (int)atomicAdd(&a.hdr->work, 1u);
-      const int v = run_next < run_end ? run_next : n_items;
-      run_next += a.Hkv;
-      return v;
-    };
-    int item = 0, item_next = 0;
+    Piece cur;
+    bool have = ws_next_shared(s_ws, a, cur, lane);
     // the last batch's first ring position, and whether this lane's page of
     // it was issued (every page of earlier batches was)
     uint32_t last_first = 0;
     bool last_issued = false;
-    if (lane == 0) item = claim();
-    item = __shfl_sync(0xffffffffu, item, 0);
-    int4 info = make_int4(0, 0, 0, 0), info2 = make_int4(0, 0, 0, 0);
-    if (item < n_items) {
-      info = a.chunk_info[2 * (item / a.Hkv)];
-      info2 = a.chunk_info[2 * (item / a.Hkv) + 1];
-    }
     for (uint32_t iq = 0;; ++iq) {
-      if (lane == 0) item_next = claim();
       const uint32_t slot = iq % kNIQ;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&item_empty[slot], ((iq / kNIQ) & 1u) ^ 1u, abort_flag);
@@ -232,26 +439,23 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       // first item (or its end marker) to the consumers, whose bounded wait
       // then gives up
       const bool withhold = (a.flags & PFKV_FLAG_TEST_WITHHOLD) && blockIdx.x == 0 && iq == 0;
-      if (item >= n_items) {
+      if (!have) {
         if (lane == 0) {
           items[slot].b = -1;
           if (!withhold) mbar_arrive(&item_full[slot]);
         }
         break;
       }
-      const int cg = item / a.Hkv, g = item - cg * a.Hkv;
-      const int b = info.x, p0 = info.y, p1 = info.z, L = info.w;
+      const int b = cur.b, p0 = cur.p0, p1 = cur.p1, L = cur.L;
       if (lane == 0) {
         ItemDesc d;
-        d.b = b; d.cg = cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = info2.x;
+        d.b = b; d.cg = cur.cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = cur.nb;
         items[slot] = d;
         if (!withhold) mbar_arrive(&item_full[slot]);
-      }
-      item_next = __shfl_sync(0xffffffffu, item_next, 0);
-      int4 info_next = make_int4(0, 0, 0, 0), info2_next = make_int4(0, 0, 0, 0);
-      if (item_next < n_items) {  // used by the next iteration
-        info_next = a.chunk_info[2 * (item_next / a.Hkv)];
-        info2_next = a.chunk_info[2 * (item_next / a.Hkv) + 1];
+        if (g == 0 && cur.lead) {  // the merge's view of the numbering
+          a.split_first[b] = cur.cg;
+          a.split_count[b] = cur.nb;
+        }
       }
       const int *trow = a.block_table + (size_t)b * a.MP;
       const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
@@ -321,9 +525,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         mbar_arrive(&item_done[slot]);
       }
       if (!ok) break;
-      item = item_next;
-      info = info_next;
-      info2 = info2_next;
+      have = ws_next_shared(s_ws, a, cur, lane);
     }
     // Copies still in flight land before the block may exit (the consumers
     // wait for every page they use, but on the abort path they leave early):
@@ -685,7 +887,6 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           }
           out_bg[idx] = item_st ? 0.f : acc * ofac / sm_fin[2 * jh + 1];
         }
-        if (t == 0 && item_st) atomicOr(&a.status[d.b], item_st);
       } else {
         for (int idx = t; idx < kG * kD; idx += kCT) {
           const int jh = idx / kD, dd = idx - jh * kD;
@@ -699,17 +900,19 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           a.part_o[((size_t)d.cg * a.Hq + d.g * kG) * kD + idx] = acc * ofac;
         }
         if (t < kG) a.part_ml[(size_t)d.cg * a.Hq + d.g * kG + t] = make_float2(sm_fin[2 * t], sm_fin[2 * t + 1]);
-        if (t == 0 && item_st) atomicOr(&a.status[d.b], item_st);
       }
+      // the walk's bits are the same for every KV head (same pages and tags):
+      // head 0's item reports them for the piece
+      if (t == 0 && d.g == 0) a.part_st[d.cg] = item_st;
       named_bar_sync(1, kCT);
       if (threadIdx.x == 0) mbar_arrive(&item_empty[slot]);
       if (!alive) break;
     }
   }
-  // A wait gave up somewhere in this block: every request of the call is
-  // reported as timed out (its output is not valid).
-  if (lane == 0 && *abort_flag)
-    for (int b = 0; b < a.B; ++b) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
+  // Whether a wait gave up somewhere in this block; the merge then reports
+  // every request of the call as timed out (its output is not valid).
+  __syncthreads();
+  if (threadIdx.x == 0) a.cta_abort[blockIdx.x] = *abort_flag != 0;
 }
 
 // ---------------------------------------------------------------- host side
@@ -798,30 +1001,31 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
       cache[slot] = sh;
     }
   }
-  // one equal page range per (CTA / Hkv) when requests may be cut into 3 or
-  // more pieces (the plan falls back to longest-first items when the caps
-  // leave too few ranges)
-  a.balanced = a.max_splits >= 3 ? min(sh.grid / a.Hkv, kMaxRanges) : 0;
-  // decode step: the split kernel's producer writes the new tokens (the plan
-  // grid then needs no append blocks, which would hold SMs the split CTAs
-  // are waiting for)
+  // No plan kernel: the split CTAs work out their pieces themselves (one CTA
+  // group of Hkv CTAs per page range), and the merge kernel writes status.
+  a.self_plan = 1;
+  a.ranges = max(1, min(sh.grid, kMaxCtas) / a.Hkv);
+  a.n_ctas = a.ranges * a.Hkv;
+  a.target_items = a.n_ctas * 8;
+  a.min_chunk_pages = (1024 + a.S - 1) / a.S;
+  // decode step: the split kernel's producer writes the new tokens
   a.split_append = a.append;
   a.append = 0;
-  int rc = cuda_ok(launch_plan(a, s, sh.grid * 8, (1024 + a.S - 1) / a.S), "plan kernel launch");
-  if (rc) return rc;
-  // The split kernel may start while the plan kernel runs; it waits for the
-  // plan's results (griddepcontrol.wait) before it reads them.
+  if (a.n_ctas > kMaxCtas) return PFKV_ERR_UNSUPPORTED;  // more KV heads than abort words
+  // The split kernel is a programmatic dependent of the stream's previous
+  // kernel: its CTAs take SMs as that kernel's blocks drain and wait for it
+  // to finish (griddepcontrol.wait) before touching memory.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sh.grid);
+  cfg.gridDim = dim3(a.n_ctas);
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = sh.smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  rc = cuda_ok(cudaLaunchKernelEx(&cfg, kern, mk, mv, a, sh.nst), "split kernel launch");
+  int rc = cuda_ok(cudaLaunchKernelEx(&cfg, kern, mk, mv, a, sh.nst), "split kernel launch");
   if (rc) return rc;
   cudaLaunchConfig_t mcfg = {};
   mcfg.gridDim = dim3(a.B * a.Hkv, merge_col_blocks<kD, kG>());

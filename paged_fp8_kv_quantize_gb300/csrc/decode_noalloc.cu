@@ -57,8 +57,8 @@ extern "C" int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, 
   void *scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
-  // The plan kernel of the regular path rewrites every counter it needs at
-  // the start of each call, so the buffer needs no clearing between calls.
+  // The regular path rewrites, on every call, every workspace word it reads
+  // back, so the buffer needs no clearing between calls.
   return pfkv_paged_decode_attention_fp8(cache, q, num_q_heads, seq_lens, block_table, block_tags, batch, max_pages,
                                          softmax_scale, flags, max_splits, scratch,
                                          (size_t)PFKV_NOALLOC_SCRATCH_BYTES, out, status, stream);

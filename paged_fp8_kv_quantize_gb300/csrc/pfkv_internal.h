@@ -23,9 +23,11 @@ struct WsHeader {
 
 // Decode workspace carve-up.
 struct WsLayout {
-  size_t hdr, split_first, split_count, chunk_info, cta_first, part_ml, part_o, qterms, qfac, total;
+  size_t hdr, split_first, split_count, chunk_info, cta_first, part_ml, part_o, part_st, cta_abort, qterms, qfac,
+      total;
 };
 constexpr int kMaxRanges = 1024;  // balanced plan: at most this many page ranges (one per CTA)
+constexpr int kMaxCtas = 4096;    // grouped-query split grid: at most this many CTAs (one abort word each)
 // latent: the latent-stream path also keeps each request's query as two e4m3
 // terms in the operand image its kernel loads (qterms, 72 KB per request)
 // and one factor per head (qfac).
@@ -76,6 +78,18 @@ struct DecodeArgs {
   // n_ranges says which plan was made.
   int balanced;
   int *cta_first;
+  // grouped-query path (self_plan == 1): no plan kernel; every split CTA
+  // works out its own pieces from seq_lens.  ranges = CTA groups (one CTA
+  // per KV head each); the chunk rule of small or lopsided batches takes
+  // pieces of at least min_chunk_pages pages, about target_items of them
+  // over all KV heads.  Written per call: split_first / split_count of every
+  // request with a valid length (by the head-0 CTA holding its first
+  // piece), part_st[piece] (status bits found by the head-0 item) and
+  // cta_abort[0 .. n_ctas) (1: a wait of that CTA gave up).  The merge turns
+  // them into status[] and zeroes the rows of faulted requests.
+  int self_plan, ranges, target_items, min_chunk_pages, n_ctas;
+  uint32_t *part_st;
+  int *cta_abort;
 };
 
 // Tensor-map encoder obtained from the driver without linking libcuda.

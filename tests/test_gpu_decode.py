@@ -56,18 +56,41 @@ def test_decode_shapes(dtype, si):
 
 @pytest.mark.parametrize("max_splits", [1, 2, 3, 64, 256])
 def test_split_counts(max_splits):
-    # 1, 2: longest-first plan; 3: the balanced plan's cap leaves too few
-    # ranges and it falls back to longest-first; 64, 256: balanced ranges
+    # 1, 2: chunk rule; 3: the cut rule's cap leaves too few ranges, so the
+    # CTAs fall back to the chunk rule; 64, 256: cut rule (equal page ranges)
     w = _work(400, G=4, Hkv=8, D=128, S=16, lens=[7, 1000, 4097, 20000])
     _check(w, FP8, max_splits=max_splits)
 
 
 @pytest.mark.parametrize("lens", [[16384] * 8, [16384] * 7 + [100]])
 def test_balanced_ranges_cross_requests(lens):
-    # one KV head: every CTA owns a range, and a request meets more ranges
-    # than a warp has lanes (the plan writes its chunks in two lane passes)
+    # one KV head: every CTA owns a range, and a request is cut into more
+    # pieces than a warp has lanes (pieces numbered across many CTAs, merged
+    # from more than 32 partials)
     w = _work(403, G=8, Hkv=1, D=128, S=64, lens=lens)
     _check(w, FP8, max_splits=64)
+
+
+@pytest.mark.parametrize("max_splits", [2, 5, 10, 64])
+def test_self_split_many_requests(max_splits):
+    # 70 requests: each CTA's search for its first piece takes three warp
+    # passes; bad lengths (0, -1, beyond the table) count no pages and sit
+    # between valid ones.  max_splits 2 and 5: chunk rule; 10: cut rule with
+    # fewer ranges than CTA groups (the longest request caps them); 64: cut
+    # rule
+    rng = np.random.default_rng(404)
+    lens = [int(x) for x in np.exp(rng.uniform(0, np.log(20000), size=70)).round()]
+    w = _work(404, G=4, Hkv=8, D=128, S=16, lens=lens)
+    bad = w.seq_lens.copy()
+    bad[3], bad[33], bad[64] = 0, -1, w.max_pages * 16 + 1
+    run = GpuRun(w)
+    out, st = run.decode(max_splits=max_splits, seq_lens=dev_i32(bad))
+    ref, _ = oracle_cache(w)
+    o_ref, st_ref = ref.decode(w.q, bad, w.block_table, w.block_tags, w.softmax_scale, threads=8)
+    assert list(np.nonzero(st_ref)[0]) == [3, 33, 64]
+    assert np.array_equal(st, st_ref), (st, st_ref)
+    assert not out[st != 0].any()
+    assert_close(out, o_ref, f"70 requests, max_splits={max_splits}")
 
 
 def test_per_token_scales_gqa():

@@ -90,9 +90,10 @@ def test_step_gqa(dtype, flags):
 
 @pytest.mark.parametrize("max_splits", [1, 2])
 @pytest.mark.parametrize("dtype", [FP8, BF16])
-def test_step_gqa_longest_first_plan(dtype, max_splits):
-    # max_splits < 3: the longest-first plan, items from the work counter; the
-    # new rows are still written by the item that holds each last page
+def test_step_gqa_chunk_rule(dtype, max_splits):
+    # max_splits < 3: requests cut into chunks, a range taking the chunks that
+    # start in it; the new rows are still written by the piece that holds
+    # each last page
     w = synth.make("step_lpt", 903, batch=len(LENS), q_heads=32, kv_heads=8, head_dim=128, page_size=16,
                    seq_lens=LENS, stale_block_entries=[(2, 1)], outlier_p=0.01)
     st = _run(w, dtype, abi.FLAG_TAG_CHECK, max_splits=max_splits)
