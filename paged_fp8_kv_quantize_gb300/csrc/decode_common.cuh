@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   __shared__ float s_l[256 * M::kNH];
   __shared__ float s_M[M::kNH], s_W[M::kNH];
   __shared__ float4 s_acc[256];
-  __shared__ unsigned s_st;
+  __shared__ unsigned s_or[8];  // status bits per warp
   // Latent stream: the next call's plan grid (one CTA that waits for this
   // grid) may launch at once.  Grouped-query path: the next call's split
   // grid launches only when this grid has finished.  Measured on the ragged
@@ -452,12 +452,22 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   const int t = threadIdx.x;
   float *out_bg = a.out + ((size_t)b * a.Hq + g * kG) * kD;
   const int col_lo = (int)blockIdx.y * M::kW;
+  const int h_lo = col_lo * 4 / kD;  // first head of this block's columns
   int nb, c0;
+  // each split's (m, l) for the heads of this block's columns
+  auto load_ml = [&]() {
+    for (int i = t; i < nb * M::kNH; i += 256) {
+      const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / M::kNH) * a.Hq + g * kG + h_lo + i % M::kNH]);
+      s_w[i] = ml.x;
+      s_l[i] = ml.y;
+    }
+  };
   if (a.self_plan) {
     // Grouped-query path: this kernel writes status[b].  The block of
     // (request, head 0, first columns) gathers the bits its pieces found
     // and whether any split CTA gave up; every block zeroes its columns of
-    // a faulted request.
+    // a faulted request.  The pieces' (m, l) are loaded beside their status
+    // words.
     const bool lead = g == 0 && blockIdx.y == 0;
     const int L = a.seq_lens[b];
     if (L < 1 || (long long)L > (long long)a.MP * a.S) {
@@ -470,21 +480,20 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
     // written by this call's split kernel unless one of its CTAs gave up
     // first; checked so that no read leaves the workspace
     const bool sane = nb >= 1 && nb <= a.max_splits && c0 >= 0 && c0 <= a.B * a.max_splits - nb;
-    if (t == 0) s_st = 0u;
-    __syncthreads();
     uint32_t st = 0u;
-    if (sane)
+    if (sane) {
       for (int i = t; i < nb; i += 256) st |= __ldcg(&a.part_st[c0 + i]);
-    if (st) atomicOr(&s_st, st);
-    bool gave_up = false;
-    if (lead) {
-      int any = 0;
-      for (int i = t; i < a.n_ctas; i += 256) any |= __ldcg(&a.cta_abort[i]);
-      gave_up = __syncthreads_or(any) != 0;
-    } else {
-      __syncthreads();
+      if (nb > 1) load_ml();
     }
-    st = s_st;
+    int any = 0;
+    if (lead)
+      for (int i = t; i < a.n_ctas; i += 256) any |= __ldcg(&a.cta_abort[i]);
+    st = __reduce_or_sync(0xffffffffu, st);
+    if ((t & 31) == 0) s_or[t >> 5] = st;
+    const bool gave_up = __syncthreads_or(any) != 0;
+    st = 0u;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) st |= s_or[w];
     if (lead && t == 0) a.status[b] = st | (gave_up || !sane ? (uint32_t)PFKV_ST_TIMEOUT : 0u);
     if (!sane || nb == 1) return;  // a one-piece request's rows come from the split kernel
     if (st) {
@@ -499,12 +508,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
       for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
       return;
     }
-  }
-  const int h_lo = col_lo * 4 / kD;  // first head of this block's columns
-  for (int i = t; i < nb * M::kNH; i += 256) {
-    const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / M::kNH) * a.Hq + g * kG + h_lo + i % M::kNH]);
-    s_w[i] = ml.x;
-    s_l[i] = ml.y;
+    load_ml();
   }
   __syncthreads();
   const int warp = t >> 5, lane = t & 31;

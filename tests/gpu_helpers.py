@@ -23,7 +23,7 @@ def dev_i32(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(a.astype(np.int32, copy=False)).cuda()
 
 
-class GpuRun:
+class DeviceCase:
     """Device copies of a workload's tables plus a filled GPU cache."""
 
     def __init__(self, w: synth.Workload, dtype=abi.DTYPE_FP8_E4M3, sentinel=0xA5, fill_flags=0, num_pages=None,

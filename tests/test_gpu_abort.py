@@ -6,7 +6,7 @@ on the same context must match the oracle."""
 import numpy as np
 import pytest
 
-from gpu_helpers import GpuRun, assert_close
+from gpu_helpers import DeviceCase, assert_close
 from oracle_helpers import oracle_cache
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
@@ -18,7 +18,7 @@ def test_withheld_item_times_out_and_context_stays_usable(dtype):
     lens = [300, 2000, 17, 4097, 1, 700]
     w = synth.make("abort", 950, batch=len(lens), q_heads=32, kv_heads=8, head_dim=128, page_size=16,
                    seq_lens=lens, outlier_p=0.01)
-    run = GpuRun(w, dtype)
+    run = DeviceCase(w, dtype)
     _, st = run.decode(flags=abi.FLAG_TAG_CHECK | abi.FLAG_TEST_WITHHOLD)
     assert np.all(st & abi.ST_TIMEOUT), st
     out, st2 = run.decode(flags=abi.FLAG_TAG_CHECK)
@@ -34,7 +34,7 @@ def test_latent_withheld_item_times_out_and_context_stays_usable():
     w = synth.make("abort_lat", 951, batch=len(lens), q_heads=64, kv_heads=1, head_dim=576, v_head_dim=512,
                    kv_shared=True, page_size=64, seq_lens=lens, scale_mode=synth.PER_TOKEN,
                    softmax_scale=1.0 / 24.0)
-    run = GpuRun(w)
+    run = DeviceCase(w)
     _, st = run.decode(flags=abi.FLAG_TAG_CHECK | abi.FLAG_TEST_WITHHOLD)
     assert np.all(st & abi.ST_TIMEOUT), st
     out, st2 = run.decode(flags=abi.FLAG_TAG_CHECK)

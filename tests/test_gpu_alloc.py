@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import GpuRun, dev_i32
+from gpu_helpers import DeviceCase, dev_i32
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
 pytestmark = pytest.mark.gpu
@@ -105,7 +105,7 @@ def test_moved_page_aborts_the_old_owner():
                    room_tokens=20, num_pages=12)
     P = w.num_pages
     ga = abi.PageAllocator(P)
-    run = GpuRun(w, fill=False)
+    run = DeviceCase(w, fill=False)
     table = np.full_like(w.block_table, -1)
     btags = np.zeros_like(w.block_tags)
     for b in range(w.batch):

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import GpuRun, dev_bf16, dev_i32
+from gpu_helpers import DeviceCase, dev_bf16, dev_i32
 from oracle_helpers import oracle_cache
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
@@ -56,7 +56,7 @@ def test_bulk_fill_matches_oracle(dtype, ci):
     if dtype == abi.DTYPE_BF16 and kw.get("scale_mode") == synth.PER_TOKEN:
         kw["scale_mode"] = synth.PER_HEAD
     w = _small(200 + ci, **kw)
-    run = GpuRun(w, dtype)
+    run = DeviceCase(w, dtype)
     ref, st = oracle_cache(w, dtype)
     assert not run.fill_status.cpu().numpy().any() and not st.any()
     _compare_pools(run, ref)
@@ -64,7 +64,7 @@ def test_bulk_fill_matches_oracle(dtype, ci):
 
 def test_tiny_fill_and_decode_step_append():
     w = synth.tiny()
-    run = GpuRun(w)
+    run = DeviceCase(w)
     ref, _ = oracle_cache(w)
     _compare_pools(run, ref)
     # one decode-step append per request at position L (row_req NULL path), tag check on
@@ -81,7 +81,7 @@ def test_tiny_fill_and_decode_step_append():
 def test_refused_rows_write_nothing():
     w = synth.make("ref", 21, batch=5, q_heads=8, kv_heads=2, head_dim=128, page_size=16, seq_lens=[3, 3, 3, 3, 3],
                    room_tokens=16)
-    run = GpuRun(w, fill=False)
+    run = DeviceCase(w, fill=False)
     run.cache.k_scale.fill_(0.01)
     run.cache.v_scale.fill_(0.02)
     ref = oracle.Cache(w.num_pages, 16, 2, 128, 128, False, oracle.DTYPE_FP8, oracle.SCALE_PER_HEAD, w.page_tags,

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import GpuRun, assert_close, dev_bf16, dev_i32
+from gpu_helpers import DeviceCase, assert_close, dev_bf16, dev_i32
 from oracle_helpers import oracle_cache_subset
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
@@ -31,7 +31,7 @@ def _sample(w, n_short=2, n_long=2):
 @pytest.mark.parametrize("dtype", [abi.DTYPE_FP8_E4M3, abi.DTYPE_BF16])
 def test_gqa_batch32_full_size(dtype):
     w = synth.gqa()
-    run = GpuRun(w, dtype)
+    run = DeviceCase(w, dtype)
     out, st = run.decode(flags=FLAGS)
     assert not st.any()
     idx = _sample(w)
@@ -46,7 +46,7 @@ def test_gqa_batch32_full_size(dtype):
 def test_long_context_full_size_scattered_pool():
     # 8 x 131072 tokens, pages scattered over a pool 8x larger than needed
     w = synth.long_ctx(num_pages=8 * 8 * 2048)
-    run = GpuRun(w)
+    run = DeviceCase(w)
     out, st = run.decode(flags=FLAGS)
     assert not st.any()
     idx = np.array([3])
@@ -61,7 +61,7 @@ def test_ragged_batch64_100_steps():
     decodes; parity at steps 0, 1, 50 and 99; status of all 64 requests and
     of every append bit-exact."""
     w = synth.ragged()
-    run = GpuRun(w)
+    run = DeviceCase(w)
     assert not run.fill_status.cpu().numpy().any()
     c, ctab, ctags, used = oracle_cache_subset(w, np.arange(w.batch))
     B = w.batch
@@ -100,7 +100,7 @@ def test_ragged_batch64_100_fused_steps():
     steps; parity at steps 0, 1, 50 and 99, status of every checked step and
     the final pool bytes bit-exact."""
     w = synth.ragged()
-    run = GpuRun(w)
+    run = DeviceCase(w)
     c, ctab, ctags, used = oracle_cache_subset(w, np.arange(w.batch))
     B = w.batch
     ws = torch.empty(abi.decode_workspace_bytes(run.cache, B, w.q_heads, w.max_splits), dtype=torch.uint8,

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import GpuRun, assert_close, dev_i32
+from gpu_helpers import DeviceCase, assert_close, dev_i32
 from oracle_helpers import oracle_cache
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
@@ -21,7 +21,7 @@ def _work(seed, *, G, Hkv, D, S, lens, scale_mode=synth.PER_HEAD, outlier_p=0.01
 
 
 def _check(w, dtype, flags=0, max_splits=None, threads=8):
-    run = GpuRun(w, dtype)
+    run = DeviceCase(w, dtype)
     ref, _ = oracle_cache(w, dtype)
     out, st = run.decode(flags=flags, max_splits=max_splits)
     o_ref, st_ref = ref.decode(w.q, w.seq_lens, w.block_table, w.block_tags, w.softmax_scale, flags=flags,
@@ -83,7 +83,7 @@ def test_self_split_many_requests(max_splits):
     w = _work(404, G=4, Hkv=8, D=128, S=16, lens=lens)
     bad = w.seq_lens.copy()
     bad[3], bad[33], bad[64] = 0, -1, w.max_pages * 16 + 1
-    run = GpuRun(w)
+    run = DeviceCase(w)
     out, st = run.decode(max_splits=max_splits, seq_lens=dev_i32(bad))
     ref, _ = oracle_cache(w)
     o_ref, st_ref = ref.decode(w.q, bad, w.block_table, w.block_tags, w.softmax_scale, threads=8)
@@ -110,7 +110,7 @@ def test_tiny_config_tag_check():
 
 def test_tag_on_off_identical_when_valid():
     w = _work(402, G=4, Hkv=8, D=128, S=16, lens=[100, 2000, 3333])
-    run = GpuRun(w)
+    run = DeviceCase(w)
     a, sa = run.decode(flags=0)
     b, sb = run.decode(flags=abi.FLAG_TAG_CHECK)
     assert not sa.any() and not sb.any() and np.array_equal(a, b)
@@ -119,7 +119,7 @@ def test_tag_on_off_identical_when_valid():
 def test_stale_entry_past_context_not_inspected_and_oob():
     w = synth.make("st", 403, batch=4, q_heads=32, kv_heads=8, head_dim=128, page_size=16,
                    seq_lens=[40, 40, 40, 40], room_tokens=64)
-    run = GpuRun(w)
+    run = DeviceCase(w)
     tags = w.block_tags.copy()
     tags[0, 3] ^= 1  # entry 3 >= ceil(40/16) = 3: never read
     tags[1, 2] ^= 1  # read: stale
@@ -139,7 +139,7 @@ def test_stale_entry_past_context_not_inspected_and_oob():
 @pytest.mark.parametrize("dtype", [FP8, BF16])
 def test_page_permutation_bit_identical_on_gpu(dtype):
     w = _work(404, G=4, Hkv=8, D=128, S=16, lens=[17, 700, 2500])
-    run1 = GpuRun(w, dtype)
+    run1 = DeviceCase(w, dtype)
     a, _ = run1.decode(flags=abi.FLAG_TAG_CHECK)
     perm = np.random.default_rng(5).permutation(w.num_pages)
     w2 = _work(404, G=4, Hkv=8, D=128, S=16, lens=[17, 700, 2500])
@@ -147,7 +147,7 @@ def test_page_permutation_bit_identical_on_gpu(dtype):
     w2.block_table = np.where(valid, perm[np.maximum(w.block_table, 0)], -1).astype(np.int32)
     w2.page_tags = np.zeros_like(w.page_tags)
     w2.page_tags[perm] = w.page_tags
-    run2 = GpuRun(w2, dtype)
+    run2 = DeviceCase(w2, dtype)
     b, _ = run2.decode(flags=abi.FLAG_TAG_CHECK)
     assert np.array_equal(a, b)
 
@@ -159,7 +159,7 @@ def test_special_cases_on_gpu():
     off = w.rows_of(2)[0]
     f[off:] = 0.625  # requests 2 and 3: constant V
     w.v_rows[:] = synth.bf16_bits(f)
-    run = GpuRun(w, BF16)
+    run = DeviceCase(w, BF16)
     out, st = run.decode()
     assert not st.any()
     for b in (0, 1):
@@ -171,7 +171,7 @@ def test_special_cases_on_gpu():
 
 def test_empty_batch_and_deterministic():
     w = _work(406, G=4, Hkv=8, D=128, S=16, lens=[3000, 10, 5000])
-    run = GpuRun(w)
+    run = DeviceCase(w)
     a, _ = run.decode()
     b, _ = run.decode()
     assert np.array_equal(a, b)
@@ -183,7 +183,7 @@ def test_empty_batch_and_deterministic():
 
 def test_host_errors():
     w = _work(407, G=4, Hkv=8, D=128, S=16, lens=[10])
-    run = GpuRun(w)
+    run = DeviceCase(w)
     with pytest.raises(abi.PfkvError) as e:  # wrong entry point for the cache dtype
         abi.paged_decode_attention_bf16(run.cache, run.q, run.seq_lens, run.table, run.tags, 1.0)
     assert e.value.code == -4

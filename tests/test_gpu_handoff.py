@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import GpuRun, dev_i32
+from gpu_helpers import DeviceCase, dev_i32
 from oracle_helpers import oracle_cache
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
@@ -23,7 +23,7 @@ def test_handoff_matches_oracle(case):
     else:
         w = synth.make("ho", 600, batch=4, q_heads=32, kv_heads=8, head_dim=128, page_size=16,
                        seq_lens=[40, 300, 17, 1000])
-    src = GpuRun(w, abi.DTYPE_BF16)
+    src = DeviceCase(w, abi.DTYPE_BF16)
     ref_src, _ = oracle_cache(w, oracle.DTYPE_BF16)
     used = np.unique(w.block_table[w.block_table >= 0])
     rng = np.random.default_rng(5)

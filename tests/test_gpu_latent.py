@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_helpers import GpuRun, assert_close, dev_i32
+from gpu_helpers import DeviceCase, assert_close, dev_i32
 from oracle_helpers import oracle_cache, oracle_cache_subset
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
@@ -21,7 +21,7 @@ def _lat(seed, lens, **kw):
 
 
 def _check(w, flags=0, max_splits=None, tables=None):
-    run = GpuRun(w)
+    run = DeviceCase(w)
     ref, _ = oracle_cache(w)
     bt, tags, lens = tables if tables else (w.block_table, w.block_tags, w.seq_lens)
     out, st = run.decode(flags=flags, max_splits=max_splits, table=dev_i32(bt), tags=dev_i32(tags),
@@ -55,7 +55,7 @@ def test_latent_tags_oob_and_bad_length():
 
 def test_latent_full_size_sampled():
     w = synth.latent()
-    run = GpuRun(w)
+    run = DeviceCase(w)
     out, st = run.decode(flags=abi.FLAG_TAG_CHECK)
     assert not st.any()
     order = np.argsort(w.seq_lens, kind="stable")

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import GpuRun, assert_close, dev_bf16, dev_i32
+from gpu_helpers import DeviceCase, assert_close, dev_bf16, dev_i32
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,7 @@ def _run(w, dtype, flags, max_splits=None):
     hist, k_new, v_new = _split(w)
     mode = w.scale_mode if dtype == FP8 else synth.PER_HEAD
     # GPU: calibrate on all rows, append history, then the one-call step
-    run = GpuRun(w, dtype, fill=False)
+    run = DeviceCase(w, dtype, fill=False)
     if dtype == FP8 and mode == synth.PER_HEAD:
         abi.calibrate_scales(dev_bf16(w.k_rows), run.cache.k_scale)
         abi.calibrate_scales(dev_bf16(w.v_rows), run.cache.v_scale)

@@ -1,0 +1,192 @@
+"""The grouped-query split kernel's work split, restated in Python and checked
+for the properties the merge relies on (host logic, no GPU).
+
+Every split CTA works out its own pieces from the lengths: the requests'
+pages, concatenated in request order, are cut into R ranges
+[floor(kT/R), floor((k+1)T/R)); CTA group k takes range k.  Cut rule: a piece
+is the part of one request inside one range.  Chunk rule (small or lopsided
+batches): requests are cut into chunks of about cp pages, at most max_splits
+of them, and a range takes the chunks that start in it.  The restatement
+follows the kernel step by step (the first piece found by a 32-request pass,
+then a walk), so that its index arithmetic can be checked here on many
+batches: every valid request is tiled exactly once, in order, by pieces
+numbered first_b .. first_b + n_b - 1 with n_b <= max_splits; piece numbers
+are distinct and fit the workspace (batch * max_splits); each request has a
+first piece (whose CTA records the numbering); under the cut rule every
+busy range holds the same number of pages to within one.  The kernel itself
+is checked end to end against the oracle by the GPU parity tests."""
+import random
+
+import pytest
+
+
+def _pages(L, S, max_len):
+    return 0 if (L < 1 or L > max_len) else (L + S - 1) // S
+
+
+def _count(w, off, p, ms):
+    """Pieces of a request of p > 0 pages starting at page off, and the chunk length."""
+    if not w["chunks"]:
+        R, T = w["R"], w["T"]
+        return ((off + p) * R - 1) // T - ((off + 1) * R - 1) // T + 1, 1
+    cp = w["cp"]
+    nn = 1 if cp >= p else (p + cp - 1) // cp
+    nn = min(nn, ms)
+    q = (p + nn - 1) // nn
+    return (p + q - 1) // q, q
+
+
+def _init(lens, S, MP, Hkv, ms, ranges, target, min_chunk, blk):
+    B = len(lens)
+    w = {"max_len": MP * S}
+    P = [_pages(L, S, w["max_len"]) for L in lens]
+    T = sum(P)
+    mx = max(P) if P else 0
+    R = min(ranges, T)
+    if mx > 0 and ms >= 3:
+        R = min(R, (ms - 2) * T // mx)
+    w["chunks"] = not (ms >= 3 and T > 0 and R >= 1 and 4 * R >= 3 * ranges)
+    if w["chunks"]:
+        R = min(ranges, T)
+        w["cp"] = max((T * Hkv + target - 1) // target, min_chunk)
+    else:
+        w["cp"] = 0
+    w.update(T=T, R=max(R, 1), k=blk // Hkv, b=B, off=0, first=0, c=0)
+    if T == 0 or w["k"] >= w["R"]:
+        return w
+    w["r0"] = w["k"] * T // w["R"]
+    w["r1"] = (w["k"] + 1) * T // w["R"]
+    off_c = first_c = 0
+    for base in range(0, B, 32):  # one warp pass: 32 requests, scans of pages and pieces
+        acc_p, acc_n = off_c, first_c
+        for b in range(base, base + 32):
+            p = P[b] if b < B else 0
+            off, first = acc_p, acc_n
+            acc_p += p
+            n, ppc = _count(w, off, p, ms) if p > 0 else (0, 1)
+            acc_n += n
+            has, c_lo = False, 0
+            if p > 0 and off < w["r1"] and off + p > w["r0"]:
+                if not w["chunks"]:
+                    has = True
+                else:
+                    assert w["r0"] - off < p  # the kernel keeps this in 32 bits
+                    c_lo = 0 if off >= w["r0"] else (w["r0"] - off + ppc - 1) // ppc
+                    has = c_lo < n and off + c_lo * ppc < w["r1"]
+            if has:  # the lowest lane with a piece in the range
+                w.update(b=b, off=off, first=first, c=c_lo)
+                return w
+        off_c, first_c = acc_p, acc_n
+    return w
+
+
+def _next(w, lens, S, ms):
+    B = len(lens)
+    while w["b"] < B:
+        p = _pages(lens[w["b"]], S, w["max_len"])
+        if p == 0:
+            w["b"] += 1
+            continue
+        if w["off"] >= w["r1"]:
+            return None
+        n, ppc = _count(w, w["off"], p, ms)
+        if not w["chunks"]:
+            j = w["k"] - ((w["off"] + 1) * w["R"] - 1) // w["T"]
+            p0 = max(w["r0"], w["off"]) - w["off"]
+            p1 = min(w["r1"], w["off"] + p) - w["off"]
+        else:
+            if w["c"] >= n:
+                w["first"] += n
+                w["off"] += p
+                w["b"] += 1
+                w["c"] = 0
+                continue
+            if w["off"] + w["c"] * ppc >= w["r1"]:
+                return None
+            j = w["c"]
+            w["c"] += 1
+            p0 = j * ppc
+            p1 = min(p0 + ppc, p)
+        cg = w["first"] + j
+        # the kernel ends the walk here instead; it must never be needed
+        assert 0 <= j < n <= ms and 0 <= p0 < p1 <= p and cg < B * ms, (j, n, p0, p1, p, cg)
+        piece = dict(b=w["b"], cg=cg, p0=p0, p1=p1, nb=n, j=j)
+        if not w["chunks"]:
+            w["first"] += n
+            w["off"] += p
+            w["b"] += 1
+        return piece
+    return None
+
+
+def _check(lens, S, MP, Hkv, ms, grid):
+    """Run every CTA group's walk; check the tiling.  Returns (chunk rule?, pieces)."""
+    B = len(lens)
+    ranges = max(1, grid // Hkv)
+    target, min_chunk = ranges * Hkv * 8, (1024 + S - 1) // S
+    pieces, loads, chunks = [], [], None
+    for k in range(ranges):
+        w = _init(lens, S, MP, Hkv, ms, ranges, target, min_chunk, k * Hkv)
+        chunks = w["chunks"]
+        tot = 0
+        while (pc := _next(w, lens, S, ms)) is not None:
+            pieces.append(pc)
+            tot += pc["p1"] - pc["p0"]
+        loads.append(tot)
+    cgs = [pc["cg"] for pc in pieces]
+    assert len(cgs) == len(set(cgs)), "a piece number used twice"
+    by_b = {}
+    for pc in pieces:
+        by_b.setdefault(pc["b"], []).append(pc)
+    first = 0
+    for b in range(B):
+        p = _pages(lens[b], S, MP * S)
+        if p == 0:
+            assert b not in by_b
+            continue
+        ps = sorted(by_b[b], key=lambda x: x["j"])
+        n = ps[0]["nb"]
+        assert len(ps) == n <= ms and all(x["nb"] == n for x in ps), (b, n, len(ps))
+        assert [x["j"] for x in ps] == list(range(n))
+        assert [x["cg"] for x in ps] == list(range(first, first + n))
+        assert ps[0]["p0"] == 0 and ps[-1]["p1"] == p
+        assert all(x["p1"] == y["p0"] for x, y in zip(ps, ps[1:]))
+        first += n
+    assert first <= B * ms
+    if not chunks and sum(loads):
+        busy = [x for x in loads if x]
+        assert max(busy) - min(busy) <= 1, loads
+    return chunks, len(pieces)
+
+
+def test_bench_shapes():
+    rng = random.Random(1)
+    lens = [int(round(2 ** rng.uniform(0, 16))) for _ in range(64)]
+    assert _check(lens, 16, 4096, 8, 64, 456)[0] is False      # ragged batch: cut rule
+    assert _check([131072] * 8, 16, 8192, 8, 64, 456) == (False, 64)
+    assert _check([37, 100], 16, 8, 8, 64, 456) == (True, 2)   # tiny: chunk rule
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_batches(seed):
+    rng = random.Random(100 + seed)
+    rules = set()
+    for _ in range(400):
+        B = rng.choice([1, 2, 3, 5, 31, 32, 33, 64, 65, 100, 300])
+        S = rng.choice([16, 32, 64])
+        MP = rng.choice([1, 2, 8, 64, 600])
+        Hkv = rng.choice([1, 2, 4, 8, 16])
+        ms = rng.choice([1, 2, 3, 4, 8, 64, 256])
+        grid = rng.choice([1, 7, 64, 152, 304, 456])
+        kind = rng.random()
+        lens = []
+        for _ in range(B):
+            if kind < 0.3:
+                L = rng.randint(1, MP * S)
+            elif kind < 0.6:
+                L = int(round(2 ** rng.uniform(0, max(1.0, (MP * S).bit_length()))))
+            else:  # bad lengths between valid ones
+                L = rng.choice([0, -3, 1, S, S + 1, MP * S, MP * S + 1, rng.randint(1, MP * S)])
+            lens.append(L)
+        rules.add(_check(lens, S, MP, Hkv, ms, grid)[0])
+    assert rules == {True, False}

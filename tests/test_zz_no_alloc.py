@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import ABS_TOL, GpuRun, assert_close
+from gpu_helpers import ABS_TOL, DeviceCase, assert_close
 from paged_fp8_kv_quantize_gb300 import abi, synth
 
 pytestmark = pytest.mark.gpu
@@ -35,7 +35,7 @@ def test_noalloc_matches_regular_entry_point_twice():
     lens = list(rng.integers(1, 6000, size=12)) + [1, 16, 17]
     w = synth.make("noalloc", 900, batch=len(lens), q_heads=32, kv_heads=8, head_dim=128, page_size=16,
                    seq_lens=lens, outlier_p=0.01, stale_block_entries=[(3, 0)])
-    run = GpuRun(w)
+    run = DeviceCase(w)
     flags = abi.FLAG_TAG_CHECK
     max_splits = 16
     assert abi.decode_workspace_bytes(run.cache, w.batch, w.q_heads, max_splits) <= abi.NOALLOC_SCRATCH_BYTES
@@ -59,7 +59,7 @@ def test_noalloc_matches_regular_entry_point_twice():
 def test_noalloc_rejects_requests_beyond_its_buffer():
     w = synth.make("noalloc_big", 901, batch=2, q_heads=32, kv_heads=8, head_dim=128, page_size=16,
                    seq_lens=[100, 200])
-    run = GpuRun(w)
+    run = DeviceCase(w)
     # 256 splits x 32 heads x 128 dims needs far more than the fixed buffer for a large batch
     big_batch = 4096
     assert abi.decode_workspace_bytes(run.cache, big_batch, 32, 256) > abi.NOALLOC_SCRATCH_BYTES
