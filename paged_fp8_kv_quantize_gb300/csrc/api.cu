@@ -138,6 +138,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.target_items = 0;
   a.min_chunk_pages = 1;
   a.n_ctas = 0;
+  a.piece_cost = 0;
   a.part_st = reinterpret_cast<uint32_t *>(w + L.part_st);
   a.cta_abort = reinterpret_cast<int *>(w + L.cta_abort);
   a.qterms = w + L.qterms;

@@ -147,6 +147,7 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, floa
 struct WorkSplit {
   long long T, R, r0, r1, cp, max_len;
   int k, chunks;
+  int c0;  // cut rule: overhead length placed before each request's pages on the cut line
   // walk: next request to look at, its first page in the concatenation, the
   // number of its first piece, and (chunk rule) its next chunk
   int b;
@@ -190,10 +191,13 @@ __device__ __forceinline__ int ws_pages(const WorkSplit &w, int L, int S) {
   return (L < 1 || (long long)L > w.max_len) ? 0 : (int)(((unsigned)L + (unsigned)S - 1u) / (unsigned)S);
 }
 
-// Pieces of a request of p > 0 pages whose first page is page `off` of the
-// concatenation; *ppc: chunk length (chunk rule only).
+// Pieces of a request of p > 0 pages whose segment of the cut line starts
+// at `off` (its pages start at off + c0); *ppc: chunk length (chunk rule).
 __device__ __forceinline__ int ws_count(const WorkSplit &w, long long off, int p, int max_splits, int *ppc) {
-  if (!w.chunks) return (int)(div_floor((off + p) * w.R - 1, w.T) - div_floor((off + 1) * w.R - 1, w.T) + 1);
+  if (!w.chunks) {
+    const long long s0 = off + w.c0;
+    return (int)(div_floor((s0 + p) * w.R - 1, w.T) - div_floor((s0 + 1) * w.R - 1, w.T) + 1);
+  }
   int nn = w.cp >= p ? 1 : (int)(((unsigned)p + (unsigned)w.cp - 1u) / (unsigned)w.cp);
   if (nn > max_splits) nn = max_splits;
   const int q = (int)(((unsigned)p + (unsigned)nn - 1u) / (unsigned)nn);
@@ -207,21 +211,25 @@ __device__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
   const int S = a.S;
   w.max_len = (long long)a.MP * S;
   long long tot = 0;
-  int mx = 0;
+  int mx = 0, nv = 0;
   for (int b = lane; b < a.B; b += 32) {
     const int p = ws_pages(w, __ldg(&a.seq_lens[b]), S);
     tot += p;
     mx = p > mx ? p : mx;
+    nv += p > 0;
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     tot += __shfl_xor_sync(0xffffffffu, tot, o);
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    nv += __shfl_xor_sync(0xffffffffu, nv, o);
   }
-  const long long T = tot, ranges = a.ranges;
-  long long R = ranges < T ? ranges : T;
+  long long T = tot;
+  const long long ranges = a.ranges, c = a.piece_cost;
+  const long long Tc = T + c * nv;  // the cut rule's line: pages plus c before each request
+  long long R = ranges < Tc ? ranges : Tc;
   if (mx > 0 && a.max_splits >= 3) {
-    const long long cap = div_floor((long long)(a.max_splits - 2) * T, mx);
+    const long long cap = div_floor((long long)(a.max_splits - 2) * Tc, mx + c);
     if (R > cap) R = cap;
   }
   w.chunks = !(a.max_splits >= 3 && T > 0 && R >= 1 && 4 * R >= 3 * ranges);
@@ -229,8 +237,11 @@ __device__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
     R = ranges < T ? ranges : T;
     const long long cp = div_floor(T * a.Hkv + a.target_items - 1, a.target_items);
     w.cp = cp < a.min_chunk_pages ? a.min_chunk_pages : cp;
+    w.c0 = 0;
   } else {
     w.cp = 0;
+    w.c0 = (int)c;
+    T = Tc;
   }
   w.T = T;
   w.R = R < 1 ? 1 : R;
@@ -244,13 +255,14 @@ __device__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
   for (int base = 0; base < a.B; base += 32) {
     const int b = base + lane;
     const int p = b < a.B ? ws_pages(w, __ldg(&a.seq_lens[b]), S) : 0;
-    long long xp = p;
+    const long long seg = p > 0 ? p + w.c0 : 0;  // the request's segment of the cut line
+    long long xp = seg;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const long long y = __shfl_up_sync(0xffffffffu, xp, o);
       if (lane >= o) xp += y;
     }
-    const long long off = off_c + xp - p;
+    const long long off = off_c + xp - seg;
     int ppc = 1, n = 0;
     if (p > 0) n = ws_count(w, off, p, a.max_splits, &ppc);
     long long xn = n;
@@ -262,7 +274,7 @@ __device__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
     const long long first = first_c + xn - n;
     bool has = false;
     int c_lo = 0;
-    if (p > 0 && off < w.r1 && off + p > w.r0) {
+    if (p > 0 && off + w.c0 < w.r1 && off + w.c0 + p > w.r0) {
       if (!w.chunks) {
         has = true;
       } else {
@@ -297,14 +309,15 @@ __device__ bool ws_next(WorkSplit &w, const DecodeArgs &a, Piece &pc) {
       ++w.b;
       continue;
     }
-    if (w.off >= w.r1) return false;
+    if (w.off + w.c0 >= w.r1) return false;
     int ppc = 1;
     const int n = ws_count(w, w.off, p, a.max_splits, &ppc);
     long long j, p0, p1;
     if (!w.chunks) {
-      j = (long long)w.k - div_floor((w.off + 1) * w.R - 1, w.T);
-      p0 = (w.r0 > w.off ? w.r0 : w.off) - w.off;
-      p1 = (w.r1 < w.off + p ? w.r1 : w.off + p) - w.off;
+      const long long s0 = w.off + w.c0;  // the request's first page on the cut line
+      j = (long long)w.k - div_floor((s0 + 1) * w.R - 1, w.T);
+      p0 = (w.r0 > s0 ? w.r0 : s0) - s0;
+      p1 = (w.r1 < s0 + p ? w.r1 : s0 + p) - s0;
     } else {
       if (w.c >= n) {
         w.first += n;
@@ -330,7 +343,7 @@ __device__ bool ws_next(WorkSplit &w, const DecodeArgs &a, Piece &pc) {
     pc.lead = j == 0;
     if (!w.chunks) {
       w.first += n;
-      w.off += p;
+      w.off += p + w.c0;
       ++w.b;
     }
     return true;
@@ -944,6 +957,10 @@ int make_pool_map(CUtensorMap *map, const void *pool, int dtype, int D, int S, i
 }
 
 constexpr int kNCW = 4;
+// Cut rule: each request's segment of the cut line starts with this many
+// pages' worth of overhead, so that a range holding many short requests
+// (many pieces, each with its own set-up and finish) gets fewer pages.
+constexpr int kPieceCost = 16;
 
 // Launch shape of one split-kernel instantiation for one (page size, scale
 // mode), worked out on its first use and reused afterwards, so that later
@@ -1008,6 +1025,7 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
   a.n_ctas = a.ranges * a.Hkv;
   a.target_items = a.n_ctas * 8;
   a.min_chunk_pages = (1024 + a.S - 1) / a.S;
+  a.piece_cost = kPieceCost;
   // decode step: the split kernel's producer writes the new tokens
   a.split_append = a.append;
   a.append = 0;

@@ -88,6 +88,7 @@ struct DecodeArgs {
   // cta_abort[0 .. n_ctas) (1: a wait of that CTA gave up).  The merge turns
   // them into status[] and zeroes the rows of faulted requests.
   int self_plan, ranges, target_items, min_chunk_pages, n_ctas;
+  int piece_cost;  // cut rule: pages' worth of time one piece costs beyond its pages
   uint32_t *part_st;
   int *cta_abort;
 };

@@ -25,10 +25,10 @@ def _pages(L, S, max_len):
 
 
 def _count(w, off, p, ms):
-    """Pieces of a request of p > 0 pages starting at page off, and the chunk length."""
+    """Pieces of a request of p > 0 pages whose cost segment starts at off, and the chunk length."""
     if not w["chunks"]:
-        R, T = w["R"], w["T"]
-        return ((off + p) * R - 1) // T - ((off + 1) * R - 1) // T + 1, 1
+        R, T, c = w["R"], w["T"], w["c0"]
+        return ((off + c + p) * R - 1) // T - ((off + c + 1) * R - 1) // T + 1, 1
     cp = w["cp"]
     nn = 1 if cp >= p else (p + cp - 1) // cp
     nn = min(nn, ms)
@@ -36,37 +36,42 @@ def _count(w, off, p, ms):
     return (p + q - 1) // q, q
 
 
-def _init(lens, S, MP, Hkv, ms, ranges, target, min_chunk, blk):
+def _init(lens, S, MP, Hkv, ms, ranges, target, min_chunk, blk, cost=0):
     B = len(lens)
     w = {"max_len": MP * S}
     P = [_pages(L, S, w["max_len"]) for L in lens]
     T = sum(P)
     mx = max(P) if P else 0
-    R = min(ranges, T)
+    Tc = T + cost * sum(1 for p in P if p)  # the cut rule's line: pages plus `cost` per request
+    R = min(ranges, Tc)
     if mx > 0 and ms >= 3:
-        R = min(R, (ms - 2) * T // mx)
+        R = min(R, (ms - 2) * Tc // (mx + cost))
     w["chunks"] = not (ms >= 3 and T > 0 and R >= 1 and 4 * R >= 3 * ranges)
     if w["chunks"]:
         R = min(ranges, T)
         w["cp"] = max((T * Hkv + target - 1) // target, min_chunk)
+        w["c0"] = 0
     else:
         w["cp"] = 0
+        w["c0"] = cost
+        T = Tc
     w.update(T=T, R=max(R, 1), k=blk // Hkv, b=B, off=0, first=0, c=0)
     if T == 0 or w["k"] >= w["R"]:
         return w
     w["r0"] = w["k"] * T // w["R"]
     w["r1"] = (w["k"] + 1) * T // w["R"]
     off_c = first_c = 0
-    for base in range(0, B, 32):  # one warp pass: 32 requests, scans of pages and pieces
+    c0 = w["c0"]
+    for base in range(0, B, 32):  # one warp pass: 32 requests, scans of cost and pieces
         acc_p, acc_n = off_c, first_c
         for b in range(base, base + 32):
             p = P[b] if b < B else 0
             off, first = acc_p, acc_n
-            acc_p += p
+            acc_p += p + c0 if p else 0
             n, ppc = _count(w, off, p, ms) if p > 0 else (0, 1)
             acc_n += n
             has, c_lo = False, 0
-            if p > 0 and off < w["r1"] and off + p > w["r0"]:
+            if p > 0 and off + c0 < w["r1"] and off + c0 + p > w["r0"]:
                 if not w["chunks"]:
                     has = True
                 else:
@@ -87,13 +92,15 @@ def _next(w, lens, S, ms):
         if p == 0:
             w["b"] += 1
             continue
-        if w["off"] >= w["r1"]:
+        c0 = w["c0"]
+        if w["off"] + c0 >= w["r1"]:
             return None
         n, ppc = _count(w, w["off"], p, ms)
         if not w["chunks"]:
-            j = w["k"] - ((w["off"] + 1) * w["R"] - 1) // w["T"]
-            p0 = max(w["r0"], w["off"]) - w["off"]
-            p1 = min(w["r1"], w["off"] + p) - w["off"]
+            s0 = w["off"] + c0  # first real page on the cost line
+            j = w["k"] - ((s0 + 1) * w["R"] - 1) // w["T"]
+            p0 = max(w["r0"], s0) - s0
+            p1 = min(w["r1"], s0 + p) - s0
         else:
             if w["c"] >= n:
                 w["first"] += n
@@ -113,25 +120,36 @@ def _next(w, lens, S, ms):
         piece = dict(b=w["b"], cg=cg, p0=p0, p1=p1, nb=n, j=j)
         if not w["chunks"]:
             w["first"] += n
-            w["off"] += p
+            w["off"] += p + c0
             w["b"] += 1
         return piece
     return None
 
 
-def _check(lens, S, MP, Hkv, ms, grid):
+def _check(lens, S, MP, Hkv, ms, grid, cost=0):
     """Run every CTA group's walk; check the tiling.  Returns (chunk rule?, pieces)."""
     B = len(lens)
     ranges = max(1, grid // Hkv)
     target, min_chunk = ranges * Hkv * 8, (1024 + S - 1) // S
     pieces, loads, chunks = [], [], None
     for k in range(ranges):
-        w = _init(lens, S, MP, Hkv, ms, ranges, target, min_chunk, k * Hkv)
+        w = _init(lens, S, MP, Hkv, ms, ranges, target, min_chunk, k * Hkv, cost)
         chunks = w["chunks"]
         tot = 0
         while (pc := _next(w, lens, S, ms)) is not None:
             pieces.append(pc)
             tot += pc["p1"] - pc["p0"]
+        if not chunks and w["k"] < w["R"]:
+            # the range's share of the cost line: its pages plus the overhead
+            # segments of the requests that start inside it
+            c0, off, virt = w["c0"], 0, 0
+            for L in lens:
+                p = _pages(L, S, MP * S)
+                if p:
+                    virt += max(0, min(w["r1"], off + c0) - max(w["r0"], off))
+                    off += p + c0
+            assert tot + virt == w["r1"] - w["r0"], (k, tot, virt)
+            tot += virt
         loads.append(tot)
     cgs = [pc["cg"] for pc in pieces]
     assert len(cgs) == len(set(cgs)), "a piece number used twice"
@@ -167,8 +185,9 @@ def test_bench_shapes():
     assert _check([37, 100], 16, 8, 8, 64, 456) == (True, 2)   # tiny: chunk rule
 
 
-@pytest.mark.parametrize("seed", range(4))
-def test_random_batches(seed):
+@pytest.mark.parametrize("cost", [0, 3])
+@pytest.mark.parametrize("seed", range(2))
+def test_random_batches(seed, cost):
     rng = random.Random(100 + seed)
     rules = set()
     for _ in range(400):
@@ -188,5 +207,5 @@ def test_random_batches(seed):
             else:  # bad lengths between valid ones
                 L = rng.choice([0, -3, 1, S, S + 1, MP * S, MP * S + 1, rng.randint(1, MP * S)])
             lens.append(L)
-        rules.add(_check(lens, S, MP, Hkv, ms, grid)[0])
+        rules.add(_check(lens, S, MP, Hkv, ms, grid, cost)[0])
     assert rules == {True, False}
