@@ -129,19 +129,24 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, floa
 // ---------------------------------------------------------------- work split
 //
 // There is no plan kernel on this path: every CTA works out its own share
-// from the lengths, and all CTAs reach the same answer.  The requests' pages,
-// concatenated in request order (T pages in all, a request with a bad length
-// counting none), are cut into R ranges [floor(kT/R), floor((k+1)T/R)); CTA
-// k * Hkv + h takes range k for KV head h.  Pieces of a request are numbered
-// consecutively in request order over the whole call (the merge finds a
-// request's pieces at split_first[b] .. + split_count[b]).  Two rules:
-//  - cut: a piece is the part of one request inside one range, so every
-//    CTA gets the same number of pages to within one.  R is capped so that
-//    no request is cut into more than max_splits pieces (a request of p
-//    pages meets at most ceil(p R / T) + 1 ranges); the rule is used when
+// from the lengths, and all CTAs reach the same answer.  The requests, in
+// request order (a request with a bad length counting nothing), lie on a
+// line of T units that is cut into R ranges [floor(kT/R), floor((k+1)T/R));
+// CTA k * Hkv + h takes range k for KV head h.  Pieces of a request are
+// numbered consecutively in request order over the whole call (the merge
+// finds a request's pieces at split_first[b] .. + split_count[b]).  Two
+// rules:
+//  - cut: a request's segment of the line is c0 units of overhead followed
+//    by its pages (c0 = piece_cost: a piece's set-up and finish, and the
+//    consumer warps a short piece leaves idle, cost about that many pages'
+//    time); a piece is the part of one request's pages inside one range, so
+//    every CTA gets the same pages + overhead to within one.  R is capped so
+//    that no request is cut into more than max_splits pieces (a segment of
+//    s units meets at most ceil(s R / T) + 1 ranges); the rule is used when
 //    max_splits >= 3 and the caps leave at least 3/4 of the CTA groups.
-//  - chunk: each request is first cut into at most max_splits chunks of
-//    about cp pages; a range takes the chunks that start inside it.  Used
+//  - chunk: the line is the bare pages (c0 = 0); each request is first cut
+//    into at most max_splits chunks of about cp pages, and a range takes the
+//    chunks that start inside it.  Used
 //    for small batches (T below the number of CTA groups) and batches whose
 //    longest request the split cap would otherwise leave on few CTAs.
 struct WorkSplit {

@@ -1,19 +1,22 @@
 """The grouped-query split kernel's work split, restated in Python and checked
 for the properties the merge relies on (host logic, no GPU).
 
-Every split CTA works out its own pieces from the lengths: the requests'
-pages, concatenated in request order, are cut into R ranges
-[floor(kT/R), floor((k+1)T/R)); CTA group k takes range k.  Cut rule: a piece
-is the part of one request inside one range.  Chunk rule (small or lopsided
-batches): requests are cut into chunks of about cp pages, at most max_splits
-of them, and a range takes the chunks that start in it.  The restatement
+Every split CTA works out its own pieces from the lengths: the requests, in
+request order, lie on a line of T units cut into R ranges
+[floor(kT/R), floor((k+1)T/R)); CTA group k takes range k.  Cut rule: each
+request's segment of the line is `cost` units of per-piece overhead followed
+by its pages, and a piece is the part of one request's pages inside one
+range.  Chunk rule (small or lopsided batches): the line is the bare pages,
+requests are cut into chunks of about cp pages, at most max_splits of them,
+and a range takes the chunks that start in it.  The restatement
 follows the kernel step by step (the first piece found by a 32-request pass,
 then a walk), so that its index arithmetic can be checked here on many
 batches: every valid request is tiled exactly once, in order, by pieces
 numbered first_b .. first_b + n_b - 1 with n_b <= max_splits; piece numbers
 are distinct and fit the workspace (batch * max_splits); each request has a
-first piece (whose CTA records the numbering); under the cut rule every
-busy range holds the same number of pages to within one.  The kernel itself
+first piece (whose CTA records the numbering); under the cut rule each
+range's pages plus the overhead units inside it fill the range exactly, and
+every busy range holds the same share to within one.  The kernel itself
 is checked end to end against the oracle by the GPU parity tests."""
 import random
 
@@ -177,15 +180,16 @@ def _check(lens, S, MP, Hkv, ms, grid, cost=0):
     return chunks, len(pieces)
 
 
-def test_bench_shapes():
+@pytest.mark.parametrize("cost", [0, 16])  # 16: the kernel's piece cost
+def test_bench_shapes(cost):
     rng = random.Random(1)
     lens = [int(round(2 ** rng.uniform(0, 16))) for _ in range(64)]
-    assert _check(lens, 16, 4096, 8, 64, 456)[0] is False      # ragged batch: cut rule
-    assert _check([131072] * 8, 16, 8192, 8, 64, 456) == (False, 64)
-    assert _check([37, 100], 16, 8, 8, 64, 456) == (True, 2)   # tiny: chunk rule
+    assert _check(lens, 16, 4096, 8, 64, 456, cost)[0] is False      # ragged batch: cut rule
+    assert _check([131072] * 8, 16, 8192, 8, 64, 456, cost) == (False, 64)
+    assert _check([37, 100], 16, 8, 8, 64, 456, cost) == (True, 2)   # tiny: chunk rule
 
 
-@pytest.mark.parametrize("cost", [0, 3])
+@pytest.mark.parametrize("cost", [0, 3, 16])
 @pytest.mark.parametrize("seed", range(2))
 def test_random_batches(seed, cost):
     rng = random.Random(100 + seed)
