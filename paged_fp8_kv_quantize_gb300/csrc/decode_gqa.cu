@@ -30,9 +30,11 @@
 //                merges the partials of a request cut into several pieces
 //                by the log-sum-exp rule, split weights staged in shared
 //                memory and splits spread over thread groups.
-//   A request with a data-fault bit gets zero output.  Each kernel is a
-//   programmatic dependent of the kernel before it, so its launch and
-//   prologue overlap that kernel's tail.
+//   A request with a data-fault bit gets zero output.  The merge is a
+//   programmatic dependent of the split kernel, so its launch and prologue
+//   overlap the split's tail.  The split kernel is launched the same way,
+//   but a previous call's merge releases it only when it has finished:
+//   split CTAs placed beside running merge CTAs slowed back-to-back calls.
 #include <math.h>
 
 #include <mutex>
