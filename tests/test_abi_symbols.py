@@ -34,7 +34,9 @@ def test_host_only_entry_points():
     assert "workspace" in abi.strerror(-5)
     d = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, 16)
     n = abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 64)
-    # header + plan + split descriptors + (m, l) and O partials for every (request, split, head)
+    # header, per-request split index and count, split descriptors, (m, l) and
+    # O partials for every (request, split, head), a status word per split and
+    # an abort word per split CTA
     fixed = 64 * 64 * 32 * (8 + 4 * 128) + 64 * 64 * 32
     assert fixed <= n < fixed + 64 * 1024
 
@@ -58,6 +60,13 @@ def test_argument_errors_return_before_any_cuda_call():
     empty_tail = [None, 32, None, None, None, 0, 8, 1.0, 0, 64, None, 0, None, None, None]
     assert f(ctypes.byref(ok), *empty_tail) == 0
     assert g(ctypes.byref(ok), None, None, 0, None, None, None, None, 0, 1, 0, None, None) == 0
+    # batch * max_pages above 2^40: the kernels' page arithmetic would leave
+    # its exact range, so the call is refused (2^21 x 2^19 = 2^40 passes this
+    # check and stops at the next one, the NULL buffers)
+    big = [None, 32, None, None, None, 1 << 21, 1 << 20, 1.0, 0, 64, None, 0, None, None, None]
+    assert f(ctypes.byref(ok), *big) == -2
+    edge = [None, 32, None, None, None, 1 << 21, 1 << 19, 1.0, 0, 64, None, 0, None, None, None]
+    assert f(ctypes.byref(ok), *edge) == -1
 
 
 def test_page_allocator_host_checks():
