@@ -171,8 +171,9 @@ size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32
  * pfkv_decode_workspace_bytes(cache, batch, num_q_heads, max_splits) bytes;
  * its contents need no initialisation and are scratch between calls.
  * Supported: head_dim 64 or 128 with groups 1, 2, 4, 8 (page_size a
- * multiple of 16, at most 256); the latent stream head_dim 576 / v_head_dim
- * 512 with 64 query heads (FP8, PER_TOKEN, page_size 64).
+ * multiple of 16, at most 256; at most 4096 KV heads, else
+ * PFKV_ERR_UNSUPPORTED); the latent stream head_dim 576 / v_head_dim 512
+ * with 64 query heads (FP8, PER_TOKEN, page_size 64).
  * pfkv_paged_decode_attention_fp8 requires an FP8 cache, _bf16 a BF16 cache.
  */
 int pfkv_paged_decode_attention_fp8(const pfkv_cache *cache, const void *q, int32_t num_q_heads,
