@@ -38,21 +38,16 @@ int num_sms() {
 
 static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool latent) {
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
   WsLayout w;
   const size_t slots = (size_t)batch * max_splits * q_heads;
-  w.hdr = 0;
-  w.split_first = up256(sizeof(WsHeader));
+  w.split_first = 0;
   w.split_count = w.split_first + up256(sizeof(int) * ((size_t)batch + 1));
-  w.chunk_info = w.split_count + up256(sizeof(int) * (size_t)batch);
-  w.cta_first = w.chunk_info + up256(2 * sizeof(int4) * (size_t)batch * max_splits);
-  w.part_ml = w.cta_first + up256(sizeof(int) * (kMaxRanges + 1));
+  w.part_ml = w.split_count + up256(sizeof(int) * (size_t)batch);
   w.part_o = w.part_ml + up256(sizeof(float2) * slots);
   w.part_st = w.part_o + up256(sizeof(float) * slots * v_dim);
   w.cta_abort = w.part_st + up256(sizeof(uint32_t) * (size_t)batch * max_splits);
-  w.qterms = w.cta_abort + up256(sizeof(int) * (size_t)kMaxCtas);
-  w.qfac = w.qterms + (latent ? up256(kLatentQTermBytes * (size_t)batch) : 0);
-  w.total = w.qfac + (latent ? up256(sizeof(float) * (size_t)batch * q_heads) : 0);
+  w.total = w.cta_abort + up256(sizeof(int) * (size_t)kMaxCtas);
   return w;
 }
 
@@ -103,7 +98,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   if (Hq % c->num_kv_heads) return PFKV_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(out)) return PFKV_ERR_ALIGN;
   if (c->page_size % 16 || c->page_size > 256) return PFKV_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(batch, Hq, c->v_head_dim, max_splits, is_latent(c));
+  const WsLayout L = ws_layout(batch, Hq, c->v_head_dim, max_splits);
   if (ws_bytes < L.total) return PFKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return PFKV_ERR_ALIGN;
 
@@ -118,22 +113,15 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.sm_scale_log2 = softmax_scale * 1.4426950408889634f;
   a.flags = flags; a.max_splits = max_splits;
   uint8_t *w = static_cast<uint8_t *>(ws);
-  a.hdr = reinterpret_cast<WsHeader *>(w + L.hdr);
   a.split_first = reinterpret_cast<int *>(w + L.split_first);
   a.split_count = reinterpret_cast<int *>(w + L.split_count);
-  a.chunk_info = reinterpret_cast<int4 *>(w + L.chunk_info);
   a.part_ml = reinterpret_cast<float2 *>(w + L.part_ml);
   a.part_o = reinterpret_cast<float *>(w + L.part_o);
   a.out = out; a.status = status;
   a.append = k_new != nullptr;
-  a.split_append = 0;
   a.k_new = static_cast<const uint16_t *>(k_new);
   a.v_new = static_cast<const uint16_t *>(v_new);
   a.cache = *c;
-  a.qprep = 0;
-  a.balanced = 0;
-  a.cta_first = reinterpret_cast<int *>(w + L.cta_first);
-  a.self_plan = 0;
   a.ranges = 0;
   a.target_items = 0;
   a.min_chunk_pages = 1;
@@ -141,8 +129,6 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.piece_cost = 0;
   a.part_st = reinterpret_cast<uint32_t *>(w + L.part_st);
   a.cta_abort = reinterpret_cast<int *>(w + L.cta_abort);
-  a.qterms = w + L.qterms;
-  a.qfac = reinterpret_cast<float *>(w + L.qfac);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (c->kv_shared) {
     if (!is_latent(c) || Hq != 64 || c->dtype != PFKV_DTYPE_FP8_E4M3 || c->scale_mode != PFKV_SCALE_PER_TOKEN ||
@@ -202,7 +188,7 @@ int pfkv_kv_append_quantize(const pfkv_cache *cache, const void *k_new, const vo
 
 size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32_t num_q_heads, int32_t max_splits) {
   if (!cache || batch < 0 || num_q_heads < 1 || max_splits < 1) return 0;
-  return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits, is_latent(cache)).total;
+  return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits).total;
 }
 
 int pfkv_paged_decode_attention_fp8(const pfkv_cache *cache, const void *q, int32_t num_q_heads,

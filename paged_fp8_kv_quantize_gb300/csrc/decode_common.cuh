@@ -1,7 +1,7 @@
-// decode_common.cuh -- pieces shared by the decode kernels: the split plan
-// (flash-decoding work list) and the log-sum-exp merge of split partials.
-// Included by each decode translation unit; everything here has internal
-// linkage.
+// decode_common.cuh -- pieces shared by the decode kernels: the work split
+// (flash-decoding pieces, worked out by every CTA from the lengths) and the
+// log-sum-exp merge of split partials.  Included by each decode translation
+// unit; everything here has internal linkage.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -23,392 +23,248 @@ struct ItemDesc {
   int nb;  // splits of request b
 };
 
-// ---------------------------------------------------------------- plan
+// ---------------------------------------------------------------- work split
+//
+// There is no plan kernel: every CTA works out its own share from the
+// lengths, and all CTAs reach the same answer.  The requests, in
+// request order (a request with a bad length counting nothing), lie on a
+// line of T units that is cut into R ranges [floor(kT/R), floor((k+1)T/R));
+// CTA k * Hkv + h takes range k for KV head h (the latent stream: Hkv = 1).  Pieces of a request are
+// numbered consecutively in request order over the whole call (the merge
+// finds a request's pieces at split_first[b] .. + split_count[b]).  Two
+// rules:
+//  - cut: a request's segment of the line is c0 units of overhead followed
+//    by its pages (c0 = piece_cost: a piece's set-up and finish, and the
+//    consumer warps a short piece leaves idle, cost about that many pages'
+//    time); a piece is the part of one request's pages inside one range, so
+//    every CTA gets the same pages + overhead to within one.  R is capped so
+//    that no request is cut into more than max_splits pieces (a segment of
+//    s units meets at most ceil(s R / T) + 1 ranges); the rule is used when
+//    max_splits >= 3 and the caps leave at least 3/4 of the CTA groups.
+//  - chunk: the line is the bare pages (c0 = 0); each request is first cut
+//    into at most max_splits chunks of about cp pages, and a range takes the
+//    chunks that start inside it.  Used
+//    for small batches (T below the number of CTA groups) and batches whose
+//    longest request the split cap would otherwise leave on few CTAs.
+struct WorkSplit {
+  long long T, R, r0, r1, cp, max_len;
+  int k, chunks;
+  int c0;  // cut rule: overhead length placed before each request's pages on the cut line
+  // walk: next request to look at, its first page in the concatenation, the
+  // number of its first piece, and (chunk rule) its next chunk
+  int b;
+  long long off, first, c;
+};
 
-constexpr int kSortMax = 2048;  // requests ordered by length when the batch is at most this
+struct Piece {
+  int b, cg, p0, p1, L, nb;
+  bool lead;  // the request's first piece: its CTA of head 0 records the numbering
+};
 
-// Blocks after the first (decode step only): one warp per (request, K|V,
-// head) writes the step's new token at position seq_lens[b] - 1.  The split
-// kernel's grid-dependency wait covers this whole grid, so its page reads
-// see the new rows.  Status is the planning block's: the attention inspects
-// the same destination page under the same rules, so every refusal here is
-// also a status bit there.
-__device__ __forceinline__ void plan_append(const DecodeArgs &a) {
-  // heads of the cache itself (a work-item view such as the latent kernel's
-  // head groups may use another Hkv in the rest of DecodeArgs)
-  const int H = a.cache.num_kv_heads;
-  const int units = (a.cache.kv_shared ? 1 : 2) * H;
-  const int gw = (int)(blockIdx.x - 1) * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5);
-  const int b = gw / units, unit = gw - b * units;
-  if (b >= a.B) return;
-  const int part = unit / H, h = unit - part * H, lane = threadIdx.x & 31;
-  const bool fp8 = a.cache.dtype == PFKV_DTYPE_FP8_E4M3;
-  const bool regs = append_row_fits(a.cache);
-  AppendRow r;
-  if (regs)  // the row and its scale load while the destination is looked up
-    r = fp8 ? append_row_load<true>(a.cache, a.k_new, a.v_new, b, part, h, lane)
-            : append_row_load<false>(a.cache, a.k_new, a.v_new, b, part, h, lane);
-  const int pos = a.seq_lens[b] - 1;
-  int page = -1;
-  if (append_target(a.cache, b, pos, a.block_table, a.block_tags, a.MP, a.flags, &page)) return;
-  if (regs) {
-    if (fp8) append_row_store<true>(a.cache, r, part, h, page, pos, lane);
-    else append_row_store<false>(a.cache, r, part, h, page, pos, lane);
-  } else {
-    if (fp8) append_row_wide<true>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, lane);
-    else append_row_wide<false>(a.cache, a.k_new, a.v_new, b, part, h, page, pos, lane);
-  }
-}
-
-// Append blocks of the plan grid (decode step only).
-__host__ __device__ inline int plan_append_blocks(const DecodeArgs &a) {
-  if (!a.append) return 0;
-  const long long warps = (long long)a.B * (a.cache.kv_shared ? 1 : 2) * a.cache.num_kv_heads;
-  return (int)((warps + 31) / 32);
-}
-
-// Number of plan-grid blocks: the planning block, the append blocks, and
-// (latent stream) one query-term block per request.
-__host__ __device__ inline int plan_blocks(const DecodeArgs &a) { return 1 + plan_append_blocks(a) + (a.qprep ? a.B : 0); }
-
-// Query terms of request b for the latent-stream kernel.  Head h's bf16 row
-// q (576 values) is scaled by 2^-e_h, e_h = the exponent that puts max|q| in
-// [128, 256), and written as T1 = e4m3(q 2^-e_h), T2 = e4m3(q 2^-e_h - T1):
-// T1 + T2 equals the scaled row exactly for every element of magnitude at
-// least 2^-2 (a bf16 significand has 8 bits, each term carries 4), the
-// rest to within 2^-10.  The terms form one 128-row operand: row
-// R = 32 (h / 16) + 16 t + h % 16 holds term t of head h.  Columns 0-511 of
-// row R are stored as 512 plain bytes at R * 512 (loaded into tensor memory
-// by the kernel), columns 512-575 as the 64-byte-swizzled shared-memory
-// image at 65536: 16-byte chunk j of row R at 65536 + R * 64 +
-// 16 (j ^ ((R >> 1) & 3)).  qfac[h] = softmax scale * log2(e) * 2^e_h.
-__device__ __forceinline__ void plan_qprep(const DecodeArgs &a, int b) {
-  __shared__ float s_qinv[64];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint16_t *q = static_cast<const uint16_t *>(a.q) + (size_t)b * 64 * 576;
-  for (int h = warp; h < 64; h += (int)(blockDim.x >> 5)) {
-    float m = 0.f;
-    for (int k = lane; k < 576; k += 32) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)q[h * 576 + k] << 16)));
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) {
-      int e = 8;
-      if (m > 0.f) frexpf(m, &e);  // m = f 2^e, f in [0.5, 1)
-      s_qinv[h] = ldexpf(1.f, 8 - e);
-      a.qfac[(size_t)b * 64 + h] = a.sm_scale_log2 * ldexpf(1.f, e - 8);
+// The work split runs once per call, at the start of every CTA, as code the
+// call has not run yet: an SM fetches it from memory line by line (measured,
+// latent-stream kernel: about 1 us per KB of straight-line code run for the
+// first time in a call).  Its helpers are therefore compiled once
+// (noinline) rather than copied into every call site, which keeps the
+// start-up path short.
+//
+// floor(x / y) for x >= 0 and y >= 1 (the entry points bound batch *
+// max_pages by 2^40, and every dividend here is at most 2^12 times a page
+// count, so x < 2^53).  Operands that fit 32 bits -- every practical batch --
+// take the 32-bit unsigned division; larger ones a bitwise long division.
+// No floating point: double precision is slow on this part (an earlier
+// reciprocal-estimate form in fp64 cost 0.3-0.6 us per call).
+__device__ __forceinline__ unsigned long long div_floor_wide(unsigned long long x, unsigned long long y) {
+  unsigned long long q = 0, r = 0;
+  for (int i = 63; i >= 0; --i) {
+    r = (r << 1) | ((x >> i) & 1ull);
+    if (r >= y) {
+      r -= y;
+      q |= 1ull << i;
     }
   }
-  __syncthreads();
-  uint8_t *dst = a.qterms + (size_t)b * kLatentQTermBytes;
-  for (int u = tid; u < 64 * 36; u += (int)blockDim.x) {
-    const int h = u / 36, r = u % 36;
-    const int k0 = 16 * r;  // 16 columns starting here (r < 36 covers all 576)
-    const int R1 = 32 * (h >> 4) + (h & 15), R2 = R1 + 16;  // rows of T1 and T2 of head h
-    size_t off1, off2;
-    if (r < 32) {
-      off1 = (size_t)R1 * 512 + 16 * r;
-      off2 = (size_t)R2 * 512 + 16 * r;
-    } else {
-      const int j = r - 32;
-      off1 = (size_t)65536 + R1 * 64 + 16 * (j ^ ((R1 >> 1) & 3));
-      off2 = (size_t)65536 + R2 * 64 + 16 * (j ^ ((R2 >> 1) & 3));
-    }
-    uint32_t t1[4], t2[4];
-    {
-      const uint4 *src = reinterpret_cast<const uint4 *>(q + h * 576 + k0);
-      const uint4 v0 = src[0], v1 = src[1];
-      const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      const float inv = s_qinv[h];
-#pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        const float x0 = __uint_as_float(wv[i] << 16) * inv, x1 = __uint_as_float(wv[i] & 0xffff0000u) * inv;
-        const float x2 = __uint_as_float(wv[i + 1] << 16) * inv, x3 = __uint_as_float(wv[i + 1] & 0xffff0000u) * inv;
-        const uint32_t a01 = f32x2_to_e4m3x2(x0, x1), a23 = f32x2_to_e4m3x2(x2, x3);
-        const uint32_t h01 = e4m3x2_to_f16x2(a01), h23 = e4m3x2_to_f16x2(a23);
-        const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
-        const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
-        t1[i / 2] = a01 | (a23 << 16);
-        t2[i / 2] = f32x2_to_e4m3x2(x0 - f01.x, x1 - f01.y) | (f32x2_to_e4m3x2(x2 - f23.x, x3 - f23.y) << 16);
-      }
-    }
-    *reinterpret_cast<uint4 *>(dst + off1) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
-    *reinterpret_cast<uint4 *>(dst + off2) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
-  }
+  return q;
 }
 
-// Exclusive prefix over the block (1024 threads) of one int64 per thread;
-// returns this thread's prefix, the block total in *total.  s_w: 33 entries.
-__device__ __forceinline__ long long block_excl_scan(long long v, long long *s_w, long long *total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  long long x = v;
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_w[wid] = x;
-  __syncthreads();
-  if (wid == 0) {
-    long long w = lane < (int)(blockDim.x >> 5) ? s_w[lane] : 0;
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    s_w[lane] = w;  // inclusive prefix of warp totals
-  }
-  __syncthreads();
-  const long long r = (wid ? s_w[wid - 1] : 0) + x - v;
-  *total = s_w[(blockDim.x >> 5) - 1];
-  __syncthreads();
-  return r;
+__device__ __noinline__ long long div_floor(long long x, long long y) {
+  const unsigned long long ux = (unsigned long long)x, uy = (unsigned long long)y;
+  if (((ux | uy) >> 32) == 0ull) return (long long)((uint32_t)ux / (uint32_t)uy);
+  return (long long)div_floor_wide(ux, uy);
 }
 
-// Balanced plan: the requests' pages, concatenated in request order (T in
-// all), are cut into R ranges [floor(kT/R), floor((k+1)T/R)), one per CTA;
-// an item is the part of one request inside one range.  Every CTA gets the
-// same number of pages to within one, and at most R + B - 1 partial results
-// are written.  R <= ranges, R <= T, and R is small enough that no request
-// is cut into more than max_splits pieces (a request of p pages meets at
-// most ceil(p R / T) + 1 ranges).  Returns false, having written nothing
-// but status, when those caps leave fewer than 3/4 of `ranges`.
-__device__ bool plan_balanced(const DecodeArgs &a, int ranges) {
-  __shared__ long long s_w[33];
-  __shared__ long long s_tot, s_max, s_pcarry, s_icarry;
-  // one pass of up to 1024 requests, handed from the thread that sized a
-  // request to the warp that writes its chunks (one chunk per lane)
-  __shared__ long long s_off[1024];
-  __shared__ int s_np[1024], s_kf[1024], s_n[1024], s_first[1024];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+__device__ __forceinline__ int ws_pages(const WorkSplit &w, int L, int S) {
+  return (L < 1 || (long long)L > w.max_len) ? 0 : (int)(((unsigned)L + (unsigned)S - 1u) / (unsigned)S);
+}
+
+// Pieces of a request of p > 0 pages whose segment of the cut line starts
+// at `off` (its pages start at off + c0); *ppc: chunk length (chunk rule).
+__device__ __noinline__ int ws_count(const WorkSplit &w, long long off, int p, int max_splits, int *ppc) {
+  if (!w.chunks) {
+    const long long s0 = off + w.c0;
+    return (int)(div_floor((s0 + p) * w.R - 1, w.T) - div_floor((s0 + 1) * w.R - 1, w.T) + 1);
+  }
+  int nn = w.cp >= p ? 1 : (int)(((unsigned)p + (unsigned)w.cp - 1u) / (unsigned)w.cp);
+  if (nn > max_splits) nn = max_splits;
+  const int q = (int)(((unsigned)p + (unsigned)nn - 1u) / (unsigned)nn);
+  *ppc = q;
+  return (int)(((unsigned)p + (unsigned)q - 1u) / (unsigned)q);
+}
+
+// Warp-wide (all 32 lanes, same result in each): the rule, R and this CTA's
+// range, then the first request with a piece in it.
+__device__ __noinline__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
   const int S = a.S;
-  const long long max_len = (long long)a.MP * S;
-  long long tot = 0, mx = 0;
-  for (int b = tid; b < a.B; b += blockDim.x) {
-    const int L = a.seq_lens[b];
-    const bool bad = L < 1 || (long long)L > max_len;
-    a.status[b] = bad ? PFKV_ST_BAD_LEN : 0u;
-    const long long p = bad ? 0 : (L + S - 1) / S;
+  w.max_len = (long long)a.MP * S;
+  long long tot = 0;
+  int mx = 0, nv = 0;
+  for (int b = lane; b < a.B; b += 32) {
+    const int p = ws_pages(w, __ldg(&a.seq_lens[b]), S);
     tot += p;
     mx = p > mx ? p : mx;
+    nv += p > 0;
   }
+#pragma unroll
   for (int o = 16; o; o >>= 1) {
     tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    const long long y = __shfl_xor_sync(0xffffffffu, mx, o);
-    mx = y > mx ? y : mx;
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    nv += __shfl_xor_sync(0xffffffffu, nv, o);
   }
-  if (tid == 0) { s_tot = 0; s_max = 0; s_pcarry = 0; s_icarry = 0; }
-  __syncthreads();
-  if ((tid & 31) == 0) {
-    atomicAdd(reinterpret_cast<unsigned long long *>(&s_tot), (unsigned long long)tot);
-    atomicMax(reinterpret_cast<unsigned long long *>(&s_max), (unsigned long long)mx);
-  }
-  __syncthreads();
-  const long long T = s_tot, pmax = s_max;
-  long long R = ranges;
-  if (R > T) R = T;
-  if (pmax > 0) {
-    const long long cap = (long long)(a.max_splits - 2) * T / pmax;
+  long long T = tot;
+  const long long ranges = a.ranges, c = a.piece_cost;
+  const long long Tc = T + c * nv;  // the cut rule's line: pages plus c before each request
+  long long R = ranges < Tc ? ranges : Tc;
+  if (mx > 0 && a.max_splits >= 3) {
+    const long long cap = div_floor((long long)(a.max_splits - 2) * Tc, mx + c);
     if (R > cap) R = cap;
   }
-  if (R > kMaxRanges) R = kMaxRanges;
-  if (R < 1) R = 1;
-  if (T > 0 && 4 * R < 3 * (long long)ranges) return false;
-  if (tid == 0 && T == 0) a.cta_first[0] = 0;
-  for (int base = 0; base < a.B; base += blockDim.x) {
-    const int b = base + tid;
-    long long pages = 0;
-    int L = 0;
-    if (b < a.B) {
-      L = a.seq_lens[b];
-      pages = (L < 1 || (long long)L > max_len) ? 0 : (L + S - 1) / S;
+  w.chunks = !(a.max_splits >= 3 && T > 0 && R >= 1 && 4 * R >= 3 * ranges);
+  if (w.chunks) {
+    R = ranges < T ? ranges : T;
+    const long long cp = div_floor(T * a.Hkv + a.target_items - 1, a.target_items);
+    w.cp = cp < a.min_chunk_pages ? a.min_chunk_pages : cp;
+    w.c0 = 0;
+  } else {
+    w.cp = 0;
+    w.c0 = (int)c;
+    T = Tc;
+  }
+  w.T = T;
+  w.R = R < 1 ? 1 : R;
+  w.k = (int)blockIdx.x / a.Hkv;
+  w.b = a.B;  // no pieces unless found below
+  w.off = w.first = w.c = 0;
+  if (T == 0 || w.k >= w.R) return;
+  w.r0 = div_floor((long long)w.k * T, w.R);
+  w.r1 = div_floor((long long)(w.k + 1) * T, w.R);
+  long long off_c = 0, first_c = 0;  // totals of earlier passes
+  for (int base = 0; base < a.B; base += 32) {
+    const int b = base + lane;
+    const int p = b < a.B ? ws_pages(w, __ldg(&a.seq_lens[b]), S) : 0;
+    const long long seg = p > 0 ? p + w.c0 : 0;  // the request's segment of the cut line
+    long long xp = seg;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, xp, o);
+      if (lane >= o) xp += y;
     }
-    long long ptot;
-    const long long off = s_pcarry + block_excl_scan(pages, s_w, &ptot);
-    long long kf = 0, kl = -1;
-    if (pages > 0) {
-      kf = ((off + 1) * R - 1) / T;          // range holding the first page
-      kl = ((off + pages) * R - 1) / T;      // range holding the last page
+    const long long off = off_c + xp - seg;
+    int ppc = 1, n = 0;
+    if (p > 0) n = ws_count(w, off, p, a.max_splits, &ppc);
+    long long xn = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, xn, o);
+      if (lane >= o) xn += y;
     }
-    const long long n = pages > 0 ? kl - kf + 1 : 0;
-    long long itot;
-    const long long first = s_icarry + block_excl_scan(n, s_w, &itot);
-    if (b < a.B) {
-      a.split_first[b] = (int)first;
-      a.split_count[b] = (int)n;
+    const long long first = first_c + xn - n;
+    bool has = false;
+    int c_lo = 0;
+    if (p > 0 && off + w.c0 < w.r1 && off + w.c0 + p > w.r0) {
+      if (!w.chunks) {
+        has = true;
+      } else {
+        // r0 - off < p here, so the chunk index fits an int
+        c_lo = off >= w.r0 ? 0 : (int)((unsigned)(w.r0 - off + ppc - 1) / (unsigned)ppc);
+        has = c_lo < n && off + (long long)c_lo * ppc < w.r1;
+      }
     }
-    s_off[tid] = off;
-    s_np[tid] = (int)pages;
-    s_kf[tid] = (int)kf;
-    s_n[tid] = b < a.B ? (int)n : 0;
-    s_first[tid] = (int)first;
-    __syncthreads();
-    // chunk descriptors: warp per request, lane per chunk
-    const int in_pass = min((int)blockDim.x, a.B - base);
-    for (int i = wid; i < in_pass; i += (int)(blockDim.x >> 5)) {
-      const int bi = base + i, ni = s_n[i], fi = s_first[i];
-      const long long oi = s_off[i], pi = s_np[i];
-      if (ni == 0) {  // bad length: no item writes this request's rows
-        for (size_t k = lane; k < (size_t)a.Hq * a.Dv; k += 32) a.out[(size_t)bi * a.Hq * a.Dv + k] = 0.f;
+    const unsigned m = __ballot_sync(0xffffffffu, has);
+    if (m) {
+      const int src = __ffs(m) - 1;
+      w.b = base + src;
+      w.off = __shfl_sync(0xffffffffu, off, src);
+      w.first = __shfl_sync(0xffffffffu, first, src);
+      w.c = __shfl_sync(0xffffffffu, c_lo, src);
+      return;
+    }
+    off_c += __shfl_sync(0xffffffffu, xp, 31);
+    first_c += __shfl_sync(0xffffffffu, xn, 31);
+  }
+}
+
+// The CTA's next piece, in request order (uniform across the warp); false
+// when the range has none left.  A piece that would break the workspace
+// bounds ends the walk instead of being used (it cannot occur when the
+// rules above hold).
+__device__ __noinline__ bool ws_next(WorkSplit &w, const DecodeArgs &a, Piece &pc) {
+  while (w.b < a.B) {
+    const int L = __ldg(&a.seq_lens[w.b]);
+    const int p = ws_pages(w, L, a.S);
+    if (p == 0) {
+      ++w.b;
+      continue;
+    }
+    if (w.off + w.c0 >= w.r1) return false;
+    int ppc = 1;
+    const int n = ws_count(w, w.off, p, a.max_splits, &ppc);
+    long long j, p0, p1;
+    if (!w.chunks) {
+      const long long s0 = w.off + w.c0;  // the request's first page on the cut line
+      j = (long long)w.k - div_floor((s0 + 1) * w.R - 1, w.T);
+      p0 = (w.r0 > s0 ? w.r0 : s0) - s0;
+      p1 = (w.r1 < s0 + p ? w.r1 : s0 + p) - s0;
+    } else {
+      if (w.c >= n) {
+        w.first += n;
+        w.off += p;
+        ++w.b;
+        w.c = 0;
         continue;
       }
-      const int Li = a.seq_lens[bi];
-      for (int j = lane; j < ni; j += 32) {
-        const long long k = s_kf[i] + j;
-        const long long r0 = k * T / R, r1 = (k + 1) * T / R;
-        const long long p0 = (r0 > oi ? r0 : oi) - oi, p1 = (r1 < oi + pi ? r1 : oi + pi) - oi;
-        a.chunk_info[2 * (fi + j)] = make_int4(bi, (int)p0, (int)p1, Li);
-        a.chunk_info[2 * (fi + j) + 1] = make_int4(ni, j, (int)k, 0);
-        if (j > 0 || oi == r0) a.cta_first[k] = fi + j;  // first item of range k
-      }
+      if (w.off + w.c * ppc >= w.r1) return false;
+      j = w.c++;
+      p0 = j * ppc;
+      p1 = p0 + ppc < p ? p0 + ppc : p;
     }
-    __syncthreads();
-    if (tid == 0) {
-      s_pcarry += ptot;
-      s_icarry += itot;
+    const long long cg = w.first + j;
+    if (j < 0 || j >= n || n > a.max_splits || p0 < 0 || p0 >= p1 || p1 > p || cg >= (long long)a.B * a.max_splits)
+      return false;
+    pc.b = w.b;
+    pc.cg = (int)cg;
+    pc.p0 = (int)p0;
+    pc.p1 = (int)p1;
+    pc.L = L;
+    pc.nb = n;
+    pc.lead = j == 0;
+    if (!w.chunks) {
+      w.first += n;
+      w.off += p + w.c0;
+      ++w.b;
     }
-    __syncthreads();
+    return true;
   }
-  if (tid == 0) {
-    a.cta_first[R] = (int)s_icarry;
-    a.hdr->n_chunks = (int)s_icarry;
-    a.hdr->n_items = (int)s_icarry * a.Hkv;
-    a.hdr->work = 0u;
-    a.hdr->err = 0u;
-    a.hdr->chunk_pages = (int)R;
-    a.hdr->n_ranges = (int)R;
-  }
-  return true;
+  return false;
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(DecodeArgs a, int target_items, int min_chunk_pages) {
-  // Launched as a programmatic dependent: the stream's earlier work is
-  // complete from here.  Only then may the split kernel launch (it waits for
-  // this grid's results before reading them): its CTAs must not take SMs
-  // while the previous call's merge still runs.
-  pdl_wait();
-  pdl_launch_dependents();
-  if (blockIdx.x > 0) {
-    const int nab = plan_append_blocks(a);
-    if ((int)blockIdx.x <= nab) plan_append(a);
-    else plan_qprep(a, (int)blockIdx.x - 1 - nab);
-    return;
-  }
-  if (a.balanced > 0 && plan_balanced(a, a.balanced)) return;
-  __shared__ long long s_red[32];
-  __shared__ int s_scan[32];
-  __shared__ int s_carry;
-  __shared__ int s_order[kSortMax];  // position -> request, longest first
-  __shared__ int s_pages[kSortMax];  // request -> pages (0 for a bad length)
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int S = a.S;
-  const long long max_len = (long long)a.MP * S;
-  const bool sorted = a.B <= kSortMax;
-  auto pages_of = [&](int b) -> int {
-    if (sorted) return s_pages[b];
-    const int L = a.seq_lens[b];
-    return (L < 1 || (long long)L > max_len) ? 0 : (L + S - 1) / S;
-  };
-  // status (bad lengths) and total pages, which sets the split size
-  long long tot = 0;
-  for (int b = tid; b < a.B; b += blockDim.x) {
-    const int L = a.seq_lens[b];
-    const bool bad = L < 1 || (long long)L > max_len;
-    a.status[b] = bad ? PFKV_ST_BAD_LEN : 0u;
-    if (!bad) tot += (L + S - 1) / S;
-    if (sorted) s_pages[b] = bad ? 0 : (L + S - 1) / S;
-  }
-  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  if (lane == 0) s_red[wid] = tot;
-  __syncthreads();
-  if (wid == 0) {
-    long long v = lane < (int)(blockDim.x >> 5) ? s_red[lane] : 0;
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) s_red[0] = v;
-  }
-  __syncthreads();
-  const long long total_units = s_red[0] * a.Hkv;
-  long long cp = (total_units + target_items - 1) / target_items;
-  if (cp < min_chunk_pages) cp = min_chunk_pages;
-  if (sorted)  // rank by (pages descending, index ascending)
-    for (int b = tid; b < a.B; b += blockDim.x) {
-      const int pb = pages_of(b);
-      int rank = 0;
-      for (int o = 0; o < a.B; ++o) {
-        const int po = pages_of(o);
-        rank += (po > pb) || (po == pb && o < b);
-      }
-      s_order[rank] = b;
-    }
-  if (tid == 0) s_carry = 0;
-  __syncthreads();
-  // split counts and their exclusive prefix in processing order, 1024 per pass
-  for (int base = 0; base < a.B; base += blockDim.x) {
-    const int r = base + tid;
-    const int b = r < a.B ? (sorted ? s_order[r] : r) : -1;
-    int n = 0, ppc = 0, pages = 0;
-    if (b >= 0) {
-      pages = pages_of(b);
-      if (pages) {
-        long long nn = (pages + cp - 1) / cp;
-        if (nn > a.max_splits) nn = a.max_splits;
-        ppc = (int)((pages + nn - 1) / nn);
-        n = (pages + ppc - 1) / ppc;
-      }
-    }
-    int x = n;
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) s_scan[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-      int v = lane < (int)(blockDim.x >> 5) ? s_scan[lane] : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      s_scan[lane] = v;  // inclusive prefix of warp totals
-    }
-    __syncthreads();
-    const int warp_off = wid ? s_scan[wid - 1] : 0;
-    const int excl = s_carry + warp_off + x - n;
-    if (b >= 0) {
-      a.split_first[b] = excl;
-      a.split_count[b] = n;
-      const int L = a.seq_lens[b];
-      for (int c = 0; c < n; ++c) {
-        a.chunk_info[2 * (excl + c)] = make_int4(b, c * ppc, min((c + 1) * ppc, pages), L);
-        a.chunk_info[2 * (excl + c) + 1] = make_int4(n, c, 0, 0);
-      }
-      if (n == 0)  // bad length: no split writes this request's rows
-        for (size_t k = 0; k < (size_t)a.Hq * a.Dv; ++k) a.out[(size_t)b * a.Hq * a.Dv + k] = 0.f;
-    }
-    __syncthreads();
-    if (tid == blockDim.x - 1) s_carry = excl + n;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    a.hdr->n_chunks = s_carry;
-    a.hdr->n_items = s_carry * a.Hkv;
-    a.hdr->work = 0u;
-    a.hdr->err = 0u;
-    a.hdr->chunk_pages = (int)cp;
-    a.hdr->n_ranges = 0;
-  }
-}
-
-// The plan grid, launched as a programmatic dependent of the stream's
-// previous kernel: its launch overlaps that kernel's tail, and it waits for
-// it (griddepcontrol.wait) before touching memory.
-inline cudaError_t launch_plan(const DecodeArgs &a, cudaStream_t s, int target_items, int min_chunk_pages) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan_blocks(a));
-  cfg.blockDim = dim3(1024);
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, plan_kernel, a, target_items, min_chunk_pages);
+// ws_next on a state kept in shared memory (one copy per warp), so that it
+// holds no registers while the pages go out.
+__device__ __forceinline__ bool ws_next_shared(WorkSplit &s, const DecodeArgs &a, Piece &pc, int lane) {
+  WorkSplit w = s;
+  __syncwarp();
+  const bool r = ws_next(w, a, pc);
+  if (lane == 0) s = w;
+  __syncwarp();
+  return r;
 }
 
 // ---------------------------------------------------------------- merge
@@ -440,75 +296,57 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   __shared__ float s_M[M::kNH], s_W[M::kNH];
   __shared__ float4 s_acc[256];
   __shared__ unsigned s_or[8];  // status bits per warp
-  // Latent stream: the next call's plan grid (one CTA that waits for this
-  // grid) may launch at once.  Grouped-query path: the next call's split
-  // grid launches only when this grid has finished.  Measured on the ragged
-  // batch of 64: letting it launch at this grid's start made the back-to-back
-  // call 165 us instead of 120 us, and at the end of this grid's wait 148 us
-  // (146 us with both kernels asking for the largest shared-memory carveout).
-  if (!a.self_plan) pdl_launch_dependents();
+  // The next call's split grid launches only when this grid has finished.
+  // Measured on the ragged batch of 64 (grouped-query path): letting it
+  // launch at this grid's start made the back-to-back call 165 us instead of
+  // 120 us, and at the end of this grid's wait 148 us (146 us with both
+  // kernels asking for the largest shared-memory carveout).
   pdl_wait();  // partials and status of the split kernel are visible from here on
   const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
   const int t = threadIdx.x;
   float *out_bg = a.out + ((size_t)b * a.Hq + g * kG) * kD;
   const int col_lo = (int)blockIdx.y * M::kW;
   const int h_lo = col_lo * 4 / kD;  // first head of this block's columns
-  int nb, c0;
-  // each split's (m, l) for the heads of this block's columns
-  auto load_ml = [&]() {
-    for (int i = t; i < nb * M::kNH; i += 256) {
-      const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / M::kNH) * a.Hq + g * kG + h_lo + i % M::kNH]);
-      s_w[i] = ml.x;
-      s_l[i] = ml.y;
-    }
-  };
-  if (a.self_plan) {
-    // Grouped-query path: this kernel writes status[b].  The block of
-    // (request, head 0, first columns) gathers the bits its pieces found
-    // and whether any split CTA gave up; every block zeroes its columns of
-    // a faulted request.  The pieces' (m, l) are loaded beside their status
-    // words.
-    const bool lead = g == 0 && blockIdx.y == 0;
-    const int L = a.seq_lens[b];
-    if (L < 1 || (long long)L > (long long)a.MP * a.S) {
-      for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
-      if (lead && t == 0) a.status[b] = PFKV_ST_BAD_LEN;
-      return;
-    }
-    nb = a.split_count[b];
-    c0 = a.split_first[b];
-    // written by this call's split kernel unless one of its CTAs gave up
-    // first; checked so that no read leaves the workspace
-    const bool sane = nb >= 1 && nb <= a.max_splits && c0 >= 0 && c0 <= a.B * a.max_splits - nb;
-    uint32_t st = 0u;
-    if (sane) {
-      for (int i = t; i < nb; i += 256) st |= __ldcg(&a.part_st[c0 + i]);
-      if (nb > 1) load_ml();
-    }
-    int any = 0;
-    if (lead)
-      for (int i = t; i < a.n_ctas; i += 256) any |= __ldcg(&a.cta_abort[i]);
-    st = __reduce_or_sync(0xffffffffu, st);
-    if ((t & 31) == 0) s_or[t >> 5] = st;
-    const bool gave_up = __syncthreads_or(any) != 0;
-    st = 0u;
+  // This kernel writes status[b].  The block of (request, head group 0, first
+  // columns) gathers the bits the request's pieces found and whether any
+  // split CTA gave up; every block zeroes its columns of a faulted request.
+  // The pieces' (m, l) are loaded beside their status words.
+  const bool lead = g == 0 && blockIdx.y == 0;
+  const int L = a.seq_lens[b];
+  if (L < 1 || (long long)L > (long long)a.MP * a.S) {
+    for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
+    if (lead && t == 0) a.status[b] = PFKV_ST_BAD_LEN;
+    return;
+  }
+  const int nb = a.split_count[b];
+  const int c0 = a.split_first[b];
+  // written by this call's split kernel unless one of its CTAs gave up
+  // first; checked so that no read leaves the workspace
+  const bool sane = nb >= 1 && nb <= a.max_splits && c0 >= 0 && c0 <= a.B * a.max_splits - nb;
+  uint32_t st = 0u;
+  if (sane) {
+    for (int i = t; i < nb; i += 256) st |= __ldcg(&a.part_st[c0 + i]);
+    if (nb > 1)  // each piece's (m, l) for the heads of this block's columns
+      for (int i = t; i < nb * M::kNH; i += 256) {
+        const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / M::kNH) * a.Hq + g * kG + h_lo + i % M::kNH]);
+        s_w[i] = ml.x;
+        s_l[i] = ml.y;
+      }
+  }
+  int any = 0;
+  if (lead)
+    for (int i = t; i < a.n_ctas; i += 256) any |= __ldcg(&a.cta_abort[i]);
+  st = __reduce_or_sync(0xffffffffu, st);
+  if ((t & 31) == 0) s_or[t >> 5] = st;
+  const bool gave_up = __syncthreads_or(any) != 0;
+  st = 0u;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) st |= s_or[w];
-    if (lead && t == 0) a.status[b] = st | (gave_up || !sane ? (uint32_t)PFKV_ST_TIMEOUT : 0u);
-    if (!sane || nb == 1) return;  // a one-piece request's rows come from the split kernel
-    if (st) {
-      for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
-      return;
-    }
-  } else {
-    nb = a.split_count[b];
-    if (nb <= 1) return;  // finished by the split kernel (or zeroed by the plan kernel)
-    c0 = a.split_first[b];
-    if (__ldcg(&a.status[b]) != 0u) {
-      for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
-      return;
-    }
-    load_ml();
+  for (int w = 0; w < 8; ++w) st |= s_or[w];
+  if (lead && t == 0) a.status[b] = st | (gave_up || !sane ? (uint32_t)PFKV_ST_TIMEOUT : 0u);
+  if (!sane || nb == 1) return;  // a one-piece request's rows come from the split kernel
+  if (st) {
+    for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
+    return;
   }
   __syncthreads();
   const int warp = t >> 5, lane = t & 31;

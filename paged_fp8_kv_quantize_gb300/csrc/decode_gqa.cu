@@ -128,247 +128,6 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, floa
   __syncwarp();
 }
 
-// ---------------------------------------------------------------- work split
-//
-// There is no plan kernel on this path: every CTA works out its own share
-// from the lengths, and all CTAs reach the same answer.  The requests, in
-// request order (a request with a bad length counting nothing), lie on a
-// line of T units that is cut into R ranges [floor(kT/R), floor((k+1)T/R));
-// CTA k * Hkv + h takes range k for KV head h.  Pieces of a request are
-// numbered consecutively in request order over the whole call (the merge
-// finds a request's pieces at split_first[b] .. + split_count[b]).  Two
-// rules:
-//  - cut: a request's segment of the line is c0 units of overhead followed
-//    by its pages (c0 = piece_cost: a piece's set-up and finish, and the
-//    consumer warps a short piece leaves idle, cost about that many pages'
-//    time); a piece is the part of one request's pages inside one range, so
-//    every CTA gets the same pages + overhead to within one.  R is capped so
-//    that no request is cut into more than max_splits pieces (a segment of
-//    s units meets at most ceil(s R / T) + 1 ranges); the rule is used when
-//    max_splits >= 3 and the caps leave at least 3/4 of the CTA groups.
-//  - chunk: the line is the bare pages (c0 = 0); each request is first cut
-//    into at most max_splits chunks of about cp pages, and a range takes the
-//    chunks that start inside it.  Used
-//    for small batches (T below the number of CTA groups) and batches whose
-//    longest request the split cap would otherwise leave on few CTAs.
-struct WorkSplit {
-  long long T, R, r0, r1, cp, max_len;
-  int k, chunks;
-  int c0;  // cut rule: overhead length placed before each request's pages on the cut line
-  // walk: next request to look at, its first page in the concatenation, the
-  // number of its first piece, and (chunk rule) its next chunk
-  int b;
-  long long off, first, c;
-};
-
-struct Piece {
-  int b, cg, p0, p1, L, nb;
-  bool lead;  // the request's first piece: its CTA of head 0 records the numbering
-};
-
-// floor(x / y) for 0 <= x < 2^53 and y >= 1, with no call to a 64-bit
-// division routine (the entry points bound batch * max_pages by 2^40, and
-// every dividend here is at most 2^12 times a page count).  A reciprocal
-// estimate (rcp.approx.f64) refined by two Newton-Raphson steps
-// r <- r (2 - y r) is close to full double precision, so x * r is within a
-// few units of the quotient; the exact integer remainder then corrects it.
-// The correction steps are bounded (16, against at most about 4 needed); a
-// result left wrong by a violated precondition is caught by the callers'
-// bounds checks rather than looping.
-__device__ __forceinline__ long long div_floor(long long x, long long y) {
-  const double yd = (double)y;
-  double r;
-  asm("rcp.approx.ftz.f64 %0, %1;" : "=d"(r) : "d"(yd));
-  r = fma(r, fma(-yd, r, 1.0), r);
-  r = fma(r, fma(-yd, r, 1.0), r);
-  long long q = (long long)((double)x * r);
-  long long rem = x - q * y;
-  for (int i = 0; i < 16 && rem < 0; ++i) {
-    --q;
-    rem += y;
-  }
-  for (int i = 0; i < 16 && rem >= y; ++i) {
-    ++q;
-    rem -= y;
-  }
-  return q;
-}
-
-__device__ __forceinline__ int ws_pages(const WorkSplit &w, int L, int S) {
-  return (L < 1 || (long long)L > w.max_len) ? 0 : (int)(((unsigned)L + (unsigned)S - 1u) / (unsigned)S);
-}
-
-// Pieces of a request of p > 0 pages whose segment of the cut line starts
-// at `off` (its pages start at off + c0); *ppc: chunk length (chunk rule).
-__device__ __forceinline__ int ws_count(const WorkSplit &w, long long off, int p, int max_splits, int *ppc) {
-  if (!w.chunks) {
-    const long long s0 = off + w.c0;
-    return (int)(div_floor((s0 + p) * w.R - 1, w.T) - div_floor((s0 + 1) * w.R - 1, w.T) + 1);
-  }
-  int nn = w.cp >= p ? 1 : (int)(((unsigned)p + (unsigned)w.cp - 1u) / (unsigned)w.cp);
-  if (nn > max_splits) nn = max_splits;
-  const int q = (int)(((unsigned)p + (unsigned)nn - 1u) / (unsigned)nn);
-  *ppc = q;
-  return (int)(((unsigned)p + (unsigned)q - 1u) / (unsigned)q);
-}
-
-// Warp-wide (all 32 lanes, same result in each): the rule, R and this CTA's
-// range, then the first request with a piece in it.
-__device__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
-  const int S = a.S;
-  w.max_len = (long long)a.MP * S;
-  long long tot = 0;
-  int mx = 0, nv = 0;
-  for (int b = lane; b < a.B; b += 32) {
-    const int p = ws_pages(w, __ldg(&a.seq_lens[b]), S);
-    tot += p;
-    mx = p > mx ? p : mx;
-    nv += p > 0;
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    nv += __shfl_xor_sync(0xffffffffu, nv, o);
-  }
-  long long T = tot;
-  const long long ranges = a.ranges, c = a.piece_cost;
-  const long long Tc = T + c * nv;  // the cut rule's line: pages plus c before each request
-  long long R = ranges < Tc ? ranges : Tc;
-  if (mx > 0 && a.max_splits >= 3) {
-    const long long cap = div_floor((long long)(a.max_splits - 2) * Tc, mx + c);
-    if (R > cap) R = cap;
-  }
-  w.chunks = !(a.max_splits >= 3 && T > 0 && R >= 1 && 4 * R >= 3 * ranges);
-  if (w.chunks) {
-    R = ranges < T ? ranges : T;
-    const long long cp = div_floor(T * a.Hkv + a.target_items - 1, a.target_items);
-    w.cp = cp < a.min_chunk_pages ? a.min_chunk_pages : cp;
-    w.c0 = 0;
-  } else {
-    w.cp = 0;
-    w.c0 = (int)c;
-    T = Tc;
-  }
-  w.T = T;
-  w.R = R < 1 ? 1 : R;
-  w.k = (int)blockIdx.x / a.Hkv;
-  w.b = a.B;  // no pieces unless found below
-  w.off = w.first = w.c = 0;
-  if (T == 0 || w.k >= w.R) return;
-  w.r0 = div_floor((long long)w.k * T, w.R);
-  w.r1 = div_floor((long long)(w.k + 1) * T, w.R);
-  long long off_c = 0, first_c = 0;  // totals of earlier passes
-  for (int base = 0; base < a.B; base += 32) {
-    const int b = base + lane;
-    const int p = b < a.B ? ws_pages(w, __ldg(&a.seq_lens[b]), S) : 0;
-    const long long seg = p > 0 ? p + w.c0 : 0;  // the request's segment of the cut line
-    long long xp = seg;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, xp, o);
-      if (lane >= o) xp += y;
-    }
-    const long long off = off_c + xp - seg;
-    int ppc = 1, n = 0;
-    if (p > 0) n = ws_count(w, off, p, a.max_splits, &ppc);
-    long long xn = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, xn, o);
-      if (lane >= o) xn += y;
-    }
-    const long long first = first_c + xn - n;
-    bool has = false;
-    int c_lo = 0;
-    if (p > 0 && off + w.c0 < w.r1 && off + w.c0 + p > w.r0) {
-      if (!w.chunks) {
-        has = true;
-      } else {
-        // r0 - off < p here, so the chunk index fits an int
-        c_lo = off >= w.r0 ? 0 : (int)((unsigned)(w.r0 - off + ppc - 1) / (unsigned)ppc);
-        has = c_lo < n && off + (long long)c_lo * ppc < w.r1;
-      }
-    }
-    const unsigned m = __ballot_sync(0xffffffffu, has);
-    if (m) {
-      const int src = __ffs(m) - 1;
-      w.b = base + src;
-      w.off = __shfl_sync(0xffffffffu, off, src);
-      w.first = __shfl_sync(0xffffffffu, first, src);
-      w.c = __shfl_sync(0xffffffffu, c_lo, src);
-      return;
-    }
-    off_c += __shfl_sync(0xffffffffu, xp, 31);
-    first_c += __shfl_sync(0xffffffffu, xn, 31);
-  }
-}
-
-// The CTA's next piece, in request order (uniform across the warp); false
-// when the range has none left.  A piece that would break the workspace
-// bounds ends the walk instead of being used (it cannot occur when the
-// rules above hold).
-__device__ bool ws_next(WorkSplit &w, const DecodeArgs &a, Piece &pc) {
-  while (w.b < a.B) {
-    const int L = __ldg(&a.seq_lens[w.b]);
-    const int p = ws_pages(w, L, a.S);
-    if (p == 0) {
-      ++w.b;
-      continue;
-    }
-    if (w.off + w.c0 >= w.r1) return false;
-    int ppc = 1;
-    const int n = ws_count(w, w.off, p, a.max_splits, &ppc);
-    long long j, p0, p1;
-    if (!w.chunks) {
-      const long long s0 = w.off + w.c0;  // the request's first page on the cut line
-      j = (long long)w.k - div_floor((s0 + 1) * w.R - 1, w.T);
-      p0 = (w.r0 > s0 ? w.r0 : s0) - s0;
-      p1 = (w.r1 < s0 + p ? w.r1 : s0 + p) - s0;
-    } else {
-      if (w.c >= n) {
-        w.first += n;
-        w.off += p;
-        ++w.b;
-        w.c = 0;
-        continue;
-      }
-      if (w.off + w.c * ppc >= w.r1) return false;
-      j = w.c++;
-      p0 = j * ppc;
-      p1 = p0 + ppc < p ? p0 + ppc : p;
-    }
-    const long long cg = w.first + j;
-    if (j < 0 || j >= n || n > a.max_splits || p0 < 0 || p0 >= p1 || p1 > p || cg >= (long long)a.B * a.max_splits)
-      return false;
-    pc.b = w.b;
-    pc.cg = (int)cg;
-    pc.p0 = (int)p0;
-    pc.p1 = (int)p1;
-    pc.L = L;
-    pc.nb = n;
-    pc.lead = j == 0;
-    if (!w.chunks) {
-      w.first += n;
-      w.off += p + w.c0;
-      ++w.b;
-    }
-    return true;
-  }
-  return false;
-}
-
-// ws_next on a state kept in shared memory (one copy per warp), so that it
-// holds no registers while the pages go out.
-__device__ __forceinline__ bool ws_next_shared(WorkSplit &s, const DecodeArgs &a, Piece &pc, int lane) {
-  WorkSplit w = s;
-  __syncwarp();
-  const bool r = ws_next(w, a, pc);
-  if (lane == 0) s = w;
-  __syncwarp();
-  return r;
-}
-
 // Bounded wait that ignores the abort flag: the page loader's way out, so
 // that a block that gave up still lets its own copies land before it exits.
 __device__ __forceinline__ void drain_wait_full(uint64_t *bar, uint32_t parity) {
@@ -427,6 +186,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       tma_prefetch_desc(&tmV);
     }
     const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
+    const uint64_t stream_pol = l2_evict_first_policy();
     // Pages of one batch are issued by separate lanes at once.  A batch never
     // holds more pages than the ring has stages, so no two lanes of a batch
     // share a stage and every empty-barrier wait is for the stage's previous
@@ -485,7 +245,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       // Lanes 0-15 hold 8 values each of the K row, lanes 16-31 of the V row,
       // loaded now so that their latency hides behind the walk.
       const int i_new = (L - 1) / S;
-      const bool has_new = a.split_append && p0 <= i_new && i_new < p1;
+      const bool has_new = a.append && p0 <= i_new && i_new < p1;
       const int nv_part = lane >> 4, nv_k = (lane & 15) * 8;
       const bool nv_lane = has_new && nv_k < kD;
       uint4 nv = make_uint4(0u, 0u, 0u, 0u);
@@ -520,16 +280,16 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
             } else {
               mbar_arrive_expect_tx(&full[st], sp.page_bytes);
               if constexpr (C::kRowBytes == 256) {
-                tma_load_5d(stage, &tmK, &full[st], 0, 0, 0, g, pid);
-                tma_load_5d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, 0, g, pid);
+                tma_load_5d_stream(stage, &tmK, &full[st], 0, 0, 0, g, pid, stream_pol);
+                tma_load_5d_stream(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, 0, g, pid, stream_pol);
               } else {
-                tma_load_4d(stage, &tmK, &full[st], 0, 0, g, pid);
-                tma_load_4d(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, g, pid);
+                tma_load_4d_stream(stage, &tmK, &full[st], 0, 0, g, pid, stream_pol);
+                tma_load_4d_stream(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, g, pid, stream_pol);
               }
               if (per_token) {
                 const size_t rr = ((size_t)pid * a.Hkv + g) * S;
-                bulk_load(stage + 2 * S * C::kRowBytes, a.k_scale + rr, 4u * S, &full[st]);
-                bulk_load(stage + 2 * S * C::kRowBytes + 4 * S, a.v_scale + rr, 4u * S, &full[st]);
+                bulk_load_stream(stage + 2 * S * C::kRowBytes, a.k_scale + rr, 4u * S, &full[st], stream_pol);
+                bulk_load_stream(stage + 2 * S * C::kRowBytes + 4 * S, a.v_scale + rr, 4u * S, &full[st], stream_pol);
               }
             }
           }
@@ -1027,15 +787,11 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
   }
   // No plan kernel: the split CTAs work out their pieces themselves (one CTA
   // group of Hkv CTAs per page range), and the merge kernel writes status.
-  a.self_plan = 1;
   a.ranges = max(1, min(sh.grid, kMaxCtas) / a.Hkv);
   a.n_ctas = a.ranges * a.Hkv;
   a.target_items = a.n_ctas * 8;
   a.min_chunk_pages = (1024 + a.S - 1) / a.S;
   a.piece_cost = kPieceCost;
-  // decode step: the split kernel's producer writes the new tokens
-  a.split_append = a.append;
-  a.append = 0;
   if (a.n_ctas > kMaxCtas) return PFKV_ERR_UNSUPPORTED;  // more KV heads than abort words
   // The split kernel is a programmatic dependent of the stream's previous
   // kernel: its CTAs take SMs as that kernel's blocks drain and wait for it

@@ -23,20 +23,28 @@
 //        terms, about 12 significant bits) by the softmax warps.
 // The softmax normaliser l is summed from the fp32 probabilities.
 //
-// One CTA per SM, persistent; work item = (request, range of its pages), all
-// 64 heads.  Warp 0 loads pages into a five-page ring (TMA, bounds and tag
-// checks beside the copies); warp 1 owns tensor memory and issues the QK^T
-// MMAs and warps 6 and 7 the PV MMAs of two value chunks each (one thread
-// each, so that the instruction streams overlap on the tensor pipe); warps
-// 2-5 and 8-11 run the softmax: warp w reads tensor-memory quarter w % 4,
-// i.e. heads 16 q .. 16 q + 15, and one half of the page's tokens, each
-// lane one head and 16 tokens; the two warps of a quarter agree on each
-// page's maximum through shared memory, so the running maxima are identical
-// in both and the sums are per thread.  A running maximum moves only when it
-// grows by more than 8x; O^T, whose columns are heads and whose lanes are
-// values, is then rescaled by the softmax warps before the page's PV, a
-// hand-off that costs nothing on the pages that need none.  Partials are
-// merged by the shared log-sum-exp merge kernel.
+// One CTA per SM, persistent.  There is no plan kernel: every CTA works out
+// its pieces from the lengths (the shared work split: the requests' pages,
+// plus a small per-piece overhead, cut into one equal range per CTA); a
+// piece is a request's part of the range, all 64 heads.  Warp 0 loads pages
+// into a five-page ring (TMA, bounds and tag checks beside the copies; in a
+// decode step it first writes the request's new row into its page); warp 1
+// owns tensor memory and issues the QK^T MMAs and warps 6 and 7 the PV MMAs
+// of two value chunks each (one thread each, so that the instruction
+// streams overlap on the tensor pipe); warps 2-5 and 8-11 run the softmax:
+// warp w reads tensor-memory quarter w % 4, i.e. heads 16 q .. 16 q + 15,
+// and one half of the page's tokens, each lane one head and 16 tokens; the
+// two warps of a quarter agree on each page's maximum through shared
+// memory, so the running maxima are identical in both and the sums are per
+// thread.  The softmax warps also write each piece's query terms (tensor
+// memory and the shared-memory tail), the next piece's as soon as the last
+// QK^T of the current one has read the operand, before the current piece's
+// result is read out, so that the next piece's QK^T overlaps that read-out.
+// A running maximum moves only when it grows by more than 8x; O^T, whose
+// columns are heads and whose lanes are values, is then rescaled by the
+// softmax warps before the page's PV, a hand-off that costs nothing on the
+// pages that need none.  Partials of a request cut into several pieces are
+// merged by the shared log-sum-exp merge kernel, which also writes status.
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -56,15 +64,19 @@ constexpr uint32_t kBlk = kTS * 128;          // 8192: one 128-byte column block
 // swizzle), columns 512-575 as one 64-byte block (64-byte swizzle).
 constexpr uint32_t kPageTail = 4 * kBlk;      // 32768
 constexpr uint32_t kPageSm = kPageTail + kTS * 64;  // 36864
-// Query image per request (written by the plan grid): 128 rows x 512 bytes
-// for tensor memory, then the 64-byte-swizzled 128 x 64 tail.  Row r of the
-// operand is term r / 16 % 2 of head 16 (r / 32) + r % 16.
-constexpr uint32_t kQMainBytes = 128 * 512;   // 65536
+// Query operand: 128 rows, row R = 32 (h / 16) + 16 t + h % 16 holds term t
+// of head h; columns 0-511 live in tensor memory, columns 512-575 in shared
+// memory as a 128 x 64 image with the 64-byte swizzle.
 constexpr uint32_t kQTailBytes = 128 * 64;    // 8192
-static_assert(kQMainBytes + kQTailBytes == kLatentQTermBytes, "query image size");
-constexpr int kPT = 3;                        // e4m3 terms of the probabilities
+constexpr int kPieceCostLatent = 2;           // pages' worth of time a piece costs beyond its pages
+constexpr int kPT = 4;                        // 8-bit terms of the probabilities (at most)
 constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
-constexpr uint32_t kPBuf = kPT * kPTerm;      // 12288
+constexpr uint32_t kPBuf = kPT * kPTerm;      // 16384
+// A page whose largest value (its largest per-token scale x 448) exceeds this
+// carries its probabilities in four terms instead of three: the output's
+// error grows with the values' magnitude, and three terms (about 12
+// significant bits) keep it within 2e-3 only for values up to about this.
+constexpr float kFourTermAt = 8.f;
 constexpr int kNst = 5;                       // pages in flight per CTA
 constexpr int kPrefetch = 6;                  // pages pulled into L2 ahead of their copy
 constexpr int kTThreads = 384;                // producer, QK issuer, softmax x4, two PV issuers, softmax x4
@@ -75,13 +87,17 @@ constexpr float kTheta = 3.f;                 // log2 growth of a running max th
 constexpr float kPExp = 4.75f;                // P'' = p (s_t / s_ref) 2^kPExp <= 2^kTheta * 2 * 2^4.75 < 448
 constexpr uint32_t kIdQK = umma_idesc_e4m3(128, 64, 0, 0);
 constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 64, 1, 0);
+constexpr uint32_t kIdPV5 = kIdPV | (1u << 10);  // B (the last probability term) in e5m2
 
-// Softmax-warp scratch, floats: beta[2][64] | l[2 halves][64] | m[64] | resc_tag[2] (uint32) | pad |
+// Softmax-warp scratch, floats: beta[2][64] | l[2 halves][64] | m[64] | resc_tag[2] (uint32) |
+// four-term flag per P buffer [2] (uint32) | pad |
 // page maxima exchanged by the two warps of a lane quarter, float2 [2 pages][2 halves][64]
-constexpr int kWgBeta = 0, kWgL = 128, kWgM = 256, kWgTag = 320, kWgX = 328, kWgFloats = kWgX + 2 * 2 * 2 * 64;
+// | query maxima exchanged by the two warps of a lane quarter [2 halves][64]
+constexpr int kWgBeta = 0, kWgL = 128, kWgM = 256, kWgTag = 320, kWgFour = 322, kWgX = 328, kWgQm = kWgX + 2 * 2 * 2 * 64,
+              kWgFloats = kWgQm + 2 * 64;
 
 struct TcSmem {
-  uint32_t ring, qtail, p, scales, wg, bars, items, total;
+  uint32_t ring, qtail, p, scales, wg, bars, items, ws, total;
 };
 
 __host__ __device__ constexpr TcSmem tc_smem() {
@@ -90,10 +106,11 @@ __host__ __device__ constexpr TcSmem tc_smem() {
   s.qtail = s.ring + kNst * kPageSm;           // query tail (A of the last two QK^T steps)
   s.p = s.qtail + kQTailBytes;                 // 2 buffers x kPT P^T terms
   s.scales = s.p + 2 * kPBuf;                  // kNst x 64 per-token scales
-  s.wg = s.scales + kNst * kTS * 4;            // softmax-warp scratch (see below)
-  s.bars = s.wg + 4 * kWgFloats;               // softmax-warp scratch (layout above)
+  s.wg = s.scales + kNst * kTS * 4;            // softmax-warp scratch (layout above)
+  s.bars = s.wg + 4 * kWgFloats;
   s.items = s.bars + 8 * (2 * kNst + 14 + 3 * kNIQ);
-  s.total = s.items + (sizeof(ItemDesc) + 4) * kNIQ + 16;
+  s.ws = (s.items + (sizeof(ItemDesc) + 4) * kNIQ + 16 + 15) & ~15u;  // the page loader's work-split state
+  s.total = s.ws + sizeof(WorkSplit);
   return s;
 }
 static_assert(tc_smem().total + 1024 <= 232448, "shared memory plan exceeds one SM");
@@ -107,8 +124,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 struct Bars {
-  uint64_t *full, *empty, *s_full, *s_empty, *p_full, *p_empty, *q_full, *q_empty, *q_tfull, *o_empty, *r_done,
-      *drain;
+  uint64_t *full, *empty, *s_full, *s_empty, *p_full, *p_empty, *q_ready, *q_empty, *o_empty, *r_done, *drain;
   uint64_t *item_full, *item_empty, *item_done;
 };
 
@@ -121,9 +137,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
   r.s_empty = b; b += 2;
   r.p_full = b; b += 2;
   r.p_empty = b; b += 2;
-  r.q_full = b; b += 1;
+  r.q_ready = b; b += 1;
   r.q_empty = b; b += 1;
-  r.q_tfull = b; b += 1;
   r.o_empty = b; b += 1;
   r.r_done = b; b += 1;
   r.drain = b; b += 1;
@@ -135,33 +150,43 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
 
 // ---------------------------------------------------------------- producer (warp 0)
 
+// Decode step: the request's new token goes to slot `pos` % 64 of the page
+// that lane `src` of the batch looked up, unless that page is outside the
+// pool or (tag check on) its tag does not match; the walk reports those cases
+// in the request's status as for any page.  Quantized exactly as the append
+// does (per-token scale amax / 448, or 1 for an all-zero row; x / s with
+// IEEE division, round to nearest even, saturating).  The stores are made
+// visible to the tensor-copy engine before the page is copied.
+__device__ __forceinline__ void write_new_row(const DecodeArgs &a, const AppendRow &r, int src, int pid_lane,
+                                              bool bad_lane, int pos, int lane) {
+  const int pid = __shfl_sync(0xffffffffu, pid_lane, src);
+  if (__shfl_sync(0xffffffffu, bad_lane, src)) return;
+  append_row_store<true>(a.cache, r, 0, 0, pid, pos, lane);
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
 __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorMap &map, const CUtensorMap &map_tail,
-                                            uint8_t *smem,
-                                            const Bars &B, ItemDesc *items, uint32_t *item_status,
+                                            uint8_t *smem, const Bars &B, ItemDesc *items, uint32_t *item_status,
                                             volatile int *abort_flag) {
   const TcSmem sp = tc_smem();
   const int lane = threadIdx.x & 31;
-  const int n_items = a.hdr->n_items;
   const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
+  const uint64_t stream_pol = l2_evict_first_policy();
   uint32_t g = 0;  // pages issued by this CTA
-  uint32_t it = 0, q_loads = 0;
   bool ok = true;
-  // balanced plan: this CTA's items are a fixed run; otherwise items are
-  // taken from a shared counter
-  const int n_ranges = a.hdr->n_ranges;
-  int next = 0, last = 0;
-  if (n_ranges > 0 && (int)blockIdx.x < n_ranges) {
-    next = a.cta_first[blockIdx.x];
-    last = a.cta_first[blockIdx.x + 1];
+  // This CTA's pieces, worked out from the lengths; the next one is found
+  // once the current one's pages have gone out.
+  WorkSplit &s_ws = *reinterpret_cast<WorkSplit *>(smem + sp.ws);
+  {
+    WorkSplit w;
+    ws_init(w, a, lane);
+    if (lane == 0) s_ws = w;
+    __syncwarp();
   }
-  for (;; ++it) {
-    int item = 0;
-    if (n_ranges > 0) {
-      item = next < last ? next++ : n_items;
-    } else {
-      if (lane == 0) item = (int)atomicAdd(&a.hdr->work, 1u);
-      item = __shfl_sync(0xffffffffu, item, 0);
-    }
+  Piece cur;
+  bool have = ws_next_shared(s_ws, a, cur, lane);
+  for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
     bool w = true;
     if (lane == 0) w = mbar_wait(&B.item_empty[slot], ((it / kNIQ) & 1u) ^ 1u, abort_flag);
@@ -170,28 +195,34 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
     // first item (or its end marker) to the other warps, whose bounded waits
     // then give up
     const bool withhold = (a.flags & PFKV_FLAG_TEST_WITHHOLD) && blockIdx.x == 0 && it == 0;
-    if (item >= n_items) {
+    if (!have) {
       if (lane == 0) {
         items[slot].b = -1;
         if (!withhold) mbar_arrive(&B.item_full[slot]);
       }
       break;
     }
-    const int4 info = a.chunk_info[2 * item], info2 = a.chunk_info[2 * item + 1];
-    const int b = info.x, p0 = info.y, p1 = info.z;
+    const int b = cur.b, p0 = cur.p0, p1 = cur.p1, L = cur.L;
     if (lane == 0) {
       ItemDesc d;
-      d.b = b; d.cg = item; d.g = 0; d.p0 = p0; d.p1 = p1; d.L = info.w; d.ring = g; d.nb = info2.x;
+      d.b = b; d.cg = cur.cg; d.g = 0; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = g; d.nb = cur.nb;
       items[slot] = d;
       if (!withhold) mbar_arrive(&B.item_full[slot]);
-      // the last 64 columns of the request's query terms (the A operand of
-      // the last two QK^T steps), once the previous item's last QK^T is done
-      if (mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag)) {
-        mbar_arrive_expect_tx(B.q_full, kQTailBytes);
-        bulk_load(smem + sp.qtail, a.qterms + (size_t)b * kLatentQTermBytes + kQMainBytes, kQTailBytes, B.q_full);
-        ++q_loads;
+      if (cur.lead) {  // the merge's view of the numbering
+        a.split_first[b] = cur.cg;
+        a.split_count[b] = cur.nb;
       }
     }
+    // the item's query rows (72 KB) into L2 well before the softmax warps
+    // turn them into the query operand
+    if (lane == 0) bulk_prefetch_l2(static_cast<const uint16_t *>(a.q) + (size_t)b * kTH * kTD, kTH * kTD * 2);
+    // Decode step: the piece holding the request's last page writes the new
+    // token's row into that page before copying it; the row is loaded now so
+    // that its latency hides behind the walk.
+    const int i_new = (L - 1) / kTS;
+    const bool has_new = a.append && p0 <= i_new && i_new < p1;
+    AppendRow nrow;
+    if (has_new) nrow = append_row_load<true>(a.cache, a.k_new, nullptr, b, 0, 0, lane);
     const int *trow = a.block_table + (size_t)b * a.MP;
     const uint32_t *tagrow = a.block_tags + (size_t)b * a.MP;
     uint32_t st_bits = 0;
@@ -207,6 +238,8 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
         page_tag = __ldg(&a.page_tags[pid]);
         want_tag = __ldg(&tagrow[i]);
       }
+      if (has_new && i0 <= i_new && i_new < i0 + 32)
+        write_new_row(a, nrow, i_new - i0, pid, oob || page_tag != want_tag, L - 1, lane);
       const int cnt = min(32, p1 - i0);
       // pages kPrefetch ahead of the copies are pulled into L2, so that a copy
       // issued when a ring slot frees up finds its page there
@@ -215,30 +248,34 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
         const bool bad = __shfl_sync(0xffffffffu, oob, k);
         if (lane == 0 && !bad) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d(&map, 128 * c, 0, pk);
-          tma_prefetch_l2_3d(&map_tail, 512, 0, pk);
-          bulk_prefetch_l2(a.k_scale + (size_t)pk * kTS, kTS * 4);
+          for (int c = 0; c < 4; ++c) tma_prefetch_l2_3d_stream(&map, 128 * c, 0, pk, stream_pol);
+          tma_prefetch_l2_3d_stream(&map_tail, 512, 0, pk, stream_pol);
+          bulk_prefetch_l2_stream(a.k_scale + (size_t)pk * kTS, kTS * 4, stream_pol);
         }
       };
-      for (int k = 0; k < min(kPrefetch, cnt); ++k) prefetch(k);
+      // (the CTA's first kNst pages go straight into an empty ring: no prefetch)
+      for (int k = 0; k < min(kPrefetch, cnt); ++k)
+        if (g + (uint32_t)k >= (uint32_t)kNst) prefetch(k);
       for (int k = 0; k < cnt; ++k) {
         if (k + kPrefetch < cnt) prefetch(k + kPrefetch);
         const int pk = __shfl_sync(0xffffffffu, pid, k);
-        const bool ok_k = __shfl_sync(0xffffffffu, oob, k);
+        const bool bad_k = __shfl_sync(0xffffffffu, oob, k);
         bool w = true;
         if (lane == 0) {
           const uint32_t r = g + (uint32_t)k, st = r % kNst;
           w = mbar_wait(&B.empty[st], ((r / kNst) & 1u) ^ 1u, abort_flag);
           if (w) {
-            if (ok_k) {
+            if (bad_k) {
               mbar_arrive(&B.full[st]);  // never fetched; the request is aborted
             } else {
               mbar_arrive_expect_tx(&B.full[st], kPageSm + kTS * 4);
               uint8_t *stage = smem + sp.ring + st * kPageSm;
 #pragma unroll
-              for (int c = 0; c < 4; ++c) tma_load_3d(stage + c * kBlk, &map, &B.full[st], 128 * c, 0, pk);
-              tma_load_3d(stage + kPageTail, &map_tail, &B.full[st], 512, 0, pk);
-              bulk_load(smem + sp.scales + st * (kTS * 4), a.k_scale + (size_t)pk * kTS, kTS * 4, &B.full[st]);
+              for (int c = 0; c < 4; ++c)
+                tma_load_3d_stream(stage + c * kBlk, &map, &B.full[st], 128 * c, 0, pk, stream_pol);
+              tma_load_3d_stream(stage + kPageTail, &map_tail, &B.full[st], 512, 0, pk, stream_pol);
+              bulk_load_stream(smem + sp.scales + st * (kTS * 4), a.k_scale + (size_t)pk * kTS, kTS * 4, &B.full[st],
+                               stream_pol);
             }
           }
         }
@@ -254,17 +291,14 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
     }
     if (lane == 0) {
       item_status[slot] = st_bits;
-      if (st_bits) atomicOr(&a.status[b], st_bits);
       mbar_arrive(&B.item_done[slot]);
     }
     if (!ok) break;
+    have = ws_next_shared(s_ws, a, cur, lane);
   }
-  // Copies still in flight land before the block may exit: the last pages
-  // issued and the last query load.
-  if (lane == 0) {
+  // Copies still in flight land before the block may exit.
+  if (lane == 0)
     for (uint32_t k = g > kNst ? g - kNst : 0; k < g; ++k) drain_wait(&B.full[k % kNst], (k / kNst) & 1u);
-    if (q_loads) drain_wait(B.q_full, (q_loads - 1) & 1u);
-  }
 }
 
 // ---------------------------------------------------------------- MMA issuers (warps 1 and 6, one thread each)
@@ -290,7 +324,8 @@ __device__ __forceinline__ TcDesc tc_desc(uint8_t *smem) {
 
 // QK^T issuer (warp 1): S[sb] = [T1; T2 rows] . K_page^T for every page in
 // order, as soon as the page has landed and the softmax warps have read the
-// S buffer's previous page.
+// S buffer's previous page.  After an item's last page it commits q_empty:
+// the query operand may then be replaced by the next item's.
 __device__ __forceinline__ void tc_mma_qk(uint8_t *smem, const Bars &B, const ItemDesc *items, uint32_t tmem,
                                           volatile int *abort_flag) {
   const TcDesc dd = tc_desc(smem);
@@ -302,7 +337,7 @@ __device__ __forceinline__ void tc_mma_qk(uint8_t *smem, const Bars &B, const It
     mbar_arrive(&B.item_empty[slot]);
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
-    if (!mbar_wait(B.q_full, it & 1u, abort_flag) || !mbar_wait(B.q_tfull, it & 1u, abort_flag)) break;
+    if (!mbar_wait(B.q_ready, it & 1u, abort_flag)) break;  // the item's query terms are in place
     bool ok = true;
     for (uint32_t j = 0; j < n; ++j) {
       const uint32_t gp = g + j, st = gp % kNst, sb = gp & 1u;
@@ -343,6 +378,7 @@ __device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const It
   const TcSmem sp = tc_smem();
   const TcDesc dd = tc_desc(smem);
   const volatile uint32_t *resc_tag = reinterpret_cast<const uint32_t *>(smem + sp.wg) + kWgTag;
+  const volatile uint32_t *four_flag = reinterpret_cast<const uint32_t *>(smem + sp.wg) + kWgFour;
   uint32_t g = 0, n_resc = 0;
   for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
@@ -369,14 +405,19 @@ __device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const It
       tc_fence_after();
       const uint64_t pg = (uint64_t)((st * kPageSm) >> 4), pp = (uint64_t)((pb * kPBuf) >> 4);
       const uint32_t first = j == 0 ? 0u : 1u;
+      // three terms (e4m3, e4m3, e5m2) or four (e4m3 x 3, e5m2), as the softmax warps chose for the page
+      const bool four = four_flag[pb] != 0u;
 #pragma unroll
       for (int c = 2 * half; c < 2 * half + 2; ++c)
 #pragma unroll
-        for (int t = 0; t < kPT; ++t)
+        for (int t = 0; t < kPT; ++t) {
+          if (t == kPT - 1 && !four) continue;
+          const uint32_t id = (t == kPT - 1 || (t == kPT - 2 && !four)) ? kIdPV5 : kIdPV;
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
             umma_e4m3(tmem + kColO + 64 * c, dd.vt + pg + (uint64_t)((c * kBlk + ks * 4096) >> 4),
-                      dd.pt + pp + (uint64_t)((t * kPTerm + ks * 256) >> 4), kIdPV, (t == 0 && ks == 0) ? first : 1u);
+                      dd.pt + pp + (uint64_t)((t * kPTerm + ks * 256) >> 4), id, (t == 0 && ks == 0) ? first : 1u);
+        }
       umma_commit(&B.empty[st]);
       umma_commit(&B.p_empty[pb]);
     }
@@ -403,26 +444,127 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool v) {
 // All softmax warps (barrier 1).
 __device__ __forceinline__ bool wg_bar_or(bool v) { return bar_or(1, kSmxThreads, v); }
 
-__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
-  return r;
+// The 8-bit terms of a pair of non-negative floats (lo -> low byte), each
+// rounded to nearest even from fp32: t1 = e4m3(x), t2 = e4m3(x - t1), then
+// either t3 = e5m2(x - t1 - t2) (three terms, about 12 significant bits for
+// the large weights) or t3 = e4m3(x - t1 - t2), t4 = e5m2(x - t1 - t2 - t3)
+// (four terms, about 15 bits; t4 = 0 otherwise).  Every difference is exact
+// in fp32 (a term is within a factor two of what it rounds, or zero).  The
+// last term is e5m2 for its range (down to 2^-16, against 2^-9 for e4m3): it
+// keeps the share of the many small weights far below the running maximum,
+// which e4m3 alone would flush to zero.  Returns the pair the terms
+// represent, t1 + t2 + t3 + t4, exactly.
+__device__ __forceinline__ float2 p_terms2(float lo, float hi, bool four, uint32_t &t1, uint32_t &t2, uint32_t &t3,
+                                           uint32_t &t4) {
+  t1 = f32x2_to_e4m3x2(lo, hi);
+  const uint32_t b1 = e4m3x2_to_f16x2(t1);
+  const float2 d1 = __half22float2(*reinterpret_cast<const __half2 *>(&b1));
+  const float r1x = lo - d1.x, r1y = hi - d1.y;
+  t2 = f32x2_to_e4m3x2(r1x, r1y);
+  const uint32_t b2 = e4m3x2_to_f16x2(t2);
+  const float2 d2 = __half22float2(*reinterpret_cast<const __half2 *>(&b2));
+  const float r2x = r1x - d2.x, r2y = r1y - d2.y;
+  float2 rep = make_float2(d1.x + d2.x, d1.y + d2.y);
+  if (four) {
+    t3 = f32x2_to_e4m3x2(r2x, r2y);
+    const uint32_t b3 = e4m3x2_to_f16x2(t3);
+    const float2 d3 = __half22float2(*reinterpret_cast<const __half2 *>(&b3));
+    t4 = f32x2_to_e5m2x2(r2x - d3.x, r2y - d3.y);
+    const uint32_t b4 = e5m2x2_to_f16x2(t4);
+    const float2 d4 = __half22float2(*reinterpret_cast<const __half2 *>(&b4));
+    rep.x = (rep.x + d3.x) + d4.x;
+    rep.y = (rep.y + d3.y) + d4.y;
+  } else {
+    t3 = f32x2_to_e5m2x2(r2x, r2y);
+    const uint32_t b3 = e5m2x2_to_f16x2(t3);
+    const float2 d3 = __half22float2(*reinterpret_cast<const __half2 *>(&b3));
+    t4 = 0u;
+    rep.x += d3.x;
+    rep.y += d3.y;
+  }
+  return rep;
 }
 
-// Three e4m3 terms of a pair of non-negative floats (lo -> low byte), split
-// in f16: x = f16(x), t1 = e4m3(x), t2 = e4m3(x - t1), t3 = e4m3(x - t1 - t2);
-// each difference is exact in f16.
-__device__ __forceinline__ void three_terms2(float lo, float hi, uint32_t &t1, uint32_t &t2, uint32_t &t3) {
-  const __half2 x = __floats2half2_rn(lo, hi);
-  const uint32_t xb = *reinterpret_cast<const uint32_t *>(&x);
-  t1 = f16x2_to_e4m3x2(xb);
-  const uint32_t b1 = e4m3x2_to_f16x2(t1);
-  const __half2 r1 = __hsub2(x, *reinterpret_cast<const __half2 *>(&b1));
-  const uint32_t r1b = *reinterpret_cast<const uint32_t *>(&r1);
-  t2 = f16x2_to_e4m3x2(r1b);
-  const uint32_t b2 = e4m3x2_to_f16x2(t2);
-  const __half2 r2 = __hsub2(r1, *reinterpret_cast<const __half2 *>(&b2));
-  t3 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&r2));
+// Eight codes of term t of the query values v (eight bf16) scaled by inv, a
+// power of two: T1 = e4m3(x), T2 = e4m3(x - T1) (the difference is exact in
+// fp32); both rounded to nearest even.
+__device__ __forceinline__ uint2 q_term8(uint4 v, float inv, int t) {
+  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[2];
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    const float x0 = __uint_as_float(wv[i] << 16) * inv, x1 = __uint_as_float(wv[i] & 0xffff0000u) * inv;
+    const float x2 = __uint_as_float(wv[i + 1] << 16) * inv, x3 = __uint_as_float(wv[i + 1] & 0xffff0000u) * inv;
+    const uint32_t a01 = f32x2_to_e4m3x2(x0, x1), a23 = f32x2_to_e4m3x2(x2, x3);
+    const uint32_t h01 = e4m3x2_to_f16x2(a01), h23 = e4m3x2_to_f16x2(a23);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+    const uint32_t t2 = f32x2_to_e4m3x2(x0 - f01.x, x1 - f01.y) | (f32x2_to_e4m3x2(x2 - f23.x, x3 - f23.y) << 16);
+    o[i / 2] = t ? t2 : (a01 | (a23 << 16));
+  }
+  return make_uint2(o[0], o[1]);
+}
+
+// The query operand of request b, written by the softmax warps.  Head h's
+// bf16 row (576 values) is scaled by 2^-e_h, e_h the exponent that puts
+// max|q| in [128, 256), and written as T1 = e4m3(q 2^-e_h) and
+// T2 = e4m3(q 2^-e_h - T1): T1 + T2 equals the scaled row exactly for every
+// element of magnitude at least 2^-2 (a bf16 significand has 8 bits, each
+// term carries 4), the rest to within 2^-10.  Warp (quarter q, half x), lane
+// l writes row R = 32 q + l (head 16 q + l % 16, term l / 16): tensor-memory
+// columns 64 x .. 64 x + 63 (values 256 x .. 256 x + 255) and, for x = 0,
+// the row's 64-byte tail (values 512-575) into the swizzled shared-memory
+// image (16-byte chunk j of row R at R * 64 + 16 (j ^ ((R >> 1) & 3))).  The
+// two warps of a quarter exchange their partial maxima (barrier 2 + q, which
+// also ORs their failure flags).  Returns this lane's score factor
+// softmax scale * log2(e) * 2^e_h.  Whole warp; arrives on q_ready.  One
+// compiled copy for both call sites (first item, next item), so that its
+// code is fetched from memory once per call.
+__device__ __noinline__ float q_prep(const DecodeArgs &a, int b, uint32_t tq, uint8_t *qtail, float *s_qm,
+                                        uint64_t *q_ready, int q, int x, int lane, bool &fail) {
+  const int h = 16 * q + (lane & 15), t = lane >> 4, R = 32 * q + lane;
+  const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + ((size_t)b * kTH + h) * kTD);
+  float m = 0.f;
+  if (!fail) {
+    // this lane's half of the head's values in this warp's columns (and of the tail)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = amax8(__ldg(src + 32 * x + 16 * t + i), m);
+    if (x == 0)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = amax8(__ldg(src + 64 + 4 * t + i), m);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    if (lane < 16) s_qm[x * kTH + h] = m;
+  }
+  fail = bar_or(2 + q, 64, fail);
+  if (fail) return 0.f;
+  m = fmaxf(m, s_qm[(x ^ 1) * kTH + h]);
+  int e = 8;
+  if (m > 0.f) frexpf(m, &e);  // m = f 2^e, f in [0.5, 1)
+  const float inv = ldexpf(1.f, 8 - e);
+#pragma unroll 1
+  for (int k = 0; k < 2; ++k) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint2 c = q_term8(__ldg(src + 32 * x + 16 * k + i), inv, t);
+      r[2 * i] = c.x;
+      r[2 * i + 1] = c.y;
+    }
+    tmem_st32(tq + kColQ + 32 * (2 * x + k), r);
+  }
+  if (x == 0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint2 c0 = q_term8(__ldg(src + 64 + 2 * j), inv, t), c1 = q_term8(__ldg(src + 64 + 2 * j + 1), inv, t);
+      *reinterpret_cast<uint4 *>(qtail + R * 64 + 16 * (j ^ ((R >> 1) & 3))) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+    }
+    fence_async_smem();
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(q_ready);
+  return a.sm_scale_log2 * ldexpf(1.f, e - 8);
 }
 
 // Softmax warp w (2-5 and 8-11) reads tensor-memory quarter q = w % 4, i.e.
@@ -446,13 +588,28 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
   float *s_beta = wsc + kWgBeta, *s_l = wsc + kWgL, *s_m = wsc + kWgM;
   float2 *s_x = reinterpret_cast<float2 *>(wsc + kWgX);
   volatile uint32_t *resc_tag = reinterpret_cast<uint32_t *>(wsc + kWgTag);
+  volatile uint32_t *four_flag = reinterpret_cast<uint32_t *>(wsc + kWgFour);
   const float *scales = reinterpret_cast<const float *>(smem + sp.scales);
   uint8_t *pbase = smem + sp.p;
   const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
   // P^T (K-major, no swizzle): byte (head, token) at (head % 8) * 16 + (head / 8) * 512 +
   // (token / 16) * 128 + token % 16; this thread writes the 16-token chunk tb / 16
   const uint32_t p_off = (h & 7) * 16 + (h >> 3) * 512 + (tb / 16) * 128;
+  uint8_t *qtail = smem + sp.qtail;
+  float *s_qm = wsc + kWgQm;
   uint32_t g = 0, n_resc = 0;
+  float cq = 0.f;  // score factor of this lane's head for the current item
+  {
+    // the first item's query (the operand starts out free)
+    bool fail = !mbar_wait(&B.item_full[0], 0, abort_flag);
+    fail = wg_bar_or(fail);
+    const int b0 = fail ? -1 : items[0].b;
+    if (b0 >= 0) {
+      cq = q_prep(a, b0, tq, qtail, s_qm, B.q_ready, q, x, lane, fail);
+      fail = wg_bar_or(fail);
+    }
+    if (fail) return;
+  }
   for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
     bool fail = !mbar_wait(&B.item_full[slot], (it / kNIQ) & 1u, abort_flag);
@@ -460,29 +617,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     const ItemDesc d = items[slot];
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
-    // this item's query rows into tensor memory (this warp: columns 64 x ..
-    // 64 x + 63 of its quarter's rows), once the previous item's last QK^T
-    // is done with them
-    fail = __any_sync(0xffffffffu, !mbar_wait(B.q_empty, (it & 1u) ^ 1u, abort_flag));  // warp-uniform
-    if (!fail) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.qterms + (size_t)d.b * kLatentQTermBytes +
-                                                         (size_t)(32 * q + lane) * 512);
-#pragma unroll 1
-      for (int k = 2 * x; k < 2 * x + 2; ++k) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(src + 8 * k + i);
-          r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
-        }
-        tmem_st32(tq + kColQ + 32 * k, r);
-      }
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(B.q_tfull);
-    const float cq = __ldg(&a.qfac[(size_t)d.b * kTH + h]);
+    float cq_next = cq;
     float m = kNegInf, l = 0.f, s_ref = 0.f;
     // Rescale hand-off for page gq (not an item's first page): once every
     // warp's P^T and scale factors for it are in, if any head asked for it,
@@ -578,14 +713,24 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       l *= alpha;
       m = m_new;
       s_ref = s_new;
-      // P'' = 2^(z - m) (s_t / s_ref) 2^kPExp as three e4m3 terms; l sums 2^(z - m)
+      // P'' = 2^(z - m) (s_t / s_ref) 2^kPExp as three or four 8-bit terms
+      // (four when the page holds large values: smx is the same in every
+      // softmax warp, so they all choose alike).  l sums the weights exactly
+      // as the terms carry them (the represented P'' divided by
+      // (s_t / s_ref) 2^kPExp), so that the output is a weighted mean of the
+      // value rows with the weights the PV product used: a dominant token's
+      // rounding cancels against its own share of l, and a weight too small
+      // for the terms drops out of both.
+      const bool four = smx * 448.f > kFourTermAt;
+      if (wt == 0) four_flag[sb] = four ? 1u : 0u;  // read by the PV issuers after p_full
       const float w = exp2f(kPExp) / s_ref;
-      uint32_t t1[8], t2[8], t3[8];
+      uint32_t t1[8], t2[8], t3[8], t4[8];
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
-        const float e0 = fast_exp2(v[i] - m), e1 = fast_exp2(v[i + 1] - m);
-        l += e0 + e1;
-        three_terms2(e0 * sv[i] * w, e1 * sv[i + 1] * w, t1[i / 2], t2[i / 2], t3[i / 2]);
+        const float sw0 = sv[i] * w, sw1 = sv[i + 1] * w;
+        const float2 rep = p_terms2(fast_exp2(v[i] - m) * sw0, fast_exp2(v[i + 1] - m) * sw1, four, t1[i / 2],
+                                    t2[i / 2], t3[i / 2], t4[i / 2]);
+        l += (rep.x > 0.f ? rep.x * fast_rcp(sw0) : 0.f) + (rep.y > 0.f ? rep.y * fast_rcp(sw1) : 0.f);
       }
       uint8_t *pt = pbase + sb * kPBuf + p_off;
       *reinterpret_cast<uint4 *>(pt) =
@@ -594,6 +739,9 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
           make_uint4(t2[0] | (t2[1] << 16), t2[2] | (t2[3] << 16), t2[4] | (t2[5] << 16), t2[6] | (t2[7] << 16));
       *reinterpret_cast<uint4 *>(pt + 2 * kPTerm) =
           make_uint4(t3[0] | (t3[1] << 16), t3[2] | (t3[3] << 16), t3[4] | (t3[5] << 16), t3[6] | (t3[7] << 16));
+      if (four)
+        *reinterpret_cast<uint4 *>(pt + 3 * kPTerm) =
+            make_uint4(t4[0] | (t4[1] << 16), t4[2] | (t4[3] << 16), t4[4] | (t4[5] << 16), t4[6] | (t4[7] << 16));
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -603,6 +751,20 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     }
     if (n > 1) rescale_check(g + n - 1, fail);  // the item's last page
     if (wg_bar_or(fail)) break;
+    // ---- the next item's query, as soon as this item's last QK^T has read
+    // the operand, so that the next item's first QK^T overlaps the read-out
+    // below
+    {
+      const uint32_t nslot = (it + 1) % kNIQ;
+      fail = !mbar_wait(&B.item_full[nslot], ((it + 1) / kNIQ) & 1u, abort_flag);
+      if (wg_bar_or(fail)) break;
+      const int b_next = items[nslot].b;
+      if (b_next >= 0) {
+        fail = __any_sync(0xffffffffu, !mbar_wait(B.q_empty, it & 1u, abort_flag));  // warp-uniform
+        cq_next = q_prep(a, b_next, tq, qtail, s_qm, B.q_ready, q, x, lane, fail);
+        if (wg_bar_or(fail)) break;
+      }
+    }
     // ---- the item's result: wait for its last PV and its status
     const uint32_t gl = g + n - 1;
     fail = !mbar_wait(&B.p_empty[gl & 1u], (gl >> 1) & 1u, abort_flag) ||
@@ -634,11 +796,13 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       }
     }
     if (d.nb != 1 && wt < kTH) a.part_ml[(size_t)d.cg * kTH + wt] = make_float2(s_m[wt], s_l[wt] + s_l[kTH + wt]);
+    if (wt == 0) a.part_st[d.cg] = stv;  // the merge ORs the pieces' bits into the request's status
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(B.o_empty);
     named_bar_sync(1, kSmxThreads);  // the scratch is reused by the next item
     if (wt == 0) mbar_arrive(&B.item_empty[slot]);
+    cq = cq_next;
     g += n;
   }
 }
@@ -666,9 +830,8 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
       mbar_init(&B.p_full[i], kSmxThreads / 32);
       mbar_init(&B.p_empty[i], 2);  // a commit from each PV issuer
     }
-    mbar_init(B.q_full, 1);
+    mbar_init(B.q_ready, kSmxThreads / 32);
     mbar_init(B.q_empty, 1);
-    mbar_init(B.q_tfull, kSmxThreads / 32);
     mbar_init(B.o_empty, kSmxThreads / 32);
     mbar_init(B.r_done, kSmxThreads / 32);
     mbar_init(B.drain, 3);  // one commit from each MMA issuer
@@ -710,10 +873,9 @@ __global__ void __launch_bounds__(kTThreads, 1) latent_tc_kernel(const __grid_co
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  // A wait gave up somewhere in this block: every request of the call is
-  // reported as timed out (its output is not valid).
-  if (threadIdx.x == 0 && *abort_flag)
-    for (int b = 0; b < a.B; ++b) atomicOr(&a.status[b], PFKV_ST_TIMEOUT);
+  // Whether a wait gave up somewhere in this block; the merge then reports
+  // every request of the call as timed out (its output is not valid).
+  if (threadIdx.x == 0) a.cta_abort[blockIdx.x] = *abort_flag != 0;
 }
 
 }  // namespace
@@ -736,11 +898,10 @@ static int make_stream_map(CUtensorMap *map, const void *pool, int P, uint32_t b
 }
 
 int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
-  // Work items are splits of a request, all 64 heads each.
+  // Work items are pieces of a request, all 64 heads each.
   DecodeArgs a = a0;
   a.Hkv = 1;
   a.G = kTH;
-  a.qprep = 1;
   CUtensorMap map, map_tail;
   int rc = make_stream_map(&map, a.k_pool, a.P, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
@@ -760,12 +921,15 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
       if (dev < 64) attr_set[dev] = true;
     }
   }
-  const int grid = num_sms();
-  // one equal page range per CTA when requests may be cut into 3 or more
-  // pieces; otherwise longest-first items from a shared counter
-  a.balanced = a.max_splits >= 3 ? (grid < kMaxRanges ? grid : kMaxRanges) : 0;
-  rc = cuda_ok(launch_plan(a, s, grid * 2, 8), "plan kernel launch");
-  if (rc) return rc;
+  // One CTA per SM, each taking one range of the requests' pages (no plan
+  // kernel); small or lopsided batches fall back to chunks of at least 8
+  // pages, about two per CTA.
+  const int grid = min(num_sms(), kMaxCtas);
+  a.ranges = grid;
+  a.n_ctas = grid;
+  a.target_items = 2 * grid;
+  a.min_chunk_pages = 8;
+  a.piece_cost = kPieceCostLatent;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -778,7 +942,8 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   cfg.numAttrs = 1;
   rc = cuda_ok(cudaLaunchKernelEx(&cfg, latent_tc_kernel, map, map_tail, a), "latent kernel launch");
   if (rc) return rc;
-  // merge in blocks of 16 heads
+  // status of every request, and the merge of requests cut into several
+  // pieces, in blocks of 16 heads
   DecodeArgs m = a;
   m.Hkv = kTH / 16;
   m.G = 16;

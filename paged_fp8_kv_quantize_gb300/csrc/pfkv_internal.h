@@ -10,29 +10,12 @@
 
 namespace pfkv {
 
-// Workspace header (first 256 bytes of the decode workspace).
-struct WsHeader {
-  int n_chunks;     // sum over requests of split count
-  int n_items;      // n_chunks * num_kv_heads
-  unsigned work;    // dynamic work counter
-  unsigned err;     // nonzero: a kernel wait timed out
-  int chunk_pages;  // pages per split target (balanced plan: number of ranges)
-  int n_ranges;     // > 0: balanced plan with this many ranges; 0: items from the work counter
-  int pad[58];
-};
-
 // Decode workspace carve-up.
 struct WsLayout {
-  size_t hdr, split_first, split_count, chunk_info, cta_first, part_ml, part_o, part_st, cta_abort, qterms, qfac,
-      total;
+  size_t split_first, split_count, part_ml, part_o, part_st, cta_abort, total;
 };
-constexpr int kMaxRanges = 1024;  // balanced plan: at most this many page ranges (one per CTA)
-constexpr int kMaxCtas = 4096;    // grouped-query split grid: at most this many CTAs (one abort word each)
-// latent: the latent-stream path also keeps each request's query as two e4m3
-// terms in the operand image its kernel loads (qterms, 72 KB per request)
-// and one factor per head (qfac).
-WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool latent);
-constexpr size_t kLatentQTermBytes = 128 * 576;  // 128 operand rows (two terms x 64 heads) x 576 codes
+constexpr int kMaxCtas = 4096;  // decode split grid: at most this many CTAs (one abort word each)
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits);
 
 struct DecodeArgs {
   // cache
@@ -50,44 +33,28 @@ struct DecodeArgs {
   uint32_t flags;
   int max_splits;
   // workspace and outputs
-  WsHeader *hdr;
-  int *split_first, *split_count;  // per request: index of its first split, number of splits
-  int4 *chunk_info;  // per split, two int4: {request, first page, end page, length}, {splits of the request, 0, 0, 0}
+  int *split_first, *split_count;  // per request: number of its first piece, number of pieces
   float2 *part_ml;
   float *part_o;
   float *out;
   uint32_t *status;
-  // decode step only: new rows k_new / v_new [B][Hkv][D] bf16 go to
-  // position seq_lens[b] - 1 of each request before attention, through
-  // `cache` (the same pools, writable).  append == 1: the plan grid writes
-  // them; split_append == 1: the grouped-query split kernel's producer
-  // writes each (request, KV head)'s row just before it copies that page.
-  int append, split_append;
+  // decode step only (append == 1): the new rows k_new / v_new [B][Hkv][D]
+  // bf16 go to position seq_lens[b] - 1 of each request; the split kernel's
+  // page loader writes each (request, KV head)'s row through `cache` (the same
+  // pools, writable) just before it copies that page.
+  int append;
   const uint16_t *k_new, *v_new;
   pfkv_cache cache;
-  // latent-stream path only (qprep == 1): the plan grid writes the query
-  // terms and per-head factors of every request here
-  int qprep;
-  uint8_t *qterms;
-  float *qfac;
-  // balanced plan (balanced > 0: at most that many ranges): the concatenated
-  // page list of all requests is cut into equal ranges; range r covers
-  // chunks cta_first[r] .. cta_first[r + 1] - 1, taken for KV head h by CTA
-  // r * Hkv + h.  The plan falls back to longest-first items from the work
-  // counter when fewer than 3/4 of the ranges survive its caps; the header's
-  // n_ranges says which plan was made.
-  int balanced;
-  int *cta_first;
-  // grouped-query path (self_plan == 1): no plan kernel; every split CTA
-  // works out its own pieces from seq_lens.  ranges = CTA groups (one CTA
-  // per KV head each); the chunk rule of small or lopsided batches takes
-  // pieces of at least min_chunk_pages pages, about target_items of them
-  // over all KV heads.  Written per call: split_first / split_count of every
-  // request with a valid length (by the head-0 CTA holding its first
-  // piece), part_st[piece] (status bits found by the head-0 item) and
-  // cta_abort[0 .. n_ctas) (1: a wait of that CTA gave up).  The merge turns
-  // them into status[] and zeroes the rows of faulted requests.
-  int self_plan, ranges, target_items, min_chunk_pages, n_ctas;
+  // Work split (no plan kernel): every split CTA works out its own pieces
+  // from seq_lens.  ranges = CTA groups (one CTA per KV head each); the chunk
+  // rule of small or lopsided batches takes pieces of at least
+  // min_chunk_pages pages, about target_items of them over all KV heads.
+  // Written per call: split_first / split_count of every request with a
+  // valid length (by the head-0 CTA holding its first piece), part_st[piece]
+  // (status bits found by the head-0 item) and cta_abort[0 .. n_ctas) (1: a
+  // wait of that CTA gave up).  The merge turns them into status[] and zeroes
+  // the rows of faulted requests.
+  int ranges, target_items, min_chunk_pages, n_ctas;
   int piece_cost;  // cut rule: pages' worth of time one piece costs beyond its pages
   uint32_t *part_st;
   int *cta_abort;

@@ -34,10 +34,10 @@ def test_host_only_entry_points():
     assert "workspace" in abi.strerror(-5)
     d = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, 16)
     n = abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 64)
-    # header, per-request split index and count, split descriptors, (m, l) and
-    # O partials for every (request, split, head), a status word per split and
-    # an abort word per split CTA
-    fixed = 64 * 64 * 32 * (8 + 4 * 128) + 64 * 64 * 32
+    # per-request piece index and count, (m, l) and O partials for every
+    # (request, piece, head), a status word per piece and an abort word per
+    # split CTA
+    fixed = 64 * 64 * 32 * (8 + 4 * 128) + 64 * 64 * 4
     assert fixed <= n < fixed + 64 * 1024
 
 
