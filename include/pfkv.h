@@ -170,10 +170,13 @@ size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32
  * are merged with the log-sum-exp rule.  workspace must hold
  * pfkv_decode_workspace_bytes(cache, batch, num_q_heads, max_splits) bytes;
  * its contents need no initialisation and are scratch between calls.
- * Supported: head_dim 64 or 128 with groups 1, 2, 4, 8 (page_size a
- * multiple of 16, at most 256; at most 4096 KV heads, else
+ * Supported: head_dim 64 or 128 with any group size num_q_heads /
+ * num_kv_heads (page_size a multiple of 16, at most 256; a group of more
+ * than 8 query heads is run as ceil(G / 8) groups of at most 8 that each
+ * read the KV head, and num_kv_heads * ceil(G / 8) may not exceed 4096, else
  * PFKV_ERR_UNSUPPORTED); the latent stream head_dim 576 / v_head_dim 512
- * with 64 query heads (FP8, PER_TOKEN, page_size 64).
+ * with 64 query heads (FP8, PER_TOKEN, page_size 64).  num_q_heads must be a
+ * multiple of num_kv_heads (PFKV_ERR_SHAPE).
  * pfkv_paged_decode_attention_fp8 requires an FP8 cache, _bf16 a BF16 cache.
  */
 int pfkv_paged_decode_attention_fp8(const pfkv_cache *cache, const void *q, int32_t num_q_heads,

@@ -108,6 +108,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.k_pool = c->k_pool; a.v_pool = c->v_pool; a.k_scale = c->k_scale; a.v_scale = c->v_scale;
   a.page_tags = c->page_tags;
   a.q = q; a.Hq = Hq; a.G = Hq / c->num_kv_heads;
+  a.kv_sub = 1; a.Gs = a.G;
   a.seq_lens = seq_lens; a.block_table = block_table; a.block_tags = block_tags;
   a.B = batch; a.MP = max_pages;
   a.sm_scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -136,8 +137,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
       return PFKV_ERR_UNSUPPORTED;
     return launch_latent_decode(a, s);
   }
-  if ((c->head_dim != 64 && c->head_dim != 128) || (a.G != 1 && a.G != 2 && a.G != 4 && a.G != 8))
-    return PFKV_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return PFKV_ERR_UNSUPPORTED;
   if (c->dtype == PFKV_DTYPE_BF16 && c->scale_mode != PFKV_SCALE_PER_HEAD) return PFKV_ERR_SHAPE;
   return launch_gqa_decode(a, s);
 }

@@ -17,6 +17,20 @@ namespace {
 constexpr float kNegInf = -INFINITY;
 constexpr int kNIQ = 4;  // item descriptors in flight per CTA
 
+// One virtual KV head's KV head and query heads (see DecodeArgs::kv_sub).
+struct HeadGroup {
+  int kv, first, count;
+};
+
+__device__ __forceinline__ HeadGroup head_group(const DecodeArgs &a, int v) {
+  HeadGroup r;
+  r.kv = v / a.kv_sub;
+  const int sub = v - r.kv * a.kv_sub;
+  r.first = r.kv * a.G + sub * a.Gs;
+  r.count = min(a.Gs, a.G - sub * a.Gs);
+  return r;
+}
+
 struct ItemDesc {
   int b, cg, g, p0, p1, L;
   uint32_t ring;
@@ -303,10 +317,13 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   // kernels asking for the largest shared-memory carveout).
   pdl_wait();  // partials and status of the split kernel are visible from here on
   const int b = blockIdx.x / a.Hkv, g = blockIdx.x - b * a.Hkv;
+  const HeadGroup hg = head_group(a, g);
   const int t = threadIdx.x;
-  float *out_bg = a.out + ((size_t)b * a.Hq + g * kG) * kD;
+  float *out_bg = a.out + ((size_t)b * a.Hq + hg.first) * kD;
   const int col_lo = (int)blockIdx.y * M::kW;
   const int h_lo = col_lo * 4 / kD;  // first head of this block's columns
+  // float4 columns of this block that belong to real heads of the group
+  const int col_hi = min(col_lo + M::kW, hg.count * kD / 4);
   // This kernel writes status[b].  The block of (request, head group 0, first
   // columns) gathers the bits the request's pieces found and whether any
   // split CTA gave up; every block zeroes its columns of a faulted request.
@@ -314,7 +331,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   const bool lead = g == 0 && blockIdx.y == 0;
   const int L = a.seq_lens[b];
   if (L < 1 || (long long)L > (long long)a.MP * a.S) {
-    for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
+    for (int i = 4 * col_lo + t; i < 4 * col_hi; i += 256) out_bg[i] = 0.f;
     if (lead && t == 0) a.status[b] = PFKV_ST_BAD_LEN;
     return;
   }
@@ -328,7 +345,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
     for (int i = t; i < nb; i += 256) st |= __ldcg(&a.part_st[c0 + i]);
     if (nb > 1)  // each piece's (m, l) for the heads of this block's columns
       for (int i = t; i < nb * M::kNH; i += 256) {
-        const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / M::kNH) * a.Hq + g * kG + h_lo + i % M::kNH]);
+        if (h_lo + i % M::kNH >= hg.count) continue;  // a padding slot of the group
+        const float2 ml = __ldcg(&a.part_ml[(size_t)(c0 + i / M::kNH) * a.Hq + hg.first + h_lo + i % M::kNH]);
         s_w[i] = ml.x;
         s_l[i] = ml.y;
       }
@@ -345,12 +363,13 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   if (lead && t == 0) a.status[b] = st | (gave_up || !sane ? (uint32_t)PFKV_ST_TIMEOUT : 0u);
   if (!sane || nb == 1) return;  // a one-piece request's rows come from the split kernel
   if (st) {
-    for (int i = 4 * col_lo + t; i < 4 * (col_lo + M::kW); i += 256) out_bg[i] = 0.f;
+    for (int i = 4 * col_lo + t; i < 4 * col_hi; i += 256) out_bg[i] = 0.f;
     return;
   }
+  if (col_hi <= col_lo) return;  // only padding slots in this block
   __syncthreads();
   const int warp = t >> 5, lane = t & 31;
-  if (warp < M::kNH) {
+  if (warp < M::kNH && h_lo + warp < hg.count) {
     const int hh = warp;
     float Mx = -INFINITY;
     for (int c = lane; c < nb; c += 32) Mx = fmaxf(Mx, s_w[c * M::kNH + hh]);
@@ -370,17 +389,18 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   const size_t cstride = (size_t)a.Hq * kD / 4;
   const int col = col_lo + t % M::kW, grp = t / M::kW;
   const int jh = col * 4 / kD - h_lo;
-  const float4 *po = reinterpret_cast<const float4 *>(a.part_o + ((size_t)c0 * a.Hq + g * kG) * kD) + col;
+  const float4 *po = reinterpret_cast<const float4 *>(a.part_o + ((size_t)c0 * a.Hq + hg.first) * kD) + col;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool real = col < col_hi;
 #pragma unroll 4
-  for (int c = grp; c < nb; c += M::kGroups) {
+  for (int c = grp; real && c < nb; c += M::kGroups) {
     const float w = s_w[c * M::kNH + jh];
     const float4 v = __ldcg(po + (size_t)c * cstride);
     acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
   }
   s_acc[t] = acc;
   __syncthreads();
-  if (t < M::kW) {
+  if (t < M::kW && real) {
     for (int k = 1; k < M::kGroups; ++k) {
       const float4 v = s_acc[t + k * M::kW];
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;

@@ -109,7 +109,7 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, floa
   const int pid = __shfl_sync(0xffffffffu, pid_lane, src);
   const bool refused = __shfl_sync(0xffffffffu, oob_lane || stale_lane, src);
   if (refused) return;
-  const size_t row = ((size_t)pid * a.Hkv + g) * a.S + slot;
+  const size_t row = ((size_t)pid * a.cache.num_kv_heads + g) * a.S + slot;
   if constexpr (kFp8) {
     if (per_token) {
       float amax = amax8(v, 0.f);  // lanes without values hold zeros
@@ -195,7 +195,12 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     uint32_t ring = 0;
     // This CTA's pieces for KV head g, worked out from the lengths; the next
     // piece is found once the current one's pages have gone out.
-    const int g = (int)blockIdx.x % a.Hkv;
+    // this CTA's head group: virtual KV head vg, which reads KV head g (a KV
+    // head whose query heads are cut into several groups is read by one CTA
+    // of each group; every one of them writes a decode step's new row, the
+    // same bytes, before its own copy of the page)
+    const int vg = (int)blockIdx.x % a.Hkv;
+    const int g = vg / a.kv_sub;
     __shared__ WorkSplit s_ws;
     {
       WorkSplit w;
@@ -229,10 +234,10 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       const int b = cur.b, p0 = cur.p0, p1 = cur.p1, L = cur.L;
       if (lane == 0) {
         ItemDesc d;
-        d.b = b; d.cg = cur.cg; d.g = g; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = cur.nb;
+        d.b = b; d.cg = cur.cg; d.g = vg; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = ring; d.nb = cur.nb;
         items[slot] = d;
         if (!withhold) mbar_arrive(&item_full[slot]);
-        if (g == 0 && cur.lead) {  // the merge's view of the numbering
+        if (vg == 0 && cur.lead) {  // the merge's view of the numbering
           a.split_first[b] = cur.cg;
           a.split_count[b] = cur.nb;
         }
@@ -251,7 +256,8 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       uint4 nv = make_uint4(0u, 0u, 0u, 0u);
       float nv_scale = 1.f;
       if (nv_lane) {
-        nv = *reinterpret_cast<const uint4 *>((nv_part ? a.v_new : a.k_new) + ((size_t)b * a.Hkv + g) * kD + nv_k);
+        nv = *reinterpret_cast<const uint4 *>((nv_part ? a.v_new : a.k_new) +
+                                              ((size_t)b * a.cache.num_kv_heads + g) * kD + nv_k);
         if (kFp8 && !per_token) nv_scale = __ldg(&(nv_part ? a.v_scale : a.k_scale)[g]);
       }
       for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages) {
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
                 tma_load_4d_stream(stage + S * C::kRowBytes, &tmV, &full[st], 0, 0, g, pid, stream_pol);
               }
               if (per_token) {
-                const size_t rr = ((size_t)pid * a.Hkv + g) * S;
+                const size_t rr = ((size_t)pid * a.cache.num_kv_heads + g) * S;
                 bulk_load_stream(stage + 2 * S * C::kRowBytes, a.k_scale + rr, 4u * S, &full[st], stream_pol);
                 bulk_load_stream(stage + 2 * S * C::kRowBytes + 4 * S, a.v_scale + rr, 4u * S, &full[st], stream_pol);
               }
@@ -352,13 +358,15 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       const ItemDesc d = items[slot];
       if (d.b < 0) break;
 
-      // query fragments of the group's heads (row gid of the B operand)
+      // query fragments of the group's heads (row gid of the B operand; rows
+      // past the group's heads are padding, zero)
+      const HeadGroup hg = head_group(a, d.g);
       uint32_t qf[C::kKsteps][2];
       float mult[2];
       {
-        const int h = d.g * kG + gid;
+        const int h = hg.first + gid;
         float qv[kD / 4];
-        if (gid < kG) {
+        if (gid < hg.count) {
           const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) +
                                                               ((size_t)d.b * a.Hq + h) * kD + tq * (kD / 4));
 #pragma unroll
@@ -400,7 +408,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           }
         }
         float base = a.sm_scale_log2;
-        if (kFp8 && !per_token) base *= __ldg(&a.k_scale[d.g]);
+        if (kFp8 && !per_token) base *= __ldg(&a.k_scale[hg.kv]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int ec = __shfl_sync(0xffffffffu, e, ((2 * tq + c) & 7) * 4);
@@ -652,11 +660,11 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
       named_bar_sync(1, kCT);
       const uint32_t item_st = (uint32_t)sm_ctl[0];
       float ofac = 1.f;
-      if constexpr (kFp8) ofac = (per_token ? 1.f : __ldg(&a.v_scale[d.g])) / C::kPScale;
-      float *out_bg = a.out + ((size_t)d.b * a.Hq + d.g * kG) * kD;  // rows of this (request, KV head)
+      if constexpr (kFp8) ofac = (per_token ? 1.f : __ldg(&a.v_scale[hg.kv])) / C::kPScale;
+      float *out_bg = a.out + ((size_t)d.b * a.Hq + hg.first) * kD;  // rows of this (request, head group)
       if (d.nb == 1) {
         // the item covers the whole request: finish it here
-        for (int idx = t; idx < kG * kD; idx += kCT) {
+        for (int idx = t; idx < hg.count * kD; idx += kCT) {
           const int jh = idx / kD, dd = idx - jh * kD;
           const float M = sm_fin[2 * jh];
           float acc = 0.f;
@@ -668,7 +676,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           out_bg[idx] = item_st ? 0.f : acc * ofac / sm_fin[2 * jh + 1];
         }
       } else {
-        for (int idx = t; idx < kG * kD; idx += kCT) {
+        for (int idx = t; idx < hg.count * kD; idx += kCT) {
           const int jh = idx / kD, dd = idx - jh * kD;
           const float M = sm_fin[2 * jh];
           float acc = 0.f;
@@ -677,9 +685,9 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
             const float mw = sm_m[w * kG + jh];
             if (mw != kNegInf) acc += sm_o[(w * kG + jh) * kD + dd] * fast_exp2(mw - M);
           }
-          a.part_o[((size_t)d.cg * a.Hq + d.g * kG) * kD + idx] = acc * ofac;
+          a.part_o[((size_t)d.cg * a.Hq + hg.first) * kD + idx] = acc * ofac;
         }
-        if (t < kG) a.part_ml[(size_t)d.cg * a.Hq + d.g * kG + t] = make_float2(sm_fin[2 * t], sm_fin[2 * t + 1]);
+        if (t < hg.count) a.part_ml[(size_t)d.cg * a.Hq + hg.first + t] = make_float2(sm_fin[2 * t], sm_fin[2 * t + 1]);
       }
       // the walk's bits are the same for every KV head (same pages and tags):
       // head 0's item reports them for the piece
@@ -817,14 +825,26 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
   return cuda_ok(cudaLaunchKernelEx(&mcfg, merge_kernel<kD, kG>, a), "merge kernel launch");
 }
 
+// Any group size: up to 8 query heads per CTA group (the register-operand
+// MMA's N dimension); a larger group is cut into kv_sub head groups of Gs
+// heads each, run as virtual KV heads (every group reads the KV head's
+// pages: the groups of one KV head are neighbouring CTAs, whose copies of a
+// page mostly meet in L2).  The kernel is instantiated for 1, 2, 4 or 8
+// head slots; a group of Gs heads takes the next of these and leaves the
+// other slots as zero-query padding whose results are never written.
 template <bool kFp8, int kD>
-int dispatch_g(const DecodeArgs &a, cudaStream_t s, const CUtensorMap &mk, const CUtensorMap &mv) {
-  switch (a.G) {
+int dispatch_g(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, const CUtensorMap &mv) {
+  DecodeArgs a = a_in;
+  a.kv_sub = (a.G + 7) / 8;
+  a.Gs = (a.G + a.kv_sub - 1) / a.kv_sub;
+  if ((long long)a.Hkv * a.kv_sub > kMaxCtas) return PFKV_ERR_UNSUPPORTED;
+  a.Hkv *= a.kv_sub;
+  const int slots = a.Gs <= 1 ? 1 : a.Gs <= 2 ? 2 : a.Gs <= 4 ? 4 : 8;
+  switch (slots) {
     case 1: return run_split<kFp8, kD, 1>(a, s, mk, mv);
     case 2: return run_split<kFp8, kD, 2>(a, s, mk, mv);
     case 4: return run_split<kFp8, kD, 4>(a, s, mk, mv);
-    case 8: return run_split<kFp8, kD, 8>(a, s, mk, mv);
-    default: return PFKV_ERR_UNSUPPORTED;
+    default: return run_split<kFp8, kD, 8>(a, s, mk, mv);
   }
 }
 

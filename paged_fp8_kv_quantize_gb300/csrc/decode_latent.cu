@@ -945,8 +945,10 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   // status of every request, and the merge of requests cut into several
   // pieces, in blocks of 16 heads
   DecodeArgs m = a;
-  m.Hkv = kTH / 16;
-  m.G = 16;
+  m.Hkv = kTH / 16;  // four groups of 16 query heads, all on the one stream
+  m.kv_sub = kTH / 16;
+  m.G = kTH;
+  m.Gs = 16;
   cudaLaunchConfig_t mcfg = {};
   mcfg.gridDim = dim3(a.B * m.Hkv, merge_col_blocks<kTDv, 16>());
   mcfg.blockDim = dim3(256);

@@ -25,7 +25,13 @@ struct DecodeArgs {
   const uint32_t *page_tags;
   // request batch
   const void *q;
-  int Hq, G;
+  int Hq, G;  // query heads; query heads per KV head
+  // Head groups (grouped-query path): the G query heads of a KV head are cut
+  // into kv_sub groups of up to Gs heads, each run as a "virtual" KV head by
+  // its own CTAs; Hkv then counts virtual heads (num_kv_heads * kv_sub).
+  // Virtual head v reads KV head v / kv_sub for query heads
+  // (v / kv_sub) G + (v % kv_sub) Gs .. + min(Gs, G - (v % kv_sub) Gs) - 1.
+  int kv_sub, Gs;
   const int *seq_lens, *block_table;
   const uint32_t *block_tags;
   int B, MP;

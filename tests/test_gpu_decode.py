@@ -54,6 +54,44 @@ def test_decode_shapes(dtype, si):
     _check(_work(300 + si, G=G, Hkv=Hkv, D=D, S=S, lens=lens), dtype)
 
 
+# Group sizes outside 1, 2, 4, 8: up to 8 query heads per head group, with
+# padding slots (3, 5, 6, 7), and larger groups cut into several head groups
+# that read the same KV head (12, 16, 24, 64).  The attention is the plain
+# definition for any grouping of query heads over KV heads.
+GENERAL_G = [
+    # (G, Hkv, D, S)
+    (3, 4, 128, 16),
+    (5, 2, 64, 16),
+    (6, 2, 128, 32),
+    (7, 1, 64, 64),
+    (12, 2, 128, 16),
+    (16, 2, 128, 16),
+    (16, 4, 64, 64),
+    (24, 1, 128, 16),
+    (64, 1, 64, 16),
+]
+
+
+@pytest.mark.parametrize("dtype", [FP8, BF16])
+@pytest.mark.parametrize("gi", range(len(GENERAL_G)))
+def test_decode_general_group_sizes(dtype, gi):
+    G, Hkv, D, S = GENERAL_G[gi]
+    rng = np.random.default_rng(700 + gi)
+    lens = list(rng.integers(1, 2500, size=5)) + [1, S + 1, 4000]
+    _check(_work(700 + gi, G=G, Hkv=Hkv, D=D, S=S, lens=lens), dtype, flags=abi.FLAG_TAG_CHECK)
+
+
+def test_decode_general_group_per_token_and_faults():
+    # G = 16 (two head groups per KV head) with per-token scales, a stale tag,
+    # an out-of-pool page and a bad length, over several splits
+    w = _work(710, G=16, Hkv=2, D=128, S=16, lens=[3000, 700, 1500, 20, 2200], scale_mode=synth.PER_TOKEN,
+              stale_block_entries=[(1, 3)])
+    w.block_table[2, 5] = w.num_pages + 7
+    w.seq_lens[3] = w.max_pages * 16 + 1
+    run, out, st = _check(w, FP8, flags=abi.FLAG_TAG_CHECK, max_splits=8)
+    assert list(st) == [0, abi.ST_STALE_TAG, abi.ST_PAGE_OOB, abi.ST_BAD_LEN, 0]
+
+
 @pytest.mark.parametrize("max_splits", [1, 2, 3, 64, 256])
 def test_split_counts(max_splits):
     # 1, 2: chunk rule; 3: the cut rule's cap leaves too few ranges, so the
@@ -191,7 +229,7 @@ def test_host_errors():
         abi.paged_decode_attention_fp8(run.cache, run.q, run.seq_lens, run.table, run.tags, 1.0,
                                        workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert e.value.code == -5
-    q3 = torch.zeros(1, 24, 128, dtype=torch.bfloat16, device="cuda")  # 24 heads: group 3 unsupported
+    q20 = torch.zeros(1, 20, 128, dtype=torch.bfloat16, device="cuda")  # 20 query heads over 8 KV heads
     with pytest.raises(abi.PfkvError) as e:
-        abi.paged_decode_attention_fp8(run.cache, q3, run.seq_lens, run.table, run.tags, 1.0)
-    assert e.value.code == -3
+        abi.paged_decode_attention_fp8(run.cache, q20, run.seq_lens, run.table, run.tags, 1.0)
+    assert e.value.code == -2

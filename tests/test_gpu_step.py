@@ -101,7 +101,8 @@ def test_step_gqa_chunk_rule(dtype, max_splits):
 
 
 @pytest.mark.parametrize("dtype", [FP8, BF16])
-@pytest.mark.parametrize("shape", [(8, 1, 128, 64), (4, 2, 64, 16), (2, 4, 64, 32)])
+@pytest.mark.parametrize("shape", [(8, 1, 128, 64), (4, 2, 64, 16), (2, 4, 64, 32), (3, 2, 128, 16),
+                                   (16, 2, 64, 16)])
 def test_step_other_shapes(dtype, shape):
     # group sizes 8 and 2, head width 64, pages of 64 and 32 tokens: the new
     # rows are written by the item holding each request's last page
