@@ -24,7 +24,7 @@
  *    request's tokens, o = sum p v, evaluated in fp64 on the dequantized
  *    cache.
  *
- * Readings where the pages are silent (each one also listed in the design doc):
+ * Readings where the pages are silent (the plainest one the rest supports):
  *  R1  encode saturates: |y| > 448 encodes as +-448 (E4M3FN has no inf).
  *  R2  the sign survives rounding to zero: -tiny -> 0x80.
  *  R3  quantize divides: code = e4m3(fp32(x) / s), an IEEE fp32 division.

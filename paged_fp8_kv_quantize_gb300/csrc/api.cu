@@ -38,6 +38,9 @@ int num_sms() {
 
 static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Every size here is bounded by the callers (batch < 2^31, max_splits <= 256,
+// q_heads <= kMaxQHeads, v_dim <= kMaxHeadDim), so the products below stay
+// far inside size_t.
 WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
   WsLayout w;
   const size_t slots = (size_t)batch * max_splits * q_heads;
@@ -53,6 +56,11 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Largest query-head count and head width a decode call accepts (far above
+// any model's; they bound the workspace arithmetic).
+constexpr int kMaxQHeads = 65536;
+constexpr int kMaxHeadDim = 4096;
+
 static bool is_latent(const pfkv_cache *c) {
   return c->kv_shared && c->num_kv_heads == 1 && c->head_dim == 576 && c->v_head_dim == 512;
 }
@@ -62,6 +70,7 @@ static int check_cache(const pfkv_cache *c) {
   if (!c) return PFKV_ERR_NULL;
   if (c->num_pages < 1 || c->page_size < 1 || c->num_kv_heads < 1 || c->head_dim < 1 || c->v_head_dim < 1)
     return PFKV_ERR_SHAPE;
+  if (c->head_dim > kMaxHeadDim || c->v_head_dim > kMaxHeadDim || c->num_kv_heads > kMaxQHeads) return PFKV_ERR_SHAPE;
   if (c->dtype != PFKV_DTYPE_BF16 && c->dtype != PFKV_DTYPE_FP8_E4M3) return PFKV_ERR_DTYPE;
   if (c->scale_mode != PFKV_SCALE_PER_HEAD && c->scale_mode != PFKV_SCALE_PER_TOKEN) return PFKV_ERR_SHAPE;
   if (!c->k_pool) return PFKV_ERR_NULL;
@@ -80,15 +89,26 @@ static int check_cache(const pfkv_cache *c) {
   return PFKV_OK;
 }
 
+// The checks a decode call makes before it looks at the workspace (shared
+// with the no-allocation entry point, so that both return the same code for
+// the same bad arguments).
+int decode_precheck(int want_dtype, const pfkv_cache *c, int32_t Hq, int32_t batch, int32_t max_pages,
+                    int32_t max_splits) {
+  int rc = check_cache(c);
+  if (rc) return rc;
+  if (c->dtype != want_dtype) return PFKV_ERR_DTYPE;
+  if (batch < 0 || max_pages < 1 || Hq < 1 || Hq > kMaxQHeads || max_splits < 1 || max_splits > 256)
+    return PFKV_ERR_SHAPE;
+  return PFKV_OK;
+}
+
 static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int32_t Hq, const int32_t *seq_lens,
                          const int32_t *block_table, const uint32_t *block_tags, int32_t batch, int32_t max_pages,
                          float softmax_scale, uint32_t flags, int32_t max_splits, void *ws, size_t ws_bytes,
                          float *out, uint32_t *status, void *stream, const void *k_new = nullptr,
                          const void *v_new = nullptr) {
-  int rc = check_cache(c);
+  const int rc = decode_precheck(want_dtype, c, Hq, batch, max_pages, max_splits);
   if (rc) return rc;
-  if (c->dtype != want_dtype) return PFKV_ERR_DTYPE;
-  if (batch < 0 || max_pages < 1 || Hq < 1 || max_splits < 1 || max_splits > 256) return PFKV_ERR_SHAPE;
   // the kernels' page arithmetic assumes at most 2^40 pages in one call
   if ((uint64_t)batch * (uint64_t)max_pages > (1ull << 40)) return PFKV_ERR_SHAPE;
   if (!isfinite(softmax_scale)) return PFKV_ERR_SHAPE;
@@ -188,8 +208,13 @@ int pfkv_kv_append_quantize(const pfkv_cache *cache, const void *k_new, const vo
 
 size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32_t num_q_heads, int32_t max_splits) {
   if (!cache || batch < 0 || num_q_heads < 1 || max_splits < 1) return 0;
+  // sizes a decode call would refuse: no workspace fits them
+  if (num_q_heads > kMaxQHeads || max_splits > 256 || cache->v_head_dim < 1 || cache->v_head_dim > kMaxHeadDim)
+    return SIZE_MAX;
   return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits).total;
 }
+
+
 
 int pfkv_paged_decode_attention_fp8(const pfkv_cache *cache, const void *q, int32_t num_q_heads,
                                     const int32_t *seq_lens, const int32_t *block_table,

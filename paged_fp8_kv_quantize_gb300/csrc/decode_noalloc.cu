@@ -49,9 +49,11 @@ extern "C" int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, 
                                                        const uint32_t *block_tags, int32_t batch, int32_t max_pages,
                                                        float softmax_scale, uint32_t flags, int32_t max_splits,
                                                        float *out, uint32_t *status, void *stream) {
-  if (!cache) return PFKV_ERR_NULL;
-  if (batch < 0 || num_q_heads < 1 || max_splits < 1) return PFKV_ERR_SHAPE;
-  // Reject, before touching the device, any call whose scratch would not fit.
+  // The regular entry point's own checks first, so that a bad descriptor or
+  // size gives the same code here as there; then, before touching the
+  // device, any call whose scratch would not fit is rejected.
+  const int pre = pfkv::decode_precheck(PFKV_DTYPE_FP8_E4M3, cache, num_q_heads, batch, max_pages, max_splits);
+  if (pre) return pre;
   if (pfkv_decode_workspace_bytes(cache, batch, num_q_heads, max_splits) > (size_t)PFKV_NOALLOC_SCRATCH_BYTES)
     return PFKV_ERR_WORKSPACE;
   void *scratch = nullptr;

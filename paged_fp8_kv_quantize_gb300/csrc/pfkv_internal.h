@@ -92,6 +92,10 @@ int launch_page_realloc(void *state, uint32_t *page_tags, const int *pages, int 
 int launch_calibrate(const void *rows, int64_t n_rows, int heads, int dim, float *scale, cudaStream_t s);
 int launch_encode(const float *x, uint8_t *codes, int64_t n, cudaStream_t s);
 
+// The argument checks a decode call makes before it looks at the workspace.
+int decode_precheck(int want_dtype, const pfkv_cache *c, int32_t Hq, int32_t batch, int32_t max_pages,
+                    int32_t max_splits);
+
 // Records the CUDA error behind a PFKV_ERR_CUDA return (per host thread).
 int cuda_fail(cudaError_t e, const char *where);
 inline int cuda_ok(cudaError_t e, const char *where = "kernel launch") {

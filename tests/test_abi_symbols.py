@@ -69,6 +69,44 @@ def test_argument_errors_return_before_any_cuda_call():
     assert f(ctypes.byref(ok), *edge) == -1
 
 
+def test_workspace_size_bounds_and_huge_head_counts():
+    # sizes a decode call refuses get no workspace size (SIZE_MAX), so that a
+    # caller sizing a buffer from it cannot be handed a wrapped-around small
+    # number; the decode itself refuses them before any CUDA call
+    ok = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None)
+    size_max = ctypes.c_size_t(-1).value
+    assert abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(ok), 64, 1 << 30, 64) == size_max
+    assert abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(ok), 64, 32, 100000) == size_max
+    wide = abi.CacheDesc(100, 16, 8, 128, 1 << 20, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None)
+    assert abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(wide), 64, 32, 64) == size_max
+    f = abi.lib.pfkv_paged_decode_attention_fp8
+    huge_heads = [None, 1 << 30, None, None, None, 4, 8, 1.0, 0, 64, None, 0, None, None, None]
+    assert f(ctypes.byref(ok), *huge_heads) == -2
+
+
+def test_noalloc_entry_point_checks_like_the_regular_one():
+    # every bad argument gives the same code from both entry points, before
+    # any device work (none of these calls reaches a CUDA call)
+    f = abi.lib.pfkv_paged_decode_attention_fp8
+    g = abi.lib.pfkv_paged_decode_attention_fp8_noalloc
+    cases = [
+        (None, 32, 4, 8, 64),                                                                  # NULL cache
+        (abi.CacheDesc(100, 16, 8, 128, -5, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None), 32, 4, 8, 64),
+        (abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_BF16, 0, 16, 16, None, None, None), 32, 4, 8, 64),
+        (abi.CacheDesc(100, 16, 8, 128, 128, 0, 9, 0, 16, 16, 16, 16, None), 32, 4, 8, 64),  # unknown dtype
+        (abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 17, 16, 16, 16, None), 32, 4, 8, 64),
+        (abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None), 0, 4, 8, 64),
+        (abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None), 32, -1, 8, 64),
+        (abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None), 32, 4, 8, 0),
+        (abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, None), 32, 4, 8, 300),
+    ]
+    for desc, hq, batch, mp, splits in cases:
+        d = None if desc is None else ctypes.byref(desc)
+        a = f(d, None, hq, None, None, None, batch, mp, 1.0, 0, splits, None, 0, None, None, None)
+        b = g(d, None, hq, None, None, None, batch, mp, 1.0, 0, splits, None, None, None)
+        assert a == b and a < 0, (a, b)
+
+
 def test_page_allocator_host_checks():
     L = abi.lib
     n = L.pfkv_page_allocator_bytes(1000)
