@@ -10,8 +10,15 @@ runs tag-checked paged decode attention over every request's context.
 
 Prints ONE JSON line (rank 0).  value = algorithmic KV GB/s of the step with
 inputs resident in HBM; e2e = the same with per-step inputs copied from
-pinned host memory and results copied back inside the timed region.
+pinned host memory and results copied back inside the timed region (on a
+second stream, double-buffered, overlapping the neighbouring steps).
 Inputs are larger than L2 (the cache alone is ~0.8 GB), so no flush.
+Also reported: per-call p50/p95 (one-call graphs, events between replays),
+the tag check's on/off ratio with a bootstrap interval and its p95, the BF16
+cache, the other benchmark shapes (grouped-query batch, long contexts over
+a pool of 80% of the free memory and over a dense pool, the latent stream),
+and the CPU oracle on the host cores (all cores and one thread on the ragged
+batch, all cores on the other shapes).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -147,6 +154,23 @@ def global_max(value, dist=None, device="cpu"):
     return float(t.item())
 
 
+def percentile(xs, q):
+    xs = sorted(xs)
+    if not xs:
+        return None
+    k = (len(xs) - 1) * q / 100.0
+    lo, hi = int(math.floor(k)), int(math.ceil(k))
+    return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+
+
+def bootstrap_ci(xs, stat=statistics.median, n=2000, seed=7):
+    """95% percentile-bootstrap interval of stat over the samples xs."""
+    rng = np.random.default_rng(seed)
+    arr = np.asarray(xs, dtype=np.float64)
+    vals = [stat(arr[rng.integers(0, arr.size, arr.size)]) for _ in range(n)]
+    return [percentile(vals, 2.5), percentile(vals, 97.5)]
+
+
 def job_throughput(units_per_rank, world, max_ms):
     """Whole-job rate: every rank runs the same replica, timed by the slowest."""
     return world * units_per_rank / (max_ms * 1e-3)
@@ -172,7 +196,7 @@ def recorded_traffic():
 # ---------------------------------------------------------------- CPU oracle leg
 
 
-def oracle_step_sample(w, frac):
+def oracle_step_sample(w, frac, threads=None):
     """Build the oracle's cache for a bounded sample of requests; return a callable step.
 
     The oracle runs with the tag check off: it skips the attention of an
@@ -201,7 +225,7 @@ def oracle_step_sample(w, frac):
     sel = np.isin(w.row_req, idx)
     rr = np.searchsorted(idx, w.row_req[sel]).astype(np.int32)
     c.append(w.k_rows[sel], w.v_rows[sel], w.row_pos[sel], ctab, w.block_tags[idx], row_req=rr, batch=idx.size)
-    threads = len(os.sched_getaffinity(0))
+    threads = threads or len(os.sched_getaffinity(0))
     lens0 = w.seq_lens[idx].astype(np.int32)
     state = {"j": 0}
 
@@ -217,6 +241,52 @@ def oracle_step_sample(w, frac):
     desc = (f"{idx.size} of {w.batch} requests ({int(lens0.sum())} of {total} context tokens), full step each, "
             f"tag check off")
     return step, threads, desc, idx.size
+
+
+def oracle_config_timings(latent_w=None):
+    """The oracle as it stands, timed on the host cores on the other
+    benchmark shapes: the tiny, grouped-query and long-context batches in
+    full, and one call of the latent-stream batch (decode only; the cache is
+    built first).  Returns {name: {...}}."""
+    import oracle
+
+    threads = len(os.sched_getaffinity(0))
+    res = {}
+
+    def one(name, w, fp8_per_head=True):
+        idx = np.arange(w.batch)
+        tab = w.block_table
+        used = np.unique(tab[tab >= 0])
+        remap = np.full(w.num_pages, -1, dtype=np.int64)
+        remap[used] = np.arange(used.size)
+        ctab = np.where(tab >= 0, remap[np.maximum(tab, 0)], -1).astype(np.int32)
+        ks = vs = None
+        if fp8_per_head:
+            ks = oracle.calibrate_per_head(w.k_rows)
+            vs = None if w.kv_shared else oracle.calibrate_per_head(w.v_rows)
+        c = oracle.Cache(used.size, w.page_size, w.kv_heads, w.head_dim, w.v_head_dim, w.kv_shared, oracle.DTYPE_FP8,
+                         w.scale_mode, w.page_tags[used], ks, vs)
+        c.append(w.k_rows, w.v_rows, w.row_pos, ctab, w.block_tags, row_req=w.row_req, batch=w.batch)
+        t0 = time.perf_counter()
+        c.decode(w.q, w.seq_lens, ctab, w.block_tags, w.softmax_scale, flags=0, threads=threads)
+        dt = time.perf_counter() - t0
+        if w.kv_shared:
+            tokens = int(w.seq_lens.astype(np.int64).sum())
+            pages = int(((w.seq_lens.astype(np.int64) + w.page_size - 1) // w.page_size).sum())
+            nbytes = tokens * (w.head_dim + 4) + pages * 8 + w.q.size * 2 + w.batch * w.q_heads * w.v_head_dim * 4
+        else:
+            nbytes = decode_alg_bytes(w.seq_lens, w.kv_heads, w.head_dim, w.page_size, w.q_heads, w.head_dim,
+                                      tag_check=False)
+        res[name] = {"seconds": dt, "value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads,
+                     "context_tokens": int(w.seq_lens.astype(np.int64).sum()), "tag_check": "off"}
+        del c
+
+    one("tiny", synth.tiny())
+    one("gqa", synth.gqa())
+    one("long", synth.long_ctx())
+    if latent_w is not None:
+        one("latent_one_call", latent_w, fp8_per_head=False)
+    return res
 
 
 def run_reference(args, w):
@@ -272,6 +342,9 @@ def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
     g = capture(call, n_calls)
     g.replay()
     ms = time_graph(g) / n_calls
+    g1 = capture(call, 1)
+    g1.replay()
+    each = time_graph.each(g1, 30)
     # tag check on / off, alternated (all tags valid)
     g_off = capture(lambda j: call(j, flags=0), n_calls)
     g_off.replay()
@@ -288,17 +361,21 @@ def bench_latent(abi, wl, dev, i32, bf16, capture, time_graph, peak, n_calls):
     # probability terms, 512 values x 64 heads).
     mma_flops = pages * S * (2 * 2 * wl.q_heads * wl.head_dim + 2 * 3 * wl.q_heads * wl.v_head_dim)
     tpeak, tpeak_kind = fp8_dense_peak_tflops()
-    tach = mma_flops / (ms * 1e-3) / 1e12
+    tach = flops / (ms * 1e-3) / 1e12
     return {"workload": "latent-shared stream: batch 64, lengths U[4096, 32768], 64 q heads over one 576-wide "
                         "FP8 stream (V = first 512), per-token scales, page 64, tag check on",
-            "us_per_call": ms * 1e3, "kv_gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak,
+            "us_per_call": ms * 1e3, "p50_us": statistics.median(each) * 1e3, "p95_us": percentile(each, 95) * 1e3,
+            "kv_gbs": nbytes / (ms * 1e-3) / 1e9, "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak,
             "tflops": flops / (ms * 1e-3) / 1e12, "context_tokens": tokens, "alg_bytes_per_call": nbytes,
             "decode_tokens_per_s": B / (ms * 1e-3), "aborted_requests": int((st.cpu().numpy() != 0).sum()),
             "tag_check_ratio_on_over_off": statistics.median(ratios),
-            "roofline": {"bound": "tensor", "kernel": "latent_tc_kernel (plan + kernel + merge)", "achieved": tach,
+            "roofline": {"bound": "tensor", "kernel": "latent_tc_kernel + merge_kernel", "achieved": tach,
                          "peak": tpeak, "peak_kind": tpeak_kind, "unit": "TFLOP/s", "frac": tach / tpeak,
-                         "mma_flops_per_call": mma_flops,
-                         "what": "executed e4m3 MMA work (query terms x2, probability terms x3, whole pages)"}}
+                         "flops_per_call": flops, "what": "algorithmic flops: 2 x 64 heads x (576 + 512) per token",
+                         "executed_mma_flops_per_call": mma_flops,
+                         "executed_frac": mma_flops / (ms * 1e-3) / 1e12 / tpeak,
+                         "executed_what": "e4m3 MMA work as issued: query terms x2, probability terms x3 (x4 on pages "
+                                          "with values above 8), whole pages"}}
 
 
 
@@ -332,8 +409,12 @@ def bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_cal
     g = capture(call, n_calls)
     g.replay()
     ms = time_graph(g) / n_calls
+    g1 = capture(call, 1)
+    g1.replay()
+    each = time_graph.each(g1, 30)
     nbytes = decode_alg_bytes(w.seq_lens, w.kv_heads, w.head_dim, w.page_size, w.q_heads, w.head_dim, fp8=fp8)
-    res = {"us_per_call": ms * 1e3, "kv_gbs": nbytes / (ms * 1e-3) / 1e9,
+    res = {"us_per_call": ms * 1e3, "p50_us": statistics.median(each) * 1e3, "p95_us": percentile(each, 95) * 1e3,
+           "kv_gbs": nbytes / (ms * 1e-3) / 1e9,
            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / peak, "alg_bytes_per_call": nbytes,
            "aborted_requests": int((st.cpu().numpy() != 0).sum()), "pool_pages": P}
     del cache, ws
@@ -359,19 +440,24 @@ def bench_configs(abi, dev, i32, bf16, capture, time_graph, peak, n_calls):
                   "bf16": bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
                                               abi.DTYPE_BF16)}
     del w
-    # long contexts, pages scattered over a pool of half the free device memory (FP8 K + V)
-    free, _ = torch.cuda.mem_get_info(dev)
-    big = int(0.5 * free) // (2 * 64 * 128)
-    w = synth.long_ctx(num_pages=big)
-    res["long"] = {"workload": f"batch 8 x 131072 tokens, 8 q / 1 KV head, head_dim 128, page 64, pages scattered "
-                               f"over a pool of {big} pages (half the free device memory), tag check on",
-                   "fp8": bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
-                                              abi.DTYPE_FP8_E4M3, num_pages=big)}
-    del w
-    w = synth.long_ctx()
-    res["long"]["bf16"] = bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls,
-                                              abi.DTYPE_BF16)
-    res["long"]["bf16"]["pool"] = "1.25x the pages needed"
+    # long contexts: pages scattered over a pool that fills ~80% of the free
+    # device memory (each cache type in turn, the same byte budget), and the
+    # same batch over a dense pool (1.25x the pages needed, permuted), which
+    # separates the cost of scattering the pages over the whole device
+    res["long"] = {"workload": "batch 8 x 131072 tokens, 8 q / 1 KV head, head_dim 128, page 64, tag check on"}
+    for name, dtype, esz in (("fp8", abi.DTYPE_FP8_E4M3, 1), ("bf16", abi.DTYPE_BF16, 2)):
+        free, _ = torch.cuda.mem_get_info(dev)
+        big = int(0.8 * free) // (2 * 64 * 128 * esz)
+        w = synth.long_ctx(num_pages=big)
+        r = bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls, dtype, num_pages=big)
+        r["pool"] = f"{big} pages scattered over {big * 2 * 64 * 128 * esz / 2**30:.1f} GiB (80% of the free memory)"
+        res["long"][name] = r
+        del w
+        w = synth.long_ctx()
+        r = bench_decode_config(abi, w, dev, i32, bf16, capture, time_graph, peak, n_calls, dtype)
+        r["pool"] = "1.25x the pages needed, permuted (dense)"
+        res["long"][name + "_dense_pool"] = r
+        del w
     return res
 
 
@@ -489,6 +575,19 @@ def main():
         torch.cuda.synchronize()
         return global_max(e0.elapsed_time(e1), dist, dev)
 
+    def time_each(g, n):
+        """Per-replay times (ms) of n back-to-back replays (events between them)."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(n):
+            g.replay()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+    time_graph.each = time_each
+
     K = args.steps
     fp8 = caches["fp8"]
     # warm-up: W untimed steps
@@ -512,6 +611,18 @@ def main():
     ms_dec = time_graph(g_dec) / K
     dec_gbs = statistics.mean(dec_bytes) / (ms_dec * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
+    # per-call distribution: one call per graph, 60 back-to-back replays with
+    # an event between replays (inputs larger than L2, so no flush)
+    g1_step = capture(lambda j: step(fp8, j), 1)
+    g1_dec = capture(lambda j: step(fp8, j, do_append=False), 1)
+    g1_step.replay()
+    g1_dec.replay()
+    each_step, each_dec = time_each(g1_step, 60), time_each(g1_dec, 60)
+    per_call = {"step": {"p50_us": statistics.median(each_step) * 1e3, "p95_us": percentile(each_step, 95) * 1e3,
+                         "replays": 60},
+                "decode": {"p50_us": statistics.median(each_dec) * 1e3, "p95_us": percentile(each_dec, 95) * 1e3,
+                           "replays": 60},
+                "what": "one call per CUDA graph, replayed back to back, CUDA events between replays"}
 
     extra = {}
     if not args.no_variants:
@@ -522,23 +633,38 @@ def main():
         used = w.block_table >= 0
         valid_np[w.block_table[used]] = w.block_tags[used]
         stale_tags = fp8.page_tags
-        fp8.page_tags = i32(valid_np)
+        valid_tags = i32(valid_np)  # kept alive while the graphs below use it
+        fp8.page_tags = valid_tags
         g_on = capture(lambda j: step(fp8, j, do_append=False), K)
         g_off = capture(lambda j: step(fp8, j, flags=0, do_append=False), K)
+        g1_on = capture(lambda j: step(fp8, j, do_append=False), 1)
+        g1_off = capture(lambda j: step(fp8, j, flags=0, do_append=False), 1)
         fp8.page_tags = stale_tags
-        g_on.replay()
-        g_off.replay()
+        for gg in (g_on, g_off, g1_on, g1_off):
+            gg.replay()
         ratios, on_ms, off_ms = [], [], []
-        for _ in range(11):
+        n_alt = 21
+        for _ in range(n_alt):
             a = time_graph(g_on)
             b = time_graph(g_off)
             on_ms.append(a)
             off_ms.append(b)
             ratios.append(a / b)
-        extra["tag_check_overhead"] = {"median_ratio_on_over_off": statistics.median(ratios),
-                                       "on_us_per_call": statistics.median(on_ms) / K * 1e3,
-                                       "off_us_per_call": statistics.median(off_ms) / K * 1e3, "alternations": 11,
-                                       "tags": "all valid in both arms"}
+        each_on, each_off = [], []
+        for _ in range(3):  # per-call distributions, interleaved in blocks of 20 replays
+            each_on += time_each(g1_on, 20)
+            each_off += time_each(g1_off, 20)
+        extra["tag_check_overhead"] = {
+            "median_ratio_on_over_off": statistics.median(ratios), "ratio_ci95": bootstrap_ci(ratios),
+            "on_us_per_call": statistics.median(on_ms) / K * 1e3, "off_us_per_call": statistics.median(off_ms) / K * 1e3,
+            "alternations": n_alt,
+            "p95_ratio_on_over_off": percentile(each_on, 95) / percentile(each_off, 95),
+            "on_p50_us": statistics.median(each_on) * 1e3, "on_p95_us": percentile(each_on, 95) * 1e3,
+            "off_p50_us": statistics.median(each_off) * 1e3, "off_p95_us": percentile(each_off, 95) * 1e3,
+            "tags": "all valid in both arms",
+            "what": "ratio: median over alternated K-call graph replays, 95% bootstrap interval of the median; "
+                    "p50/p95: one-call graphs, 60 replays each arm"}
+        del g_on, g_off, g1_on, g1_off
         g_unf = capture(lambda j: step_unfused(fp8, j), K)
         g_unf.replay()
         ms_unf = time_graph(g_unf) / K
@@ -558,15 +684,20 @@ def main():
         extra["configs"] = bench_configs(abi, dev, i32, bf16, capture, time_graph, peak, max(3, K // 5))
 
     # ---- latent-shared stream (64 heads over one 576-wide FP8 stream, batch 64)
+    latent_w = None
     if not args.no_latent:
         del caches
         torch.cuda.empty_cache()
-        extra["latent"] = bench_latent(abi, synth.latent(), dev, i32, bf16, capture, time_graph, peak,
-                                       max(3, K // 5))
+        latent_w = synth.latent()
+        extra["latent"] = bench_latent(abi, latent_w, dev, i32, bf16, capture, time_graph, peak, max(3, K // 5))
 
     # ---- end to end: per-step inputs from pinned host memory, results back to host.
     # A step's inputs sit in one pinned row (q | k | v | lengths) and go over in
-    # one copy; its results (out | status) come back in one copy.
+    # one copy; its results (out | status) come back in one copy.  The copies
+    # run on a second stream, double-buffered, so that step j + 1's inputs go
+    # over while step j runs and step j's results come back while step j + 1
+    # runs (a serving loop's pipeline); every step's copies stay inside the
+    # timed graph.
     def as_bytes(a):
         return np.ascontiguousarray(a).reshape(T, -1).view(np.uint8)
 
@@ -574,33 +705,65 @@ def main():
              as_bytes(np.stack([lens0 + j + 1 for j in range(T)]).astype(np.int32))]
     offs = np.cumsum([0] + [p.shape[1] for p in parts])
     h_in = torch.from_numpy(np.concatenate(parts, axis=1)).pin_memory()
-    d_in = torch.empty(int(offs[-1]), dtype=torch.uint8, device=dev)
-    d_q = d_in[offs[0]:offs[1]].view(torch.bfloat16).view(B, Hq, D)
-    d_k = d_in[offs[1]:offs[2]].view(torch.bfloat16).view(B, Hkv, D)
-    d_v = d_in[offs[2]:offs[3]].view(torch.bfloat16).view(B, Hkv, D)
-    d_len = d_in[offs[3]:offs[4]].view(torch.int32)
     n_out = B * Hq * D * 4
-    d_res = torch.empty(n_out + B * 4, dtype=torch.uint8, device=dev)
-    out_e, st_e = d_res[:n_out].view(torch.float32).view(B, Hq, D), d_res[n_out:].view(torch.int32)
-    h_res = torch.empty(n_out + B * 4, dtype=torch.uint8).pin_memory()
+    d_in = [torch.empty(int(offs[-1]), dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_res = [torch.empty(n_out + B * 4, dtype=torch.uint8, device=dev) for _ in range(2)]
+    h_res = [torch.empty(n_out + B * 4, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)
 
-    def e2e_step(j):
-        d_in.copy_(h_in[j % T], non_blocking=True)
+    def e2e_call(j):
+        di, dr = d_in[j % 2], d_res[j % 2]
+        d_q = di[offs[0]:offs[1]].view(torch.bfloat16).view(B, Hq, D)
+        d_k = di[offs[1]:offs[2]].view(torch.bfloat16).view(B, Hkv, D)
+        d_v = di[offs[2]:offs[3]].view(torch.bfloat16).view(B, Hkv, D)
+        d_len = di[offs[3]:offs[4]].view(torch.int32)
+        out_e, st_e = dr[:n_out].view(torch.float32).view(B, Hq, D), dr[n_out:].view(torch.int32)
         abi.paged_decode_step(fp8, d_k, d_v, d_q, d_len, table, tags, w.softmax_scale, flags=FLAGS,
                               max_splits=max_splits, workspace=ws, out=out_e, status=st_e)
-        h_res.copy_(d_res, non_blocking=True)
 
-    g_e2e = capture(e2e_step, K)
-    # the replayed graph must move the bytes: poison the device input and the
-    # host result, replay, and check both copies happened
-    d_in.fill_(0xFF)
-    h_res.zero_()
+    def capture_e2e(n):
+        g = torch.cuda.CUDAGraph()
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_cmp = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            cap = torch.cuda.current_stream()
+            copy_stream.wait_stream(cap)
+            with torch.cuda.stream(copy_stream):
+                d_in[0].copy_(h_in[0], non_blocking=True)
+                ev_in[0].record(copy_stream)
+            for j in range(n):
+                cap.wait_event(ev_in[j])
+                if j >= 2:
+                    cap.wait_event(ev_out[j - 2])  # d_res[j % 2] has been read back
+                e2e_call(j)
+                ev_cmp[j].record(cap)
+                with torch.cuda.stream(copy_stream):
+                    if j + 1 < n:
+                        if j >= 1:
+                            copy_stream.wait_event(ev_cmp[j - 1])  # d_in[(j + 1) % 2] is free
+                        d_in[(j + 1) % 2].copy_(h_in[(j + 1) % T], non_blocking=True)
+                        ev_in[j + 1].record(copy_stream)
+                    copy_stream.wait_event(ev_cmp[j])
+                    h_res[j % 2].copy_(d_res[j % 2], non_blocking=True)
+                    ev_out[j].record(copy_stream)
+            cap.wait_stream(copy_stream)
+        return g
+
+    g_e2e = capture_e2e(K)
+    # the replayed graph must move the bytes: poison the device inputs and the
+    # host results, replay, and check that the last step's copies happened
+    for t_ in d_in:
+        t_.fill_(0xFF)
+    for t_ in h_res:
+        t_.zero_()
     torch.cuda.synchronize()
     g_e2e.replay()
     torch.cuda.synchronize()
-    assert torch.equal(d_in.cpu(), h_in[(K - 1) % T]), "end-to-end graph did not copy the step inputs"
-    assert torch.equal(h_res, d_res.cpu()), "end-to-end graph did not copy the step results back"
-    assert h_res.any(), "end-to-end graph left the host result empty"
+    last = (K - 1) % 2
+    assert torch.equal(d_in[last].cpu(), h_in[(K - 1) % T]), "end-to-end graph did not copy the step inputs"
+    assert torch.equal(h_res[last], d_res[last].cpu()), "end-to-end graph did not copy the step results back"
+    assert h_res[last].any(), "end-to-end graph left the host result empty"
     ms_e2e = time_graph(g_e2e)
     e2e_val = job_throughput(sum(step_bytes), world, ms_e2e) / 1e9
     h2d = int(offs[-1])
@@ -618,6 +781,17 @@ def main():
         dt = time.perf_counter() - t0
         cpu = {"value": tot / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{n_cpu} consecutive steps over {desc}", "seconds": dt}
+        # the same sample on one thread (at least a few seconds, whole steps)
+        stepc1, _, _, _ = oracle_step_sample(w, args.cpu_frac, threads=1)
+        t0 = time.perf_counter()
+        tot1, n1 = 0, 0
+        while n1 == 0 or time.perf_counter() - t0 < args.cpu_seconds / 2:
+            tot1 += stepc1()
+            n1 += 1
+        dt1 = time.perf_counter() - t0
+        cpu["single_thread"] = {"value": tot1 / dt1 / 1e9, "unit": "GB/s", "cores": 1, "steps": n1, "seconds": dt1}
+        if not args.no_variants:
+            cpu["configs"] = oracle_config_timings(latent_w)
 
     st_final = st_dec.cpu().numpy()
     launches_per_step = 2  # split (page loader also appends the new tokens), merge kernels
@@ -638,6 +812,7 @@ def main():
                      "frac": dec_gbs / peak, "us_per_launch": ms_dec * 1e3,
                      "alg_bytes_per_launch": statistics.mean(dec_bytes), "traffic": recorded_traffic(),
                      "traffic_kernel": "gqa_split_kernel alone (ncu dram read + write per launch)"},
+        "per_call": per_call,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e / K},
         "gpu_launches": K * launches_per_step,

@@ -70,6 +70,22 @@ struct WorkSplit {
   long long off, first, c;
 };
 
+// The fields of DecodeArgs the work split reads, passed on their own so that
+// the split's functions (compiled once, not inlined) never take the kernel
+// parameter's address, which would move all of it to local memory.
+struct WsArgs {
+  const int *seq_lens;
+  int B, S, MP, max_splits, ranges, piece_cost, target_items, min_chunk_pages, Hkv;
+};
+
+__device__ __forceinline__ WsArgs ws_args(const DecodeArgs &a) {
+  WsArgs w;
+  w.seq_lens = a.seq_lens;
+  w.B = a.B; w.S = a.S; w.MP = a.MP; w.max_splits = a.max_splits; w.ranges = a.ranges; w.piece_cost = a.piece_cost;
+  w.target_items = a.target_items; w.min_chunk_pages = a.min_chunk_pages; w.Hkv = a.Hkv;
+  return w;
+}
+
 struct Piece {
   int b, cg, p0, p1, L, nb;
   bool lead;  // the request's first piece: its CTA of head 0 records the numbering
@@ -126,7 +142,7 @@ __device__ __noinline__ int ws_count(const WorkSplit &w, long long off, int p, i
 
 // Warp-wide (all 32 lanes, same result in each): the rule, R and this CTA's
 // range, then the first request with a piece in it.
-__device__ __noinline__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane) {
+__device__ __noinline__ void ws_init(WorkSplit &w, const WsArgs &a, int lane) {
   const int S = a.S;
   w.max_len = (long long)a.MP * S;
   long long tot = 0;
@@ -220,7 +236,7 @@ __device__ __noinline__ void ws_init(WorkSplit &w, const DecodeArgs &a, int lane
 // when the range has none left.  A piece that would break the workspace
 // bounds ends the walk instead of being used (it cannot occur when the
 // rules above hold).
-__device__ __noinline__ bool ws_next(WorkSplit &w, const DecodeArgs &a, Piece &pc) {
+__device__ __noinline__ bool ws_next(WorkSplit &w, const WsArgs &a, Piece &pc) {
   while (w.b < a.B) {
     const int L = __ldg(&a.seq_lens[w.b]);
     const int p = ws_pages(w, L, a.S);
@@ -272,7 +288,7 @@ __device__ __noinline__ bool ws_next(WorkSplit &w, const DecodeArgs &a, Piece &p
 
 // ws_next on a state kept in shared memory (one copy per warp), so that it
 // holds no registers while the pages go out.
-__device__ __forceinline__ bool ws_next_shared(WorkSplit &s, const DecodeArgs &a, Piece &pc, int lane) {
+__device__ __forceinline__ bool ws_next_shared(WorkSplit &s, const WsArgs &a, Piece &pc, int lane) {
   WorkSplit w = s;
   __syncwarp();
   const bool r = ws_next(w, a, pc);
@@ -361,11 +377,16 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
 #pragma unroll
   for (int w = 0; w < 8; ++w) st |= s_or[w];
   if (lead && t == 0) a.status[b] = st | (gave_up || !sane ? (uint32_t)PFKV_ST_TIMEOUT : 0u);
-  if (!sane || nb == 1) return;  // a one-piece request's rows come from the split kernel
+  if (!sane) return;
+  // A faulted request's rows are zeroed here, one-piece requests included:
+  // the split kernel writes a one-piece request's rows itself, but only head
+  // group 0's walk checks tags, so the other groups' CTAs do not know of a
+  // stale page.
   if (st) {
     for (int i = 4 * col_lo + t; i < 4 * col_hi; i += 256) out_bg[i] = 0.f;
     return;
   }
+  if (nb == 1) return;  // a one-piece request's rows come from the split kernel
   if (col_hi <= col_lo) return;  // only padding slots in this block
   __syncthreads();
   const int warp = t >> 5, lane = t & 31;

@@ -202,14 +202,15 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
     const int vg = (int)blockIdx.x % a.Hkv;
     const int g = vg / a.kv_sub;
     __shared__ WorkSplit s_ws;
+    const WsArgs wa = ws_args(a);
     {
       WorkSplit w;
-      ws_init(w, a, lane);
+      ws_init(w, wa, lane);
       if (lane == 0) s_ws = w;
       __syncwarp();
     }
     Piece cur;
-    bool have = ws_next_shared(s_ws, a, cur, lane);
+    bool have = ws_next_shared(s_ws, wa, cur, lane);
     // the last batch's first ring position, and whether this lane's page of
     // it was issued (every page of earlier batches was)
     uint32_t last_first = 0;
@@ -267,11 +268,16 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         const int pid = valid ? __ldg(&trow[i]) : 0;
         const bool oob = valid && (pid < 0 || pid >= a.P);
         uint32_t page_tag = 0, want_tag = 0;
-        if (tag_check && valid && !oob) {  // loads issued now, compared after the copies
+        // Tags: the walk's bits are reported by head group 0 only (the pages
+        // and tags are the same for every head group of the request), so the
+        // other groups load tags only for the page a decode step writes into
+        // (whose refusal each group decides for its own rows).
+        const bool dest_batch = has_new && i0 <= i_new && i_new < i0 + batch_pages;
+        if (tag_check && (vg == 0 || dest_batch) && valid && !oob) {  // issued now, compared after the copies
           page_tag = __ldg(&a.page_tags[pid]);
           want_tag = __ldg(&tagrow[i]);
         }
-        if (has_new && i0 <= i_new && i_new < i0 + batch_pages)
+        if (dest_batch)
           write_new_row<kFp8, kD>(a, nv, nv_scale, nv_lane, nv_part, nv_k, i_new - i0, pid, oob,
                                   page_tag != want_tag, g, (L - 1) % S, per_token);
         bool lane_ok = true;
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         mbar_arrive(&item_done[slot]);
       }
       if (!ok) break;
-      have = ws_next_shared(s_ws, a, cur, lane);
+      have = ws_next_shared(s_ws, wa, cur, lane);
     }
     // Copies still in flight land before the block may exit (the consumers
     // wait for every page they use, but on the abort path they leave early):

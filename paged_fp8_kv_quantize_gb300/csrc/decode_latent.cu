@@ -178,14 +178,15 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
   // This CTA's pieces, worked out from the lengths; the next one is found
   // once the current one's pages have gone out.
   WorkSplit &s_ws = *reinterpret_cast<WorkSplit *>(smem + sp.ws);
+  const WsArgs wa = ws_args(a);
   {
     WorkSplit w;
-    ws_init(w, a, lane);
+    ws_init(w, wa, lane);
     if (lane == 0) s_ws = w;
     __syncwarp();
   }
   Piece cur;
-  bool have = ws_next_shared(s_ws, a, cur, lane);
+  bool have = ws_next_shared(s_ws, wa, cur, lane);
   for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
     bool w = true;
@@ -294,7 +295,7 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
       mbar_arrive(&B.item_done[slot]);
     }
     if (!ok) break;
-    have = ws_next_shared(s_ws, a, cur, lane);
+    have = ws_next_shared(s_ws, wa, cur, lane);
   }
   // Copies still in flight land before the block may exit.
   if (lane == 0)
@@ -520,10 +521,10 @@ __device__ __forceinline__ uint2 q_term8(uint4 v, float inv, int t) {
 // softmax scale * log2(e) * 2^e_h.  Whole warp; arrives on q_ready.  One
 // compiled copy for both call sites (first item, next item), so that its
 // code is fetched from memory once per call.
-__device__ __noinline__ float q_prep(const DecodeArgs &a, int b, uint32_t tq, uint8_t *qtail, float *s_qm,
-                                        uint64_t *q_ready, int q, int x, int lane, bool &fail) {
+__device__ __noinline__ float q_prep(const uint16_t *qbase, float sm_scale_log2, int b, uint32_t tq, uint8_t *qtail,
+                                     float *s_qm, uint64_t *q_ready, int q, int x, int lane, bool &fail) {
   const int h = 16 * q + (lane & 15), t = lane >> 4, R = 32 * q + lane;
-  const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) + ((size_t)b * kTH + h) * kTD);
+  const uint4 *src = reinterpret_cast<const uint4 *>(qbase + ((size_t)b * kTH + h) * kTD);
   float m = 0.f;
   if (!fail) {
     // this lane's half of the head's values in this warp's columns (and of the tail)
@@ -564,7 +565,7 @@ __device__ __noinline__ float q_prep(const DecodeArgs &a, int b, uint32_t tq, ui
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(q_ready);
-  return a.sm_scale_log2 * ldexpf(1.f, e - 8);
+  return sm_scale_log2 * ldexpf(1.f, e - 8);
 }
 
 // Softmax warp w (2-5 and 8-11) reads tensor-memory quarter q = w % 4, i.e.
@@ -605,7 +606,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     fail = wg_bar_or(fail);
     const int b0 = fail ? -1 : items[0].b;
     if (b0 >= 0) {
-      cq = q_prep(a, b0, tq, qtail, s_qm, B.q_ready, q, x, lane, fail);
+      cq = q_prep(static_cast<const uint16_t *>(a.q), a.sm_scale_log2, b0, tq, qtail, s_qm, B.q_ready, q, x, lane, fail);
       fail = wg_bar_or(fail);
     }
     if (fail) return;
@@ -761,7 +762,8 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       const int b_next = items[nslot].b;
       if (b_next >= 0) {
         fail = __any_sync(0xffffffffu, !mbar_wait(B.q_empty, it & 1u, abort_flag));  // warp-uniform
-        cq_next = q_prep(a, b_next, tq, qtail, s_qm, B.q_ready, q, x, lane, fail);
+        cq_next = q_prep(static_cast<const uint16_t *>(a.q), a.sm_scale_log2, b_next, tq, qtail, s_qm, B.q_ready, q, x,
+                         lane, fail);
         if (wg_bar_or(fail)) break;
       }
     }
