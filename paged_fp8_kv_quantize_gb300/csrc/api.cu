@@ -49,7 +49,8 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
   w.part_ml = w.split_count + up256(sizeof(int) * (size_t)batch);
   w.part_o = w.part_ml + up256(sizeof(float2) * slots);
   w.part_st = w.part_o + up256(sizeof(float) * slots * v_dim);
-  w.cta_abort = w.part_st + up256(sizeof(uint32_t) * (size_t)batch * max_splits);
+  // a status word per piece and head group (at most q_heads head groups)
+  w.cta_abort = w.part_st + up256(sizeof(uint32_t) * (size_t)batch * max_splits * q_heads);
   w.total = w.cta_abort + up256(sizeof(int) * (size_t)kMaxCtas);
   return w;
 }
@@ -147,6 +148,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.target_items = 0;
   a.min_chunk_pages = 1;
   a.n_ctas = 0;
+  a.st_groups = 1;
   a.piece_cost = 0;
   a.part_st = reinterpret_cast<uint32_t *>(w + L.part_st);
   a.cta_abort = reinterpret_cast<int *>(w + L.cta_abort);

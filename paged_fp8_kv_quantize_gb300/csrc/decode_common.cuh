@@ -43,10 +43,11 @@ struct ItemDesc {
 // lengths, and all CTAs reach the same answer.  The requests, in
 // request order (a request with a bad length counting nothing), lie on a
 // line of T units that is cut into R ranges [floor(kT/R), floor((k+1)T/R));
-// CTA k * Hkv + h takes range k for KV head h (the latent stream: Hkv = 1).  Pieces of a request are
-// numbered consecutively in request order over the whole call (the merge
-// finds a request's pieces at split_first[b] .. + split_count[b]).  Two
-// rules:
+// CTA k * Hkv + h takes range k for KV head h (the latent stream: Hkv = 1).  Piece j of request b
+// is numbered b * max_splits + j (j < max_splits under both rules), so that
+// no CTA needs the piece counts of the requests before its own; the merge
+// finds a request's pieces at split_first[b] = b * max_splits ..
+// + split_count[b].  Two rules:
 //  - cut: a request's segment of the line is c0 units of overhead followed
 //    by its pages (c0 = piece_cost: a piece's set-up and finish, and the
 //    consumer warps a short piece leaves idle, cost about that many pages'
@@ -64,10 +65,10 @@ struct WorkSplit {
   long long T, R, r0, r1, cp, max_len;
   int k, chunks;
   int c0;  // cut rule: overhead length placed before each request's pages on the cut line
-  // walk: next request to look at, its first page in the concatenation, the
-  // number of its first piece, and (chunk rule) its next chunk
+  // walk: next request to look at, its first unit on the line, and (chunk
+  // rule) its next chunk
   int b;
-  long long off, first, c;
+  long long off, c;
 };
 
 // The fields of DecodeArgs the work split reads, passed on their own so that
@@ -182,15 +183,15 @@ __device__ __noinline__ void ws_init(WorkSplit &w, const WsArgs &a, int lane) {
   w.R = R < 1 ? 1 : R;
   w.k = (int)blockIdx.x / a.Hkv;
   w.b = a.B;  // no pieces unless found below
-  w.off = w.first = w.c = 0;
+  w.off = w.c = 0;
   if (T == 0 || w.k >= w.R) return;
   w.r0 = div_floor((long long)w.k * T, w.R);
   w.r1 = div_floor((long long)(w.k + 1) * T, w.R);
-  long long off_c = 0, first_c = 0;  // totals of earlier passes
+  long long off_c = 0;  // line units of earlier passes
   for (int base = 0; base < a.B; base += 32) {
     const int b = base + lane;
     const int p = b < a.B ? ws_pages(w, __ldg(&a.seq_lens[b]), S) : 0;
-    const long long seg = p > 0 ? p + w.c0 : 0;  // the request's segment of the cut line
+    const long long seg = p > 0 ? p + w.c0 : 0;  // the request's segment of the line
     long long xp = seg;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -198,21 +199,14 @@ __device__ __noinline__ void ws_init(WorkSplit &w, const WsArgs &a, int lane) {
       if (lane >= o) xp += y;
     }
     const long long off = off_c + xp - seg;
-    int ppc = 1, n = 0;
-    if (p > 0) n = ws_count(w, off, p, a.max_splits, &ppc);
-    long long xn = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, xn, o);
-      if (lane >= o) xn += y;
-    }
-    const long long first = first_c + xn - n;
     bool has = false;
     int c_lo = 0;
     if (p > 0 && off + w.c0 < w.r1 && off + w.c0 + p > w.r0) {
       if (!w.chunks) {
         has = true;
       } else {
+        int ppc = 1;
+        const int n = ws_count(w, off, p, a.max_splits, &ppc);
         // r0 - off < p here, so the chunk index fits an int
         c_lo = off >= w.r0 ? 0 : (int)((unsigned)(w.r0 - off + ppc - 1) / (unsigned)ppc);
         has = c_lo < n && off + (long long)c_lo * ppc < w.r1;
@@ -223,12 +217,10 @@ __device__ __noinline__ void ws_init(WorkSplit &w, const WsArgs &a, int lane) {
       const int src = __ffs(m) - 1;
       w.b = base + src;
       w.off = __shfl_sync(0xffffffffu, off, src);
-      w.first = __shfl_sync(0xffffffffu, first, src);
       w.c = __shfl_sync(0xffffffffu, c_lo, src);
       return;
     }
     off_c += __shfl_sync(0xffffffffu, xp, 31);
-    first_c += __shfl_sync(0xffffffffu, xn, 31);
   }
 }
 
@@ -255,7 +247,6 @@ __device__ __noinline__ bool ws_next(WorkSplit &w, const WsArgs &a, Piece &pc) {
       p1 = (w.r1 < s0 + p ? w.r1 : s0 + p) - s0;
     } else {
       if (w.c >= n) {
-        w.first += n;
         w.off += p;
         ++w.b;
         w.c = 0;
@@ -266,9 +257,8 @@ __device__ __noinline__ bool ws_next(WorkSplit &w, const WsArgs &a, Piece &pc) {
       p0 = j * ppc;
       p1 = p0 + ppc < p ? p0 + ppc : p;
     }
-    const long long cg = w.first + j;
-    if (j < 0 || j >= n || n > a.max_splits || p0 < 0 || p0 >= p1 || p1 > p || cg >= (long long)a.B * a.max_splits)
-      return false;
+    if (j < 0 || j >= n || n > a.max_splits || p0 < 0 || p0 >= p1 || p1 > p) return false;
+    const long long cg = (long long)w.b * a.max_splits + j;
     pc.b = w.b;
     pc.cg = (int)cg;
     pc.p0 = (int)p0;
@@ -277,7 +267,6 @@ __device__ __noinline__ bool ws_next(WorkSplit &w, const WsArgs &a, Piece &pc) {
     pc.nb = n;
     pc.lead = j == 0;
     if (!w.chunks) {
-      w.first += n;
       w.off += p + w.c0;
       ++w.b;
     }
@@ -357,8 +346,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   // first; checked so that no read leaves the workspace
   const bool sane = nb >= 1 && nb <= a.max_splits && c0 >= 0 && c0 <= a.B * a.max_splits - nb;
   uint32_t st = 0u;
-  if (sane) {
-    for (int i = t; i < nb; i += 256) st |= __ldcg(&a.part_st[c0 + i]);
+  if (sane) {  // every piece's status word, one per head group of the pieces' kernel
+    for (int i = t; i < nb * a.st_groups; i += 256) st |= __ldcg(&a.part_st[(size_t)c0 * a.st_groups + i]);
     if (nb > 1)  // each piece's (m, l) for the heads of this block's columns
       for (int i = t; i < nb * M::kNH; i += 256) {
         if (h_lo + i % M::kNH >= hg.count) continue;  // a padding slot of the group

@@ -261,19 +261,23 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
                                               ((size_t)b * a.cache.num_kv_heads + g) * kD + nv_k);
         if (kFp8 && !per_token) nv_scale = __ldg(&(nv_part ? a.v_scale : a.k_scale)[g]);
       }
-      for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages) {
+      int kb = 0;  // batch number within the piece
+      for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages, ++kb) {
         last_first = ring;
         const int i = i0 + lane;
         const bool valid = lane < batch_pages && i < p1;
         const int pid = valid ? __ldg(&trow[i]) : 0;
         const bool oob = valid && (pid < 0 || pid >= a.P);
         uint32_t page_tag = 0, want_tag = 0;
-        // Tags: the walk's bits are reported by head group 0 only (the pages
-        // and tags are the same for every head group of the request), so the
-        // other groups load tags only for the page a decode step writes into
-        // (whose refusal each group decides for its own rows).
+        // Tags: every head group of a page range walks the same pages, so each
+        // batch's tags are checked by one of them, in turn (batch kb of piece
+        // cg by head group (cg + kb) mod Hkv); each group reports what it
+        // found in its own status word of the piece, and the merge ORs them.
+        // A decode step's destination page is checked by every group (each
+        // decides the refusal of its own rows).
         const bool dest_batch = has_new && i0 <= i_new && i_new < i0 + batch_pages;
-        if (tag_check && (vg == 0 || dest_batch) && valid && !oob) {  // issued now, compared after the copies
+        const bool my_batch = (int)(((unsigned)cur.cg + (unsigned)kb) % (unsigned)a.Hkv) == vg;
+        if (tag_check && (my_batch || dest_batch) && valid && !oob) {  // issued now, compared after the copies
           page_tag = __ldg(&a.page_tags[pid]);
           want_tag = __ldg(&tagrow[i]);
         }
@@ -695,9 +699,8 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
         }
         if (t < hg.count) a.part_ml[(size_t)d.cg * a.Hq + hg.first + t] = make_float2(sm_fin[2 * t], sm_fin[2 * t + 1]);
       }
-      // the walk's bits are the same for every KV head (same pages and tags):
-      // head 0's item reports them for the piece
-      if (t == 0 && d.g == 0) a.part_st[d.cg] = item_st;
+      // this head group's share of the walk's bits (the merge ORs the groups')
+      if (t == 0) a.part_st[(size_t)d.cg * a.Hkv + d.g] = item_st;
       named_bar_sync(1, kCT);
       if (threadIdx.x == 0) mbar_arrive(&item_empty[slot]);
       if (!alive) break;
@@ -803,6 +806,7 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
   // group of Hkv CTAs per page range), and the merge kernel writes status.
   a.ranges = max(1, min(sh.grid, kMaxCtas) / a.Hkv);
   a.n_ctas = a.ranges * a.Hkv;
+  a.st_groups = a.Hkv;
   a.target_items = a.n_ctas * 8;
   a.min_chunk_pages = (1024 + a.S - 1) / a.S;
   a.piece_cost = kPieceCost;

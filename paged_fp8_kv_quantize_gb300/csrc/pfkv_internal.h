@@ -56,11 +56,13 @@ struct DecodeArgs {
   // rule of small or lopsided batches takes pieces of at least
   // min_chunk_pages pages, about target_items of them over all KV heads.
   // Written per call: split_first / split_count of every request with a
-  // valid length (by the head-0 CTA holding its first piece), part_st[piece]
-  // (status bits found by the head-0 item) and cta_abort[0 .. n_ctas) (1: a
+  // valid length (by the head-0 CTA holding its first piece),
+  // part_st[piece * st_groups + group] (status bits found by each head
+  // group's item of the piece) and cta_abort[0 .. n_ctas) (1: a
   // wait of that CTA gave up).  The merge turns them into status[] and zeroes
   // the rows of faulted requests.
   int ranges, target_items, min_chunk_pages, n_ctas;
+  int st_groups;  // status words per piece in part_st (grouped-query path: one per head group)
   int piece_cost;  // cut rule: pages' worth of time one piece costs beyond its pages
   uint32_t *part_st;
   int *cta_abort;

@@ -35,9 +35,9 @@ def test_host_only_entry_points():
     d = abi.CacheDesc(100, 16, 8, 128, 128, 0, abi.DTYPE_FP8_E4M3, 0, 16, 16, 16, 16, 16)
     n = abi.lib.pfkv_decode_workspace_bytes(ctypes.byref(d), 64, 32, 64)
     # per-request piece index and count, (m, l) and O partials for every
-    # (request, piece, head), a status word per piece and an abort word per
-    # split CTA
-    fixed = 64 * 64 * 32 * (8 + 4 * 128) + 64 * 64 * 4
+    # (request, piece, head), a status word per piece and head group (at most
+    # one group per query head) and an abort word per split CTA
+    fixed = 64 * 64 * 32 * (8 + 4 * 128 + 4)
     assert fixed <= n < fixed + 64 * 1024
 
 

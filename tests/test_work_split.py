@@ -12,8 +12,9 @@ and a range takes the chunks that start in it.  The restatement
 follows the kernel step by step (the first piece found by a 32-request pass,
 then a walk), so that its index arithmetic can be checked here on many
 batches: every valid request is tiled exactly once, in order, by pieces
-numbered first_b .. first_b + n_b - 1 with n_b <= max_splits; piece numbers
-are distinct and fit the workspace (batch * max_splits); each request has a
+numbered b * max_splits .. b * max_splits + n_b - 1 with n_b <= max_splits
+(so a CTA needs no piece counts of other requests); piece numbers are
+distinct and fit the workspace (batch * max_splits); each request has a
 first piece (whose CTA records the numbering); under the cut rule each
 range's pages plus the overhead units inside it fill the range exactly, and
 every busy range holds the same share to within one.  The kernel itself
@@ -58,33 +59,32 @@ def _init(lens, S, MP, Hkv, ms, ranges, target, min_chunk, blk, cost=0):
         w["cp"] = 0
         w["c0"] = cost
         T = Tc
-    w.update(T=T, R=max(R, 1), k=blk // Hkv, b=B, off=0, first=0, c=0)
+    w.update(T=T, R=max(R, 1), k=blk // Hkv, b=B, off=0, c=0)
     if T == 0 or w["k"] >= w["R"]:
         return w
     w["r0"] = w["k"] * T // w["R"]
     w["r1"] = (w["k"] + 1) * T // w["R"]
-    off_c = first_c = 0
+    off_c = 0
     c0 = w["c0"]
-    for base in range(0, B, 32):  # one warp pass: 32 requests, scans of cost and pieces
-        acc_p, acc_n = off_c, first_c
+    for base in range(0, B, 32):  # one warp pass: 32 requests, a scan of the line
+        acc_p = off_c
         for b in range(base, base + 32):
             p = P[b] if b < B else 0
-            off, first = acc_p, acc_n
+            off = acc_p
             acc_p += p + c0 if p else 0
-            n, ppc = _count(w, off, p, ms) if p > 0 else (0, 1)
-            acc_n += n
             has, c_lo = False, 0
             if p > 0 and off + c0 < w["r1"] and off + c0 + p > w["r0"]:
                 if not w["chunks"]:
                     has = True
                 else:
+                    n, ppc = _count(w, off, p, ms)
                     assert w["r0"] - off < p  # the kernel keeps this in 32 bits
                     c_lo = 0 if off >= w["r0"] else (w["r0"] - off + ppc - 1) // ppc
                     has = c_lo < n and off + c_lo * ppc < w["r1"]
             if has:  # the lowest lane with a piece in the range
-                w.update(b=b, off=off, first=first, c=c_lo)
+                w.update(b=b, off=off, c=c_lo)
                 return w
-        off_c, first_c = acc_p, acc_n
+        off_c = acc_p
     return w
 
 
@@ -106,7 +106,6 @@ def _next(w, lens, S, ms):
             p1 = min(w["r1"], s0 + p) - s0
         else:
             if w["c"] >= n:
-                w["first"] += n
                 w["off"] += p
                 w["b"] += 1
                 w["c"] = 0
@@ -117,12 +116,11 @@ def _next(w, lens, S, ms):
             w["c"] += 1
             p0 = j * ppc
             p1 = min(p0 + ppc, p)
-        cg = w["first"] + j
+        cg = w["b"] * ms + j
         # the kernel ends the walk here instead; it must never be needed
         assert 0 <= j < n <= ms and 0 <= p0 < p1 <= p and cg < B * ms, (j, n, p0, p1, p, cg)
         piece = dict(b=w["b"], cg=cg, p0=p0, p1=p1, nb=n, j=j)
         if not w["chunks"]:
-            w["first"] += n
             w["off"] += p + c0
             w["b"] += 1
         return piece
@@ -159,7 +157,6 @@ def _check(lens, S, MP, Hkv, ms, grid, cost=0):
     by_b = {}
     for pc in pieces:
         by_b.setdefault(pc["b"], []).append(pc)
-    first = 0
     for b in range(B):
         p = _pages(lens[b], S, MP * S)
         if p == 0:
@@ -169,11 +166,10 @@ def _check(lens, S, MP, Hkv, ms, grid, cost=0):
         n = ps[0]["nb"]
         assert len(ps) == n <= ms and all(x["nb"] == n for x in ps), (b, n, len(ps))
         assert [x["j"] for x in ps] == list(range(n))
-        assert [x["cg"] for x in ps] == list(range(first, first + n))
+        assert [x["cg"] for x in ps] == list(range(b * ms, b * ms + n))
         assert ps[0]["p0"] == 0 and ps[-1]["p1"] == p
         assert all(x["p1"] == y["p0"] for x, y in zip(ps, ps[1:]))
-        first += n
-    assert first <= B * ms
+    assert all(0 <= x < B * ms for x in cgs)
     if not chunks and sum(loads):
         busy = [x for x in loads if x]
         assert max(busy) - min(busy) <= 1, loads
