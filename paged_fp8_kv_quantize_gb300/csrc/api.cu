@@ -41,7 +41,7 @@ static size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 // Every size here is bounded by the callers (batch < 2^31, max_splits <= 256,
 // q_heads <= kMaxQHeads, v_dim <= kMaxHeadDim), so the products below stay
 // far inside size_t.
-WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool latent) {
   WsLayout w;
   const size_t slots = (size_t)batch * max_splits * q_heads;
   w.split_first = 0;
@@ -51,7 +51,9 @@ WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits) {
   w.part_st = w.part_o + up256(sizeof(float) * slots * v_dim);
   // a status word per piece and head group (at most q_heads head groups)
   w.cta_abort = w.part_st + up256(sizeof(uint32_t) * (size_t)batch * max_splits * q_heads);
-  w.total = w.cta_abort + up256(sizeof(int) * (size_t)kMaxCtas);
+  w.qterms = w.cta_abort + up256(sizeof(int) * (size_t)kMaxCtas);
+  w.qfac = w.qterms + (latent ? up256(kLatentQTermBytes * (size_t)batch) : 0);
+  w.total = w.qfac + (latent ? up256(sizeof(float) * (size_t)batch * q_heads) : 0);
   return w;
 }
 
@@ -119,7 +121,7 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   if (Hq % c->num_kv_heads) return PFKV_ERR_SHAPE;
   if (!aligned16(q) || !aligned16(out)) return PFKV_ERR_ALIGN;
   if (c->page_size % 16 || c->page_size > 256) return PFKV_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(batch, Hq, c->v_head_dim, max_splits);
+  const WsLayout L = ws_layout(batch, Hq, c->v_head_dim, max_splits, is_latent(c));
   if (ws_bytes < L.total) return PFKV_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return PFKV_ERR_ALIGN;
 
@@ -152,6 +154,8 @@ static int decode_common(int want_dtype, const pfkv_cache *c, const void *q, int
   a.piece_cost = 0;
   a.part_st = reinterpret_cast<uint32_t *>(w + L.part_st);
   a.cta_abort = reinterpret_cast<int *>(w + L.cta_abort);
+  a.qterms = w + L.qterms;
+  a.qfac = reinterpret_cast<float *>(w + L.qfac);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (c->kv_shared) {
     if (!is_latent(c) || Hq != 64 || c->dtype != PFKV_DTYPE_FP8_E4M3 || c->scale_mode != PFKV_SCALE_PER_TOKEN ||
@@ -213,7 +217,7 @@ size_t pfkv_decode_workspace_bytes(const pfkv_cache *cache, int32_t batch, int32
   // sizes a decode call would refuse: no workspace fits them
   if (num_q_heads > kMaxQHeads || max_splits > 256 || cache->v_head_dim < 1 || cache->v_head_dim > kMaxHeadDim)
     return SIZE_MAX;
-  return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits).total;
+  return ws_layout(batch, num_q_heads, cache->v_head_dim, max_splits, is_latent(cache)).total;
 }
 
 

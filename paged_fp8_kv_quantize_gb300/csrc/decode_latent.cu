@@ -21,9 +21,11 @@
 //        probabilities, with the token's scale folded in relative to a
 //        running reference scale, are written as P1 + P2 + P3 (three e4m3
 //        terms, about 12 significant bits) by the softmax warps.
-// The softmax normaliser l is summed from the fp32 probabilities.
+// The softmax normaliser l sums the weights as the terms carry them.
 //
-// One CTA per SM, persistent.  There is no plan kernel: every CTA works out
+// A small kernel first writes every request's query terms into the
+// workspace (one block per request and 16 heads).  The decode kernel: one
+// CTA per SM, persistent.  There is no plan kernel: every CTA works out
 // its pieces from the lengths (the shared work split: the requests' pages,
 // plus a small per-piece overhead, cut into one equal range per CTA); a
 // piece is a request's part of the range, all 64 heads.  Warp 0 loads pages
@@ -36,7 +38,7 @@
 // and one half of the page's tokens, each lane one head and 16 tokens; the
 // two warps of a quarter agree on each page's maximum through shared
 // memory, so the running maxima are identical in both and the sums are per
-// thread.  The softmax warps also write each piece's query terms (tensor
+// thread.  The softmax warps also load each piece's query terms (tensor
 // memory and the shared-memory tail), the next piece's as soon as the last
 // QK^T of the current one has read the operand, before the current piece's
 // result is read out, so that the next piece's QK^T overlaps that read-out.
@@ -91,10 +93,12 @@ constexpr uint32_t kIdPV5 = kIdPV | (1u << 10);  // B (the last probability term
 
 // Softmax-warp scratch, floats: beta[2][64] | l[2 halves][64] | m[64] | resc_tag[2] (uint32) |
 // four-term flag per P buffer [2] (uint32) | pad |
-// page maxima exchanged by the two warps of a lane quarter, float2 [2 pages][2 halves][64]
-// | query maxima exchanged by the two warps of a lane quarter [2 halves][64]
-constexpr int kWgBeta = 0, kWgL = 128, kWgM = 256, kWgTag = 320, kWgFour = 322, kWgX = 328, kWgQm = kWgX + 2 * 2 * 2 * 64,
-              kWgFloats = kWgQm + 2 * 64;
+// page maxima exchanged by the two warps of a lane quarter: scores [2 pages][2 halves][64] and
+// per-token scales [2 pages][2 halves][4 quarters] | per softmax warp, the reciprocal scales of
+// its 32 tokens of the current page [8][32]
+constexpr int kWgBeta = 0, kWgL = 128, kWgM = 256, kWgTag = 320, kWgFour = 322, kWgX = 328,
+              kWgSmx = kWgX + 2 * 2 * 64, kWgInv = kWgSmx + 2 * 2 * 4, kWgFloats = kWgInv + 8 * 32;
+static_assert(kWgInv % 4 == 0, "the reciprocal scales are read as float4");
 
 struct TcSmem {
   uint32_t ring, qtail, p, scales, wg, bars, items, ws, total;
@@ -445,18 +449,44 @@ __device__ __forceinline__ bool bar_or(int id, int nthreads, bool v) {
 // All softmax warps (barrier 1).
 __device__ __forceinline__ bool wg_bar_or(bool v) { return bar_or(1, kSmxThreads, v); }
 
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+__device__ __forceinline__ uint32_t f16x2_to_e5m2x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
+}
+
 // The 8-bit terms of a pair of non-negative floats (lo -> low byte), each
-// rounded to nearest even from fp32: t1 = e4m3(x), t2 = e4m3(x - t1), then
-// either t3 = e5m2(x - t1 - t2) (three terms, about 12 significant bits for
-// the large weights) or t3 = e4m3(x - t1 - t2), t4 = e5m2(x - t1 - t2 - t3)
-// (four terms, about 15 bits; t4 = 0 otherwise).  Every difference is exact
-// in fp32 (a term is within a factor two of what it rounds, or zero).  The
-// last term is e5m2 for its range (down to 2^-16, against 2^-9 for e4m3): it
-// keeps the share of the many small weights far below the running maximum,
-// which e4m3 alone would flush to zero.  Returns the pair the terms
-// represent, t1 + t2 + t3 + t4, exactly.
+// rounded to nearest even.  Three terms (pages of small values): x is
+// rounded to f16 and split as t1 = e4m3(x), t2 = e4m3(x - t1),
+// t3 = e5m2(x - t1 - t2), every difference exact in f16 (about 11
+// significant bits, packed f16 arithmetic).  Four terms (pages with large
+// values, whose output needs more): split from fp32 as t1 = e4m3(x),
+// t2 = e4m3(x - t1), t3 = e4m3(x - t1 - t2), t4 = e5m2(x - t1 - t2 - t3),
+// every difference exact in fp32 (about 15 bits).  The last term is e5m2 for
+// its range (down to 2^-16, against 2^-9 for e4m3): it keeps the share of
+// the many small weights far below the running maximum, which e4m3 alone
+// would flush to zero.  Returns the pair the terms represent, exactly.
 __device__ __forceinline__ float2 p_terms2(float lo, float hi, bool four, uint32_t &t1, uint32_t &t2, uint32_t &t3,
                                            uint32_t &t4) {
+  if (!four) {
+    const __half2 x = __floats2half2_rn(lo, hi);
+    t1 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&x));
+    const uint32_t b1 = e4m3x2_to_f16x2(t1);
+    const __half2 r1 = __hsub2(x, *reinterpret_cast<const __half2 *>(&b1));
+    t2 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&r1));
+    const uint32_t b2 = e4m3x2_to_f16x2(t2);
+    const __half2 r2 = __hsub2(r1, *reinterpret_cast<const __half2 *>(&b2));
+    t3 = f16x2_to_e5m2x2(*reinterpret_cast<const uint32_t *>(&r2));
+    const uint32_t b3 = e5m2x2_to_f16x2(t3);
+    const __half2 r3 = __hsub2(r2, *reinterpret_cast<const __half2 *>(&b3));
+    t4 = 0u;
+    return __half22float2(__hsub2(x, r3));
+  }
   t1 = f32x2_to_e4m3x2(lo, hi);
   const uint32_t b1 = e4m3x2_to_f16x2(t1);
   const float2 d1 = __half22float2(*reinterpret_cast<const __half2 *>(&b1));
@@ -465,107 +495,116 @@ __device__ __forceinline__ float2 p_terms2(float lo, float hi, bool four, uint32
   const uint32_t b2 = e4m3x2_to_f16x2(t2);
   const float2 d2 = __half22float2(*reinterpret_cast<const __half2 *>(&b2));
   const float r2x = r1x - d2.x, r2y = r1y - d2.y;
-  float2 rep = make_float2(d1.x + d2.x, d1.y + d2.y);
-  if (four) {
-    t3 = f32x2_to_e4m3x2(r2x, r2y);
-    const uint32_t b3 = e4m3x2_to_f16x2(t3);
-    const float2 d3 = __half22float2(*reinterpret_cast<const __half2 *>(&b3));
-    t4 = f32x2_to_e5m2x2(r2x - d3.x, r2y - d3.y);
-    const uint32_t b4 = e5m2x2_to_f16x2(t4);
-    const float2 d4 = __half22float2(*reinterpret_cast<const __half2 *>(&b4));
-    rep.x = (rep.x + d3.x) + d4.x;
-    rep.y = (rep.y + d3.y) + d4.y;
-  } else {
-    t3 = f32x2_to_e5m2x2(r2x, r2y);
-    const uint32_t b3 = e5m2x2_to_f16x2(t3);
-    const float2 d3 = __half22float2(*reinterpret_cast<const __half2 *>(&b3));
-    t4 = 0u;
-    rep.x += d3.x;
-    rep.y += d3.y;
-  }
-  return rep;
+  t3 = f32x2_to_e4m3x2(r2x, r2y);
+  const uint32_t b3 = e4m3x2_to_f16x2(t3);
+  const float2 d3 = __half22float2(*reinterpret_cast<const __half2 *>(&b3));
+  t4 = f32x2_to_e5m2x2(r2x - d3.x, r2y - d3.y);
+  const uint32_t b4 = e5m2x2_to_f16x2(t4);
+  const float2 d4 = __half22float2(*reinterpret_cast<const __half2 *>(&b4));
+  return make_float2(((d1.x + d2.x) + d3.x) + d4.x, ((d1.y + d2.y) + d3.y) + d4.y);
 }
 
-// Eight codes of term t of the query values v (eight bf16) scaled by inv, a
-// power of two: T1 = e4m3(x), T2 = e4m3(x - T1) (the difference is exact in
-// fp32); both rounded to nearest even.
-__device__ __forceinline__ uint2 q_term8(uint4 v, float inv, int t) {
-  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[2];
-#pragma unroll
-  for (int i = 0; i < 4; i += 2) {
-    const float x0 = __uint_as_float(wv[i] << 16) * inv, x1 = __uint_as_float(wv[i] & 0xffff0000u) * inv;
-    const float x2 = __uint_as_float(wv[i + 1] << 16) * inv, x3 = __uint_as_float(wv[i + 1] & 0xffff0000u) * inv;
-    const uint32_t a01 = f32x2_to_e4m3x2(x0, x1), a23 = f32x2_to_e4m3x2(x2, x3);
-    const uint32_t h01 = e4m3x2_to_f16x2(a01), h23 = e4m3x2_to_f16x2(a23);
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
-    const uint32_t t2 = f32x2_to_e4m3x2(x0 - f01.x, x1 - f01.y) | (f32x2_to_e4m3x2(x2 - f23.x, x3 - f23.y) << 16);
-    o[i / 2] = t ? t2 : (a01 | (a23 << 16));
+// Query terms of the latent stream, one block per (request, 16 heads),
+// before the decode kernel.  Head h's bf16 row (576 values) is scaled by
+// 2^-e_h, e_h the exponent that puts max|q| in [128, 256), and written as
+// T1 = e4m3(q 2^-e_h) and T2 = e4m3(q 2^-e_h - T1), both rounded to nearest
+// even: T1 + T2 equals the scaled row exactly for every element of magnitude
+// at least 2^-2 (a bf16 significand has 8 bits, each term carries 4), the
+// rest to within 2^-10.  The terms form one 128-row operand: row
+// R = 32 (h / 16) + 16 t + h % 16 holds term t of head h.  Columns 0-511 of
+// row R are stored as 512 plain bytes at R * 512 (the decode kernel loads
+// them into tensor memory), columns 512-575 as the 64-byte-swizzled
+// shared-memory image at 65536 (16-byte chunk j of row R at 65536 + R * 64 +
+// 16 (j ^ ((R >> 1) & 3))).  qfac[b][h] = softmax scale * log2(e) * 2^e_h.
+__global__ void __launch_bounds__(256) qterm_kernel(const DecodeArgs a) {
+  __shared__ float s_inv[16];
+  pdl_wait();  // the stream's earlier work is complete from here on
+  pdl_launch_dependents();
+  const int b = blockIdx.x >> 2, hq = blockIdx.x & 3;  // request, group of 16 heads
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint16_t *q = static_cast<const uint16_t *>(a.q) + ((size_t)b * kTH + 16 * hq) * kTD;
+  for (int hh = warp; hh < 16; hh += 8) {
+    float m = 0.f;
+    for (int k = lane; k < kTD / 8; k += 32) m = amax8(*reinterpret_cast<const uint4 *>(q + hh * kTD + 8 * k), m);
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) {
+      int e = 8;
+      if (m > 0.f) frexpf(m, &e);  // m = f 2^e, f in [0.5, 1)
+      s_inv[hh] = ldexpf(1.f, 8 - e);
+      a.qfac[(size_t)b * kTH + 16 * hq + hh] = a.sm_scale_log2 * ldexpf(1.f, e - 8);
+    }
   }
-  return make_uint2(o[0], o[1]);
+  __syncthreads();
+  uint8_t *dst = a.qterms + (size_t)b * kLatentQTermBytes;
+  for (int u = tid; u < 16 * 36; u += (int)blockDim.x) {
+    const int hh = u / 36, r = u - hh * 36;  // head of the group, 16-value chunk of its row
+    const int R1 = 32 * hq + hh, R2 = R1 + 16;  // rows of T1 and T2
+    size_t off1, off2;
+    if (r < 32) {
+      off1 = (size_t)R1 * 512 + 16 * r;
+      off2 = (size_t)R2 * 512 + 16 * r;
+    } else {
+      const int j = r - 32;
+      off1 = (size_t)65536 + R1 * 64 + 16 * (j ^ ((R1 >> 1) & 3));
+      off2 = (size_t)65536 + R2 * 64 + 16 * (j ^ ((R2 >> 1) & 3));
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(q + hh * kTD + 16 * r);
+    const uint4 v0 = src[0], v1 = src[1];
+    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const float inv = s_inv[hh];
+    uint32_t t1[4], t2[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const float x0 = __uint_as_float(wv[i] << 16) * inv, x1 = __uint_as_float(wv[i] & 0xffff0000u) * inv;
+      const float x2 = __uint_as_float(wv[i + 1] << 16) * inv, x3 = __uint_as_float(wv[i + 1] & 0xffff0000u) * inv;
+      const uint32_t a01 = f32x2_to_e4m3x2(x0, x1), a23 = f32x2_to_e4m3x2(x2, x3);
+      const uint32_t h01 = e4m3x2_to_f16x2(a01), h23 = e4m3x2_to_f16x2(a23);
+      const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+      const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+      t1[i / 2] = a01 | (a23 << 16);
+      t2[i / 2] = f32x2_to_e4m3x2(x0 - f01.x, x1 - f01.y) | (f32x2_to_e4m3x2(x2 - f23.x, x3 - f23.y) << 16);
+    }
+    *reinterpret_cast<uint4 *>(dst + off1) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
+    *reinterpret_cast<uint4 *>(dst + off2) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
+  }
 }
 
-// The query operand of request b, written by the softmax warps.  Head h's
-// bf16 row (576 values) is scaled by 2^-e_h, e_h the exponent that puts
-// max|q| in [128, 256), and written as T1 = e4m3(q 2^-e_h) and
-// T2 = e4m3(q 2^-e_h - T1): T1 + T2 equals the scaled row exactly for every
-// element of magnitude at least 2^-2 (a bf16 significand has 8 bits, each
-// term carries 4), the rest to within 2^-10.  Warp (quarter q, half x), lane
-// l writes row R = 32 q + l (head 16 q + l % 16, term l / 16): tensor-memory
-// columns 64 x .. 64 x + 63 (values 256 x .. 256 x + 255) and, for x = 0,
-// the row's 64-byte tail (values 512-575) into the swizzled shared-memory
-// image (16-byte chunk j of row R at R * 64 + 16 (j ^ ((R >> 1) & 3))).  The
-// two warps of a quarter exchange their partial maxima (barrier 2 + q, which
-// also ORs their failure flags).  Returns this lane's score factor
-// softmax scale * log2(e) * 2^e_h.  Whole warp; arrives on q_ready.  One
-// compiled copy for both call sites (first item, next item), so that its
-// code is fetched from memory once per call.
-__device__ __noinline__ float q_prep(const uint16_t *qbase, float sm_scale_log2, int b, uint32_t tq, uint8_t *qtail,
-                                     float *s_qm, uint64_t *q_ready, int q, int x, int lane, bool &fail) {
-  const int h = 16 * q + (lane & 15), t = lane >> 4, R = 32 * q + lane;
-  const uint4 *src = reinterpret_cast<const uint4 *>(qbase + ((size_t)b * kTH + h) * kTD);
-  float m = 0.f;
-  if (!fail) {
-    // this lane's half of the head's values in this warp's columns (and of the tail)
+// The query operand of request b into this warp's share: tensor-memory
+// columns 64 x .. 64 x + 63 of rows 32 q .. 32 q + 31 (lane = row) and, for
+// the warps of half 0, those rows' 64-byte tails of the shared-memory image
+// (copied as the query-term kernel laid them out).  Returns the score factor
+// of this lane's head.  Whole warp; arrives on q_ready.  One compiled copy
+// for both call sites (first item, next item).
+__device__ __noinline__ float q_load(const uint8_t *qterms, const float *qfac, int b, uint32_t tq, uint8_t *qtail,
+                                     uint64_t *q_ready, int q, int x, int lane) {
+  const int R = 32 * q + lane;
+  const uint4 *src = reinterpret_cast<const uint4 *>(qterms + (size_t)b * kLatentQTermBytes + (size_t)R * 512);
+  uint4 tail[4];
+  if (x == 0) {
+    const uint4 *ts = reinterpret_cast<const uint4 *>(qterms + (size_t)b * kLatentQTermBytes + 65536 + R * 64);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) m = amax8(__ldg(src + 32 * x + 16 * t + i), m);
-    if (x == 0)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) m = amax8(__ldg(src + 64 + 4 * t + i), m);
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-    if (lane < 16) s_qm[x * kTH + h] = m;
+    for (int i = 0; i < 4; ++i) tail[i] = __ldcg(ts + i);
   }
-  fail = bar_or(2 + q, 64, fail);
-  if (fail) return 0.f;
-  m = fmaxf(m, s_qm[(x ^ 1) * kTH + h]);
-  int e = 8;
-  if (m > 0.f) frexpf(m, &e);  // m = f 2^e, f in [0.5, 1)
-  const float inv = ldexpf(1.f, 8 - e);
 #pragma unroll 1
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 2 * x; k < 2 * x + 2; ++k) {
     uint32_t r[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint2 c = q_term8(__ldg(src + 32 * x + 16 * k + i), inv, t);
-      r[2 * i] = c.x;
-      r[2 * i + 1] = c.y;
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = __ldcg(src + 8 * k + i);
+      r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
     }
-    tmem_st32(tq + kColQ + 32 * (2 * x + k), r);
+    tmem_st32(tq + kColQ + 32 * k, r);
   }
   if (x == 0) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint2 c0 = q_term8(__ldg(src + 64 + 2 * j), inv, t), c1 = q_term8(__ldg(src + 64 + 2 * j + 1), inv, t);
-      *reinterpret_cast<uint4 *>(qtail + R * 64 + 16 * (j ^ ((R >> 1) & 3))) = make_uint4(c0.x, c0.y, c1.x, c1.y);
-    }
+    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4 *>(qtail + R * 64 + 16 * i) = tail[i];
     fence_async_smem();
   }
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(q_ready);
-  return sm_scale_log2 * ldexpf(1.f, e - 8);
+  return __ldcg(&qfac[(size_t)b * kTH + 16 * q + (lane & 15)]);
 }
 
 // Softmax warp w (2-5 and 8-11) reads tensor-memory quarter q = w % 4, i.e.
@@ -587,7 +626,8 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
   const int tb = 32 * x + 16 * half;            // first token of the page this thread owns
   float *wsc = reinterpret_cast<float *>(smem + sp.wg);
   float *s_beta = wsc + kWgBeta, *s_l = wsc + kWgL, *s_m = wsc + kWgM;
-  float2 *s_x = reinterpret_cast<float2 *>(wsc + kWgX);
+  float *s_x = wsc + kWgX, *s_smx = wsc + kWgSmx;
+  float *s_inv = wsc + kWgInv + 32 * (wt >> 5);  // this warp's 32 tokens
   volatile uint32_t *resc_tag = reinterpret_cast<uint32_t *>(wsc + kWgTag);
   volatile uint32_t *four_flag = reinterpret_cast<uint32_t *>(wsc + kWgFour);
   const float *scales = reinterpret_cast<const float *>(smem + sp.scales);
@@ -597,7 +637,6 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
   // (token / 16) * 128 + token % 16; this thread writes the 16-token chunk tb / 16
   const uint32_t p_off = (h & 7) * 16 + (h >> 3) * 512 + (tb / 16) * 128;
   uint8_t *qtail = smem + sp.qtail;
-  float *s_qm = wsc + kWgQm;
   uint32_t g = 0, n_resc = 0;
   float cq = 0.f;  // score factor of this lane's head for the current item
   {
@@ -605,10 +644,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     bool fail = !mbar_wait(&B.item_full[0], 0, abort_flag);
     fail = wg_bar_or(fail);
     const int b0 = fail ? -1 : items[0].b;
-    if (b0 >= 0) {
-      cq = q_prep(static_cast<const uint16_t *>(a.q), a.sm_scale_log2, b0, tq, qtail, s_qm, B.q_ready, q, x, lane, fail);
-      fail = wg_bar_or(fail);
-    }
+    if (b0 >= 0) cq = q_load(a.qterms, a.qfac, b0, tq, qtail, B.q_ready, q, x, lane);
     if (fail) return;
   }
   for (uint32_t it = 0;; ++it) {
@@ -684,9 +720,15 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
           const float4 s4 = *reinterpret_cast<const float4 *>(&scales[st * kTS + tb + i]);
           sv[i] = s4.x; sv[i + 1] = s4.y; sv[i + 2] = s4.z; sv[i + 3] = s4.w;
         }
+        {
+          // 1 / s_t of token 32 x + lane (0 past the end), for the normaliser below
+          const float s_me = scales[st * kTS + 32 * x + lane];
+          s_inv[lane] = (d.p0 + (int)j) * kTS + 32 * x + lane < d.L && s_me > 0.f ? fast_rcp(s_me) : 0.f;
+        }
+        const bool all_valid = tok0 + 16 <= d.L;  // (warp-uniform per lane half) no token past the end
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const bool valid = tok0 + i < d.L;
+          const bool valid = all_valid || tok0 + i < d.L;
           if (!valid) sv[i] = 0.f;
           v[i] = valid ? v[i] * cq * sv[i] : kNegInf;  // z in log2 units
           mt = fmaxf(mt, v[i]);
@@ -694,16 +736,17 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
         }
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
         smx = fmaxf(smx, __shfl_xor_sync(0xffffffffu, smx, 16));
-        if (lane < 16) s_x[(sb * 2 + x) * kTH + h] = make_float2(mt, smx);
+        if (lane < 16) s_x[(sb * 2 + x) * kTH + h] = mt;
+        if (lane == 0) s_smx[(sb * 2 + x) * 4 + q] = smx;  // the same for every head
       }
       if (bar_or(2 + q, 64, fail)) {
         fail = true;
         break;
       }
       {
-        const float2 o = s_x[(sb * 2 + (x ^ 1)) * kTH + h];  // the other half of the page
-        mt = fmaxf(mt, o.x);
-        smx = fmaxf(smx, o.y);
+        // the other half of the page
+        mt = fmaxf(mt, s_x[(sb * 2 + (x ^ 1)) * kTH + h]);
+        smx = fmaxf(smx, s_smx[(sb * 2 + (x ^ 1)) * 4 + q]);
       }
       const float s_new = smx > 2.f * s_ref ? smx : s_ref;
       const float m_new = mt > m + kTheta ? mt : m;
@@ -725,14 +768,22 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       const bool four = smx * 448.f > kFourTermAt;
       if (wt == 0) four_flag[sb] = four ? 1u : 0u;  // read by the PV issuers after p_full
       const float w = exp2f(kPExp) / s_ref;
+      __syncwarp();  // s_inv
+      float inv[16];
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const float4 r4 = *reinterpret_cast<const float4 *>(&s_inv[16 * half + i]);
+        inv[i] = r4.x; inv[i + 1] = r4.y; inv[i + 2] = r4.z; inv[i + 3] = r4.w;
+      }
       uint32_t t1[8], t2[8], t3[8], t4[8];
+      float lp = 0.f;  // this page's share of l, times w
 #pragma unroll
       for (int i = 0; i < 16; i += 2) {
-        const float sw0 = sv[i] * w, sw1 = sv[i + 1] * w;
-        const float2 rep = p_terms2(fast_exp2(v[i] - m) * sw0, fast_exp2(v[i + 1] - m) * sw1, four, t1[i / 2],
-                                    t2[i / 2], t3[i / 2], t4[i / 2]);
-        l += (rep.x > 0.f ? rep.x * fast_rcp(sw0) : 0.f) + (rep.y > 0.f ? rep.y * fast_rcp(sw1) : 0.f);
+        const float2 rep = p_terms2(fast_exp2(v[i] - m) * (sv[i] * w), fast_exp2(v[i + 1] - m) * (sv[i + 1] * w),
+                                    four, t1[i / 2], t2[i / 2], t3[i / 2], t4[i / 2]);
+        lp = fmaf(rep.x, inv[i], fmaf(rep.y, inv[i + 1], lp));
       }
+      l = fmaf(lp, s_ref * exp2f(-kPExp), l);
       uint8_t *pt = pbase + sb * kPBuf + p_off;
       *reinterpret_cast<uint4 *>(pt) =
           make_uint4(t1[0] | (t1[1] << 16), t1[2] | (t1[3] << 16), t1[4] | (t1[5] << 16), t1[6] | (t1[7] << 16));
@@ -762,8 +813,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       const int b_next = items[nslot].b;
       if (b_next >= 0) {
         fail = __any_sync(0xffffffffu, !mbar_wait(B.q_empty, it & 1u, abort_flag));  // warp-uniform
-        cq_next = q_prep(static_cast<const uint16_t *>(a.q), a.sm_scale_log2, b_next, tq, qtail, s_qm, B.q_ready, q, x,
-                         lane, fail);
+        if (!fail) cq_next = q_load(a.qterms, a.qfac, b_next, tq, qtail, B.q_ready, q, x, lane);
         if (wg_bar_or(fail)) break;
       }
     }
@@ -935,6 +985,15 @@ int launch_latent_decode(const DecodeArgs &a0, cudaStream_t s) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // the query terms of every request (one block per request and 16 heads)
+  cudaLaunchConfig_t qcfg = {};
+  qcfg.gridDim = dim3(a.B * 4);
+  qcfg.blockDim = dim3(256);
+  qcfg.stream = s;
+  qcfg.attrs = attr;
+  qcfg.numAttrs = 1;
+  rc = cuda_ok(cudaLaunchKernelEx(&qcfg, qterm_kernel, a), "query-term kernel launch");
+  if (rc) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTThreads);

@@ -12,10 +12,14 @@ namespace pfkv {
 
 // Decode workspace carve-up.
 struct WsLayout {
-  size_t split_first, split_count, part_ml, part_o, part_st, cta_abort, total;
+  size_t split_first, split_count, part_ml, part_o, part_st, cta_abort, qterms, qfac, total;
 };
 constexpr int kMaxCtas = 4096;  // decode split grid: at most this many CTAs (one abort word each)
-WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits);
+// latent: the latent-stream path also keeps each request's query as two e4m3
+// terms in the operand image its kernel loads (qterms, 72 KB per request)
+// and one factor per head (qfac), written by its query-term kernel.
+WsLayout ws_layout(int batch, int q_heads, int v_dim, int max_splits, bool latent);
+constexpr size_t kLatentQTermBytes = 128 * 576;  // 128 operand rows (two terms x 64 heads) x 576 codes
 
 struct DecodeArgs {
   // cache
@@ -63,6 +67,9 @@ struct DecodeArgs {
   // the rows of faulted requests.
   int ranges, target_items, min_chunk_pages, n_ctas;
   int st_groups;  // status words per piece in part_st (grouped-query path: one per head group)
+  // latent-stream path: the query terms and per-head factors (see ws_layout)
+  uint8_t *qterms;
+  float *qfac;
   int piece_cost;  // cut rule: pages' worth of time one piece costs beyond its pages
   uint32_t *part_st;
   int *cta_abort;
