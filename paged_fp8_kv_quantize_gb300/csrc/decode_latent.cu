@@ -702,15 +702,11 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
         {
           tc_fence_after();
           uint32_t r[32];
-          tmem_ld32(tq + kColS + 64 * sb + 32 * x, r);  // tokens 32 x .. 32 x + 31 of this lane's row
+          // T1 (rows 0-15 of the quarter) and T2 (rows 16-31) of head h, tokens tb .. tb + 15
+          tmem_ld_pair16(tq + kColS + 64 * sb + 32 * x, r);
           tc_fence_before();
-          // T1 + T2: the partner lane (l ^ 16) holds the other term of the same head
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t give = half ? r[i] : r[16 + i];
-            const uint32_t take = __shfl_xor_sync(0xffffffffu, give, 16);
-            v[i] = __uint_as_float(half ? r[16 + i] : r[i]) + __uint_as_float(take);
-          }
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]) + __uint_as_float(r[16 + i]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&B.s_empty[sb]);

@@ -426,6 +426,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// Whole warp, two 16-lane blocks of this warp's quarter: lanes 0-15 and
+// 16-31 of the quarter starting at taddr's lane, 16 columns each.  Thread t
+// reads lane t % 16 of each block, columns c .. c + 15 (t < 16) or
+// c + 16 .. c + 31 (t >= 16), c = taddr's column: r[0..15] from the first
+// block, r[16..31] from the second, so that a thread holds the same columns
+// of two rows 16 lanes apart.  One statement with its completion wait.
+__device__ __forceinline__ void tmem_ld_pair16(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32], 16;\n"
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%33], 16;\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : PFKV_R8(0), PFKV_R8(8), PFKV_R8(16), PFKV_R8(24)
+      : "r"(taddr), "r"(taddr + (16u << 16))
+      : "memory");
+}
 #undef PFKV_R8
 #define PFKV_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
                    "r"(r[i + 6]), "r"(r[i + 7])
