@@ -118,6 +118,8 @@ __host__ __device__ constexpr TcSmem tc_smem() {
   return s;
 }
 static_assert(tc_smem().total + 1024 <= 232448, "shared memory plan exceeds one SM");
+static_assert(kLatentQTermBytes == 2 * kPageSm && kQTailBytes == kSmxThreads * 32 && kTH <= kTS,
+              "the query image fills two ring entries; each softmax thread copies 32 bytes of its tail");
 
 // Bounded wait that ignores the abort flag: used on the way out, so that a
 // block that gave up still lets its own copies and MMAs land before it exits.
@@ -177,7 +179,7 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
   const int lane = threadIdx.x & 31;
   const bool tag_check = (a.flags & PFKV_FLAG_TAG_CHECK) != 0u;
   const uint64_t stream_pol = l2_evict_first_policy();
-  uint32_t g = 0;  // pages issued by this CTA
+  uint32_t g = 0;  // ring entries (query images and pages) issued by this CTA
   bool ok = true;
   // This CTA's pieces, worked out from the lengths; the next one is found
   // once the current one's pages have gone out.
@@ -209,6 +211,7 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
     }
     const int b = cur.b, p0 = cur.p0, p1 = cur.p1, L = cur.L;
     if (lane == 0) {
+      // ring entries g, g + 1: the query image; g + 2 + j: page p0 + j
       ItemDesc d;
       d.b = b; d.cg = cur.cg; d.g = 0; d.p0 = p0; d.p1 = p1; d.L = L; d.ring = g; d.nb = cur.nb;
       items[slot] = d;
@@ -218,9 +221,27 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
         a.split_count[b] = cur.nb;
       }
     }
-    // the item's query rows (72 KB) into L2 well before the softmax warps
-    // turn them into the query operand
-    if (lane == 0) bulk_prefetch_l2(static_cast<const uint16_t *>(a.q) + (size_t)b * kTH * kTD, kTH * kTD * 2);
+    // The item's query image in two ring entries ahead of its pages, with
+    // its score factors in the first entry's scale slot: copied with the
+    // page stream, so that reaching them costs the consumers no memory round
+    // trip at the item change.
+    {
+      uint32_t nq = 0;
+      if (lane == 0)
+        for (; nq < 2; ++nq) {
+          const uint32_t r = g + nq, st = r % kNst;
+          if (!mbar_wait(&B.empty[st], ((r / kNst) & 1u) ^ 1u, abort_flag)) break;
+          mbar_arrive_expect_tx(&B.full[st], kPageSm + (nq == 0 ? kTH * 4 : 0));
+          bulk_load_stream(smem + sp.ring + st * kPageSm, a.qterms + (size_t)b * kLatentQTermBytes + nq * kPageSm,
+                           kPageSm, &B.full[st], stream_pol);
+          if (nq == 0)
+            bulk_load_stream(smem + sp.scales + st * (kTS * 4), a.qfac + (size_t)b * kTH, kTH * 4, &B.full[st],
+                             stream_pol);
+        }
+      nq = __shfl_sync(0xffffffffu, nq, 0);
+      g += nq;
+      ok = nq == 2;
+    }
     // Decode step: the piece holding the request's last page writes the new
     // token's row into that page before copying it; the row is loaded now so
     // that its latency hides behind the walk.
@@ -328,9 +349,10 @@ __device__ __forceinline__ TcDesc tc_desc(uint8_t *smem) {
 }
 
 // QK^T issuer (warp 1): S[sb] = [T1; T2 rows] . K_page^T for every page in
-// order, as soon as the page has landed and the softmax warps have read the
-// S buffer's previous page.  After an item's last page it commits q_empty:
-// the query operand may then be replaced by the next item's.
+// order (page j of an item in ring entry ring + 2 + j), as soon as the page
+// has landed and the softmax warps have read the S buffer's previous page.
+// After an item's last page it commits q_empty: the query operand may then be
+// replaced by the next item's.
 __device__ __forceinline__ void tc_mma_qk(uint8_t *smem, const Bars &B, const ItemDesc *items, uint32_t tmem,
                                           volatile int *abort_flag) {
   const TcDesc dd = tc_desc(smem);
@@ -342,11 +364,11 @@ __device__ __forceinline__ void tc_mma_qk(uint8_t *smem, const Bars &B, const It
     mbar_arrive(&B.item_empty[slot]);
     if (d.b < 0) break;
     const uint32_t n = (uint32_t)(d.p1 - d.p0);
-    if (!mbar_wait(B.q_ready, it & 1u, abort_flag)) break;  // the item's query terms are in place
+    if (!mbar_wait(B.q_ready, it & 1u, abort_flag)) break;  // the item's query operand is in place
     bool ok = true;
     for (uint32_t j = 0; j < n; ++j) {
-      const uint32_t gp = g + j, st = gp % kNst, sb = gp & 1u;
-      if (!mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
+      const uint32_t gp = g + j, sb = gp & 1u, rr = d.ring + 2 + j, st = rr % kNst;
+      if (!mbar_wait(&B.full[st], (rr / kNst) & 1u, abort_flag) ||
           !mbar_wait(&B.s_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag)) {
         ok = false;
         break;
@@ -395,7 +417,7 @@ __device__ __forceinline__ void tc_mma_pv(uint8_t *smem, const Bars &B, const It
     if (!mbar_wait(B.o_empty, (it & 1u) ^ 1u, abort_flag)) break;
     bool ok = true;
     for (uint32_t j = 0; j < n; ++j) {
-      const uint32_t gp = g + j, st = gp % kNst, pb = gp & 1u;
+      const uint32_t gp = g + j, st = (d.ring + 2 + j) % kNst, pb = gp & 1u;
       if (!mbar_wait(&B.p_full[pb], (gp >> 1) & 1u, abort_flag)) {
         ok = false;
         break;
@@ -511,11 +533,16 @@ __device__ __forceinline__ float2 p_terms2(float lo, float hi, bool four, uint32
 // even: T1 + T2 equals the scaled row exactly for every element of magnitude
 // at least 2^-2 (a bf16 significand has 8 bits, each term carries 4), the
 // rest to within 2^-10.  The terms form one 128-row operand: row
-// R = 32 (h / 16) + 16 t + h % 16 holds term t of head h.  Columns 0-511 of
-// row R are stored as 512 plain bytes at R * 512 (the decode kernel loads
-// them into tensor memory), columns 512-575 as the 64-byte-swizzled
-// shared-memory image at 65536 (16-byte chunk j of row R at 65536 + R * 64 +
-// 16 (j ^ ((R >> 1) & 3))).  qfac[b][h] = softmax scale * log2(e) * 2^e_h.
+// R = 32 (h / 16) + 16 t + h % 16 holds term t of head h.  Columns 0-511
+// are laid out as sixteen blocks of 128 rows x 32 bytes: block k (columns
+// 32 k .. 32 k + 31) at 4096 k, inside it units of 8 rows x 16 bytes, the 16
+// bytes of row R, columns 32 k + 16 c .. + 15 at 4096 k + 256 (R / 8) +
+// 128 c + 16 (R % 8), so that eight consecutive rows' bytes are contiguous.
+// Columns 512-575 follow as the 64-byte-swizzled shared-memory image at
+// 65536 (16-byte chunk j of row R at 65536 + R * 64 + 16 (j ^ ((R >> 1) & 3))).
+// The decode kernel copies the whole image into two ring slots (bytes
+// 0-36863: blocks 0-8; 36864-73727: blocks 9-15 and the tail).
+// qfac[b][h] = softmax scale * log2(e) * 2^e_h.
 __global__ void __launch_bounds__(256) qterm_kernel(const DecodeArgs a) {
   __shared__ float s_inv[16];
   pdl_wait();  // the stream's earlier work is complete from here on
@@ -537,12 +564,15 @@ __global__ void __launch_bounds__(256) qterm_kernel(const DecodeArgs a) {
   __syncthreads();
   uint8_t *dst = a.qterms + (size_t)b * kLatentQTermBytes;
   for (int u = tid; u < 16 * 36; u += (int)blockDim.x) {
-    const int hh = u / 36, r = u - hh * 36;  // head of the group, 16-value chunk of its row
+    // 16-value chunk r of head hh's row: neighbouring threads take
+    // neighbouring heads, whose rows are neighbours in the image
+    const int r = u >> 4, hh = u & 15;
     const int R1 = 32 * hq + hh, R2 = R1 + 16;  // rows of T1 and T2
     size_t off1, off2;
     if (r < 32) {
-      off1 = (size_t)R1 * 512 + 16 * r;
-      off2 = (size_t)R2 * 512 + 16 * r;
+      const size_t blk = (size_t)(r >> 1) * 4096 + (size_t)(r & 1) * 128;
+      off1 = blk + (size_t)(R1 >> 3) * 256 + (R1 & 7) * 16;
+      off2 = blk + (size_t)(R2 >> 3) * 256 + (R2 & 7) * 16;
     } else {
       const int j = r - 32;
       off1 = (size_t)65536 + R1 * 64 + 16 * (j ^ ((R1 >> 1) & 3));
@@ -569,42 +599,63 @@ __global__ void __launch_bounds__(256) qterm_kernel(const DecodeArgs a) {
   }
 }
 
-// The query operand of request b into this warp's share: tensor-memory
-// columns 64 x .. 64 x + 63 of rows 32 q .. 32 q + 31 (lane = row) and, for
-// the warps of half 0, those rows' 64-byte tails of the shared-memory image
-// (copied as the query-term kernel laid them out).  Returns the score factor
-// of this lane's head.  Whole warp; arrives on q_ready.  One compiled copy
-// for both call sites (first item, next item).
-__device__ __noinline__ float q_load(const uint8_t *qterms, const float *qfac, int b, uint32_t tq, uint8_t *qtail,
-                                     uint64_t *q_ready, int q, int x, int lane) {
+// The query operand of the item whose image sits in ring entries `ring`
+// (bytes 0-36863 of the image, the score factors in its scale slot) and
+// ring + 1 (the rest; the 8 KB tail image at 28672), once both have landed.
+// Softmax thread (q, x, lane) moves row R = 32 q + lane, columns
+// 256 x .. 256 x + 255, into tensor-memory columns 64 x .. 64 x + 63 of its
+// lane (the image's 8-row x 16-byte blocks put the rows a phase of 8 lanes
+// reads in distinct banks), and bytes 32 wt .. 32 wt + 31 of the tail image
+// into the query-tail buffer.  Returns the score factor of head h, or sets
+// fail (warp-uniform) if a wait gave up.  Whole warp; arrives on q_ready.
+// The caller frees the two entries once every softmax warp is past this.
+// One compiled copy for both call sites (first item, next item).
+__device__ __noinline__ float q_take(uint8_t *smem, uint32_t ring, uint64_t *full, uint64_t *q_ready, uint32_t tq,
+                                     int wt, int h, volatile int *abort_flag, bool &fail) {
+  const TcSmem sp = tc_smem();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, x = warp >= 8 ? 1 : 0;
+  const uint32_t qa = ring % kNst, qb = (ring + 1) % kNst;
+  fail = __any_sync(0xffffffffu, !mbar_wait(&full[qa], (ring / kNst) & 1u, abort_flag) ||
+                                     !mbar_wait(&full[qb], ((ring + 1) / kNst) & 1u, abort_flag));
+  if (fail) return 0.f;
   const int R = 32 * q + lane;
-  const uint4 *src = reinterpret_cast<const uint4 *>(qterms + (size_t)b * kLatentQTermBytes + (size_t)R * 512);
-  uint4 tail[4];
-  if (x == 0) {
-    const uint4 *ts = reinterpret_cast<const uint4 *>(qterms + (size_t)b * kLatentQTermBytes + 65536 + R * 64);
+  uint32_t r[2][32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tail[i] = __ldcg(ts + i);
-  }
-#pragma unroll 1
-  for (int k = 2 * x; k < 2 * x + 2; ++k) {
-    uint32_t r[32];
+  for (int kk = 0; kk < 8; ++kk) {
+    const int k = 8 * x + kk;  // 32-byte column block of the row
+    const uint8_t *src = smem + sp.ring + (k < 9 ? qa * kPageSm + 4096 * k : qb * kPageSm + 4096 * (k - 9)) +
+                         (R >> 3) * 256 + (R & 7) * 16;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint4 v = __ldcg(src + 8 * k + i);
-      r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+    for (int c = 0; c < 2; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(src + 128 * c);
+      const int o = (kk & 3) * 8 + c * 4;
+      r[kk >> 2][o] = v.x; r[kk >> 2][o + 1] = v.y; r[kk >> 2][o + 2] = v.z; r[kk >> 2][o + 3] = v.w;
     }
-    tmem_st32(tq + kColQ + 32 * k, r);
   }
-  if (x == 0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4 *>(qtail + R * 64 + 16 * i) = tail[i];
-    fence_async_smem();
-  }
+  tmem_st32(tq + kColQ + 64 * x, r[0]);
+  tmem_st32(tq + kColQ + 64 * x + 32, r[1]);
+  const uint4 *tsrc = reinterpret_cast<const uint4 *>(smem + sp.ring + qb * kPageSm +
+                                                      (kLatentQTermBytes - kPageSm - kQTailBytes));
+  uint4 *tdst = reinterpret_cast<uint4 *>(smem + sp.qtail);
+  const uint4 v0 = tsrc[2 * wt], v1 = tsrc[2 * wt + 1];
+  tdst[2 * wt] = v0;
+  tdst[2 * wt + 1] = v1;
+  const float qf = reinterpret_cast<const float *>(smem + sp.scales)[qa * kTS + h];
+  fence_async_smem();
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(q_ready);
-  return __ldcg(&qfac[(size_t)b * kTH + 16 * q + (lane & 15)]);
+  return qf;
+}
+
+// Frees the two ring entries of a query image (two arrivals each, from two
+// softmax warps), once every softmax warp is past q_take.
+__device__ __forceinline__ void q_release(const Bars &B, uint32_t ring, int wt) {
+  if (wt == 0 || wt == 32) {
+    mbar_arrive(&B.empty[ring % kNst]);
+    mbar_arrive(&B.empty[(ring + 1) % kNst]);
+  }
 }
 
 // Softmax warp w (2-5 and 8-11) reads tensor-memory quarter q = w % 4, i.e.
@@ -636,7 +687,6 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
   // P^T (K-major, no swizzle): byte (head, token) at (head % 8) * 16 + (head / 8) * 512 +
   // (token / 16) * 128 + token % 16; this thread writes the 16-token chunk tb / 16
   const uint32_t p_off = (h & 7) * 16 + (h >> 3) * 512 + (tb / 16) * 128;
-  uint8_t *qtail = smem + sp.qtail;
   uint32_t g = 0, n_resc = 0;
   float cq = 0.f;  // score factor of this lane's head for the current item
   {
@@ -644,8 +694,10 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
     bool fail = !mbar_wait(&B.item_full[0], 0, abort_flag);
     fail = wg_bar_or(fail);
     const int b0 = fail ? -1 : items[0].b;
-    if (b0 >= 0) cq = q_load(a.qterms, a.qfac, b0, tq, qtail, B.q_ready, q, x, lane);
-    if (fail) return;
+    const uint32_t ring0 = items[0].ring;
+    if (b0 >= 0) cq = q_take(smem, ring0, B.full, B.q_ready, tq, wt, h, abort_flag, fail);
+    if (wg_bar_or(fail)) return;
+    if (b0 >= 0) q_release(B, ring0, wt);
   }
   for (uint32_t it = 0;; ++it) {
     const uint32_t slot = it % kNIQ;
@@ -690,10 +742,10 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       ++n_resc;
     };
     for (uint32_t j = 0; j < n; ++j) {
-      const uint32_t gp = g + j, sb = gp & 1u, st = gp % kNst;
+      const uint32_t gp = g + j, sb = gp & 1u, rr = d.ring + 2 + j, st = rr % kNst;
       if (!fail)
         fail = !mbar_wait(&B.s_full[sb], (gp >> 1) & 1u, abort_flag) ||
-               !mbar_wait(&B.full[st], (gp / kNst) & 1u, abort_flag) ||
+               !mbar_wait(&B.full[st], (rr / kNst) & 1u, abort_flag) ||
                !mbar_wait(&B.p_empty[sb], ((gp >> 1) & 1u) ^ 1u, abort_flag);
       fail = __any_sync(0xffffffffu, fail);  // the warp-wide tensor-memory load below needs every lane
       float v[16], sv[16];
@@ -808,9 +860,11 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       if (wg_bar_or(fail)) break;
       const int b_next = items[nslot].b;
       if (b_next >= 0) {
+        const uint32_t ring_next = items[nslot].ring;
         fail = __any_sync(0xffffffffu, !mbar_wait(B.q_empty, it & 1u, abort_flag));  // warp-uniform
-        if (!fail) cq_next = q_load(a.qterms, a.qfac, b_next, tq, qtail, B.q_ready, q, x, lane);
+        if (!fail) cq_next = q_take(smem, ring_next, B.full, B.q_ready, tq, wt, h, abort_flag, fail);
         if (wg_bar_or(fail)) break;
+        q_release(B, ring_next, wt);
       }
     }
     // ---- the item's result: wait for its last PV and its status
