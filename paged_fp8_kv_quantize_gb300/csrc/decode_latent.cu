@@ -796,6 +796,10 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
         mt = fmaxf(mt, s_x[(sb * 2 + (x ^ 1)) * kTH + h]);
         smx = fmaxf(smx, s_smx[(sb * 2 + (x ^ 1)) * 4 + q]);
       }
+      // the previous page's rescale hand-off, before this page's
+      // probabilities, so that a page held back by it waits as little as
+      // possible (every warp of this page's lane quarter is past page j - 1)
+      if (j > 1) rescale_check(g + j - 1, fail);
       const float s_new = smx > 2.f * s_ref ? smx : s_ref;
       const float m_new = mt > m + kTheta ? mt : m;
       const float alpha = fast_exp2(m - m_new);
@@ -846,8 +850,6 @@ __device__ __forceinline__ void tc_softmax(const DecodeArgs &a, uint8_t *smem, c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.p_full[sb]);
-      // the previous page's rescale, now that this page's P^T is out
-      if (j > 1) rescale_check(g + j - 1, fail);
     }
     if (n > 1) rescale_check(g + n - 1, fail);  // the item's last page
     if (wg_bar_or(fail)) break;
