@@ -291,25 +291,29 @@ __device__ __forceinline__ bool ws_next_shared(WorkSplit &s, const WsArgs &a, Pi
 // Merge launch shape: a block takes kW float4 columns of one (request, KV
 // head)'s group rows (kG heads x kD values) and spreads the splits over
 // 256 / kW thread groups; gridDim.y = kBlocks.
-template <int kD, int kG>
+template <int kD, int kG, int kWide = 1>
 struct MergeShape {
   static constexpr int kCols = kG * kD / 4;               // float4 columns of the group
   // float4 columns per block: 64, so that the splits of a column spread
   // over 4 thread groups; very wide groups (the latent stream's 16 x 512)
-  // take 256 per block, which keeps the block count down
-  static constexpr int kW = kCols < 64 ? kCols : (kCols >= 1024 ? 256 : 64);
+  // take 256 per block, which keeps the block count down.  The narrow shape
+  // (kWide = 0, for grids that would leave most SMs idle: a few requests
+  // with many pieces each) takes 16 columns and spreads a column's splits
+  // over 16 thread groups, so that each thread reads a few pieces at once
+  // and the block count grows fourfold.
+  static constexpr int kW = kWide ? (kCols < 64 ? kCols : (kCols >= 1024 ? 256 : 64)) : (kCols < 16 ? kCols : 16);
   static constexpr int kGroups = 256 / kW;                // split groups per column
   static constexpr int kBlocks = kCols / kW;
   static constexpr int kNH = kW * 4 / kD > 0 ? kW * 4 / kD : 1;  // heads a block touches
   static_assert(kCols % kW == 0 && 256 % kW == 0, "merge columns");
 };
 
-template <int kD, int kG>
-constexpr int merge_col_blocks() { return MergeShape<kD, kG>::kBlocks; }
+template <int kD, int kG, int kWide = 1>
+constexpr int merge_col_blocks() { return MergeShape<kD, kG, kWide>::kBlocks; }
 
-template <int kD, int kG>
+template <int kD, int kG, int kWide = 1>
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
-  using M = MergeShape<kD, kG>;
+  using M = MergeShape<kD, kG, kWide>;
   __shared__ float s_w[256 * M::kNH];  // per (split, head of this block): m, then the split's weight (splits <= 256)
   __shared__ float s_l[256 * M::kNH];
   __shared__ float s_M[M::kNH], s_W[M::kNH];

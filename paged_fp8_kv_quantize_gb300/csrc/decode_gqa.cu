@@ -826,13 +826,18 @@ int run_split(const DecodeArgs &a_in, cudaStream_t s, const CUtensorMap &mk, con
   cfg.numAttrs = 1;
   int rc = cuda_ok(cudaLaunchKernelEx(&cfg, kern, mk, mv, a, sh.nst), "split kernel launch");
   if (rc) return rc;
+  // the narrow merge shape when the wide one would give fewer than two
+  // blocks per SM (a few requests, many pieces each)
+  const bool narrow = (long long)a.B * a.Hkv * merge_col_blocks<kD, kG>() < 2LL * num_sms();
   cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(a.B * a.Hkv, merge_col_blocks<kD, kG>());
+  mcfg.gridDim = dim3(a.B * a.Hkv, narrow ? merge_col_blocks<kD, kG, 0>() : merge_col_blocks<kD, kG>());
   mcfg.blockDim = dim3(256);
   mcfg.stream = s;
   mcfg.attrs = attr;
   mcfg.numAttrs = 1;
-  return cuda_ok(cudaLaunchKernelEx(&mcfg, merge_kernel<kD, kG>, a), "merge kernel launch");
+  return cuda_ok(narrow ? cudaLaunchKernelEx(&mcfg, merge_kernel<kD, kG, 0>, a)
+                        : cudaLaunchKernelEx(&mcfg, merge_kernel<kD, kG>, a),
+                 "merge kernel launch");
 }
 
 // Any group size: up to 8 query heads per CTA group (the register-operand
