@@ -90,8 +90,8 @@ def test_latent_closed_forms():
     # length 1 gives the value row; a constant V (same codes and scale for
     # every token: the rope part stays below the latent part's largest value)
     # gives the constant, whatever the scores; both within the tolerance of
-    # the parity tests (the kernel carries the probabilities as three e4m3
-    # terms, about 12 significant bits)
+    # the parity tests (the kernel carries the probabilities as three or four
+    # 8-bit terms, 11 to 15 significant bits)
     w = _lat(505, [1, 1, 300, 900])
     f = synth.bf16_to_f32(w.k_rows).copy()
     off = w.rows_of(2)[0]

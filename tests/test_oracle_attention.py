@@ -29,6 +29,8 @@ CASES = [
     dict(G=8, Hkv=1, D=128, S=16),
     dict(G=2, Hkv=2, D=32, S=8, scale_mode=synth.PER_TOKEN),
     dict(G=4, Hkv=1, D=40, Dv=32, S=4, kv_shared=True, scale_mode=synth.PER_TOKEN, Hkv_=1),
+    dict(G=3, Hkv=2, D=32, S=8),
+    dict(G=16, Hkv=1, D=64, S=16, B=2),
 ]
 
 
