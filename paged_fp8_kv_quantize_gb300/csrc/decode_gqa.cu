@@ -96,18 +96,15 @@ __device__ __forceinline__ float round16(float x) {
 }
 
 // Decode step, producer warp: the new token of (request, KV head g) goes to
-// slot `slot` of the page that lane `src` of the batch looked up, unless that
-// page is out of range or (tag check on) its tag does not match; the walk
+// slot `slot` of page `pid`, unless that page is out of range or (tag check
+// on) its tag does not match (`refused`, the same on every lane); the walk
 // reports those cases in the request's status as for any page.  Quantized
 // as the append does (x / s, RNE, satfinite; per-token s = amax / 448, or 1
-// for an all-zero row).  The stores are made visible to the tensor-copy
-// engine before the page is copied (proxy fence).
+// for an all-zero row).  Whole warp.  The caller fences the stores for the
+// tensor-copy engine (proxy fence) before it copies the page.
 template <bool kFp8, int kD>
-__device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, float s, bool has, int part, int k, int src,
-                                              int pid_lane, bool oob_lane, bool stale_lane, int g, int slot,
-                                              bool per_token) {
-  const int pid = __shfl_sync(0xffffffffu, pid_lane, src);
-  const bool refused = __shfl_sync(0xffffffffu, oob_lane || stale_lane, src);
+__device__ __forceinline__ void store_new_row(const DecodeArgs &a, uint4 v, float s, bool has, int part, int k, int pid,
+                                              bool refused, int g, int slot, bool per_token) {
   if (refused) return;
   const size_t row = ((size_t)pid * a.cache.num_kv_heads + g) * a.S + slot;
   if constexpr (kFp8) {
@@ -124,8 +121,6 @@ __device__ __forceinline__ void write_new_row(const DecodeArgs &a, uint4 v, floa
   } else {
     if (has) *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(part ? a.cache.v_pool : a.cache.k_pool) + row * kD + k) = v;
   }
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  __syncwarp();
 }
 
 // Bounded wait that ignores the abort flag: the page loader's way out, so
@@ -261,6 +256,18 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
                                               ((size_t)b * a.cache.num_kv_heads + g) * kD + nv_k);
         if (kFp8 && !per_token) nv_scale = __ldg(&(nv_part ? a.v_scale : a.k_scale)[g]);
       }
+      // ... and the destination page's id, loaded now as well: the row is
+      // stored as soon as the first batch's copies are out (before them if
+      // the destination is in that batch), off the path of the destination
+      // batch, which only fences the stores before its copies
+      const int pid_new = has_new ? __ldg(&trow[i_new]) : 0;
+      bool row_stored = !has_new;
+      auto store_row = [&]() {  // whole warp
+        bool bad = pid_new < 0 || pid_new >= a.P;
+        if (tag_check && !bad) bad = __ldg(&a.page_tags[pid_new]) != __ldg(&tagrow[i_new]);
+        store_new_row<kFp8, kD>(a, nv, nv_scale, nv_lane, nv_part, nv_k, pid_new, bad, g, (L - 1) % S, per_token);
+        row_stored = true;
+      };
       int kb = 0;  // batch number within the piece
       for (int i0 = p0; i0 < p1 && ok; i0 += batch_pages, ++kb) {
         last_first = ring;
@@ -281,9 +288,11 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
           page_tag = __ldg(&a.page_tags[pid]);
           want_tag = __ldg(&tagrow[i]);
         }
-        if (dest_batch)
-          write_new_row<kFp8, kD>(a, nv, nv_scale, nv_lane, nv_part, nv_k, i_new - i0, pid, oob,
-                                  page_tag != want_tag, g, (L - 1) % S, per_token);
+        if (dest_batch) {
+          if (!row_stored) store_row();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __syncwarp();
+        }
         bool lane_ok = true;
         if (valid) {
           const uint32_t r = ring + (uint32_t)lane;
@@ -310,6 +319,7 @@ __global__ void __launch_bounds__(Cfg<kFp8, kD, kG, kNCW>::kThreads, Cfg<kFp8, k
             }
           }
         }
+        if (!row_stored) store_row();  // the first batch's copies are out
         ring += (uint32_t)min(batch_pages, p1 - i0);
         last_issued = valid && lane_ok;
         ok = __all_sync(0xffffffffu, lane_ok);

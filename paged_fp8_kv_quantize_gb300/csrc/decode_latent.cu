@@ -264,8 +264,9 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
         page_tag = __ldg(&a.page_tags[pid]);
         want_tag = __ldg(&tagrow[i]);
       }
-      if (has_new && i0 <= i_new && i_new < i0 + 32)
-        write_new_row(a, nrow, i_new - i0, pid, oob || page_tag != want_tag, L - 1, lane);
+      // a decode step's destination page (the request's last) gets the new
+      // row just before its own copy, the pages before it already in flight
+      const int dest_k = has_new && i0 <= i_new && i_new < i0 + 32 ? i_new - i0 : -1;
       const int cnt = min(32, p1 - i0);
       // pages kPrefetch ahead of the copies are pulled into L2, so that a copy
       // issued when a ring slot frees up finds its page there
@@ -284,6 +285,7 @@ __device__ __forceinline__ void tc_producer(const DecodeArgs &a, const CUtensorM
         if (g + (uint32_t)k >= (uint32_t)kNst) prefetch(k);
       for (int k = 0; k < cnt; ++k) {
         if (k + kPrefetch < cnt) prefetch(k + kPrefetch);
+        if (k == dest_k) write_new_row(a, nrow, k, pid, oob || page_tag != want_tag, L - 1, lane);
         const int pk = __shfl_sync(0xffffffffu, pid, k);
         const bool bad_k = __shfl_sync(0xffffffffu, oob, k);
         bool w = true;
