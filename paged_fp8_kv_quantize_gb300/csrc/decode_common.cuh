@@ -128,22 +128,23 @@ __device__ __forceinline__ int ws_pages(const WorkSplit &w, int L, int S) {
 }
 
 // Pieces of a request of p > 0 pages whose segment of the cut line starts
-// at `off` (its pages start at off + c0); *ppc: chunk length (chunk rule).
-__device__ __noinline__ int ws_count(const WorkSplit &w, long long off, int p, int max_splits, int *ppc) {
-  if (!w.chunks) {
-    const long long s0 = off + w.c0;
-    return (int)(div_floor((s0 + p) * w.R - 1, w.T) - div_floor((s0 + 1) * w.R - 1, w.T) + 1);
+// at `off` (its pages start at off + c0), and the chunk length (chunk rule;
+// 1 under the cut rule).  Every operand by value: the split's state stays
+// in registers (a reference would put it in local memory, and every field
+// access would become a memory round trip).
+__device__ __noinline__ int2 ws_count(bool chunks, int c0, long long R, long long T, long long cp, long long off,
+                                      int p, int max_splits) {
+  if (!chunks) {
+    const long long s0 = off + c0;
+    return make_int2((int)(div_floor((s0 + p) * R - 1, T) - div_floor((s0 + 1) * R - 1, T) + 1), 1);
   }
-  int nn = w.cp >= p ? 1 : (int)(((unsigned)p + (unsigned)w.cp - 1u) / (unsigned)w.cp);
+  int nn = cp >= p ? 1 : (int)(((unsigned)p + (unsigned)cp - 1u) / (unsigned)cp);
   if (nn > max_splits) nn = max_splits;
   const int q = (int)(((unsigned)p + (unsigned)nn - 1u) / (unsigned)nn);
-  *ppc = q;
-  return (int)(((unsigned)p + (unsigned)q - 1u) / (unsigned)q);
+  return make_int2((int)(((unsigned)p + (unsigned)q - 1u) / (unsigned)q), q);
 }
 
-// Warp-wide (all 32 lanes, same result in each): the rule, R and this CTA's
-// range, then the first request with a piece in it.
-__device__ __noinline__ void ws_init(WorkSplit &w, const WsArgs &a, int lane) {
+__device__ __forceinline__ void ws_init_regs(WorkSplit &w, const WsArgs &a, int lane) {
   const int S = a.S;
   w.max_len = (long long)a.MP * S;
   long long tot = 0;
@@ -205,8 +206,8 @@ __device__ __noinline__ void ws_init(WorkSplit &w, const WsArgs &a, int lane) {
       if (!w.chunks) {
         has = true;
       } else {
-        int ppc = 1;
-        const int n = ws_count(w, off, p, a.max_splits, &ppc);
+        const int2 np = ws_count(w.chunks, w.c0, w.R, w.T, w.cp, off, p, a.max_splits);
+        const int n = np.x, ppc = np.y;
         // r0 - off < p here, so the chunk index fits an int
         c_lo = off >= w.r0 ? 0 : (int)((unsigned)(w.r0 - off + ppc - 1) / (unsigned)ppc);
         has = c_lo < n && off + (long long)c_lo * ppc < w.r1;
@@ -224,11 +225,21 @@ __device__ __noinline__ void ws_init(WorkSplit &w, const WsArgs &a, int lane) {
   }
 }
 
+// Warp-wide (all 32 lanes, same result in each): the rule, R and this CTA's
+// range, then the first request with a piece in it.  Works on register
+// copies of its arguments and writes the state once at the end.
+__device__ __noinline__ void ws_init(WorkSplit &w_out, const WsArgs &a_in, int lane) {
+  const WsArgs a = a_in;
+  WorkSplit w{};
+  ws_init_regs(w, a, lane);
+  w_out = w;
+}
+
 // The CTA's next piece, in request order (uniform across the warp); false
 // when the range has none left.  A piece that would break the workspace
 // bounds ends the walk instead of being used (it cannot occur when the
 // rules above hold).
-__device__ __noinline__ bool ws_next(WorkSplit &w, const WsArgs &a, Piece &pc) {
+__device__ __forceinline__ bool ws_next_regs(WorkSplit &w, const WsArgs &a, Piece &pc) {
   while (w.b < a.B) {
     const int L = __ldg(&a.seq_lens[w.b]);
     const int p = ws_pages(w, L, a.S);
@@ -237,8 +248,8 @@ __device__ __noinline__ bool ws_next(WorkSplit &w, const WsArgs &a, Piece &pc) {
       continue;
     }
     if (w.off + w.c0 >= w.r1) return false;
-    int ppc = 1;
-    const int n = ws_count(w, w.off, p, a.max_splits, &ppc);
+    const int2 np = ws_count(w.chunks, w.c0, w.R, w.T, w.cp, w.off, p, a.max_splits);
+    const int n = np.x, ppc = np.y;
     long long j, p0, p1;
     if (!w.chunks) {
       const long long s0 = w.off + w.c0;  // the request's first page on the cut line
@@ -273,6 +284,18 @@ __device__ __noinline__ bool ws_next(WorkSplit &w, const WsArgs &a, Piece &pc) {
     return true;
   }
   return false;
+}
+
+// ws_next_regs on register copies of the state and the arguments; the state
+// and the piece are written back once.
+__device__ __noinline__ bool ws_next(WorkSplit &w_io, const WsArgs &a_in, Piece &pc_out) {
+  const WsArgs a = a_in;
+  WorkSplit w = w_io;
+  Piece pc{};
+  const bool r = ws_next_regs(w, a, pc);
+  w_io = w;
+  pc_out = pc;
+  return r;
 }
 
 // ws_next on a state kept in shared memory (one copy per warp), so that it
