@@ -92,12 +92,13 @@ struct Piece {
   bool lead;  // the request's first piece: its CTA of head 0 records the numbering
 };
 
-// The work split runs once per call, at the start of every CTA, as code the
-// call has not run yet: an SM fetches it from memory line by line (measured,
-// latent-stream kernel: about 1 us per KB of straight-line code run for the
-// first time in a call).  Its helpers are therefore compiled once
-// (noinline) rather than copied into every call site, which keeps the
-// start-up path short.
+// The work split runs at the start of every CTA and once per piece.  Its
+// walk is inlined into the page loaders and keeps its state in registers:
+// as separately compiled functions taking the state by reference, the state
+// lived in local memory and each call paid the calling convention's register
+// saves (measured, grouped-query kernel: the first page copy ~1 us later and
+// the ragged decode call 1.5 us longer).  The rarely needed divisions stay
+// compiled once (noinline, all operands by value).
 //
 // floor(x / y) for x >= 0 and y >= 1 (the entry points bound batch *
 // max_pages by 2^40, and every dividend here is at most 2^12 times a page
@@ -228,7 +229,7 @@ __device__ __forceinline__ void ws_init_regs(WorkSplit &w, const WsArgs &a, int 
 // Warp-wide (all 32 lanes, same result in each): the rule, R and this CTA's
 // range, then the first request with a piece in it.  Works on register
 // copies of its arguments and writes the state once at the end.
-__device__ __noinline__ void ws_init(WorkSplit &w_out, const WsArgs &a_in, int lane) {
+__device__ __forceinline__ void ws_init(WorkSplit &w_out, const WsArgs &a_in, int lane) {
   const WsArgs a = a_in;
   WorkSplit w{};
   ws_init_regs(w, a, lane);
@@ -288,7 +289,7 @@ __device__ __forceinline__ bool ws_next_regs(WorkSplit &w, const WsArgs &a, Piec
 
 // ws_next_regs on register copies of the state and the arguments; the state
 // and the piece are written back once.
-__device__ __noinline__ bool ws_next(WorkSplit &w_io, const WsArgs &a_in, Piece &pc_out) {
+__device__ __forceinline__ bool ws_next(WorkSplit &w_io, const WsArgs &a_in, Piece &pc_out) {
   const WsArgs a = a_in;
   WorkSplit w = w_io;
   Piece pc{};
