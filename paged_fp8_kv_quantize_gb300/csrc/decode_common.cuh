@@ -373,6 +373,25 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   // written by this call's split kernel unless one of its CTAs gave up
   // first; checked so that no read leaves the workspace
   const bool sane = nb >= 1 && nb <= a.max_splits && c0 >= 0 && c0 <= a.B * a.max_splits - nb;
+  // The partial O rows this thread will weigh (thread = float4 column, group
+  // of pieces), the first kPre of them loaded now beside the status words
+  // and (m, l), so that their latency overlaps those loads: in the narrow
+  // shape (a few requests, many pieces each, where the merge's round trips
+  // are the whole of its time; long-context batch 58.7 -> 57.7 us per call).
+  // The wide shape keeps its registers (the ragged batch was 0.7 us slower
+  // with it).
+  constexpr int kPre = kWide ? 0 : 4;
+  const size_t cstride = (size_t)a.Hq * kD / 4;
+  const int col = col_lo + t % M::kW, grp = t / M::kW;
+  const bool real = col < col_hi;
+  const float4 *po =
+      reinterpret_cast<const float4 *>(a.part_o + ((size_t)(sane ? c0 : 0) * a.Hq + hg.first) * kD) + col;
+  float4 pre[kPre > 0 ? kPre : 1];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int c = grp + k * M::kGroups;
+    pre[k] = sane && nb > 1 && real && c < nb ? __ldcg(po + (size_t)c * cstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   uint32_t st = 0u;
   if (sane) {  // every piece's status word, one per head group of the pieces' kernel
     for (int i = t; i < nb * a.st_groups; i += 256) st |= __ldcg(&a.part_st[(size_t)c0 * a.st_groups + i]);
@@ -424,14 +443,18 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeArgs a) {
   for (int i = t; i < nb * M::kNH; i += 256) s_w[i] = fast_exp2(s_w[i] - s_M[i % M::kNH]);
   __syncthreads();
   // thread = (float4 column, group of splits)
-  const size_t cstride = (size_t)a.Hq * kD / 4;
-  const int col = col_lo + t % M::kW, grp = t / M::kW;
   const int jh = col * 4 / kD - h_lo;
-  const float4 *po = reinterpret_cast<const float4 *>(a.part_o + ((size_t)c0 * a.Hq + hg.first) * kD) + col;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const bool real = col < col_hi;
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int c = grp + k * M::kGroups;
+    if (real && c < nb) {
+      const float w = s_w[c * M::kNH + jh];
+      acc.x += w * pre[k].x; acc.y += w * pre[k].y; acc.z += w * pre[k].z; acc.w += w * pre[k].w;
+    }
+  }
 #pragma unroll 4
-  for (int c = grp; real && c < nb; c += M::kGroups) {
+  for (int c = grp + kPre * M::kGroups; real && c < nb; c += M::kGroups) {
     const float w = s_w[c * M::kNH + jh];
     const float4 v = __ldcg(po + (size_t)c * cstride);
     acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
