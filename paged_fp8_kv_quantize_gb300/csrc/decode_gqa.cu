@@ -40,6 +40,7 @@
 #include <mutex>
 
 #include "decode_common.cuh"
+#include "merge.cuh"
 
 namespace pfkv {
 

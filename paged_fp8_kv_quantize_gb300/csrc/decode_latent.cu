@@ -52,6 +52,7 @@
 #include <mutex>
 
 #include "decode_common.cuh"
+#include "merge.cuh"
 
 namespace pfkv {
 
