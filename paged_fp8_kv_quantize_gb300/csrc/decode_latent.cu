@@ -547,15 +547,36 @@ __device__ __forceinline__ float2 p_terms2(float lo, float hi, bool four, uint32
 // 0-36863: blocks 0-8; 36864-73727: blocks 9-15 and the tail).
 // qfac[b][h] = softmax scale * log2(e) * 2^e_h.
 __global__ void __launch_bounds__(256) qterm_kernel(const DecodeArgs a) {
+  constexpr int kRowV = kTD / 8 + 1;  // uint4 per staged row: 72 + 1 of padding (spreads the rows over the banks)
+  __shared__ uint4 s_q[16 * kRowV];
   __shared__ float s_inv[16];
+  __shared__ uint64_t s_bar;
+  __shared__ int s_abort;
   pdl_wait();  // the stream's earlier work is complete from here on
   pdl_launch_dependents();
   const int b = blockIdx.x >> 2, hq = blockIdx.x & 3;  // request, group of 16 heads
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint16_t *q = static_cast<const uint16_t *>(a.q) + ((size_t)b * kTH + 16 * hq) * kTD;
+  // the 16 query rows into shared memory with one bulk copy each (one
+  // memory round trip for the block)
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(&s_bar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&s_bar, 16 * kTD * 2);
+    for (int hh = 0; hh < 16; ++hh) bulk_load(&s_q[hh * kRowV], q + hh * kTD, kTD * 2, &s_bar);
+  }
+  const bool landed = mbar_wait(&s_bar, 0, &s_abort);  // bounded
+  if (__syncthreads_or(!landed))  // the copies did not land: read the rows directly
+    for (int i = tid; i < 16 * (kTD / 8); i += (int)blockDim.x)
+      s_q[(i / (kTD / 8)) * kRowV + i % (kTD / 8)] = reinterpret_cast<const uint4 *>(q)[i];
+  __syncthreads();
   for (int hh = warp; hh < 16; hh += 8) {
     float m = 0.f;
-    for (int k = lane; k < kTD / 8; k += 32) m = amax8(*reinterpret_cast<const uint4 *>(q + hh * kTD + 8 * k), m);
+    for (int k = lane; k < kTD / 8; k += 32) m = amax8(s_q[hh * kRowV + k], m);
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (lane == 0) {
       int e = 8;
@@ -581,8 +602,7 @@ __global__ void __launch_bounds__(256) qterm_kernel(const DecodeArgs a) {
       off1 = (size_t)65536 + R1 * 64 + 16 * (j ^ ((R1 >> 1) & 3));
       off2 = (size_t)65536 + R2 * 64 + 16 * (j ^ ((R2 >> 1) & 3));
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(q + hh * kTD + 16 * r);
-    const uint4 v0 = src[0], v1 = src[1];
+    const uint4 v0 = s_q[hh * kRowV + 2 * r], v1 = s_q[hh * kRowV + 2 * r + 1];
     const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     const float inv = s_inv[hh];
     uint32_t t1[4], t2[4];
