@@ -1,7 +1,7 @@
 // append_device.cuh -- one warp writes one (row, K|V, head) of a new token
 // into the paged cache.  Used by the stand-alone append kernel and by the
-// decode step, whose plan grid appends the step's new tokens beside the
-// planning block.
+// decode step's page loaders (which write a request's new row into its page
+// just before copying that page).
 //
 // "Smaller, faster, safer: running Kimi and GLM at scale", section
 // "Quantizing the KV cache": the decode pool stores K and V as FP8 e4m3.

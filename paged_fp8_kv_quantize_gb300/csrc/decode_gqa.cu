@@ -1,5 +1,6 @@
 // decode_gqa.cu -- split-KV paged decode attention for grouped-query heads
-// (head_dim 64/128, group 1..8) over an FP8 e4m3 or a BF16 paged cache.
+// (head_dim 64/128, any group size: groups above 8 heads run as head groups
+// of up to 8) over an FP8 e4m3 or a BF16 paged cache.
 //
 // "Smaller, faster, safer: running Kimi and GLM at scale", section
 // "Quantizing the KV cache": the cache is FP8 e4m3 and the attention kernel
@@ -23,10 +24,11 @@
 //                tensor-core MMA, online softmax in fp32.  A piece that
 //                covers a whole request writes its output directly;
 //                otherwise it leaves an unnormalised partial (m, l, O).
-//   2. merge  -- one CTA per (request, KV head, block of 64 float4
-//                columns): writes each request's status (the bits its
-//                pieces found, a bad length, or a timeout anywhere in the
-//                split grid), zeroes the rows of a faulted request, and
+//   2. merge  -- one CTA per (request, head group, block of 64 -- or, for
+//                small grids, 16 -- float4 columns; merge.cuh): writes
+//                each request's status (the bits its pieces found, a bad
+//                length, or a timeout anywhere in the split grid), zeroes
+//                the rows of a faulted request, and
 //                merges the partials of a request cut into several pieces
 //                by the log-sum-exp rule, split weights staged in shared
 //                memory and splits spread over thread groups.

@@ -15,12 +15,14 @@
 //        of the row's largest); both terms are rows of A, so one MMA per K
 //        step gives T1.k and T2.k, which the softmax warps add.  A lives in
 //        tensor memory (columns 0-511 of the query) and, for the last 64
-//        columns, in shared memory; it is loaded once per work item.
+//        columns, in shared memory; the softmax warps move it there from
+//        the page ring once per work item.
 //   O^T += V^T . P^T   M = 128 values (four chunks of the 512), N = 64
 //        heads, K = 64 tokens.  V^T is the page itself read MN-major.  The
 //        probabilities, with the token's scale folded in relative to a
-//        running reference scale, are written as P1 + P2 + P3 (three e4m3
-//        terms, about 12 significant bits) by the softmax warps.
+//        running reference scale, are written by the softmax warps as three
+//        8-bit terms (e4m3, e4m3, e5m2: 11 significant bits) or, on pages
+//        with large values, four (e4m3 x 3, e5m2: about 15 bits).
 // The softmax normaliser l sums the weights as the terms carry them.
 //
 // A small kernel first writes every request's query terms into the
@@ -28,9 +30,11 @@
 // CTA per SM, persistent.  There is no plan kernel: every CTA works out
 // its pieces from the lengths (the shared work split: the requests' pages,
 // plus a small per-piece overhead, cut into one equal range per CTA); a
-// piece is a request's part of the range, all 64 heads.  Warp 0 loads pages
-// into a five-page ring (TMA, bounds and tag checks beside the copies; in a
-// decode step it first writes the request's new row into its page); warp 1
+// piece is a request's part of the range, all 64 heads.  Warp 0 loads each
+// piece's query image (two ring entries) and then its pages into a
+// five-entry ring (TMA, bounds and tag checks beside the copies; in a
+// decode step it writes the request's new row into its page just before
+// copying that page); warp 1
 // owns tensor memory and issues the QK^T MMAs and warps 6 and 7 the PV MMAs
 // of two value chunks each (one thread each, so that the instruction
 // streams overlap on the tensor pipe); warps 2-5 and 8-11 run the softmax:
