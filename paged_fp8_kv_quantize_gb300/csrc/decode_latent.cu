@@ -75,7 +75,7 @@ constexpr uint32_t kPageSm = kPageTail + kTS * 64;  // 36864
 // of head h; columns 0-511 live in tensor memory, columns 512-575 in shared
 // memory as a 128 x 64 image with the 64-byte swizzle.
 constexpr uint32_t kQTailBytes = 128 * 64;    // 8192
-constexpr int kPieceCostLatent = 2;           // pages' worth of time a piece costs beyond its pages
+constexpr int kPieceCostLatent = 4;           // pages' worth of time a piece costs beyond its pages (swept 0-12: 4 fastest)
 constexpr int kPT = 4;                        // 8-bit terms of the probabilities (at most)
 constexpr uint32_t kPTerm = kTS * kTH;        // 4096: one P^T term of one page
 constexpr uint32_t kPBuf = kPT * kPTerm;      // 16384
