@@ -232,10 +232,10 @@ int pfkv_paged_decode_attention_fp8_noalloc(const pfkv_cache *cache, const void 
  * quantized on the way in for an FP8 cache) and then attended over, together
  * with the rest of its context, as pfkv_paged_decode_attention_* does.  The
  * post's two halves of the decode pool ("Quantizing the KV cache": rows are
- * stored as FP8 and converted as they are read) in one call: for the
- * grouped-query layouts the attention kernel writes each (request, KV head)
- * row itself, just before it copies the destination page; for the latent
- * stream the launch that plans the attention writes them.
+ * stored as FP8 and converted as they are read) in one call: the attention
+ * kernel's page loader writes each (request, KV head) row itself before it
+ * copies the destination page (grouped-query layouts and the latent
+ * stream alike).
  *   k_new, v_new : bf16 [batch][num_kv_heads][head_dim]; row b goes to
  *                  logical position seq_lens[b] - 1 (seq_lens counts the new
  *                  token); v_new is ignored (may be NULL) for a kv_shared
