@@ -85,7 +85,7 @@ constexpr uint32_t kPBuf = kPT * kPTerm;      // 16384
 // significant bits) keep it within 2e-3 only for values up to about this.
 constexpr float kFourTermAt = 8.f;
 constexpr int kNst = 5;                       // pages in flight per CTA
-constexpr int kPrefetch = 6;                  // pages pulled into L2 ahead of their copy
+constexpr int kPrefetch = 1;                  // pages pulled into L2 ahead of their copy (swept 0-10: 1 fastest)
 constexpr int kTThreads = 384;                // producer, QK issuer, softmax x4, two PV issuers, softmax x4
 constexpr int kSmxThreads = 256;              // the eight softmax warps (2-5 and 8-11)
 constexpr uint32_t kTmemCols = 512;
